@@ -1,0 +1,324 @@
+"""CPU oracle for FP8 / MXFP8 quantization -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does, and
+this package never imports the product library: the two share no code.
+
+The arithmetic lives in ``oracle.c`` (plain C, compiled here with gcc on
+first use).  This module marshals numpy arrays into it and holds the one
+piece of logic that is control flow rather than arithmetic: the
+delayed-scaling state machine, written in the order the pages give it
+("HiFloat8：高性能训练之路" 1.2 and 3; "混合精度与 FP8 训练" 8.2).
+
+Inputs: BF16 tensors are numpy ``uint16`` arrays of raw BF16 bits, FP32
+tensors are numpy ``float32`` arrays.  2-D tensors are row-major.
+
+Parity unpinned by the pages (our own readings, pinned only by this
+definition and the tests): the NaN output byte 0x7F, the MX non-finite
+block (scale 0xFF, elements 0x7F), and the per-tensor special cases
+(amax 0 -> scale 1; non-finite amax -> scale 1 plus a flag; an
+overflowing quotient -> FLT_MAX).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+E4M3 = 0
+E5M2 = 1
+BF16 = 0
+FP32 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (plain gcc, no fast-math)."""
+    with _lock:
+        stale = (not os.path.exists(_LIB_PATH)) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+        if force or stale:
+            tmp = _LIB_PATH + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+                   "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    c = ctypes
+    P = c.c_void_p
+    sig = {
+        "orc_fp8_value": (c.c_double, [c.c_int, c.c_uint]),
+        "orc_fp8_max_code": (c.c_uint, [c.c_int]),
+        "orc_fp8_max": (c.c_double, [c.c_int]),
+        "orc_fp8_encode": (c.c_uint, [c.c_int, c.c_double]),
+        "orc_amax_bits": (c.c_uint32, [P, c.c_int, c.c_int64, c.c_int64]),
+        "orc_per_tensor_scale": (c.c_float, [c.c_uint32, c.c_int, c.c_int, c.POINTER(c.c_int)]),
+        "orc_reciprocal": (c.c_float, [c.c_float]),
+        "orc_cast": (None, [P, c.c_int, c.c_int64, c.c_int64, c.c_float, c.c_int, P,
+                            c.POINTER(c.c_uint64), c.c_int]),
+        "orc_mx_block": (c.c_uint8, [P, c.c_int, c.c_int, P]),
+        "orc_mx_col_blocks": (c.c_int64, [P, c.c_int, c.c_int64]),
+        "orc_mx_quantize": (None, [P, c.c_int, c.c_int64, c.c_int64, P, c.c_int, c.c_int,
+                                   c.c_int, P, P, P, P, c.c_int64, c.c_int]),
+        "orc_encode_array": (None, [c.c_int, P, c.c_int64, P, c.c_int]),
+        "orc_encode_f32_range": (None, [c.c_int, c.c_uint64, c.c_int64, P, c.c_int]),
+        "orc_max_threads": (c.c_int, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def max_threads() -> int:
+    return int(_load().orc_max_threads())
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else None
+
+
+def _dtype_code(x: np.ndarray) -> int:
+    if x.dtype == np.uint16:
+        return BF16
+    if x.dtype == np.float32:
+        return FP32
+    raise TypeError("oracle inputs are uint16 (BF16 bits) or float32")
+
+
+# --------------------------------------------------------------------------
+# Scalars
+# --------------------------------------------------------------------------
+def fp8_value(fmt: int, code: int) -> float:
+    """Value of an E4M3/E5M2 code ("混合精度与 FP8 训练" 2.1-2.2)."""
+    return float(_load().orc_fp8_value(fmt, code))
+
+
+def fp8_max(fmt: int) -> float:
+    return float(_load().orc_fp8_max(fmt))
+
+
+def fp8_max_code(fmt: int) -> int:
+    return int(_load().orc_fp8_max_code(fmt))
+
+
+def fp8_encode(fmt: int, a: float) -> int:
+    """Saturating RNE of the exact value ``a`` ("混合精度与 FP8 训练" 4.1, 8.1)."""
+    return int(_load().orc_fp8_encode(fmt, float(a)))
+
+
+def encode_array(fmt: int, a: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    q = np.empty(a.shape, dtype=np.uint8)
+    _load().orc_encode_array(fmt, _ptr(a), a.size, _ptr(q), nthreads or max_threads())
+    return q
+
+
+def encode_f32_range(fmt: int, first: int, n: int, nthreads: int = 0) -> np.ndarray:
+    """Codes of the FP32 bit patterns first .. first+n-1 (scale 1)."""
+    q = np.empty(n, dtype=np.uint8)
+    _load().orc_encode_f32_range(fmt, first, n, _ptr(q), nthreads or max_threads())
+    return q
+
+
+def bits_to_f32(bits: int) -> np.float32:
+    return np.array([bits], dtype=np.uint32).view(np.float32)[0]
+
+
+def f32_to_bits(f) -> int:
+    return int(np.array([f], dtype=np.float32).view(np.uint32)[0])
+
+
+# --------------------------------------------------------------------------
+# Per-tensor scaling
+# --------------------------------------------------------------------------
+def amax_bits(x: np.ndarray, begin: int = 0, end: int | None = None) -> int:
+    """FP32 bits of max |x| over the flat range [begin, end)."""
+    x = np.ascontiguousarray(x)
+    end = x.size if end is None else end
+    return int(_load().orc_amax_bits(_ptr(x), _dtype_code(x), begin, end))
+
+
+def amax(x: np.ndarray, begin: int = 0, end: int | None = None) -> np.float32:
+    return bits_to_f32(amax_bits(x, begin, end))
+
+
+def per_tensor_scale(amax_value_bits: int, fmt: int, margin: int) -> tuple[np.float32, bool]:
+    """Scale = fl32(fl32(F8max/amax) * 2^-margin) with the special cases."""
+    nf = ctypes.c_int(0)
+    s = _load().orc_per_tensor_scale(amax_value_bits, fmt, margin, ctypes.byref(nf))
+    return np.float32(s), bool(nf.value)
+
+
+def reciprocal(s) -> np.float32:
+    return np.float32(_load().orc_reciprocal(float(s)))
+
+
+def cast(x: np.ndarray, scale, fmt: int, begin: int = 0, end: int | None = None,
+         out: np.ndarray | None = None, nthreads: int = 0) -> tuple[np.ndarray, int]:
+    """q = RNE_sat(fl32(x * scale)) over the flat range; returns (q, sat_count)."""
+    x = np.ascontiguousarray(x)
+    end = x.size if end is None else end
+    q = np.zeros(x.size, dtype=np.uint8) if out is None else out
+    sat = ctypes.c_uint64(0)
+    _load().orc_cast(_ptr(x), _dtype_code(x), begin, end, float(np.float32(scale)), fmt,
+                     _ptr(q), ctypes.byref(sat), nthreads or max_threads())
+    return q, int(sat.value)
+
+
+def _group_bounds(rows: int, offsets) -> list[tuple[int, int]]:
+    if offsets is None:
+        return [(0, rows)]
+    o = [int(v) for v in offsets]
+    return [(o[g], o[g + 1]) for g in range(len(o) - 1)]
+
+
+def current_scaling(x: np.ndarray, fmt: int, margin: int = 0, offsets=None,
+                    nthreads: int = 0) -> dict:
+    """Per-tensor (or per-group) current scaling of a 2-D tensor.
+
+    For each group of rows: amax, scale (eq. 1 of "HiFloat8：高性能训练之路"
+    1.2, times 2^-margin), cast (eq. 2).  Returns q (flat), and per group
+    amax / scale / scale_inv (float32), sat (int) and the non-finite flag.
+    """
+    rows, cols = x.shape
+    flat = np.ascontiguousarray(x).reshape(-1)
+    q = np.zeros(flat.size, dtype=np.uint8)
+    res = {"q": q, "amax": [], "scale": [], "scale_inv": [], "sat": [], "nonfinite": []}
+    for r0, r1 in _group_bounds(rows, offsets):
+        a = amax_bits(flat, r0 * cols, r1 * cols)
+        s, nf = per_tensor_scale(a, fmt, margin)
+        _, sat = cast(flat, s, fmt, r0 * cols, r1 * cols, out=q, nthreads=nthreads)
+        res["amax"].append(bits_to_f32(a))
+        res["scale"].append(s)
+        res["scale_inv"].append(reciprocal(s))
+        res["sat"].append(sat)
+        res["nonfinite"].append(nf)
+    for k in ("amax", "scale", "scale_inv"):
+        res[k] = np.array(res[k], dtype=np.float32)
+    res["sat"] = np.array(res["sat"], dtype=np.uint64)
+    return res
+
+
+class DelayedScaling:
+    """Delayed per-tensor scaling, the state machine of the pages.
+
+    "HiFloat8：高性能训练之路" 1.2: an amax history buffer of fixed length;
+    the scale uses the max over the history (eqs. 3-4, with 2^-N); every
+    Interval steps the true amax of the current tensor is computed and
+    appended, dropping the oldest entry once the buffer is full.  Section 3
+    of the same page fixes the timing for Interval = 1: step 0 computes the
+    amax, step 1 scales with it and then records its own, and so on.
+    Section 5.2 (and "昇腾 950" 3.2): the first step after a (re)start has
+    no history, so it uses current scaling.
+
+    Readings (the design doc lists them): a step records iff step % interval == 0,
+    counting from creation or reset; the first step uses margin 0; the max
+    runs over the filled entries only.
+    """
+
+    def __init__(self, history_len: int, interval: int, margin: int, fmt: int):
+        self.H, self.interval, self.margin, self.fmt = history_len, interval, margin, fmt
+        self.reset()
+
+    def reset(self):
+        self.hist = [np.float32(0.0)] * self.H
+        self.head = 0
+        self.count = 0
+        self.step_no = 0
+        self.nonfinite = False
+
+    def _history_max_bits(self) -> int:
+        return max(f32_to_bits(v) & 0x7FFFFFFF for v in self.hist[: self.count])
+
+    def step(self, x: np.ndarray, nthreads: int = 0) -> dict:
+        flat = np.ascontiguousarray(x).reshape(-1)
+        recorded_amax = None
+        if self.count == 0:
+            a = amax_bits(flat)  # current scaling on the first step
+            scale, nf = per_tensor_scale(a, self.fmt, 0)
+            recorded_amax = a
+        else:
+            scale, nf = per_tensor_scale(self._history_max_bits(), self.fmt, self.margin)
+        if nf:
+            self.nonfinite = True
+        q, sat = cast(flat, scale, self.fmt, nthreads=nthreads)
+        recording = (self.step_no % self.interval) == 0
+        if recording:
+            if recorded_amax is None:
+                recorded_amax = amax_bits(flat)
+            if (recorded_amax & 0x7FFFFFFF) >= 0x7F800000:
+                self.nonfinite = True
+            self.hist[self.head] = bits_to_f32(recorded_amax)
+            self.head = (self.head + 1) % self.H
+            self.count = min(self.count + 1, self.H)
+        self.step_no += 1
+        return {"q": q, "scale": scale, "scale_inv": reciprocal(scale), "sat": sat,
+                "amax": bits_to_f32(recorded_amax) if recording else None,
+                "recorded": recording}
+
+
+# --------------------------------------------------------------------------
+# MXFP8
+# --------------------------------------------------------------------------
+def mx_block(values: np.ndarray, fmt: int) -> tuple[int, np.ndarray]:
+    """One MX block of k <= 32 float32 values -> (scale byte, codes)."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    q = np.zeros(v.size, dtype=np.uint8)
+    b = _load().orc_mx_block(_ptr(v), v.size, fmt, _ptr(q))
+    return int(b), q
+
+
+def mx_col_blocks(rows: int, offsets=None) -> int:
+    """sum over groups of ceil(n_g / 32) (one group when offsets is None)."""
+    if offsets is None:
+        return (rows + 31) // 32
+    o = np.ascontiguousarray(offsets, dtype=np.int64)
+    return int(_load().orc_mx_col_blocks(_ptr(o), o.size - 1, rows))
+
+
+def mx_quantize(x: np.ndarray, fmt: int, direction: int = 3, offsets=None,
+                s_col_ld: int | None = None, nthreads: int = 0) -> dict:
+    """MX quantization of a 2-D tensor (rows x cols, cols % 32 == 0).
+
+    direction: 1 rowwise, 2 columnwise, 3 both.  Returns q_row [rows, cols],
+    s_row [rows, cols/32], q_col [cols, rows] (the transpose), s_col
+    [cols, s_col_ld] with the first mx_col_blocks() entries of each row used.
+    """
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    assert cols % 32 == 0
+    G = 1 if offsets is None else len(offsets) - 1
+    o = None if offsets is None else np.ascontiguousarray(offsets, dtype=np.int64)
+    T = mx_col_blocks(rows, o)
+    ld = T if s_col_ld is None else s_col_ld
+    q_row = np.zeros((rows, cols), np.uint8) if direction & 1 else None
+    s_row = np.zeros((rows, cols // 32), np.uint8) if direction & 1 else None
+    q_col = np.zeros((cols, rows), np.uint8) if direction & 2 else None
+    s_col = np.zeros((cols, max(ld, 1)), np.uint8) if direction & 2 else None
+    dummy = np.zeros(1, np.uint8)
+    _load().orc_mx_quantize(
+        _ptr(x), _dtype_code(x), rows, cols, _ptr(o) if o is not None else None, G, fmt,
+        direction,
+        _ptr(q_row if q_row is not None else dummy), _ptr(s_row if s_row is not None else dummy),
+        _ptr(q_col if q_col is not None else dummy), _ptr(s_col if s_col is not None else dummy),
+        ld, nthreads or max_threads())
+    return {"q_row": q_row, "s_row": s_row, "q_col": q_col, "s_col": s_col, "col_blocks": T}

@@ -1,0 +1,368 @@
+/*
+ * oracle.c -- plain, slow CPU oracle for FP8 / MXFP8 quantization.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library may include,
+ * link or call this file; only the tests, the smoke check and the CPU
+ * baseline of the benchmark use it.  It shares no code, header, table or
+ * constant with the CUDA path.
+ *
+ * Every function follows one passage of the source pages:
+ *   "混合精度与 FP8 训练" (hs-black.github.io), sections 2.1-2.3 (float
+ *     fields, BF16, E4M3/E5M2), 3 (binades), 4.1 (round-to-nearest-even),
+ *     8.1 (why FP8 needs a scale, saturation), 8.2 (delayed vs current
+ *     scaling, TE's (F8max/amax)/2^margin), 13.1 (MX blocks, E8M0).
+ *   "HiFloat8：高性能训练之路" (hifloat.gccorg.com), section 1.2
+ *     (eqs. 1-4: Scale = F8max/Amax, delayed Scale with 2^-N), section 2
+ *     (MXFP8 1x32 blocks, rowwise and columnwise copies).
+ *   "Blackwell GPU MXFP8 预训练最佳实践" (51cto.com), section 4.1 (the
+ *     round-up E8M0 rule, amax = 0 gives X = -127, saturating RN cast),
+ *     section 4.2 (two copies per tensor, one per reduction axis).
+ *
+ * Arithmetic is done in double wherever a value is compared or scaled, so
+ * every comparison below is exact.  Where the definition fixes an FP32
+ * intermediate (the per-tensor scale and the product x*scale), the exact
+ * double result is rounded once to float; for one multiply or one divide of
+ * two floats, rounding the double result to float gives the correctly
+ * rounded float result (53 >= 2*24 + 2), so this is IEEE single arithmetic.
+ *
+ * Readings where the pages are silent (documented again in the design doc):
+ *   - any NaN input encodes to byte 0x7F in both formats;
+ *   - +-Inf saturates to +-max like any other overflow;
+ *   - the sign of zero is kept (0x80), except in an all-zero MX block;
+ *   - amax is the largest |x| compared on the magnitude bits, so a NaN
+ *     input makes amax NaN (largest payload wins);
+ *   - an MX block whose amax is Inf or NaN gets scale byte 0xFF and all
+ *     elements 0x7F;
+ *   - per-tensor: amax = 0 gives scale 1, a non-finite amax gives scale 1
+ *     and raises the non-finite flag, and an overflowing F8max/amax gives
+ *     FLT_MAX.
+ * Those readings are pinned only by their own definition ("parity unpinned"
+ * by the pages); everything else is pinned by page values, closed forms and
+ * library routines in tests/test_oracle_pins.py.
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_E4M3 0
+#define ORC_E5M2 1
+#define ORC_BF16 0
+#define ORC_FP32 1
+
+/* ------------------------------------------------------------------ */
+/* 8-bit float formats ("混合精度与 FP8 训练" 2.1-2.2).                   */
+/* E4M3: 4 exponent bits, bias 7, 3 mantissa bits, no infinities, a   */
+/* single NaN pattern S.1111.111, so the top binade holds 256..448.   */
+/* E5M2: IEEE style, 5 exponent bits, bias 15, 2 mantissa bits,       */
+/* exponent field 31 is Inf (mantissa 0) or NaN.                      */
+/* ------------------------------------------------------------------ */
+static int exp_bits(int fmt) { return fmt == ORC_E4M3 ? 4 : 5; }
+static int man_bits(int fmt) { return fmt == ORC_E4M3 ? 3 : 2; }
+static int bias_of(int fmt) { return fmt == ORC_E4M3 ? 7 : 15; }
+
+/* Value of an 8-bit code, straight from the field definition. */
+static double code_value_def(int fmt, unsigned code)
+{
+    unsigned sign = (code >> 7) & 1u;
+    unsigned ebits = (code >> man_bits(fmt)) & ((1u << exp_bits(fmt)) - 1u);
+    unsigned mbits = code & ((1u << man_bits(fmt)) - 1u);
+    unsigned emax_field = (1u << exp_bits(fmt)) - 1u;
+    double mag;
+    if (fmt == ORC_E4M3 && ebits == emax_field && mbits == 7u) return NAN;
+    if (fmt == ORC_E5M2 && ebits == emax_field)
+        return mbits ? NAN : (sign ? -INFINITY : INFINITY);
+    if (ebits == 0) /* subnormal: 0.m * 2^(1-bias) */
+        mag = ldexp((double)mbits, 1 - bias_of(fmt) - man_bits(fmt));
+    else            /* normal: 1.m * 2^(e-bias) */
+        mag = ldexp((double)((1u << man_bits(fmt)) | mbits),
+                    (int)ebits - bias_of(fmt) - man_bits(fmt));
+    return sign ? -mag : mag;
+}
+
+/* The definition above, tabulated once for all 256 codes of both formats
+ * when the library is loaded (a cache, not a second definition). */
+static double code_table[2][256];
+static unsigned max_code_table[2];
+
+__attribute__((constructor)) static void build_code_tables(void)
+{
+    for (int fmt = 0; fmt < 2; fmt++) {
+        unsigned c;
+        for (c = 0; c < 256u; c++) code_table[fmt][c] = code_value_def(fmt, c);
+        c = 0x7F;
+        while (!isfinite(code_table[fmt][c])) c--;
+        max_code_table[fmt] = c;
+    }
+}
+
+double orc_fp8_value(int fmt, unsigned code) { return code_table[fmt][code & 0xFFu]; }
+
+/* Largest non-negative finite code: E4M3 0x7E (448), E5M2 0x7B (57344). */
+unsigned orc_fp8_max_code(int fmt) { return max_code_table[fmt]; }
+
+double orc_fp8_max(int fmt) { return orc_fp8_value(fmt, orc_fp8_max_code(fmt)); }
+
+/*
+ * Saturating round-to-nearest-even of an exact real value a
+ * ("混合精度与 FP8 训练" 4.1 for RNE, 8.1 for saturation instead of
+ * overflow; "Blackwell GPU MXFP8 预训练最佳实践" 4.1 for the saturating
+ * RN cast).  Encoding is a search over the list of codes in value order,
+ * not bit manipulation: the nearest representable value wins, and on an
+ * exact tie the code whose last mantissa bit is 0 wins.
+ */
+unsigned orc_fp8_encode(int fmt, double a)
+{
+    unsigned maxc = orc_fp8_max_code(fmt);
+    unsigned sign, lo, hi, c;
+    double m, vlo, vhi, dlo, dhi;
+    if (isnan(a)) return 0x7Fu;
+    sign = signbit(a) ? 0x80u : 0u;
+    m = fabs(a);
+    if (m >= orc_fp8_value(fmt, maxc)) return sign | maxc; /* saturate (also Inf) */
+    /* largest code lo with value(lo) <= m (values grow with the code) */
+    lo = 0;
+    hi = maxc; /* invariant: value(lo) <= m < value(hi) */
+    while (hi - lo > 1u) {
+        unsigned mid = (lo + hi) / 2u;
+        if (orc_fp8_value(fmt, mid) <= m) lo = mid; else hi = mid;
+    }
+    vlo = orc_fp8_value(fmt, lo);
+    vhi = orc_fp8_value(fmt, hi);
+    dlo = m - vlo;
+    dhi = vhi - m;
+    if (dlo < dhi) c = lo;
+    else if (dhi < dlo) c = hi;
+    else c = (lo & 1u) ? hi : lo; /* tie: even code */
+    return sign | c;
+}
+
+/* ------------------------------------------------------------------ */
+/* Input decode: BF16 is FP32 with the low 16 bits removed            */
+/* ("混合精度与 FP8 训练" 2.2), so widening appends 16 zero bits.         */
+/* ------------------------------------------------------------------ */
+static uint32_t input_bits(const void* x, int dt, int64_t i)
+{
+    if (dt == ORC_BF16) return ((uint32_t)((const uint16_t*)x)[i]) << 16;
+    return ((const uint32_t*)x)[i];
+}
+
+static float bits_to_float(uint32_t b)
+{
+    float f;
+    memcpy(&f, &b, 4);
+    return f;
+}
+
+static uint32_t float_to_bits(float f)
+{
+    uint32_t b;
+    memcpy(&b, &f, 4);
+    return b;
+}
+
+float orc_input_value(const void* x, int dt, int64_t i) { return bits_to_float(input_bits(x, dt, i)); }
+
+/* ------------------------------------------------------------------ */
+/* amax = max |x_i| ("HiFloat8：高性能训练之路" 1.2 ComputeAmax;          */
+/* "混合精度与 FP8 训练" 8.1).  Compared on the magnitude bits, which     */
+/* orders finite values by |x| and puts NaN above Inf.                */
+/* Returned as FP32 bits.                                             */
+/* ------------------------------------------------------------------ */
+uint32_t orc_amax_bits(const void* x, int dt, int64_t begin, int64_t end)
+{
+    uint32_t best = 0;
+    for (int64_t i = begin; i < end; i++) {
+        uint32_t mag = input_bits(x, dt, i) & 0x7FFFFFFFu;
+        if (mag > best) best = mag;
+    }
+    return best;
+}
+
+/* ------------------------------------------------------------------ */
+/* Per-tensor scale.  Current scaling: Scale = F8max / Amax (eq. 1 of */
+/* "HiFloat8：高性能训练之路" 1.2); delayed scaling multiplies by 2^-N    */
+/* (eqs. 3-4 there; TE's (F8max/amax)/2^margin in "混合精度与 FP8 训练"  */
+/* 8.2).  FP32 arithmetic: the quotient is rounded to float, then the */
+/* power-of-two factor applied and rounded again.                     */
+/* ------------------------------------------------------------------ */
+float orc_per_tensor_scale(uint32_t amax_bits, int fmt, int margin, int* nonfinite)
+{
+    float amax = bits_to_float(amax_bits);
+    float s;
+    if (nonfinite) *nonfinite = 0;
+    if (!isfinite(amax)) {
+        if (nonfinite) *nonfinite = 1;
+        return 1.0f;
+    }
+    if (amax == 0.0f) return 1.0f;
+    s = (float)(orc_fp8_max(fmt) / (double)amax);
+    if (isinf(s)) s = FLT_MAX;
+    s = (float)((double)s * ldexp(1.0, -margin));
+    return s;
+}
+
+float orc_reciprocal(float s) { return (float)(1.0 / (double)s); }
+
+/* ------------------------------------------------------------------ */
+/* Scaled cast (eq. 2 of "HiFloat8：高性能训练之路" 1.2): q_i =           */
+/* RNE_sat(fl32(x_i * scale)).  sat counts elements whose scaled       */
+/* magnitude exceeds F8max (NaN excluded).                             */
+/* ------------------------------------------------------------------ */
+void orc_cast(const void* x, int dt, int64_t begin, int64_t end, float scale, int fmt,
+              uint8_t* q, uint64_t* sat, int nthreads)
+{
+    double f8max = orc_fp8_max(fmt);
+    uint64_t count = 0;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(static) reduction(+ : count) num_threads(nthreads)
+#endif
+    for (int64_t i = begin; i < end; i++) {
+        float y = (float)((double)orc_input_value(x, dt, i) * (double)scale);
+        if (!isnan(y) && fabs((double)y) > f8max) count++;
+        q[i] = (uint8_t)orc_fp8_encode(fmt, (double)y);
+    }
+    if (sat) *sat = count;
+}
+
+/* ------------------------------------------------------------------ */
+/* MX block ("Blackwell GPU MXFP8 预训练最佳实践" 4.1; "混合精度与 FP8     */
+/* 训练" 13.1).  X = ceil(log2(amax / destmax)) computed exactly: the   */
+/* smallest integer X with amax <= destmax * 2^X, saturated to the     */
+/* UE8M0 range [-127, 127]; the stored byte is X + 127.  amax = 0 gives */
+/* X = -127 and all elements 0.  Each element is RNE_sat(v / 2^X).     */
+/* ------------------------------------------------------------------ */
+uint8_t orc_mx_block(const float* v, int k, int fmt, uint8_t* q)
+{
+    uint32_t amax = 0;
+    double destmax = orc_fp8_max(fmt);
+    int X, i;
+    for (i = 0; i < k; i++) {
+        uint32_t mag = float_to_bits(v[i]) & 0x7FFFFFFFu;
+        if (mag > amax) amax = mag;
+    }
+    if (amax >= 0x7F800000u) { /* Inf or NaN in the block */
+        for (i = 0; i < k; i++) q[i] = 0x7F;
+        return 0xFF;
+    }
+    if (amax == 0) {
+        for (i = 0; i < k; i++) q[i] = 0x00;
+        return 0x00; /* X = -127 */
+    }
+    for (X = -127; X < 127; X++)
+        if ((double)bits_to_float(amax) <= ldexp(destmax, X)) break;
+    for (i = 0; i < k; i++) q[i] = (uint8_t)orc_fp8_encode(fmt, ldexp((double)v[i], -X));
+    return (uint8_t)(X + 127);
+}
+
+/* Group g covers rows [offs[g], offs[g+1]); offs == NULL means one group. */
+static int64_t grp_off(const int64_t* offs, int G, int64_t rows, int g)
+{
+    if (!offs) return g == 0 ? 0 : rows;
+    (void)G;
+    return offs[g];
+}
+
+/* Number of columnwise blocks: sum over groups of ceil(n_g / 32). */
+int64_t orc_mx_col_blocks(const int64_t* offs, int G, int64_t rows)
+{
+    int64_t t = 0;
+    int g, ng = offs ? G : 1;
+    for (g = 0; g < ng; g++) {
+        int64_t n = grp_off(offs, ng, rows, g + 1) - grp_off(offs, ng, rows, g);
+        t += (n + 31) / 32;
+    }
+    return t;
+}
+
+/*
+ * MX quantization of a rows x cols tensor, rowwise and/or columnwise
+ * ("HiFloat8：高性能训练之路" 2 and "Blackwell GPU MXFP8 预训练最佳实践"
+ * 4.2: one copy per reduction axis, both from the high-precision tensor;
+ * "混合精度与 FP8 训练" 13.1: MX does not commute with transposition).
+ *   rowwise:    blocks x[r, 32j .. 32j+31] -> q_row[r*cols + c],
+ *               s_row[r*(cols/32) + j]
+ *   columnwise: per group, blocks of 32 consecutive rows starting at the
+ *               group's first row (the last one may be shorter) ->
+ *               q_col[c*rows + r] (the transpose), s_col[c*s_col_ld + b],
+ *               b counting blocks over all groups in order.
+ * dir: 1 rowwise, 2 columnwise, 3 both.
+ */
+void orc_mx_quantize(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* offs,
+                     int G, int fmt, int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                     uint8_t* s_col, int64_t s_col_ld, int nthreads)
+{
+    int ng = offs ? G : 1;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#endif
+    if (dir & 1) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+        for (int64_t r = 0; r < rows; r++) {
+            float v[32];
+            for (int64_t j = 0; j < cols / 32; j++) {
+                for (int i = 0; i < 32; i++) v[i] = orc_input_value(x, dt, r * cols + j * 32 + i);
+                s_row[r * (cols / 32) + j] = orc_mx_block(v, 32, fmt, q_row + r * cols + j * 32);
+            }
+        }
+    }
+    if (dir & 2) {
+        int64_t base = 0;
+        for (int g = 0; g < ng; g++) {
+            int64_t r0 = grp_off(offs, ng, rows, g), r1 = grp_off(offs, ng, rows, g + 1);
+            int64_t nb = (r1 - r0 + 31) / 32;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+            for (int64_t c = 0; c < cols; c++) {
+                float v[32];
+                uint8_t qb[32];
+                for (int64_t b = 0; b < nb; b++) {
+                    int64_t rs = r0 + 32 * b;
+                    int k = (int)((r1 - rs) < 32 ? (r1 - rs) : 32);
+                    for (int i = 0; i < k; i++) v[i] = orc_input_value(x, dt, (rs + i) * cols + c);
+                    s_col[c * s_col_ld + base + b] = orc_mx_block(v, k, fmt, qb);
+                    for (int i = 0; i < k; i++) q_col[c * rows + rs + i] = qb[i];
+                }
+            }
+            base += nb;
+        }
+    }
+}
+
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Array form of orc_fp8_encode, for the tests' sweeps. */
+void orc_encode_array(int fmt, const double* a, int64_t n, uint8_t* q, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t i = 0; i < n; i++) q[i] = (uint8_t)orc_fp8_encode(fmt, a[i]);
+}
+
+/* Encode every FP32 bit pattern in [first, first + n) with scale 1; used by
+ * the exhaustive FP32 sweep (q[i] is the code of the pattern first + i). */
+void orc_encode_f32_range(int fmt, uint64_t first, int64_t n, uint8_t* q, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t i = 0; i < n; i++)
+        q[i] = (uint8_t)orc_fp8_encode(fmt, (double)bits_to_float((uint32_t)(first + (uint64_t)i)));
+}

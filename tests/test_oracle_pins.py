@@ -1,0 +1,435 @@
+"""Pins for the CPU oracle: page values, closed forms and library routines.
+
+Nothing here touches a GPU or the product library.  Each check ties the
+oracle to something other than itself: a value printed on a page
+(tests/golden/page_values.json, delayed_traces.txt), a closed form, an
+invariant, or torch's own float8 conversion, so that a plausible slip in
+the oracle (a wrong bias, a tie rounded away from even, a dropped sign, a
+floor where the rule says ceil, a transposed index) fails at least one.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import to_bf16_bits
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+PAGES = json.load(open(os.path.join(GOLD, "page_values.json"), encoding="utf-8"))
+FMT = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2}
+TORCH_FP8 = {oracle.E4M3: torch.float8_e4m3fn, oracle.E5M2: torch.float8_e5m2}
+
+
+def torch_encode(fmt, values):
+    """Library routine: clamp to +-max, then torch's RNE float8 conversion."""
+    m = oracle.fp8_max(fmt)
+    t = torch.from_numpy(np.asarray(values, dtype=np.float64)).clamp(-m, m)
+    return t.to(TORCH_FP8[fmt]).view(torch.uint8).numpy()
+
+
+# ---------------------------------------------------------------------------
+# Page values
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", PAGES["encode"], ids=lambda c: c["id"])
+def test_page_encode_examples(case):
+    fmt = FMT[case["fmt"]]
+    x = np.array([case["input"]], dtype=np.float32)
+    if case["input_dtype"] == "bf16":
+        x = to_bf16_bits(x)
+    if "amax" in case:
+        a = oracle.amax_bits(np.array([case["amax"]], dtype=np.float32))
+        s, nf = oracle.per_tensor_scale(a, fmt, 0)
+        assert not nf
+        assert float(s) == case["scale"]
+    else:
+        s = np.float32(case["scale"])
+    q, _ = oracle.cast(x, s, fmt)
+    assert q[0] == int(case["code"], 16)
+    assert oracle.fp8_value(fmt, int(q[0])) == case["value"]
+
+
+def test_page_bf16_example():
+    case = PAGES["bf16"][0]
+    b = to_bf16_bits(np.array([case["input"]], dtype=np.float32))
+    assert float(np.array([int(b[0]) << 16], dtype=np.uint32).view(np.float32)[0]) == case["bf16_value"]
+
+
+@pytest.mark.parametrize("case", PAGES["formats"], ids=lambda c: c["id"])
+def test_page_format_facts(case):
+    fmt = FMT[case["fmt"]]
+    assert oracle.fp8_max(fmt) == case["max"]
+    vals = [oracle.fp8_value(fmt, c) for c in range(256)]
+    finite_pos = sorted({v for v in vals if math.isfinite(v) and v > 0})
+    # smallest subnormal / normal
+    assert finite_pos[0] == 2.0 ** case["min_subnormal_exp"]
+    min_normal = min(v for c, v in enumerate(vals) if math.isfinite(v) and v > 0 and (c & 0x7F) >> (3 if fmt == oracle.E4M3 else 2))
+    assert min_normal == 2.0 ** case["min_normal_exp"]
+    # binades: log2(max / smallest subnormal)
+    assert round(math.log2(case["max"] / finite_pos[0]), 1) == case["binades"]
+    # values per binade [1, 2)
+    assert sum(1 for v in finite_pos if 1.0 <= v < 2.0) == case["values_per_binade"]
+    if fmt == oracle.E4M3:
+        nan_codes = [c for c in range(256) if math.isnan(vals[c])]
+        assert nan_codes == [int(c, 16) for c in case["nan_codes"]]
+        assert not any(math.isinf(v) for v in vals)
+        assert [v for v in finite_pos if v >= 256] == case["top_binade"]
+    else:
+        assert vals[0x7C] == math.inf and vals[0xFC] == -math.inf
+        assert all(math.isnan(vals[c]) for c in (0x7D, 0x7E, 0x7F))
+
+
+@pytest.mark.parametrize("fmt,count", [(oracle.E4M3, 7), (oracle.E5M2, 3)])
+def test_page_interior_values_in_1_2(fmt, count):
+    """"混合精度与 FP8 训练" 3: 10000 points in [1,2] land on 7 (E4M3) / 3 (E5M2) interior values."""
+    pts = np.linspace(1.0, 2.0, 10000)
+    q = oracle.encode_array(fmt, pts)
+    vals = {oracle.fp8_value(fmt, int(c)) for c in np.unique(q)}
+    interior = sorted(v for v in vals if 1.0 < v < 2.0)
+    assert len(interior) == count
+    if fmt == oracle.E4M3:
+        assert interior == [1.125, 1.25, 1.375, 1.5, 1.625, 1.75, 1.875]
+
+
+def test_page_delayed_saturation_T5():
+    case = PAGES["delayed_saturation"]
+    fmt = FMT[case["fmt"]]
+    d = oracle.DelayedScaling(history_len=16, interval=1, margin=case["margin"], fmt=fmt)
+    x0 = np.array([case["history_amax"], 1.0, -3.0], dtype=np.float32)
+    r0 = d.step(x0)
+    assert np.isclose(float(r0["scale"]), case["scale_before"], rtol=1e-6)
+    x1 = np.array([case["spike"], 1.0], dtype=np.float32)
+    r1 = d.step(x1)
+    assert np.isclose(float(r1["scale"]), case["scale_before"], rtol=1e-6)
+    assert np.isclose(case["spike"] * float(r1["scale"]), case["spike_scaled"], rtol=1e-6)
+    assert oracle.fp8_value(fmt, int(r1["q"][0])) == case["spike_code_value"]
+    assert np.isclose(case["spike_code_value"] / float(r1["scale"]), case["spike_dequant"], rtol=1e-6)
+    assert r1["sat"] == 1
+    r2 = d.step(np.array([1.0], dtype=np.float32))
+    assert np.isclose(float(r2["scale"]), case["scale_after"], rtol=1e-6)
+
+
+def _read_traces():
+    traces, cur = {}, None
+    for line in open(os.path.join(GOLD, "delayed_traces.txt"), encoding="utf-8"):
+        line = line.strip()
+        if line.startswith("# trace"):
+            parts = line[2:].split()
+            cur = {"name": parts[1]}
+            for kv in parts[2:]:
+                k, _, v = kv.partition("=")
+                if k in ("H", "margin") and v.isdigit():
+                    cur[k] = int(v)
+            cur["rows"] = []
+            traces[cur["name"]] = cur
+        elif line and not line.startswith("#") and cur is not None:
+            t, a, used, rec = line.split()
+            cur["rows"].append((int(t), float(a), float(used), rec == "yes"))
+    return traces
+
+
+@pytest.mark.parametrize("name", ["interval1", "interval5", "fifo"])
+def test_page_delayed_interval_traces(name):
+    tr = _read_traces()[name]
+    interval = 5 if name == "interval5" else 1
+    d = oracle.DelayedScaling(history_len=tr["H"], interval=interval, margin=tr["margin"],
+                              fmt=oracle.E4M3)
+    for t, a, used, rec in tr["rows"]:
+        r = d.step(np.array([a, -a / 2], dtype=np.float32))
+        expect, _ = oracle.per_tensor_scale(oracle.f32_to_bits(np.float32(used)), oracle.E4M3, 0)
+        assert float(r["scale"]) == float(expect), (name, t)
+        assert float(r["scale"]) == float(np.float32(448.0 / used)) or used == 0
+        assert r["recorded"] == rec, (name, t)
+        if rec:
+            assert float(r["amax"]) == a
+
+
+def test_delayed_margin_and_reset():
+    """Margin N divides the delayed scale by 2^N; the first step (and the first
+    after a reset) uses current scaling with no margin."""
+    d = oracle.DelayedScaling(history_len=4, interval=1, margin=3, fmt=oracle.E4M3)
+    r0 = d.step(np.array([2.0], dtype=np.float32))
+    assert float(r0["scale"]) == 224.0  # current scaling, margin not applied
+    r1 = d.step(np.array([1.0], dtype=np.float32))
+    assert float(r1["scale"]) == 28.0  # 448/2 / 2^3
+    d.reset()
+    r2 = d.step(np.array([0.5], dtype=np.float32))
+    assert float(r2["scale"]) == 896.0  # history forgotten: current scaling on 0.5
+
+
+@pytest.mark.parametrize("case", PAGES["mx"], ids=lambda c: c["id"])
+def test_page_mx_examples(case):
+    fmt = FMT[case["fmt"]]
+    v = np.zeros(32, dtype=np.float32)
+    v[5] = case["amax"]
+    v[7] = -case["amax"] / 3
+    byte, q = oracle.mx_block(v, fmt)
+    if "X" in case:
+        assert byte == case["scale_byte"] and byte - 127 == case["X"]
+    if case.get("all_zero"):
+        assert not q.any()
+    if "scaled_max" in case:
+        assert np.isclose(case["amax"] * 2.0 ** -case["X"], case["scaled_max"])
+        assert case["scaled_max"] < oracle.fp8_max(fmt)
+    if "X_ocp" in case:
+        ocp = math.floor(math.log2(case["amax"])) - 8  # "混合精度与 FP8 训练" 13.1 rule
+        assert ocp == case["X_ocp"]
+        assert case["amax"] * 2.0 ** -ocp > oracle.fp8_max(fmt)  # would saturate
+        assert byte - 127 == case["X_roundup"]
+        assert case["amax"] * 2.0 ** -(byte - 127) <= oracle.fp8_max(fmt)
+
+
+# ---------------------------------------------------------------------------
+# Closed forms and library routines
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_every_code_round_trips(fmt):
+    for c in range(256):
+        v = oracle.fp8_value(fmt, c)
+        if math.isnan(v):
+            assert oracle.fp8_encode(fmt, v) == 0x7F
+        elif math.isinf(v):
+            assert oracle.fp8_encode(fmt, v) == (c & 0x80) | oracle.fp8_max_code(fmt)
+        else:
+            assert oracle.fp8_encode(fmt, v) == c
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_midpoints_go_to_even_code(fmt):
+    maxc = oracle.fp8_max_code(fmt)
+    for c in range(maxc):
+        lo, hi = oracle.fp8_value(fmt, c), oracle.fp8_value(fmt, c + 1)
+        mid = (lo + hi) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.fp8_encode(fmt, mid) == even
+        assert oracle.fp8_encode(fmt, -mid) == 0x80 | even
+        # just off the midpoint goes to the nearer side
+        assert oracle.fp8_encode(fmt, np.nextafter(mid, -np.inf)) == c
+        assert oracle.fp8_encode(fmt, np.nextafter(mid, np.inf)) == c + 1
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_all_bf16_patterns_match_torch(fmt):
+    """All 2^16 BF16 patterns at scale 1 against torch's RNE float8 conversion."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    q, _ = oracle.cast(bits, 1.0, fmt)
+    finite = ~np.isnan(vals)
+    np.testing.assert_array_equal(q[finite], torch_encode(fmt, vals[finite].astype(np.float64)))
+    assert (q[~finite] == 0x7F).all()  # NaN convention
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_random_fp32_patterns_match_torch(fmt):
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 1 << 32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    # concentrate half of them in the FP8 range so that rounding is exercised
+    bits[::2] = (rng.integers(0x33000000, 0x47800000, size=bits[::2].size, dtype=np.uint64)
+                 | (rng.integers(0, 2, size=bits[::2].size, dtype=np.uint64) << 31)).astype(np.uint32)
+    vals = bits.view(np.float32)
+    q, _ = oracle.cast(vals, 1.0, fmt)
+    ok = ~np.isnan(vals)
+    np.testing.assert_array_equal(q[ok], torch_encode(fmt, vals[ok].astype(np.float64)))
+    assert (q[~ok] == 0x7F).all()
+
+
+def test_scaled_cast_matches_torch():
+    """q = RNE_sat(fl32(x*s)): fl32 product by torch float32 multiply, then torch cast."""
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(1 << 16) * 3).astype(np.float32)
+    for s in [np.float32(1.7), np.float32(22400.0), np.float32(3.0e-3), np.float32(448.0 / 7.3)]:
+        prod = (torch.from_numpy(x) * torch.tensor(s, dtype=torch.float32)).numpy()
+        for fmt in (oracle.E4M3, oracle.E5M2):
+            q, sat = oracle.cast(x, s, fmt)
+            np.testing.assert_array_equal(q, torch_encode(fmt, prod.astype(np.float64)))
+            assert sat == int((np.abs(prod) > oracle.fp8_max(fmt)).sum())
+
+
+def test_amax_matches_numpy():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(100001) * 7).astype(np.float32)
+    assert oracle.amax(x) == np.max(np.abs(x))
+    b = to_bf16_bits(x)
+    bf = (b.astype(np.uint32) << 16).view(np.float32)
+    assert oracle.amax(b) == np.max(np.abs(bf))
+    assert oracle.amax(b, 10, 20) == np.max(np.abs(bf[10:20]))
+    x[77] = -np.inf
+    assert oracle.amax(x) == np.inf
+    x[78] = np.nan
+    assert np.isnan(oracle.amax(x))
+    assert oracle.amax(np.zeros(5, np.float32)) == 0.0
+    assert oracle.amax(np.zeros(0, np.float32)) == 0.0
+
+
+def test_per_tensor_scale_definition():
+    for a in [0.02, 1.0, 3.7, 1e-30, 6e4]:
+        s, nf = oracle.per_tensor_scale(oracle.f32_to_bits(np.float32(a)), oracle.E4M3, 0)
+        assert s == np.float32(448.0) / np.float32(a) and not nf
+        s3, _ = oracle.per_tensor_scale(oracle.f32_to_bits(np.float32(a)), oracle.E4M3, 3)
+        assert s3 == np.float32(s / np.float32(8.0))
+        s5, _ = oracle.per_tensor_scale(oracle.f32_to_bits(np.float32(a)), oracle.E5M2, 0)
+        assert s5 == np.float32(57344.0) / np.float32(a)
+    # special cases (our readings)
+    assert oracle.per_tensor_scale(0, oracle.E4M3, 0) == (1.0, False)
+    assert oracle.per_tensor_scale(0x7F800000, oracle.E4M3, 0) == (1.0, True)
+    assert oracle.per_tensor_scale(0x7FC00000, oracle.E4M3, 0) == (1.0, True)
+    s, _ = oracle.per_tensor_scale(1, oracle.E4M3, 0)  # smallest subnormal: overflow
+    assert s == np.finfo(np.float32).max
+    assert oracle.reciprocal(np.float32(3.0)) == np.float32(1.0) / np.float32(3.0)
+
+
+def _ceil_log2_fraction(r: Fraction) -> int:
+    """ceil(log2 r) for a positive rational, by integer bit lengths."""
+    p, q = r.numerator, r.denominator
+    k = p.bit_length() - q.bit_length()  # floor(log2 r) is k or k-1
+    if Fraction(2) ** k > r:
+        k -= 1
+    return k if Fraction(2) ** k == r else k + 1
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_mx_scale_is_exact_ceil_log2(fmt):
+    """X = ceil(log2(amax/destmax)) over the whole BF16 range, by rational
+    arithmetic, and the invariant destmax/2 < amax*2^-X <= destmax."""
+    destmax = Fraction(oracle.fp8_max(fmt))
+    bits = np.arange(1, 0x7F80, dtype=np.uint32).astype(np.uint16)  # all positive finite BF16
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    for v in vals[::7]:
+        blk = np.zeros(32, np.float32)
+        blk[3] = v
+        blk[9] = -v / 4
+        byte, _ = oracle.mx_block(blk, fmt)
+        X = _ceil_log2_fraction(Fraction(float(v)) / destmax)
+        Xc = max(-127, min(127, X))
+        assert byte == Xc + 127
+        if Xc == X:
+            scaled = Fraction(float(v)) / Fraction(2) ** X
+            assert destmax / 2 < scaled <= destmax
+
+
+def test_mx_integer_exponent_rule():
+    """The same X by the exponent/mantissa rule: e - e_max + [m > 1.75]."""
+    for fmt, emax in ((oracle.E4M3, 8), (oracle.E5M2, 15)):
+        rng = np.random.default_rng(1)
+        bits = rng.integers(0x00800000, 0x7F800000, size=20000, dtype=np.uint64).astype(np.uint32)
+        for b in bits:
+            e = (int(b) >> 23) - 127
+            man = int(b) & 0x7FFFFF
+            X = max(-127, min(127, e - emax + (1 if man > 0x600000 else 0)))
+            blk = np.zeros(32, np.float32)
+            blk[0] = np.array([b], np.uint32).view(np.float32)[0]
+            assert oracle.mx_block(blk, fmt)[0] == X + 127
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_mx_elements_all_bf16_times_all_X(fmt):
+    """Every BF16 value scaled by every 2^-X, against torch (the MX element step)."""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    vals = vals[np.isfinite(vals)].astype(np.float64)
+    for X in range(-127, 128):
+        a = np.ldexp(vals, -X)
+        np.testing.assert_array_equal(oracle.encode_array(fmt, a), torch_encode(fmt, a))
+
+
+def test_mx_block_special_blocks():
+    z = np.zeros(32, np.float32)
+    z[4] = -0.0
+    byte, q = oracle.mx_block(z, oracle.E4M3)
+    assert byte == 0 and not q.any()  # zero block: X = -127, all 0 (no -0)
+    v = np.ones(32, np.float32)
+    v[2] = np.inf
+    assert oracle.mx_block(v, oracle.E4M3)[0] == 0xFF
+    assert (oracle.mx_block(v, oracle.E4M3)[1] == 0x7F).all()
+    v[2] = np.nan
+    assert oracle.mx_block(v, oracle.E5M2)[0] == 0xFF
+    # negative zero inside a non-zero block keeps its sign
+    v = np.ones(32, np.float32)
+    v[1] = -0.0
+    assert oracle.mx_block(v, oracle.E4M3)[1][1] == 0x80
+    # a short block (trailing rows of a group) uses only the rows present
+    b3, q3 = oracle.mx_block(np.array([1.0, -2.0, 0.5], np.float32), oracle.E4M3)
+    assert b3 == 127 - 7 and q3.size == 3  # 2/448 -> X = ceil(log2(2/448)) = -7
+
+
+def _bf16_from_f32(a):
+    return to_bf16_bits(np.asarray(a, np.float32))
+
+
+def test_mx_rowwise_matches_blocks():
+    rng = np.random.default_rng(2)
+    x = _bf16_from_f32(rng.standard_normal((5, 96)) * np.exp(rng.standard_normal((5, 1)) * 3))
+    r = oracle.mx_quantize(x, oracle.E4M3, 1)
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    for i in range(5):
+        for j in range(3):
+            b, q = oracle.mx_block(xf[i, 32 * j:32 * j + 32], oracle.E4M3)
+            assert r["s_row"][i, j] == b
+            np.testing.assert_array_equal(r["q_row"][i, 32 * j:32 * j + 32], q)
+
+
+def test_mx_columnwise_is_rowwise_of_transpose_T11():
+    """Column copy = rowwise quantization of x^T, taken from the BF16 tensor,
+    not from re-quantizing the rowwise FP8 copy ("混合精度与 FP8 训练" 13.1)."""
+    rng = np.random.default_rng(4)
+    x = _bf16_from_f32(rng.standard_normal((64, 64)) * np.exp(rng.standard_normal((64, 1)) * 2))
+    both = oracle.mx_quantize(x, oracle.E4M3, 3)
+    rt = oracle.mx_quantize(np.ascontiguousarray(x.T), oracle.E4M3, 1)
+    np.testing.assert_array_equal(both["q_col"], rt["q_row"])
+    np.testing.assert_array_equal(both["s_col"], rt["s_row"])
+    # requantizing the dequantized rowwise copy along columns gives something else
+    deq = np.empty((64, 64), np.float32)
+    for i in range(64):
+        for j in range(2):
+            s = 2.0 ** (int(both["s_row"][i, j]) - 127)
+            for k in range(32):
+                deq[i, 32 * j + k] = oracle.fp8_value(oracle.E4M3, int(both["q_row"][i, 32 * j + k])) * s
+    requant = oracle.mx_quantize(np.ascontiguousarray(deq.T), oracle.E4M3, 1)
+    assert (requant["q_row"] != both["q_col"]).any()
+
+
+def test_mx_grouped_columns_restart_at_group_offsets():
+    rng = np.random.default_rng(6)
+    rows, cols = 150, 64
+    x = _bf16_from_f32(rng.standard_normal((rows, cols)))
+    offs = np.array([0, 0, 33, 34, 100, 150], np.int64)  # empty, 33, 1, 66, 50 rows
+    r = oracle.mx_quantize(x, oracle.E4M3, 3, offsets=offs)
+    assert r["col_blocks"] == 0 + 2 + 1 + 3 + 2
+    base = 0
+    for g in range(len(offs) - 1):
+        r0, r1 = int(offs[g]), int(offs[g + 1])
+        if r1 == r0:
+            continue
+        part = oracle.mx_quantize(np.ascontiguousarray(x[r0:r1]), oracle.E4M3, 2)
+        nb = part["col_blocks"]
+        np.testing.assert_array_equal(r["q_col"][:, r0:r1], part["q_col"])
+        np.testing.assert_array_equal(r["s_col"][:, base:base + nb], part["s_col"])
+        base += nb
+    # the rowwise copy ignores groups
+    np.testing.assert_array_equal(r["q_row"], oracle.mx_quantize(x, oracle.E4M3, 1)["q_row"])
+
+
+def test_current_scaling_grouped_equals_per_slice():
+    rng = np.random.default_rng(8)
+    x = _bf16_from_f32(rng.standard_normal((40, 16)) * np.arange(1, 41)[:, None])
+    offs = np.array([0, 7, 7, 40], np.int64)
+    r = oracle.current_scaling(x, oracle.E4M3, offsets=offs)
+    assert r["amax"][1] == 0 and r["scale"][1] == 1.0  # empty group
+    for g, (a, b) in enumerate([(0, 7), (7, 40)]):
+        gi = 0 if g == 0 else 2
+        part = oracle.current_scaling(np.ascontiguousarray(x[a:b]), oracle.E4M3)
+        np.testing.assert_array_equal(r["q"].reshape(40, 16)[a:b], part["q"].reshape(b - a, 16))
+        assert r["scale"][gi] == part["scale"][0]
+
+
+def test_current_scaling_max_element_lands_at_top():
+    """Scale = F8max/amax maps the largest element to (about) F8max."""
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((32, 32)) * 5).astype(np.float32)
+    r = oracle.current_scaling(x, oracle.E4M3)
+    i = np.argmax(np.abs(x))
+    assert oracle.fp8_value(oracle.E4M3, int(r["q"][i]) & 0x7F) == 448.0
