@@ -166,6 +166,17 @@ static uint32_t float_to_bits(float f)
 
 float orc_input_value(const void* x, int dt, int64_t i) { return bits_to_float(input_bits(x, dt, i)); }
 
+/* IEEE single rounding (to nearest, ties to even) of an exact double.  C
+ * leaves the conversion of an out-of-range double undefined, so overflow is
+ * spelled out: at or beyond FLT_MAX + half an ulp the result is infinite. */
+static float to_float(double d)
+{
+    const double overflow = 0x1.ffffffp127; /* FLT_MAX + 2^103 */
+    if (d >= overflow) return INFINITY;
+    if (d <= -overflow) return -INFINITY;
+    return (float)d;
+}
+
 /* ------------------------------------------------------------------ */
 /* amax = max |x_i| ("HiFloat8：高性能训练之路" 1.2 ComputeAmax;          */
 /* "混合精度与 FP8 训练" 8.1).  Compared on the magnitude bits, which     */
@@ -199,13 +210,13 @@ float orc_per_tensor_scale(uint32_t amax_bits, int fmt, int margin, int* nonfini
         return 1.0f;
     }
     if (amax == 0.0f) return 1.0f;
-    s = (float)(orc_fp8_max(fmt) / (double)amax);
+    s = to_float(orc_fp8_max(fmt) / (double)amax);
     if (isinf(s)) s = FLT_MAX;
-    s = (float)((double)s * ldexp(1.0, -margin));
+    s = to_float((double)s * ldexp(1.0, -margin));
     return s;
 }
 
-float orc_reciprocal(float s) { return (float)(1.0 / (double)s); }
+float orc_reciprocal(float s) { return to_float(1.0 / (double)s); }
 
 /* ------------------------------------------------------------------ */
 /* Scaled cast (eq. 2 of "HiFloat8：高性能训练之路" 1.2): q_i =           */
@@ -222,7 +233,7 @@ void orc_cast(const void* x, int dt, int64_t begin, int64_t end, float scale, in
 #pragma omp parallel for schedule(static) reduction(+ : count) num_threads(nthreads)
 #endif
     for (int64_t i = begin; i < end; i++) {
-        float y = (float)((double)orc_input_value(x, dt, i) * (double)scale);
+        float y = to_float((double)orc_input_value(x, dt, i) * (double)scale);
         if (!isnan(y) && fabs((double)y) > f8max) count++;
         q[i] = (uint8_t)orc_fp8_encode(fmt, (double)y);
     }

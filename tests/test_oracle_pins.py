@@ -433,3 +433,16 @@ def test_current_scaling_max_element_lands_at_top():
     r = oracle.current_scaling(x, oracle.E4M3)
     i = np.argmax(np.abs(x))
     assert oracle.fp8_value(oracle.E4M3, int(r["q"][i]) & 0x7F) == 448.0
+
+
+def test_scaled_cast_overflow_matches_ieee_single():
+    """Products beyond the float range follow IEEE single overflow (to +-Inf),
+    then saturate; torch's float32 multiply is the reference."""
+    x = np.array([3e38, -3e38, 1.0, 2e38, -np.inf, 7e37], dtype=np.float32)
+    for s in (np.float32(448.0), np.float32(1.5), np.float32(4.0)):
+        prod = (torch.from_numpy(x) * torch.tensor(s, dtype=torch.float32)).numpy()
+        for fmt in (oracle.E4M3, oracle.E5M2):
+            q, sat = oracle.cast(x, s, fmt)
+            np.testing.assert_array_equal(q, torch_encode(fmt, prod.astype(np.float64)))
+            assert sat == int((np.abs(prod) > oracle.fp8_max(fmt)).sum())
+    assert oracle.reciprocal(np.float32(1e-45)) == np.inf
