@@ -1,0 +1,206 @@
+/*
+ * fp8q.h -- C ABI of libfp8q, FP8 / MXFP8 quantization for sm_103a (GB300).
+ *
+ * The library quantizes BF16 or FP32 tensors to 8-bit floats, the step that
+ * runs before each Fprop / Dgrad / Wgrad matmul of FP8 training:
+ *   - per-tensor amax, current scaling and delayed scaling, each followed by
+ *     a saturating round-to-nearest-even cast to E4M3 or E5M2;
+ *   - MXFP8: 1x32 blocks with one E8M0 scale each (exponent rounded up),
+ *     rowwise and columnwise (transposed), optionally per ragged group.
+ *
+ * Conventions for every entry point:
+ *   - Pointers documented as "device" are CUDA device pointers owned by the
+ *     caller; the library never frees them and never allocates on these
+ *     calls (only fp8q_delayed_create allocates, for its own state).
+ *   - All work is asynchronous on `stream` (a cudaStream_t passed as void*,
+ *     NULL = the legacy default stream).  Return codes report argument
+ *     validation and launch errors only; fp8q_last_error_string() gives the
+ *     message of the most recent failure on the calling thread.
+ *   - Inputs are contiguous row-major tensors; x must be 16-byte aligned.
+ *     dt selects the element type: FP8Q_IN_BF16 (raw BF16 bits) or
+ *     FP8Q_IN_FP32.  Outputs are raw 8-bit codes (uint8).
+ *   - Groups: group_offsets is a device int64 array of num_groups + 1 row
+ *     offsets, non-decreasing, from 0 to rows; group g is rows
+ *     [offsets[g], offsets[g+1]).  NULL means one group of all rows
+ *     (num_groups must then be 1).  Offsets that break these rules give
+ *     unspecified values but never an out-of-bounds access.
+ *   - num_groups is at most FP8Q_MAX_GROUPS.
+ *
+ * Readings of the source pages that fix bit-level results (the same as the
+ * CPU oracle's): a NaN input encodes to 0x7F in both formats; +-Inf and any
+ * overflow saturate to +-max; the sign of zero is kept except in an all-zero
+ * MX block; amax compares magnitude bits, so NaN inputs make amax NaN.
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8Q_MAX_GROUPS 4096
+
+#if defined(__GNUC__)
+#define FP8Q_API __attribute__((visibility("default")))
+#else
+#define FP8Q_API
+#endif
+
+typedef enum {
+    FP8Q_OK = 0,
+    FP8Q_ERR_INVALID_ARG = 1, /* a pointer, size, enum or alignment is invalid */
+    FP8Q_ERR_UNSUPPORTED = 2, /* valid request the library does not handle (e.g. cols % 32 for MX) */
+    FP8Q_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
+    FP8Q_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up */
+} fp8q_status;
+
+typedef enum { FP8Q_IN_BF16 = 0, FP8Q_IN_FP32 = 1 } fp8q_in_dtype;
+
+/* E4M3: bias 7, no Inf, max 448.  E5M2: IEEE style, bias 15, max 57344.
+ * ("混合精度与 FP8 训练", 2.2; "Blackwell GPU MXFP8 预训练最佳实践", 3.1) */
+typedef enum { FP8Q_E4M3 = 0, FP8Q_E5M2 = 1 } fp8q_format;
+
+typedef enum { MXFP8_ROW = 1, MXFP8_COL = 2, MXFP8_BOTH = 3 } mxfp8_dir;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+FP8Q_API int32_t fp8q_version(void);
+
+/* Message of the last failed call on this thread ("" if none). */
+FP8Q_API const char* fp8q_last_error_string(void);
+
+/*
+ * amax_out[g] = max |x| over group g, bit-exact: the FP32 value whose bits
+ * are the largest magnitude bits in the group (BF16 widened exactly), so a
+ * NaN makes the result NaN and an empty group gives 0.
+ * ("HiFloat8：高性能训练之路" 1.2, ComputeAmax; "混合精度与 FP8 训练" 8.1.)
+ *   x           device, rows*cols elements of type dt
+ *   amax_out    device float[num_groups]
+ * One reduction pass over x (2 or 4 bytes per element read).
+ */
+FP8Q_API fp8q_status fp8q_amax(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                      const int64_t* group_offsets, int32_t num_groups, float* amax_out,
+                      void* stream);
+
+/*
+ * Bytes of workspace fp8q_cast_per_tensor needs for num_groups groups.
+ */
+FP8Q_API size_t fp8q_cast_workspace_bytes(int32_t num_groups);
+
+/*
+ * Per-tensor (per-group) scaled cast:  q = RNE_sat(fl32(x * scale[g])).
+ *
+ * scale_in == NULL: current scaling ("HiFloat8：高性能训练之路" 1.2, eqs.
+ *   1-2; "混合精度与 FP8 训练" 8.2): amax[g] is reduced first, then
+ *   scale[g] = fl32(fl32(F8max / amax[g]) * 2^-margin), with amax = 0 giving
+ *   scale 1, a non-finite amax giving scale 1, and an overflowing quotient
+ *   giving FLT_MAX.  Two passes over x (read, read + write).
+ * scale_in != NULL: device float[num_groups] scales are used as given; if
+ *   amax_out is non-NULL the amax of x is reduced in the same single pass.
+ *
+ *   x              device, rows*cols elements of type dt
+ *   fmt            FP8Q_E4M3 or FP8Q_E5M2
+ *   margin         0..63
+ *   q              device uint8[rows*cols], same layout as x
+ *   amax_out       device float[G] or NULL
+ *   scale_out      device float[G] or NULL: the scale used
+ *   scale_inv_out  device float[G] or NULL: fl32(1 / scale)
+ *   sat_count_out  device uint64[G] or NULL: elements with |fl32(x*scale)|
+ *                  > F8max (NaN not counted), i.e. clamped by the cast
+ *   workspace      device, >= fp8q_cast_workspace_bytes(num_groups) bytes,
+ *                  8-byte aligned, zero-filled before its first use; every
+ *                  successful call leaves it zero-filled again.  Calls that
+ *                  may overlap on the GPU need separate workspaces.
+ */
+FP8Q_API fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                 const int64_t* group_offsets, int32_t num_groups,
+                                 int32_t fmt, int32_t margin, const float* scale_in,
+                                 uint8_t* q, float* amax_out, float* scale_out,
+                                 float* scale_inv_out, unsigned long long* sat_count_out,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Delayed scaling ("HiFloat8：高性能训练之路" 1.2 eqs. 3-4 and section 3;
+ * "混合精度与 FP8 训练" 8.2): a library-owned state holds an amax history
+ * ring of history_len entries.  Step t:
+ *   - if the history is empty (after create or reset): current scaling with
+ *     no margin on x_t;
+ *   - else scale = fl32(fl32(F8max / max(filled history)) * 2^-margin);
+ *   - q_t = RNE_sat(fl32(x_t * scale));
+ *   - if t % interval == 0 (t counted from create/reset), amax(x_t) is
+ *     computed in the same pass and appended, dropping the oldest entry when
+ *     the ring is full; a non-finite amax raises the state's flag.
+ * The host keeps step, head and count, so the call never synchronizes.
+ */
+typedef struct fp8q_delayed_state fp8q_delayed_state;
+
+/* Allocates the state on the current device (history_len 1..1024,
+ * interval >= 1, margin 0..63). */
+FP8Q_API fp8q_status fp8q_delayed_create(int32_t history_len, int32_t interval, int32_t margin,
+                                int32_t fmt, fp8q_delayed_state** out);
+FP8Q_API fp8q_status fp8q_delayed_destroy(fp8q_delayed_state* st);
+/* Empties the history and clears the flag (async on stream); step = 0. */
+FP8Q_API fp8q_status fp8q_delayed_reset(fp8q_delayed_state* st, void* stream);
+/*
+ *   x, n            device, n elements of type dt
+ *   q               device uint8[n]
+ *   scale_used_out  device float[1] or NULL; scale_inv_out likewise
+ *   amax_out        device float[1] or NULL: written on recording steps only
+ *   sat_count_out   device uint64[1] or NULL
+ * Consecutive steps on one state must be issued on one stream (or ordered).
+ */
+FP8Q_API fp8q_status fp8q_delayed_step(fp8q_delayed_state* st, const void* x, int32_t dt, int64_t n,
+                              uint8_t* q, float* scale_used_out, float* scale_inv_out,
+                              float* amax_out, unsigned long long* sat_count_out,
+                              void* stream);
+/* Copies the state to the host (synchronizes the device): history_host
+ * float[history_len] (ring order), head (next slot), count (filled entries),
+ * step, nonfinite flag.  Any output pointer may be NULL. */
+FP8Q_API fp8q_status fp8q_delayed_get(const fp8q_delayed_state* st, float* history_host, int32_t* head,
+                             int32_t* count, int64_t* step, int32_t* nonfinite);
+/* Restores a state saved by fp8q_delayed_get (checkpoint resume); clears
+ * the flag.  Synchronous. */
+FP8Q_API fp8q_status fp8q_delayed_set(fp8q_delayed_state* st, const float* history_host, int32_t head,
+                             int32_t count, int64_t step);
+
+/*
+ * Number of columnwise MX blocks per column: sum over groups of
+ * ceil(n_g / 32), from HOST offsets (NULL: ceil(rows / 32)).  Returns -1 for
+ * invalid offsets.
+ */
+FP8Q_API int64_t mxfp8_col_blocks(const int64_t* group_offsets_host, int32_t num_groups, int64_t rows);
+
+/*
+ * MXFP8 quantization ("Blackwell GPU MXFP8 预训练最佳实践" 4.1-4.2;
+ * "混合精度与 FP8 训练" 13.1; "HiFloat8：高性能训练之路" 2), one pass over x.
+ * Each block of k <= 32 values gets X = ceil(log2(amax / destmax)) computed
+ * exactly and saturated to [-127, 127] (destmax 448 for E4M3, 57344 for
+ * E5M2); the scale byte is X + 127 (E8M0), elements are RNE_sat(v / 2^X).
+ * amax = 0 gives byte 0x00 and all-zero elements; a block holding Inf or
+ * NaN gives byte 0xFF and elements 0x7F.
+ *   rowwise (dir & MXFP8_ROW): blocks x[r, 32j .. 32j+31]
+ *     q_row  device uint8[rows * cols]          (row-major, like x)
+ *     s_row  device uint8[rows * (cols / 32)]   (row-major)
+ *   columnwise (dir & MXFP8_COL): per group, blocks of 32 consecutive rows
+ *     from the group's first row, the last one possibly shorter; taken from
+ *     x itself, not from the rowwise copy; output transposed:
+ *     q_col  device uint8[cols * rows]          q_col[c * rows + r]
+ *     s_col  device uint8[cols * s_col_ld]      s_col[c * s_col_ld + b], b
+ *            numbering the column blocks of all groups in order; s_col_ld
+ *            must be >= mxfp8_col_blocks(...) for the offsets used (blocks
+ *            past s_col_ld are not written)
+ * cols % 32 == 0 is required (FP8Q_ERR_UNSUPPORTED otherwise); rows is any.
+ * Pointers of the unused direction may be NULL.
+ */
+FP8Q_API fp8q_status mxfp8_quantize(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                           const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
+                           int32_t dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                           uint8_t* s_col, int64_t s_col_ld, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

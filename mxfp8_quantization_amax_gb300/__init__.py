@@ -1,0 +1,327 @@
+"""Python binding of libfp8q: FP8 / MXFP8 quantization kernels for GB300.
+
+Thin ctypes marshalling over the C ABI declared in include/fp8q.h: every
+function takes torch CUDA tensors, checks shapes and dtypes, allocates the
+outputs with torch and calls the entry point of the same name on the
+current CUDA stream.  All arithmetic runs in the library's kernels; there is
+no fallback.  If libfp8q.so is missing, importing this package still works
+but every call raises until ``build()`` has been run.
+
+Formats: ``E4M3`` (max 448) and ``E5M2`` (max 57344).  Outputs are uint8
+tensors of raw codes; ``view(torch.float8_e4m3fn)`` / ``float8_e5m2``
+reinterprets them for torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from ._build import LIB_PATH, build as _build_lib, is_stale
+
+__all__ = [
+    "E4M3", "E5M2", "ROW", "COL", "BOTH", "build", "library_path", "lib",
+    "fp8q_amax", "fp8q_cast_per_tensor", "fp8q_cast_workspace_bytes", "DelayedScaling",
+    "mxfp8_quantize", "mxfp8_col_blocks", "Fp8qError",
+]
+
+E4M3 = 0
+E5M2 = 1
+ROW = 1
+COL = 2
+BOTH = 3
+MAX_GROUPS = 4096
+
+_c = ctypes
+_P = _c.c_void_p
+_SIGS = {
+    "fp8q_version": (_c.c_int32, []),
+    "fp8q_last_error_string": (_c.c_char_p, []),
+    "fp8q_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _P, _P]),
+    "fp8q_cast_workspace_bytes": (_c.c_size_t, [_c.c_int32]),
+    "fp8q_cast_per_tensor": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32,
+                                        _c.c_int32, _c.c_int32, _P, _P, _P, _P, _P, _P, _P,
+                                        _c.c_size_t, _P]),
+    "fp8q_delayed_create": (_c.c_int, [_c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
+                                       _c.POINTER(_P)]),
+    "fp8q_delayed_destroy": (_c.c_int, [_P]),
+    "fp8q_delayed_reset": (_c.c_int, [_P, _P]),
+    "fp8q_delayed_step": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int64, _P, _P, _P, _P, _P, _P]),
+    "fp8q_delayed_get": (_c.c_int, [_P, _P, _P, _P, _P, _P]),
+    "fp8q_delayed_set": (_c.c_int, [_P, _P, _c.c_int32, _c.c_int32, _c.c_int64]),
+    "mxfp8_col_blocks": (_c.c_int64, [_P, _c.c_int32, _c.c_int64]),
+    "mxfp8_quantize": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32,
+                                  _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_int64, _P]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class Fp8qError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile libfp8q.so for sm_103a (in-tree) and load it."""
+    global _lib
+    path = _build_lib(force=force)
+    with _lock:
+        _lib = None
+    lib()
+    return path
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise Fp8qError(f"{LIB_PATH} is missing: run mxfp8_quantization_amax_gb300.build()")
+            h = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(h, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = h
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = lib().fp8q_last_error_string().decode(errors="replace")
+        raise Fp8qError(f"{what} failed with status {status}: {msg}")
+
+
+def _ptr(t):
+    return None if t is None else _P(t.data_ptr())
+
+
+def _stream():
+    return _P(torch.cuda.current_stream().cuda_stream)
+
+
+def _dt(x: torch.Tensor) -> int:
+    if x.dtype == torch.bfloat16:
+        return 0
+    if x.dtype == torch.float32:
+        return 1
+    raise TypeError("x must be bfloat16 or float32")
+
+
+def _check_input(x: torch.Tensor):
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+
+
+def _as_2d(x: torch.Tensor):
+    if x.dim() == 2:
+        return x.shape[0], x.shape[1]
+    if x.dim() == 1:
+        return 1, x.shape[0]
+    return x.numel() // x.shape[-1], x.shape[-1]
+
+
+def _offsets(group_offsets, device):
+    if group_offsets is None:
+        return None, 1
+    o = group_offsets
+    if not isinstance(o, torch.Tensor):
+        o = torch.tensor(list(o), dtype=torch.int64)
+    o = o.to(device=device, dtype=torch.int64).contiguous()
+    return o, o.numel() - 1
+
+
+# ---------------------------------------------------------------------------
+# amax
+# ---------------------------------------------------------------------------
+def fp8q_amax(x: torch.Tensor, group_offsets=None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Per-tensor (or per-group) max |x|, bit-exact, as float32 [G]."""
+    _check_input(x)
+    rows, cols = _as_2d(x)
+    off, G = _offsets(group_offsets, x.device)
+    if out is None:
+        out = torch.empty(G, dtype=torch.float32, device=x.device)
+    _check(lib().fp8q_amax(_ptr(x), _dt(x), rows, cols, _ptr(off), G, _ptr(out), _stream()), "fp8q_amax")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# per-tensor cast
+# ---------------------------------------------------------------------------
+def fp8q_cast_workspace_bytes(num_groups: int = 1) -> int:
+    return int(lib().fp8q_cast_workspace_bytes(num_groups))
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(device, G: int, stream_id: int) -> torch.Tensor:
+    """Zero-filled workspace per (device, stream), grown as needed."""
+    need = fp8q_cast_workspace_bytes(G)
+    key = (device.index, stream_id)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(max(need, 4096), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def fp8q_cast_per_tensor(x: torch.Tensor, fmt: int = E4M3, margin: int = 0, scale_in=None,
+                         group_offsets=None, want_amax: bool = True, want_sat: bool = False,
+                         q: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> dict:
+    """q = RNE_sat(fl32(x * scale)).  scale_in None: current scaling.
+
+    Returns dict(q uint8 like x, amax, scale, scale_inv float32 [G], sat uint64 [G] or None).
+    """
+    _check_input(x)
+    rows, cols = _as_2d(x)
+    off, G = _offsets(group_offsets, x.device)
+    dev = x.device
+    q = torch.empty(x.shape, dtype=torch.uint8, device=dev) if q is None else q
+    amax = torch.empty(G, dtype=torch.float32, device=dev) if want_amax else None
+    scale = torch.empty(G, dtype=torch.float32, device=dev)
+    scale_inv = torch.empty(G, dtype=torch.float32, device=dev)
+    sat = torch.empty(G, dtype=torch.int64, device=dev) if want_sat else None
+    if scale_in is not None:
+        if not isinstance(scale_in, torch.Tensor):
+            scale_in = torch.tensor(scale_in, dtype=torch.float32)
+        scale_in = scale_in.to(device=dev, dtype=torch.float32).reshape(-1).contiguous()
+        if scale_in.numel() != G:
+            raise ValueError("scale_in must hold one scale per group")
+    stream = torch.cuda.current_stream()
+    ws = workspace if workspace is not None else _workspace(dev, G, stream.cuda_stream)
+    _check(lib().fp8q_cast_per_tensor(
+        _ptr(x), _dt(x), rows, cols, _ptr(off), G, fmt, margin, _ptr(scale_in), _ptr(q), _ptr(amax),
+        _ptr(scale), _ptr(scale_inv), _ptr(sat), _ptr(ws), ws.numel(), _P(stream.cuda_stream)),
+        "fp8q_cast_per_tensor")
+    return {"q": q, "amax": amax, "scale": scale, "scale_inv": scale_inv, "sat": sat}
+
+
+# ---------------------------------------------------------------------------
+# delayed scaling
+# ---------------------------------------------------------------------------
+class DelayedScaling:
+    """Library-owned delayed-scaling state (history ring on the device)."""
+
+    def __init__(self, history_len: int = 16, interval: int = 1, margin: int = 0, fmt: int = E4M3):
+        self.history_len, self.interval, self.margin, self.fmt = history_len, interval, margin, fmt
+        h = _P()
+        _check(lib().fp8q_delayed_create(history_len, interval, margin, fmt, ctypes.byref(h)),
+               "fp8q_delayed_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().fp8q_delayed_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self):
+        _check(lib().fp8q_delayed_reset(self._h, _stream()), "fp8q_delayed_reset")
+
+    def step(self, x: torch.Tensor, q: torch.Tensor | None = None, want_sat: bool = False,
+             outs: dict | None = None) -> dict:
+        """Cast x with the predicted scale; records amax on recording steps.
+
+        Returns dict(q, scale [1], scale_inv [1], amax [1] (valid only on
+        recording steps), sat [1] or None).
+        """
+        _check_input(x)
+        dev = x.device
+        o = outs or {}
+
+        def buf(name, dtype):
+            t = o.get(name)
+            return t if t is not None else torch.empty(1, dtype=dtype, device=dev)
+
+        q = q if q is not None else torch.empty(x.shape, dtype=torch.uint8, device=dev)
+        scale = buf("scale", torch.float32)
+        scale_inv = buf("scale_inv", torch.float32)
+        amax = buf("amax", torch.float32)
+        sat = buf("sat", torch.int64) if want_sat else None
+        _check(lib().fp8q_delayed_step(self._h, _ptr(x), _dt(x), x.numel(), _ptr(q), _ptr(scale),
+                                       _ptr(scale_inv), _ptr(amax), _ptr(sat), _stream()),
+               "fp8q_delayed_step")
+        return {"q": q, "scale": scale, "scale_inv": scale_inv, "amax": amax, "sat": sat}
+
+    def get(self) -> dict:
+        hist = (ctypes.c_float * self.history_len)()
+        head, count, nonfinite = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        step = ctypes.c_int64()
+        _check(lib().fp8q_delayed_get(self._h, ctypes.cast(hist, _P), ctypes.byref(head),
+                                      ctypes.byref(count), ctypes.byref(step), ctypes.byref(nonfinite)),
+               "fp8q_delayed_get")
+        return {"history": list(hist), "head": head.value, "count": count.value, "step": step.value,
+                "nonfinite": bool(nonfinite.value)}
+
+    def set(self, history, head: int, count: int, step: int):
+        arr = (ctypes.c_float * self.history_len)(*[float(v) for v in history])
+        _check(lib().fp8q_delayed_set(self._h, ctypes.cast(arr, _P), head, count, step), "fp8q_delayed_set")
+
+
+# ---------------------------------------------------------------------------
+# MXFP8
+# ---------------------------------------------------------------------------
+def mxfp8_col_blocks(rows: int, group_offsets=None) -> int:
+    """sum_g ceil(n_g / 32) from host offsets (None: ceil(rows / 32))."""
+    if group_offsets is None:
+        return int(lib().mxfp8_col_blocks(None, 1, rows))
+    o = torch.as_tensor(list(group_offsets) if not isinstance(group_offsets, torch.Tensor) else group_offsets,
+                        dtype=torch.int64).cpu().contiguous()
+    n = int(lib().mxfp8_col_blocks(_P(o.data_ptr()), o.numel() - 1, rows))
+    if n < 0:
+        raise ValueError("invalid group offsets")
+    return n
+
+
+def mxfp8_quantize(x: torch.Tensor, fmt: int = E4M3, direction: int = BOTH, group_offsets=None,
+                   s_col_ld: int | None = None, out: dict | None = None) -> dict:
+    """MXFP8 rowwise and/or columnwise quantization of a 2-D tensor.
+
+    Returns dict(q_row [rows, cols], s_row [rows, cols/32], q_col [cols, rows],
+    s_col [cols, s_col_ld]) (uint8; unused direction -> None).
+    """
+    _check_input(x)
+    rows, cols = _as_2d(x)
+    off, G = _offsets(group_offsets, x.device)
+    dev = x.device
+    if s_col_ld is None:
+        if group_offsets is None:
+            s_col_ld = (rows + 31) // 32
+        else:
+            host = group_offsets.cpu() if isinstance(group_offsets, torch.Tensor) else group_offsets
+            s_col_ld = mxfp8_col_blocks(rows, host)
+    o = out or {}
+
+    def buf(name, shape):
+        t = o.get(name)
+        return t if t is not None else torch.empty(shape, dtype=torch.uint8, device=dev)
+
+    q_row = s_row = q_col = s_col = None
+    if direction & ROW:
+        q_row = buf("q_row", (rows, cols))
+        s_row = buf("s_row", (rows, cols // 32 if cols % 32 == 0 else 0))
+    if direction & COL:
+        q_col = buf("q_col", (cols, rows))
+        s_col = buf("s_col", (cols, max(s_col_ld, 1)))
+    _check(lib().mxfp8_quantize(_ptr(x), _dt(x), rows, cols, _ptr(off), G, fmt, direction,
+                                _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), s_col_ld, _stream()),
+           "mxfp8_quantize")
+    return {"q_row": q_row, "s_row": s_row, "q_col": q_col, "s_col": s_col, "s_col_ld": s_col_ld}

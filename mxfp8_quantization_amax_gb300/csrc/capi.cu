@@ -1,0 +1,281 @@
+// capi.cu -- the extern "C" entry points of libfp8q: argument validation,
+// error reporting and dispatch to the launchers.  Every check that can be
+// made on the host is made here, before anything is launched.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+struct fp8q_delayed_state;
+
+namespace fp8q {
+
+fp8q_status delayed_create(int H, int interval, int margin, int fmt, fp8q_delayed_state** out);
+fp8q_status delayed_destroy(fp8q_delayed_state* st);
+fp8q_status delayed_reset(fp8q_delayed_state* st, cudaStream_t s);
+fp8q_status delayed_step(fp8q_delayed_state* st, const void* x, int dt, int64_t n, uint8_t* q,
+                         float* scale_used_out, float* scale_inv_out, float* amax_out,
+                         unsigned long long* sat_out, cudaStream_t s);
+fp8q_status delayed_get(const fp8q_delayed_state* st, float* hist, int32_t* head, int32_t* count,
+                        int64_t* step, int32_t* nonfinite);
+fp8q_status delayed_set(fp8q_delayed_state* st, const float* hist, int32_t head, int32_t count, int64_t step);
+int delayed_history_len(const fp8q_delayed_state* st);
+
+static thread_local char g_err[512];
+
+fp8q_status fail(fp8q_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+fp8q_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FP8Q_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+fp8q_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, what);
+}
+
+int sm_count() {
+  static int cache[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+size_t cast_workspace_bytes(int G) {
+  const size_t a = 64 + (size_t)8 * G;
+  return ((a + 7) & ~(size_t)7) + (size_t)8 * G;
+}
+
+CastWorkspace cast_workspace_carve(void* ws, int G) {
+  char* b = (char*)ws;
+  CastWorkspace w;
+  w.counter = (unsigned*)b;
+  w.acc = (unsigned*)(b + 64);
+  w.scale = (float*)(b + 64 + (size_t)4 * G);
+  w.sat = (unsigned long long*)(b + ((64 + (size_t)8 * G + 7) & ~(size_t)7));
+  return w;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+static fp8q_status check_common(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                const int64_t* off, int32_t G) {
+  if (dt != FP8Q_IN_BF16 && dt != FP8Q_IN_FP32) return fail(FP8Q_ERR_INVALID_ARG, "dt must be FP8Q_IN_BF16 or FP8Q_IN_FP32");
+  if (rows < 0 || cols < 0) return fail(FP8Q_ERR_INVALID_ARG, "rows and cols must be >= 0");
+  if (cols > 0 && rows > (INT64_C(1) << 62) / cols) return fail(FP8Q_ERR_INVALID_ARG, "rows * cols too large");
+  if (rows * cols > 0 && x == nullptr) return fail(FP8Q_ERR_INVALID_ARG, "x is NULL");
+  if (!aligned(x, 16)) return fail(FP8Q_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  if (off == nullptr && G != 1) return fail(FP8Q_ERR_INVALID_ARG, "num_groups must be 1 when group_offsets is NULL");
+  if (G < 1 || G > FP8Q_MAX_GROUPS) return fail(FP8Q_ERR_INVALID_ARG, "num_groups must be in [1, %d]", FP8Q_MAX_GROUPS);
+  if (off != nullptr && !aligned(off, 8)) return fail(FP8Q_ERR_INVALID_ARG, "group_offsets must be 8-byte aligned");
+  return FP8Q_OK;
+}
+
+static bool fmt_ok(int32_t fmt) { return fmt == FP8Q_E4M3 || fmt == FP8Q_E5M2; }
+
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" {
+
+int32_t fp8q_version(void) { return 10000; }
+
+const char* fp8q_last_error_string(void) { return g_err; }
+
+fp8q_status fp8q_amax(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
+                      int32_t num_groups, float* amax_out, void* stream) {
+  g_err[0] = 0;
+  fp8q_status r = check_common(x, dt, rows, cols, group_offsets, num_groups);
+  if (r != FP8Q_OK) return r;
+  if (!amax_out || !aligned(amax_out, 4)) return fail(FP8Q_ERR_INVALID_ARG, "amax_out must be a 4-byte aligned device pointer");
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float) * num_groups, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(amax_out)");
+  if (rows * cols == 0) return FP8Q_OK;
+  PtLaunch L{};
+  L.x = x;
+  L.dt = dt;
+  L.rows = rows;
+  L.cols = cols;
+  L.off = group_offsets;
+  L.G = num_groups;
+  L.fmt = FP8Q_E4M3;
+  L.acc = (unsigned*)amax_out;
+  L.stream = s;
+  return launch_amax(L, false);
+}
+
+size_t fp8q_cast_workspace_bytes(int32_t num_groups) {
+  if (num_groups < 1) num_groups = 1;
+  return cast_workspace_bytes(num_groups);
+}
+
+fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                 const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
+                                 int32_t margin, const float* scale_in, uint8_t* q, float* amax_out,
+                                 float* scale_out, float* scale_inv_out, unsigned long long* sat_count_out,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  fp8q_status r = check_common(x, dt, rows, cols, group_offsets, num_groups);
+  if (r != FP8Q_OK) return r;
+  if (!fmt_ok(fmt)) return fail(FP8Q_ERR_INVALID_ARG, "fmt must be FP8Q_E4M3 or FP8Q_E5M2");
+  if (margin < 0 || margin > 63) return fail(FP8Q_ERR_INVALID_ARG, "margin must be in [0, 63]");
+  if (rows * cols > 0 && q == nullptr) return fail(FP8Q_ERR_INVALID_ARG, "q is NULL");
+  if (!aligned(q, 16)) return fail(FP8Q_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (scale_in && !aligned(scale_in, 4)) return fail(FP8Q_ERR_INVALID_ARG, "scale_in must be 4-byte aligned");
+  if (!aligned(amax_out, 4) || !aligned(scale_out, 4) || !aligned(scale_inv_out, 4) || !aligned(sat_count_out, 8))
+    return fail(FP8Q_ERR_INVALID_ARG, "misaligned output pointer");
+  if (!workspace || !aligned(workspace, 8)) return fail(FP8Q_ERR_INVALID_ARG, "workspace must be an 8-byte aligned device pointer");
+  if (workspace_bytes < cast_workspace_bytes(num_groups))
+    return fail(FP8Q_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                cast_workspace_bytes(num_groups));
+  const CastWorkspace ws = cast_workspace_carve(workspace, num_groups);
+  PtLaunch L{};
+  L.x = x;
+  L.dt = dt;
+  L.rows = rows;
+  L.cols = cols;
+  L.off = group_offsets;
+  L.G = num_groups;
+  L.fmt = fmt;
+  L.margin = margin;
+  L.counter = ws.counter;
+  L.ws_scale = ws.scale;
+  L.q = q;
+  L.sat_acc = sat_count_out ? ws.sat : nullptr;
+  L.sat_out = sat_count_out;
+  L.stream = (cudaStream_t)stream;
+  if (scale_in == nullptr) {
+    // current scaling: amax pass (publishes scales), then the cast
+    PtLaunch A = L;
+    A.acc = ws.acc;
+    A.amax_out = amax_out;
+    A.scale_out = scale_out;
+    A.scale_inv_out = scale_inv_out;
+    A.sat_acc = nullptr;
+    if ((r = launch_amax(A, true)) != FP8Q_OK) return r;
+    L.src = kSrcWorkspace;
+    return launch_cast(L);
+  }
+  L.src = kSrcGiven;
+  L.scale_in = scale_in;
+  L.acc = amax_out ? ws.acc : nullptr;
+  L.amax_out = amax_out;
+  L.scale_out = scale_out;
+  L.scale_inv_out = scale_inv_out;
+  return launch_cast(L);
+}
+
+fp8q_status fp8q_delayed_create(int32_t history_len, int32_t interval, int32_t margin, int32_t fmt,
+                                fp8q_delayed_state** out) {
+  g_err[0] = 0;
+  if (!out) return fail(FP8Q_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (history_len < 1 || history_len > 1024) return fail(FP8Q_ERR_INVALID_ARG, "history_len must be in [1, 1024]");
+  if (interval < 1) return fail(FP8Q_ERR_INVALID_ARG, "interval must be >= 1");
+  if (margin < 0 || margin > 63) return fail(FP8Q_ERR_INVALID_ARG, "margin must be in [0, 63]");
+  if (!fmt_ok(fmt)) return fail(FP8Q_ERR_INVALID_ARG, "fmt must be FP8Q_E4M3 or FP8Q_E5M2");
+  return delayed_create(history_len, interval, margin, fmt, out);
+}
+
+fp8q_status fp8q_delayed_destroy(fp8q_delayed_state* st) {
+  g_err[0] = 0;
+  if (!st) return FP8Q_OK;
+  return delayed_destroy(st);
+}
+
+fp8q_status fp8q_delayed_reset(fp8q_delayed_state* st, void* stream) {
+  g_err[0] = 0;
+  if (!st) return fail(FP8Q_ERR_INVALID_ARG, "state is NULL");
+  return delayed_reset(st, (cudaStream_t)stream);
+}
+
+fp8q_status fp8q_delayed_step(fp8q_delayed_state* st, const void* x, int32_t dt, int64_t n, uint8_t* q,
+                              float* scale_used_out, float* scale_inv_out, float* amax_out,
+                              unsigned long long* sat_count_out, void* stream) {
+  g_err[0] = 0;
+  if (!st) return fail(FP8Q_ERR_INVALID_ARG, "state is NULL");
+  fp8q_status r = check_common(x, dt, 1, n, nullptr, 1);
+  if (r != FP8Q_OK) return r;
+  if (n > 0 && q == nullptr) return fail(FP8Q_ERR_INVALID_ARG, "q is NULL");
+  if (!aligned(q, 16)) return fail(FP8Q_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (!aligned(scale_used_out, 4) || !aligned(scale_inv_out, 4) || !aligned(amax_out, 4) || !aligned(sat_count_out, 8))
+    return fail(FP8Q_ERR_INVALID_ARG, "misaligned output pointer");
+  return delayed_step(st, x, dt, n, q, scale_used_out, scale_inv_out, amax_out, sat_count_out,
+                      (cudaStream_t)stream);
+}
+
+fp8q_status fp8q_delayed_get(const fp8q_delayed_state* st, float* history_host, int32_t* head, int32_t* count,
+                             int64_t* step, int32_t* nonfinite) {
+  g_err[0] = 0;
+  if (!st) return fail(FP8Q_ERR_INVALID_ARG, "state is NULL");
+  return delayed_get(st, history_host, head, count, step, nonfinite);
+}
+
+fp8q_status fp8q_delayed_set(fp8q_delayed_state* st, const float* history_host, int32_t head, int32_t count,
+                             int64_t step) {
+  g_err[0] = 0;
+  if (!st) return fail(FP8Q_ERR_INVALID_ARG, "state is NULL");
+  const int H = delayed_history_len(st);
+  if (head < 0 || head >= H || count < 0 || count > H || step < 0)
+    return fail(FP8Q_ERR_INVALID_ARG, "need 0 <= head < %d, 0 <= count <= %d, step >= 0", H, H);
+  return delayed_set(st, history_host, head, count, step);
+}
+
+int64_t mxfp8_col_blocks(const int64_t* off, int32_t G, int64_t rows) {
+  if (rows < 0) return -1;
+  if (off == nullptr) return (rows + 31) / 32;
+  if (G < 1 || G > FP8Q_MAX_GROUPS || off[0] != 0 || off[G] != rows) return -1;
+  int64_t t = 0;
+  for (int g = 0; g < G; g++) {
+    const int64_t n = off[g + 1] - off[g];
+    if (n < 0) return -1;
+    t += (n + 31) / 32;
+  }
+  return t;
+}
+
+fp8q_status mxfp8_quantize(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
+                           int32_t num_groups, int32_t fmt, int32_t dir, uint8_t* q_row, uint8_t* s_row,
+                           uint8_t* q_col, uint8_t* s_col, int64_t s_col_ld, void* stream) {
+  g_err[0] = 0;
+  fp8q_status r = check_common(x, dt, rows, cols, group_offsets, num_groups);
+  if (r != FP8Q_OK) return r;
+  if (!fmt_ok(fmt)) return fail(FP8Q_ERR_INVALID_ARG, "fmt must be FP8Q_E4M3 or FP8Q_E5M2");
+  if (dir != MXFP8_ROW && dir != MXFP8_COL && dir != MXFP8_BOTH)
+    return fail(FP8Q_ERR_INVALID_ARG, "dir must be MXFP8_ROW, MXFP8_COL or MXFP8_BOTH");
+  if (cols % 32 != 0) return fail(FP8Q_ERR_UNSUPPORTED, "MXFP8 needs cols %% 32 == 0 (cols = %lld)", (long long)cols);
+  if (rows * cols == 0) return FP8Q_OK;
+  if (rows > INT32_MAX / 2) return fail(FP8Q_ERR_UNSUPPORTED, "rows too large");
+  if (dir & MXFP8_ROW) {
+    if (!q_row || !s_row) return fail(FP8Q_ERR_INVALID_ARG, "q_row and s_row are required for rowwise output");
+    if (!aligned(q_row, 16)) return fail(FP8Q_ERR_INVALID_ARG, "q_row must be 16-byte aligned");
+  }
+  if (dir & MXFP8_COL) {
+    if (!q_col || !s_col) return fail(FP8Q_ERR_INVALID_ARG, "q_col and s_col are required for columnwise output");
+    if (s_col_ld < (rows + 31) / 32)
+      return fail(FP8Q_ERR_INVALID_ARG, "s_col_ld (%lld) is below ceil(rows / 32) = %lld", (long long)s_col_ld,
+                  (long long)((rows + 31) / 32));
+  }
+  return launch_mx(x, dt, rows, cols, group_offsets, num_groups, fmt, dir, q_row, s_row, q_col, s_col, s_col_ld,
+                   (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fp8q.h"
+
+namespace fp8q {
+
+// Records `msg` as this thread's last error and returns `st`.
+fp8q_status fail(fp8q_status st, const char* fmt, ...);
+// Maps a CUDA error to FP8Q_ERR_CUDA with a message naming `what`.
+fp8q_status cuda_fail(cudaError_t e, const char* what);
+// Checks cudaGetLastError() after launches.
+fp8q_status check_launch(const char* what);
+
+int sm_count();
+
+// Per-tensor workspace layout (bytes from the start of the workspace).
+struct CastWorkspace {
+  unsigned* counter;              // [1]  last-CTA ticket
+  unsigned* acc;                  // [G]  amax accumulators (FP32 bits)
+  float* scale;                   // [G]  current-scaling scales
+  unsigned long long* sat;        // [G]  saturation counters
+};
+size_t cast_workspace_bytes(int G);
+CastWorkspace cast_workspace_carve(void* ws, int G);
+
+// Scale sources of the cast kernel.
+enum ScaleSrc : int { kSrcGiven = 0, kSrcWorkspace = 1, kSrcHistory = 2 };
+
+struct PtLaunch {
+  const void* x;
+  int dt;
+  int64_t rows, cols;
+  const int64_t* off;
+  int G;
+  int fmt;
+  int margin;
+  // scale source
+  int src;
+  const float* scale_in;
+  const float* hist;
+  int hist_count;
+  // workspace / state scratch
+  unsigned* counter;
+  unsigned* acc;                 // amax accumulators or nullptr (no fused amax)
+  float* ws_scale;
+  unsigned long long* sat_acc;   // nullptr: no counting
+  // outputs
+  uint8_t* q;
+  float* amax_out;
+  float* scale_out;
+  float* scale_inv_out;
+  unsigned long long* sat_out;
+  // delayed-scaling bookkeeping: the recorded amax goes to *hist_slot, a
+  // non-finite one sets *flag
+  float* hist_slot;
+  unsigned* flag;
+  cudaStream_t stream;
+};
+
+// Amax pass.  finalize_scales: the last CTA turns acc[] into ws_scale[] and
+// the scale outputs, writes amax_out / hist_slot / flag and zeroes acc[].
+// Otherwise amax accumulates into acc[] (which the caller zeroed).
+fp8q_status launch_amax(const PtLaunch& p, bool finalize_scales);
+// Cast pass (optionally with fused amax into acc[] and saturation counts).
+fp8q_status launch_cast(const PtLaunch& p);
+
+// MXFP8.
+fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* off, int G,
+                      int fmt, int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                      uint8_t* s_col, int64_t s_col_ld, cudaStream_t stream);
+
+}  // namespace fp8q

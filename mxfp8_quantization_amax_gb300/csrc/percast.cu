@@ -1,0 +1,452 @@
+// percast.cu -- per-tensor (per-group) amax and scaled cast.
+//
+// "HiFloat8：高性能训练之路" 1.2: Scale = F8max / Amax (eq. 1), X * Scale ->
+// FP8 (eq. 2); delayed scaling replaces Amax by the history max and
+// multiplies by 2^-N (eqs. 3-4).  "混合精度与 FP8 训练" 8.1-8.2: the cast
+// saturates; computing amax costs a read of the whole tensor, which delayed
+// scaling fuses into the cast itself.
+//
+// Work is split into chunks of kChunk elements; each CTA owns a contiguous
+// run of chunks, so its group (rows [off[g], off[g+1]) of the flat tensor)
+// changes rarely.  A chunk inside one group takes the vector path: every
+// thread issues all of its 16-byte loads first, then converts.  Chunks that
+// straddle a group boundary, and the ragged tail, take an element path.
+// Per-group amax / saturation partials are reduced per CTA and merged with
+// one atomic per CTA and group; the last CTA to finish (atomic ticket, no
+// waiting) publishes the per-group results and re-zeroes the accumulators.
+#include <stdio.h>
+
+#include "fp8q_device.cuh"
+#include "internal.h"
+
+namespace fp8q {
+
+constexpr int kPtThreads = 256;
+constexpr int kChunk = 8192;  // elements per chunk: 32 per thread
+
+template <int DT> struct InT;
+template <> struct InT<kBF16> {
+  static constexpr int kPerVec = 8;  // elements per 16-byte vector
+  static __device__ __forceinline__ uint32_t bits(const void* x, int64_t i) {
+    return (uint32_t)__ldg((const unsigned short*)x + i) << 16;
+  }
+};
+template <> struct InT<kFP32> {
+  static constexpr int kPerVec = 4;
+  static __device__ __forceinline__ uint32_t bits(const void* x, int64_t i) {
+    return __ldg((const unsigned*)x + i);
+  }
+};
+
+struct KParams {
+  const void* x;
+  int64_t n, cols, rows;
+  const int64_t* off;
+  int G;
+  int64_t n_chunks;
+  float f8max;
+  int margin;
+  int src;
+  const float* scale_in;
+  const float* hist;
+  int hist_count;
+  unsigned* counter;
+  unsigned* acc;
+  float* ws_scale;
+  unsigned long long* sat_acc;
+  uint8_t* q;
+  float* amax_out;
+  float* scale_out;
+  float* scale_inv_out;
+  unsigned long long* sat_out;
+  float* hist_slot;
+  unsigned* flag;
+};
+
+__device__ __forceinline__ int group_of_elem(const KParams& p, int64_t e) {
+  if (p.off == nullptr || p.G <= 1) return 0;
+  return group_of_row(p.off, p.G, e / p.cols);
+}
+
+// Block-wide max / sum; every thread must call (block-uniform control flow).
+__device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* sh) {
+  v = warp_max_u32(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) sh[w] = v;
+  __syncthreads();
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < kPtThreads / 32; i++) r = max(r, sh[i]);
+  return r;
+}
+__device__ __forceinline__ unsigned long long block_sum(unsigned long long v, unsigned long long* sh) {
+  v = warp_sum_u64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) sh[w] = v;
+  __syncthreads();
+  unsigned long long r = 0;
+#pragma unroll
+  for (int i = 0; i < kPtThreads / 32; i++) r += sh[i];
+  return r;
+}
+
+// Last CTA to arrive returns true (all earlier CTAs' atomics are visible).
+__device__ __forceinline__ bool arrive_last(unsigned* counter) {
+  __shared__ bool last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (last) __threadfence();
+  return last;
+}
+
+// ---------------------------------------------------------------------------
+// Amax pass
+// ---------------------------------------------------------------------------
+template <int DT, bool FINALIZE>
+__global__ void __launch_bounds__(kPtThreads) amax_kernel(KParams p) {
+  __shared__ uint32_t sh_max[kPtThreads / 32];
+  const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
+  const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
+  int cur_g = -1;
+  uint32_t cur = 0;
+
+  auto flush = [&]() {  // block-uniform
+    const uint32_t m = block_max(cur, sh_max);
+    if (threadIdx.x == 0 && cur_g >= 0 && m != 0) atomicMax(p.acc + cur_g, m);
+    cur = 0;
+  };
+
+  for (int64_t c = c_begin; c < c_end; ++c) {
+    const int64_t e0 = c * kChunk;
+    const int64_t e1 = min(e0 + (int64_t)kChunk, p.n);
+    const int g0 = group_of_elem(p, e0), g1 = group_of_elem(p, e1 - 1);
+    if (g0 == g1) {
+      if (g0 != cur_g) {
+        if (cur_g >= 0) flush();
+        cur_g = g0;
+      }
+      if (e1 - e0 == kChunk) {
+        constexpr int V = kChunk / InT<DT>::kPerVec / kPtThreads;
+        uint4 v[V];
+#pragma unroll
+        for (int k = 0; k < V; k++)
+          v[k] = ld_stream((const char*)p.x + (e0 + (int64_t)(k * kPtThreads + threadIdx.x) * InT<DT>::kPerVec) * (DT == kBF16 ? 2 : 4));
+        if constexpr (DT == kBF16) {
+          uint32_t m = 0;
+#pragma unroll
+          for (int k = 0; k < V; k++) {
+            m = absmax_bf16x2(m, v[k].x);
+            m = absmax_bf16x2(m, v[k].y);
+            m = absmax_bf16x2(m, v[k].z);
+            m = absmax_bf16x2(m, v[k].w);
+          }
+          cur = max(cur, max(m << 16, m & 0xFFFF0000u));
+        } else {
+#pragma unroll
+          for (int k = 0; k < V; k++)
+            cur = max(max(cur, max(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu)),
+                      max(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu));
+        }
+      } else {
+        for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads)
+          cur = max(cur, InT<DT>::bits(p.x, e) & 0x7FFFFFFFu);
+      }
+    } else {
+      // chunk crosses group boundaries: per-thread runs, atomics on change
+      if (cur_g >= 0) flush();
+      cur_g = -1;
+      int tg = -1;
+      uint32_t tm = 0;
+      for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) {
+        const int g = group_of_elem(p, e);
+        if (g != tg) {
+          if (tg >= 0 && tm) atomicMax(p.acc + tg, tm);
+          tg = g;
+          tm = 0;
+        }
+        tm = max(tm, InT<DT>::bits(p.x, e) & 0x7FFFFFFFu);
+      }
+      if (tg >= 0 && tm) atomicMax(p.acc + tg, tm);
+    }
+  }
+  if (cur_g >= 0) flush();
+
+  if constexpr (FINALIZE) {
+    if (arrive_last(p.counter)) {
+      for (int g = threadIdx.x; g < p.G; g += kPtThreads) {
+        const uint32_t a = *(volatile unsigned*)(p.acc + g);
+        const float s = scale_from_amax(a, p.f8max, p.margin);
+        p.ws_scale[g] = s;
+        if (p.amax_out) p.amax_out[g] = __uint_as_float(a);
+        if (p.scale_out) p.scale_out[g] = s;
+        if (p.scale_inv_out) p.scale_inv_out[g] = __frcp_rn(s);
+        if (g == 0) {
+          if (p.hist_slot) *p.hist_slot = __uint_as_float(a);
+          if (p.flag && a >= 0x7F800000u) atomicOr(p.flag, 1u);
+        }
+        p.acc[g] = 0;
+      }
+      if (threadIdx.x == 0) *p.counter = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Cast pass
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float group_scale(const KParams& p, int g, float hist_scale) {
+  if (p.src == kSrcGiven) return __ldg(p.scale_in + g);
+  if (p.src == kSrcWorkspace) return *(volatile float*)(p.ws_scale + g);
+  return hist_scale;
+}
+
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
+  __shared__ uint32_t sh_max[kPtThreads / 32];
+  __shared__ unsigned long long sh_sum[kPtThreads / 32];
+  constexpr float kMax = Fmt<FMT>::kMax;
+  const bool do_amax = p.acc != nullptr;
+  const bool do_sat = p.sat_acc != nullptr;
+
+  float hist_scale = 1.0f;
+  if (p.src == kSrcHistory) {  // max over the filled history entries
+    uint32_t hm = 0;
+    for (int i = threadIdx.x; i < p.hist_count; i += kPtThreads)
+      hm = max(hm, __float_as_uint(p.hist[i]) & 0x7FFFFFFFu);
+    hist_scale = scale_from_amax(block_max(hm, sh_max), kMax, p.margin);
+  }
+  if (blockIdx.x == 0 && p.src != kSrcWorkspace) {
+    for (int g = threadIdx.x; g < p.G; g += kPtThreads) {
+      const float s = group_scale(p, g, hist_scale);
+      if (p.scale_out) p.scale_out[g] = s;
+      if (p.scale_inv_out) p.scale_inv_out[g] = __frcp_rn(s);
+    }
+  }
+
+  const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
+  const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
+  int cur_g = -1;
+  uint32_t cur = 0;
+  unsigned long long nsat = 0;
+
+  auto flush = [&]() {  // block-uniform
+    if (do_amax) {
+      const uint32_t m = block_max(cur, sh_max);
+      if (threadIdx.x == 0 && m != 0) atomicMax(p.acc + cur_g, m);
+    }
+    if (do_sat) {
+      const unsigned long long s = block_sum(nsat, sh_sum);
+      if (threadIdx.x == 0 && s != 0) atomicAdd(p.sat_acc + cur_g, s);
+    }
+    cur = 0;
+    nsat = 0;
+  };
+
+  for (int64_t c = c_begin; c < c_end; ++c) {
+    const int64_t e0 = c * kChunk;
+    const int64_t e1 = min(e0 + (int64_t)kChunk, p.n);
+    const int g0 = group_of_elem(p, e0), g1 = group_of_elem(p, e1 - 1);
+    if (g0 == g1) {
+      if (g0 != cur_g) {
+        if (cur_g >= 0) flush();
+        cur_g = g0;
+      }
+      const float s = group_scale(p, g0, hist_scale);
+      if (e1 - e0 == kChunk) {
+        constexpr int PV = InT<DT>::kPerVec;
+        constexpr int V = kChunk / PV / kPtThreads;
+        uint4 v[V];
+#pragma unroll
+        for (int k = 0; k < V; k++)
+          v[k] = ld_stream((const char*)p.x + (e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV) * (DT == kBF16 ? 2 : 4));
+#pragma unroll
+        for (int k = 0; k < V; k++) {
+          const int64_t e = e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV;
+          if constexpr (DT == kBF16) {
+            float f[8] = {bf16_lo(v[k].x), bf16_hi(v[k].x), bf16_lo(v[k].y), bf16_hi(v[k].y),
+                          bf16_lo(v[k].z), bf16_hi(v[k].z), bf16_lo(v[k].w), bf16_hi(v[k].w)};
+#pragma unroll
+            for (int i = 0; i < 8; i++) f[i] = __fmul_rn(f[i], s);
+            if (do_sat) {
+#pragma unroll
+              for (int i = 0; i < 8; i++) nsat += fabsf(f[i]) > kMax;
+            }
+            if (do_amax) {
+              uint32_t m = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(0u, v[k].x), v[k].y), v[k].z), v[k].w);
+              cur = max(cur, max(m << 16, m & 0xFFFF0000u));
+            }
+            uint2 o;
+            o.x = canon_nan4<FMT>(cvt4<FMT>(f[0], f[1], f[2], f[3]));
+            o.y = canon_nan4<FMT>(cvt4<FMT>(f[4], f[5], f[6], f[7]));
+            st_stream(p.q + e, o);
+          } else {
+            float f[4] = {__uint_as_float(v[k].x), __uint_as_float(v[k].y), __uint_as_float(v[k].z),
+                          __uint_as_float(v[k].w)};
+            if (do_amax)
+              cur = max(max(cur, max(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu)),
+                        max(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu));
+#pragma unroll
+            for (int i = 0; i < 4; i++) f[i] = __fmul_rn(f[i], s);
+            if (do_sat) {
+#pragma unroll
+              for (int i = 0; i < 4; i++) nsat += fabsf(f[i]) > kMax;
+            }
+            *(uint32_t*)(p.q + e) = canon_nan4<FMT>(cvt4<FMT>(f[0], f[1], f[2], f[3]));
+          }
+        }
+      } else {
+        for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) {
+          const uint32_t b = InT<DT>::bits(p.x, e);
+          const float f = __fmul_rn(__uint_as_float(b), s);
+          if (do_sat) nsat += fabsf(f) > kMax;
+          if (do_amax) cur = max(cur, b & 0x7FFFFFFFu);
+          p.q[e] = (uint8_t)canon_nan4<FMT>(cvt2<FMT>(f, 0.0f));
+        }
+      }
+    } else {
+      if (cur_g >= 0) flush();
+      cur_g = -1;
+      int tg = -1;
+      uint32_t tm = 0;
+      unsigned long long ts = 0;
+      float s = 1.0f;
+      for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) {
+        const int g = group_of_elem(p, e);
+        if (g != tg) {
+          if (tg >= 0) {
+            if (do_amax && tm) atomicMax(p.acc + tg, tm);
+            if (do_sat && ts) atomicAdd(p.sat_acc + tg, ts);
+          }
+          tg = g;
+          tm = 0;
+          ts = 0;
+          s = group_scale(p, g, hist_scale);
+        }
+        const uint32_t b = InT<DT>::bits(p.x, e);
+        const float f = __fmul_rn(__uint_as_float(b), s);
+        if (do_sat) ts += fabsf(f) > kMax;
+        if (do_amax) tm = max(tm, b & 0x7FFFFFFFu);
+        p.q[e] = (uint8_t)canon_nan4<FMT>(cvt2<FMT>(f, 0.0f));
+      }
+      if (tg >= 0) {
+        if (do_amax && tm) atomicMax(p.acc + tg, tm);
+        if (do_sat && ts) atomicAdd(p.sat_acc + tg, ts);
+      }
+    }
+  }
+  if (cur_g >= 0) flush();
+
+  if (do_amax || do_sat) {
+    if (arrive_last(p.counter)) {
+      for (int g = threadIdx.x; g < p.G; g += kPtThreads) {
+        if (do_amax) {
+          const uint32_t a = *(volatile unsigned*)(p.acc + g);
+          if (p.amax_out) p.amax_out[g] = __uint_as_float(a);
+          if (p.hist_slot && g == 0) {
+            *p.hist_slot = __uint_as_float(a);
+            if (a >= 0x7F800000u) atomicOr(p.flag, 1u);
+          }
+          p.acc[g] = 0;
+        }
+        if (do_sat) {
+          const unsigned long long s = *(volatile unsigned long long*)(p.sat_acc + g);
+          if (p.sat_out) p.sat_out[g] = s;
+          p.sat_acc[g] = 0;
+        }
+      }
+      if (threadIdx.x == 0) *p.counter = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static KParams make_params(const PtLaunch& L) {
+  KParams p{};
+  p.x = L.x;
+  p.rows = L.rows;
+  p.cols = L.cols;
+  p.n = L.rows * L.cols;
+  p.off = L.off;
+  p.G = L.G;
+  p.n_chunks = (p.n + kChunk - 1) / kChunk;
+  p.f8max = fmt_max(L.fmt);
+  p.margin = L.margin;
+  p.src = L.src;
+  p.scale_in = L.scale_in;
+  p.hist = L.hist;
+  p.hist_count = L.hist_count;
+  p.counter = L.counter;
+  p.acc = L.acc;
+  p.ws_scale = L.ws_scale;
+  p.sat_acc = L.sat_acc;
+  p.q = L.q;
+  p.amax_out = L.amax_out;
+  p.scale_out = L.scale_out;
+  p.scale_inv_out = L.scale_inv_out;
+  p.sat_out = L.sat_out;
+  p.hist_slot = L.hist_slot;
+  p.flag = L.flag;
+  return p;
+}
+
+template <typename K>
+static int ctas_per_sm(K kernel) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kPtThreads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  return per_sm;
+}
+
+static int grid_for(int64_t n_chunks, int per_sm) {
+  const int64_t resident = (int64_t)per_sm * sm_count();
+  int64_t g = n_chunks < resident ? n_chunks : resident;
+  return (int)(g < 1 ? 1 : g);
+}
+
+fp8q_status launch_amax(const PtLaunch& L, bool finalize_scales) {
+  KParams p = make_params(L);
+  if (L.dt == kBF16) {
+    if (finalize_scales) {
+      static int r = ctas_per_sm(amax_kernel<kBF16, true>);
+      amax_kernel<kBF16, true><<<grid_for(p.n_chunks, r), kPtThreads, 0, L.stream>>>(p);
+    } else {
+      static int r = ctas_per_sm(amax_kernel<kBF16, false>);
+      amax_kernel<kBF16, false><<<grid_for(p.n_chunks, r), kPtThreads, 0, L.stream>>>(p);
+    }
+  } else {
+    if (finalize_scales) {
+      static int r = ctas_per_sm(amax_kernel<kFP32, true>);
+      amax_kernel<kFP32, true><<<grid_for(p.n_chunks, r), kPtThreads, 0, L.stream>>>(p);
+    } else {
+      static int r = ctas_per_sm(amax_kernel<kFP32, false>);
+      amax_kernel<kFP32, false><<<grid_for(p.n_chunks, r), kPtThreads, 0, L.stream>>>(p);
+    }
+  }
+  return check_launch("amax kernel");
+}
+
+template <int DT, int FMT>
+static void launch_cast_t(const KParams& p, cudaStream_t s) {
+  static int r = ctas_per_sm(cast_kernel<DT, FMT>);
+  cast_kernel<DT, FMT><<<grid_for(p.n_chunks, r), kPtThreads, 0, s>>>(p);
+}
+
+fp8q_status launch_cast(const PtLaunch& L) {
+  KParams p = make_params(L);
+  if (L.dt == kBF16) {
+    if (L.fmt == kE4M3) launch_cast_t<kBF16, kE4M3>(p, L.stream);
+    else launch_cast_t<kBF16, kE5M2>(p, L.stream);
+  } else {
+    if (L.fmt == kE4M3) launch_cast_t<kFP32, kE4M3>(p, L.stream);
+    else launch_cast_t<kFP32, kE5M2>(p, L.stream);
+  }
+  return check_launch("cast kernel");
+}
+
+}  // namespace fp8q

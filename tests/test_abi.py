@@ -1,0 +1,116 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every entry point include/fp8q.h declares, and rejects bad arguments on the
+host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mxfp8_quantization_amax_gb300 as fq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8q.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fq.build()
+    return fq.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"FP8Q_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_symbols())
+    for n in ("fp8q_amax", "fp8q_cast_per_tensor", "fp8q_delayed_step", "mxfp8_quantize",
+              "fp8q_delayed_create", "fp8q_delayed_get", "fp8q_delayed_set", "fp8q_delayed_reset",
+              "fp8q_delayed_destroy", "mxfp8_col_blocks", "fp8q_last_error_string",
+              "fp8q_cast_workspace_bytes", "fp8q_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_only_declared_symbols_are_exported(lib):
+    """Internal helpers stay hidden (the build uses -fvisibility=hidden)."""
+    out = os.popen(f"nm -D --defined-only {fq.library_path()}").read()
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    ours = {s for s in exported if s.startswith(("fp8q", "mxfp8"))}
+    assert ours == set(declared_symbols())
+
+
+def test_binding_exposes_the_same_names():
+    for n in ("fp8q_amax", "fp8q_cast_per_tensor", "mxfp8_quantize", "mxfp8_col_blocks",
+              "fp8q_cast_workspace_bytes", "DelayedScaling"):
+        assert hasattr(fq, n)
+
+
+def test_version_and_workspace_size(lib):
+    assert lib.fp8q_version() == 10000
+    assert lib.fp8q_cast_workspace_bytes(1) >= 64 + 16
+    assert lib.fp8q_cast_workspace_bytes(64) >= 64 + 16 * 64
+
+
+def test_col_blocks_host(lib):
+    assert fq.mxfp8_col_blocks(100) == 4
+    assert fq.mxfp8_col_blocks(150, [0, 0, 33, 34, 100, 150]) == 8
+    with pytest.raises(ValueError):
+        fq.mxfp8_col_blocks(150, [0, 40, 30, 150])
+    with pytest.raises(ValueError):
+        fq.mxfp8_col_blocks(150, [0, 40, 149])
+
+
+def _status(fn, *args):
+    return fn(*args)
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    P = ctypes.c_void_p
+    buf = ctypes.create_string_buffer(256)
+    aligned = P((ctypes.addressof(buf) + 15) & ~15)
+    mis = P(aligned.value + 2)
+    # bad dtype
+    assert lib.fp8q_amax(aligned, 7, 4, 4, None, 1, aligned, None) == 1
+    # misaligned x
+    assert lib.fp8q_amax(mis, 0, 4, 4, None, 1, aligned, None) == 1
+    assert b"aligned" in lib.fp8q_last_error_string()
+    # groups without offsets
+    assert lib.fp8q_amax(aligned, 0, 4, 4, None, 3, aligned, None) == 1
+    # too many groups
+    assert lib.fp8q_amax(aligned, 0, 4, 4, aligned, 5000, aligned, None) == 1
+    # MX: cols % 32 != 0 is unsupported
+    assert lib.mxfp8_quantize(aligned, 0, 4, 48, None, 1, 0, 3, aligned, aligned, aligned, aligned, 1,
+                              None) == 2
+    # MX: bad dir / fmt
+    assert lib.mxfp8_quantize(aligned, 0, 4, 64, None, 1, 0, 0, aligned, aligned, aligned, aligned, 1,
+                              None) == 1
+    assert lib.mxfp8_quantize(aligned, 0, 4, 64, None, 1, 2, 3, aligned, aligned, aligned, aligned, 1,
+                              None) == 1
+    # MX: s_col_ld too small for the rows
+    assert lib.mxfp8_quantize(aligned, 0, 100, 64, None, 1, 0, 2, None, None, aligned, aligned, 3,
+                              None) == 1
+    # cast: margin out of range, missing workspace, small workspace
+    assert lib.fp8q_cast_per_tensor(aligned, 0, 4, 4, None, 1, 0, 99, None, aligned, None, None, None,
+                                    None, aligned, 4096, None) == 1
+    assert lib.fp8q_cast_per_tensor(aligned, 0, 4, 4, None, 1, 0, 0, None, aligned, None, None, None,
+                                    None, None, 0, None) == 1
+    assert lib.fp8q_cast_per_tensor(aligned, 0, 4, 4, None, 1, 0, 0, None, aligned, None, None, None,
+                                    None, aligned, 8, None) == 1
+    # delayed: bad history length / interval
+    h = P()
+    assert lib.fp8q_delayed_create(0, 1, 0, 0, ctypes.byref(h)) == 1
+    assert lib.fp8q_delayed_create(16, 0, 0, 0, ctypes.byref(h)) == 1
+    assert lib.fp8q_delayed_create(16, 1, 0, 5, ctypes.byref(h)) == 1
+    assert lib.fp8q_delayed_step(None, aligned, 0, 4, aligned, None, None, None, None, None) == 1
+
+
+def test_empty_mx_is_a_no_op(lib):
+    # rows * cols == 0 returns before any launch
+    assert lib.mxfp8_quantize(None, 0, 0, 64, None, 1, 0, 3, None, None, None, None, 0, None) == 0
