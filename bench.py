@@ -1,0 +1,511 @@
+"""Benchmark of the FP8 / MXFP8 quantization hot path on one node.
+
+One step = one pass of the whole path over one batch of the activation
+workload (4096x4096 BF16: N(0,1) times a per-row lognormal(0,2) factor,
+0.1% of entries x1000, 1% of the 1x32 blocks zero):
+  * mxfp8_quantize, E4M3, rowwise + columnwise        (4.0625 B/element)
+  * fp8q_cast_per_tensor, current scaling, E4M3       (5 B/element: amax read,
+                                                       cast read + write)
+  * fp8q_delayed_step, E4M3, history 16, margin 3,
+    Interval 1 (amax fused into the cast)             (3 B/element + history)
+Each op gets its own input tensor, and the step cycles over enough buffer
+sets that no input is still in L2 when it is read again.
+
+value: bytes read + written by the step's kernels, summed over all ranks,
+divided by the max over ranks of the device time of K steps (GB/s).
+roofline: the MXFP8 kernel alone, timed with CUDA events around each of its
+launches inside the timed region, against the measured HBM copy bandwidth.
+
+--workload selects another workload for the same line format:
+  activation (default), mx_8192 (MXFP8 on 8192x8192, for profiling),
+  per_tensor_1024 (1024x1024 current scaling),
+  delayed_8192 (8192x8192 delayed steps), linear_layer (A, W, E of an
+  8B-class layer, MXFP8 both directions), moe (65536x7168, 64 experts:
+  grouped MXFP8 and grouped current scaling).
+--impl reference: the CPU oracle on this host (a bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "quantize GB/s (bytes read+written) and % of GB300 HBM peak, bit-exact"
+FALLBACK_HBM_GBS = 6800.0
+E4M3, E5M2 = 0, 1
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="activation",
+                   choices=["activation", "mx_8192", "per_tensor_1024", "delayed_8192", "linear_layer", "moe"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# workloads: shapes, algorithmic bytes, host inputs
+# ---------------------------------------------------------------------------
+def mx_bytes(rows, cols, ncolblocks=None):
+    ncb = (rows + 31) // 32 if ncolblocks is None else ncolblocks
+    return rows * cols * 2 + rows * cols + rows * (cols // 32) + cols * rows + cols * ncb
+
+
+def workload_spec(name):
+    """(config dict, list of ops).  An op is a dict with 'kind', its tensor
+    shape and its algorithmic bytes per call."""
+    if name == "activation":
+        r = c = 4096
+        ops = [{"kind": "mx", "shape": (r, c), "fmt": E4M3, "bytes": mx_bytes(r, c), "gen": ("c2", 0)},
+               {"kind": "current", "shape": (r, c), "fmt": E4M3, "bytes": 5 * r * c, "gen": ("c2", 1)},
+               {"kind": "delayed", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + 4 * 16, "gen": ("c2", 2)}]
+        cfg = {"workload": "activation_4096x4096_bf16", "rows": r, "cols": c,
+               "ops": ["mxfp8 e4m3 row+col", "current scaling e4m3", "delayed e4m3 H16 margin3 interval1"]}
+        return cfg, ops
+    if name == "mx_8192":
+        r = c = 8192
+        ops = [{"kind": "mx", "shape": (r, c), "fmt": E4M3, "bytes": mx_bytes(r, c), "gen": ("c2", 0)}]
+        return {"workload": "mxfp8_8192x8192_bf16", "rows": r, "cols": c, "ops": ["mxfp8 e4m3 row+col"]}, ops
+    if name == "per_tensor_1024":
+        ops = [{"kind": "current", "shape": (1024, 1024), "fmt": E4M3, "bytes": 5 * 1024 * 1024, "gen": ("c1", 0)}]
+        return {"workload": "per_tensor_current_1024x1024_bf16", "rows": 1024, "cols": 1024}, ops
+    if name == "delayed_8192":
+        r = c = 8192
+        ops = [{"kind": "delayed", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + 64, "gen": ("c3", 0)},
+               {"kind": "delayed", "shape": (r, c), "fmt": E5M2, "bytes": 3 * r * c + 64, "gen": ("c3", 1)}]
+        return {"workload": "delayed_8192x8192_bf16", "rows": r, "cols": c,
+                "ops": ["delayed e4m3 H16 margin3 interval1", "delayed e5m2 H16 margin3 interval1"]}, ops
+    if name == "linear_layer":
+        shapes = {"A": (16384, 4096), "W": (14336, 4096), "E": (16384, 14336)}
+        ops = [{"kind": "mx", "shape": shapes[k], "fmt": E5M2 if k == "E" else E4M3,
+                "bytes": mx_bytes(*shapes[k]), "gen": ("c4", k)} for k in ("A", "W", "E")]
+        return {"workload": "linear_layer_8b_mxfp8", "A": "16384x4096", "W": "14336x4096",
+                "E": "16384x14336"}, ops
+    if name == "moe":
+        r, c = 65536, 7168
+        ops = [{"kind": "mx_grouped", "shape": (r, c), "fmt": E4M3, "bytes": None, "gen": ("c5", 0)},
+               {"kind": "current_grouped", "shape": (r, c), "fmt": E4M3, "bytes": 5 * r * c, "gen": ("c5", 0)}]
+        return {"workload": "moe_64_experts_65536x7168_bf16", "rows": r, "cols": c, "experts": 64}, ops
+    raise ValueError(name)
+
+
+def host_input(gen, shape):
+    import synth
+    kind, idx = gen
+    if kind == "c2":
+        return synth.config2(*shape, seed=2 + 100 * idx)
+    if kind == "c1":
+        return synth.config1(*shape, seed=1)
+    if kind == "c3":
+        return synth.config3_step(0, *shape, seed=3 + idx)
+    if kind == "c4":
+        t = {"A": lambda: synth.normal_outliers(*shape, seed=4, std=0.02, p=0.0005, factor=50.0, tensor=1),
+             "W": lambda: synth.normal_outliers(*shape, seed=4, std=0.02, p=0.0005, factor=50.0, tensor=2),
+             "E": lambda: synth.student_t(*shape, 3.0, seed=4, scale=1e-4, tensor=3)}
+        return t[idx]()
+    if kind == "c5":
+        return synth.student_t(*shape, 4.0, seed=5)
+    raise ValueError(kind)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(peak_key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source it was taken from is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[peak_key]
+    except (OSError, KeyError, ValueError):
+        return None
+    src = os.path.join(ROOT, d["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return d["bytes_per_launch"] if h == d.get("source_sha") else None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import mxfp8_quantization_amax_gb300 as fq
+    import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world > 1:
+        fq.build()
+    cfg, ops = workload_spec(args.workload)
+
+    # host inputs (pinned, for the end-to-end leg) and their device copies
+    offsets_host = None
+    if args.workload == "moe":
+        offsets_host = synth.moe_offsets(65536, 64, seed=5)
+        ncb = int(sum((int(offsets_host[g + 1] - offsets_host[g]) + 31) // 32 for g in range(64)))
+        for op in ops:
+            if op["kind"] == "mx_grouped":
+                op["bytes"] = mx_bytes(*op["shape"], ncolblocks=ncb)
+    host = []
+    for op in ops:
+        h = host_input(op["gen"], op["shape"])
+        host.append(torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory())
+    bytes_per_step = sum(op["bytes"] for op in ops)
+    in_bytes = sum(h.numel() * 2 for h in host)
+    # enough buffer sets that a set is out of L2 when it comes round again
+    l2 = 129 * 2 ** 20
+    per_set = in_bytes + sum(op["bytes"] - 2 * int(np.prod(op["shape"])) for op in ops)
+    nsets = max(1, min(8, -(-4 * l2 // per_set)))
+    off_dev = None if offsets_host is None else torch.from_numpy(offsets_host).to(dev)
+
+    sets = []
+    for s in range(nsets):
+        bufs = []
+        for op, h in zip(ops, host):
+            r, c = op["shape"]
+            x = h.to(dev, non_blocking=True)
+            b = {"x": x}
+            if op["kind"] in ("mx", "mx_grouped"):
+                ld = fq.mxfp8_col_blocks(r, None if offsets_host is None else list(offsets_host))
+                b["out"] = {"q_row": torch.empty((r, c), dtype=torch.uint8, device=dev),
+                            "s_row": torch.empty((r, c // 32), dtype=torch.uint8, device=dev),
+                            "q_col": torch.empty((c, r), dtype=torch.uint8, device=dev),
+                            "s_col": torch.empty((c, ld), dtype=torch.uint8, device=dev)}
+                b["ld"] = ld
+            else:
+                b["q"] = torch.empty((r, c), dtype=torch.uint8, device=dev)
+                G = 64 if op["kind"] == "current_grouped" else 1
+                b["pt"] = {k: torch.empty(G, dtype=torch.float32, device=dev) for k in ("amax", "scale", "scale_inv")}
+                b["ws"] = torch.zeros(fq.fp8q_cast_workspace_bytes(G), dtype=torch.uint8, device=dev)
+            bufs.append(b)
+        sets.append(bufs)
+    states = [fq.DelayedScaling(16, 1, 3, op["fmt"]) if op["kind"] == "delayed" else None for op in ops]
+    for bufs in sets:
+        for op, b in zip(ops, bufs):
+            if op["kind"] == "delayed":
+                b["dl"] = {k: torch.empty(1, dtype=torch.float32, device=dev) for k in ("scale", "scale_inv", "amax")}
+    torch.cuda.synchronize()
+
+    mx_events = []
+    launches = {"n": 0}
+
+    def step(i, record_mx=False):
+        bufs = sets[i % nsets]
+        for op, b, st in zip(ops, bufs, states):
+            k = op["kind"]
+            if k in ("mx", "mx_grouped"):
+                if record_mx:
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                fq.mxfp8_quantize(b["x"], op["fmt"], fq.BOTH,
+                                  group_offsets=off_dev if k == "mx_grouped" else None,
+                                  s_col_ld=b["ld"], out=b["out"])
+                if record_mx:
+                    e1.record()
+                    mx_events.append((e0, e1))
+                launches["n"] += 1
+            elif k in ("current", "current_grouped"):
+                fq.fp8q_cast_per_tensor(b["x"], op["fmt"], group_offsets=off_dev if k == "current_grouped" else None,
+                                        q=b["q"], workspace=b["ws"], out=b["pt"])
+                launches["n"] += 2
+            else:
+                st.step(b["x"], q=b["q"], outs=b["dl"])
+                launches["n"] += 1
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches["n"] = 0
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(args.steps):
+        step(i, record_mx=True)
+    t1.record()
+    torch.cuda.synchronize()
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    mx_ms = [a.elapsed_time(b) for a, b in mx_events]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # end-to-end: host inputs -> device, the step, device -> host outputs
+    e2e = None
+    if not args.no_e2e:
+        outs_host = []
+        for op in ops:
+            r, c = op["shape"]
+            if op["kind"] in ("mx", "mx_grouped"):
+                ld = sets[0][ops.index(op)]["ld"]
+                outs_host.append([torch.empty(n, dtype=torch.uint8).pin_memory()
+                                  for n in (r * c, r * (c // 32), c * r, c * ld)])
+            else:
+                outs_host.append([torch.empty(r * c, dtype=torch.uint8).pin_memory()])
+        bi = sum(h.numel() * 2 for h in host)
+        bo = sum(t.numel() for lst in outs_host for t in lst)
+
+        def e2e_step(i):
+            b = sets[i % nsets]
+            for j, op in enumerate(ops):
+                b[j]["x"].copy_(host[j], non_blocking=True)
+            step(i)
+            for j, op in enumerate(ops):
+                if op["kind"] in ("mx", "mx_grouped"):
+                    o = b[j]["out"]
+                    for dst, src in zip(outs_host[j], (o["q_row"], o["s_row"], o["q_col"], o["s_col"])):
+                        dst.copy_(src.reshape(-1), non_blocking=True)
+                else:
+                    outs_host[j][0].copy_(b[j]["q"].reshape(-1), non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        z.record()
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(z) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(world * bytes_per_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 4)}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    ms_per_step = elapsed_ms / args.steps
+    value = world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    mx_op = next((op for op in ops if op["kind"] in ("mx", "mx_grouped")), None)
+    roofline = None
+    if mx_op is not None and mx_ms:
+        # average over the launches of the first MXFP8 op of the step
+        per_step_mx = len(mx_ms) // args.steps
+        first = mx_ms[0::per_step_mx]
+        avg_ms = sum(first) / len(first)
+        achieved = mx_op["bytes"] / (avg_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                    "kernel": "mx_kernel<bf16,%s,both>" % ("e4m3" if mx_op["fmt"] == E4M3 else "e5m2"),
+                    "algorithmic_bytes_per_launch": mx_op["bytes"], "avg_launch_us": round(avg_ms * 1e3, 3),
+                    "traffic": kernel_traffic(args.workload)}
+    cfg = dict(cfg)
+    cfg["l2"] = f"{nsets} rotating buffer sets of {per_set / 2**20:.0f} MiB (> 4x L2 in total)"
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": cfg, "frac_of_hbm_peak": round(value / world / peak, 4), "roofline": roofline,
+            "e2e": e2e, "gpu_launches": launches["n"], "clocks": clocks,
+            "bytes_per_step": bytes_per_step}
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    for st in states:
+        if st is not None:
+            st.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------------------------
+# the oracle on this host: cpu_baseline and the reference arm
+# ---------------------------------------------------------------------------
+def oracle_sample_step(workload, sample_rows, inputs, states):
+    """The oracle on the first `sample_rows` rows of each op's tensor;
+    returns the algorithmic bytes it processed."""
+    import oracle
+    cfg, ops = workload_spec(workload)
+    total = 0
+    for op, x, st in zip(ops, inputs, states):
+        r, c = x.shape
+        k = op["kind"]
+        if k in ("mx", "mx_grouped"):
+            oracle.mx_quantize(x, op["fmt"], 3)
+            total += mx_bytes(r, c)
+        elif k in ("current", "current_grouped"):
+            oracle.current_scaling(x, op["fmt"])
+            total += 5 * r * c
+        else:
+            st.step(x)
+            total += 3 * r * c
+    return total
+
+
+def oracle_inputs(workload, sample_rows):
+    import oracle
+    cfg, ops = workload_spec(workload)
+    xs, states = [], []
+    for op in ops:
+        r, c = op["shape"]
+        rr = min(r, sample_rows)
+        xs.append(np.ascontiguousarray(host_input(op["gen"], (rr, c))))
+        states.append(oracle.DelayedScaling(16, 1, 3, op["fmt"]) if op["kind"] == "delayed" else None)
+    return xs, states
+
+
+def sample_rows_for(workload):
+    return {"activation": 256, "mx_8192": 128, "per_tensor_1024": 1024, "delayed_8192": 128, "linear_layer": 64,
+            "moe": 32}[workload]
+
+
+def cpu_baseline(workload, budget_s=10.0):
+    import oracle
+    rows = sample_rows_for(workload)
+    xs, states = oracle_inputs(workload, rows)
+    oracle_sample_step(workload, rows, xs, states)  # warm
+    t0 = time.perf_counter()
+    n, total = 0, 0
+    while time.perf_counter() - t0 < budget_s:
+        total += oracle_sample_step(workload, rows, xs, states)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(total / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"first {rows} rows of each op's tensor, {n} repetitions in {dt:.1f} s"}
+
+
+def run_reference(args):
+    import oracle
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    cfg, _ = workload_spec(args.workload)
+    rows = sample_rows_for(args.workload)
+    xs, states = oracle_inputs(args.workload, rows)
+    for _ in range(args.warmup):
+        oracle_sample_step(args.workload, rows, xs, states)
+    # bound the timed run to about two minutes of oracle work
+    t0 = time.perf_counter()
+    total, n = 0, 0
+    for _ in range(args.steps):
+        total += oracle_sample_step(args.workload, rows, xs, states)
+        n += 1
+        if time.perf_counter() - t0 > 120:
+            break
+    dt = time.perf_counter() - t0
+    value = total / dt / 1e9
+    cores = oracle.max_threads()
+    sample = f"first {rows} rows of each op's tensor per step, {n} of {args.steps} steps timed"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": n, "warmup": args.warmup, "ms_per_step": round(dt / n * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -72,6 +72,22 @@ FP8Q_API int32_t fp8q_version(void);
 FP8Q_API const char* fp8q_last_error_string(void);
 
 /*
+ * Synchronizes `stream`, then reports and clears device-side failures that
+ * earlier calls on this device recorded: FP8Q_ERR_TIMEOUT when a bounded
+ * wait inside a kernel (the MXFP8 pipeline's shared-memory barriers) gave
+ * up, in which case that call's outputs are incomplete.  FP8Q_OK otherwise.
+ */
+FP8Q_API fp8q_status fp8q_check_device(void* stream);
+
+/*
+ * Time budget of every bounded device-side wait, in nanoseconds (default
+ * 1e9), for kernels launched afterwards on the current device.  Waits never
+ * spin longer than this; a stalled pipeline ends its kernel and is reported
+ * by fp8q_check_device.
+ */
+FP8Q_API fp8q_status fp8q_set_wait_budget_ns(uint64_t ns);
+
+/*
  * amax_out[g] = max |x| over group g, bit-exact: the FP32 value whose bits
  * are the largest magnitude bits in the group (BF16 widened exactly), so a
  * NaN makes the result NaN and an empty group gives 0.

@@ -24,7 +24,7 @@ from ._build import LIB_PATH, build as _build_lib, is_stale
 __all__ = [
     "E4M3", "E5M2", "ROW", "COL", "BOTH", "build", "library_path", "lib",
     "fp8q_amax", "fp8q_cast_per_tensor", "fp8q_cast_workspace_bytes", "DelayedScaling",
-    "mxfp8_quantize", "mxfp8_col_blocks", "Fp8qError",
+    "mxfp8_quantize", "mxfp8_col_blocks", "Fp8qError", "check_device", "set_wait_budget_ns",
 ]
 
 E4M3 = 0
@@ -39,6 +39,8 @@ _P = _c.c_void_p
 _SIGS = {
     "fp8q_version": (_c.c_int32, []),
     "fp8q_last_error_string": (_c.c_char_p, []),
+    "fp8q_check_device": (_c.c_int, [_P]),
+    "fp8q_set_wait_budget_ns": (_c.c_int, [_c.c_uint64]),
     "fp8q_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _P, _P]),
     "fp8q_cast_workspace_bytes": (_c.c_size_t, [_c.c_int32]),
     "fp8q_cast_per_tensor": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32,
@@ -143,6 +145,15 @@ def _offsets(group_offsets, device):
     return o, o.numel() - 1
 
 
+def check_device():
+    """Synchronize the current stream and raise if a device-side wait gave up."""
+    _check(lib().fp8q_check_device(_stream()), "fp8q_check_device")
+
+
+def set_wait_budget_ns(ns: int):
+    _check(lib().fp8q_set_wait_budget_ns(int(ns)), "fp8q_set_wait_budget_ns")
+
+
 # ---------------------------------------------------------------------------
 # amax
 # ---------------------------------------------------------------------------
@@ -180,20 +191,30 @@ def _workspace(device, G: int, stream_id: int) -> torch.Tensor:
 
 def fp8q_cast_per_tensor(x: torch.Tensor, fmt: int = E4M3, margin: int = 0, scale_in=None,
                          group_offsets=None, want_amax: bool = True, want_sat: bool = False,
-                         q: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> dict:
+                         q: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                         out: dict | None = None) -> dict:
     """q = RNE_sat(fl32(x * scale)).  scale_in None: current scaling.
 
     Returns dict(q uint8 like x, amax, scale, scale_inv float32 [G], sat uint64 [G] or None).
+    `out` may hold preallocated "amax", "scale", "scale_inv", "sat" tensors.
     """
     _check_input(x)
     rows, cols = _as_2d(x)
     off, G = _offsets(group_offsets, x.device)
     dev = x.device
+    o = out or {}
+
+    def buf(name, dtype, wanted=True):
+        if not wanted:
+            return None
+        t = o.get(name)
+        return t if t is not None else torch.empty(G, dtype=dtype, device=dev)
+
     q = torch.empty(x.shape, dtype=torch.uint8, device=dev) if q is None else q
-    amax = torch.empty(G, dtype=torch.float32, device=dev) if want_amax else None
-    scale = torch.empty(G, dtype=torch.float32, device=dev)
-    scale_inv = torch.empty(G, dtype=torch.float32, device=dev)
-    sat = torch.empty(G, dtype=torch.int64, device=dev) if want_sat else None
+    amax = buf("amax", torch.float32, want_amax)
+    scale = buf("scale", torch.float32)
+    scale_inv = buf("scale_inv", torch.float32)
+    sat = buf("sat", torch.int64, want_sat)
     if scale_in is not None:
         if not isinstance(scale_in, torch.Tensor):
             scale_in = torch.tensor(scale_in, dtype=torch.float32)

@@ -99,6 +99,20 @@ int32_t fp8q_version(void) { return 10000; }
 
 const char* fp8q_last_error_string(void) { return g_err; }
 
+fp8q_status fp8q_check_device(void* stream) {
+  g_err[0] = 0;
+  unsigned word = 0;
+  fp8q_status r = mx_device_status((cudaStream_t)stream, true, &word);
+  if (r != FP8Q_OK) return r;
+  if (word & 1u) return fail(FP8Q_ERR_TIMEOUT, "a bounded device-side wait gave up; the outputs of that call are incomplete");
+  return FP8Q_OK;
+}
+
+fp8q_status fp8q_set_wait_budget_ns(uint64_t ns) {
+  g_err[0] = 0;
+  return mx_set_wait_budget((unsigned long long)ns);
+}
+
 fp8q_status fp8q_amax(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
                       int32_t num_groups, float* amax_out, void* stream) {
   g_err[0] = 0;

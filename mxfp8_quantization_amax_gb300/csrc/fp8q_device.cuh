@@ -71,6 +71,61 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
   asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w & 0x7FFF7FFFu));
   return r;
 }
+// max(|a|, |b|) per BF16 half, NaN-propagating; only the magnitude bits of
+// the result are meaningful (the sign is the xor of the operands' signs).
+__device__ __forceinline__ uint32_t absmax_nan_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Two FP32 products in one packed instruction (IEEE round to nearest, no FTZ).
+__device__ __forceinline__ void mul2(float& a, float& b, float sa, float sb) {
+  unsigned long long x, s, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(s) : "f"(sa), "f"(sb));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(s));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
+// L2 eviction policies for stores: streamed outputs leave L2 first, the
+// small scale arrays (written a few bytes at a time by many CTAs) stay until
+// their sectors are complete.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void st_u8_hint(void* p, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b8 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_u16_hint(void* p, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(p), "h"((unsigned short)v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_u32_hint(void* p, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_u64_hint(void* p, uint64_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(p), "l"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st32B_hint(void* p, const uint32_t (&d)[8], uint64_t pol) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(p),
+               "r"(d[0]), "r"(d[1]), "r"(d[2]), "r"(d[3]), "r"(d[4]), "r"(d[5]), "r"(d[6]), "r"(d[7]), "l"(pol)
+               : "memory");
+}
+
+// 32-byte store (one full sector) with no L1 allocation.
+__device__ __forceinline__ void st32B(void* p, const uint32_t (&d)[8]) {
+  asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(d[0]), "r"(d[1]),
+               "r"(d[2]), "r"(d[3]), "r"(d[4]), "r"(d[5]), "r"(d[6]), "r"(d[7])
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));

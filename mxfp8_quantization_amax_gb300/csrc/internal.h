@@ -75,4 +75,8 @@ fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const i
                       int fmt, int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                       uint8_t* s_col, int64_t s_col_ld, cudaStream_t stream);
 
+// Device failure word of the MXFP8 pipeline (synchronizes `stream`).
+fp8q_status mx_device_status(cudaStream_t stream, bool clear, unsigned* word);
+fp8q_status mx_set_wait_budget(unsigned long long ns);
+
 }  // namespace fp8q

@@ -7,38 +7,73 @@
 // rows and one along columns (transposed), both from the high-precision
 // tensor ("混合精度与 FP8 训练" 13.1: MX does not commute with transposes).
 //
-// Work unit: a tile of 32 rows x 256 columns.  The 32 rows are one
-// columnwise block: for ragged groups (MoE experts) tiles start at each
-// group's first row, the group's last tile may be shorter.  Each CTA
-// (128 threads, persistent over units) does, per tile:
-//   1. one 16-byte load per (row, 8 columns) from HBM into registers;
-//   2. rowwise pass in registers: 4 lanes own one 1x32 block, the block
-//      amax is a two-step shuffle, the E8M0 unit runs once per block, and
-//      8 codes go out as one 8-byte store;
-//   3. the raw tile goes to shared memory (row-major, 512 B per row, so row
-//      stores and the column reads below are bank-conflict free);
-//   4. columnwise pass: thread t owns columns 2t and 2t+1 and reads one
-//      32-bit word (both columns) per row, so a single packed u16x2 max
-//      gives both column amaxes; the 32 codes of each column are written
-//      as two 16-byte stores into the transposed output.
-// A shared-memory scan of the group sizes maps tile index -> (group, block).
+// Geometry.  A block is 32 rows x 256 columns; its 32 rows are one
+// columnwise MX block, so for ragged groups (MoE experts) blocks start at
+// each group's first row and a group's last block may be shorter.  A unit
+// is up to `super` consecutive blocks of one group in one 256-column strip.
+// A shared-memory scan of the group sizes maps unit index -> (group, block).
+//
+// BF16 (the training path): a persistent, warp-specialised kernel.  One
+// producer warp streams blocks into a ring of shared-memory stages with 2-D
+// TMA loads (four 64-column boxes per block, 128-byte swizzle), each stage
+// guarded by a "full" and an "empty" mbarrier; four consumer warps quantize:
+//   * rowwise: one lane per 1x32 block (four 16-byte shared loads, one
+//     E8M0 computation, one 32-byte store of the codes); the 8 lanes of a
+//     quarter-warp read 8 rows of one block, distinct bank groups after the
+//     swizzle;
+//   * columnwise: thread t owns columns 2t and 2t+1 and reads one 32-bit
+//     word (both columns) per row, so one packed abs-max gives both column
+//     amaxes; each column's 32 codes leave as one 32-byte store into the
+//     transposed output, and its scale bytes are gathered over the unit.
+// FP32 inputs take a simpler kernel: loads into registers, rowwise pass from
+// registers, the block staged in shared memory for the columnwise pass.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "fp8q_device.cuh"
 #include "internal.h"
+#include "tma.cuh"
+
+#ifndef FP8Q_MX_STAGES  // shared-memory ring depth (16 KB per stage)
+#define FP8Q_MX_STAGES 3
+#endif
+#ifndef FP8Q_MX_SUPER  // 32-row blocks per unit of the BF16 kernel
+#define FP8Q_MX_SUPER 4
+#endif
+#ifndef FP8Q_MX_SCOL_FLUSH  // scale bytes per s_col store (4 or 8)
+#define FP8Q_MX_SCOL_FLUSH 4
+#endif
+#ifndef FP8Q_MX_HINTS  // L2 evict-first data stores, evict-last scale stores
+#define FP8Q_MX_HINTS 1
+#endif
+#ifndef FP8Q_MX_SROW8  // one 8-byte s_row store per row and strip
+#define FP8Q_MX_SROW8 1
+#endif
 
 namespace fp8q {
 
-constexpr int kMxThreads = 128;
 constexpr int kTileRows = 32;
 constexpr int kTileCols = 256;
-constexpr int kRowSlots = kTileRows / (kMxThreads / 32);  // rows per warp in the rowwise pass
+constexpr int kConsumers = 128;  // 4 consumer warps
+constexpr int kStageBytes = kTileRows * kTileCols * 2;  // one BF16 block: 16 KB
+constexpr int kStages = FP8Q_MX_STAGES;
+constexpr int kTmaThreads = kConsumers + 32;  // + one producer warp
+constexpr int kSubCols = 64;                  // columns per TMA box (128 bytes)
+constexpr int kSubBytes = kTileRows * 128;    // one box in shared memory
+
+// Device-side failure word (bit 0: a bounded wait gave up) and the wait
+// budget in ns.  Read and cleared by fp8q_check_device().
+__device__ unsigned int g_mx_error;
+__device__ unsigned long long g_wait_budget_ns = 1000000000ull;
 
 struct MxParams {
   const void* x;
   int64_t rows, cols;
   const int64_t* off;  // device row offsets [G+1] or nullptr
   int G;
-  int64_t strips;       // ceil(cols / 256)
-  int64_t units;        // upper bound of tiles x strips
+  int64_t strips;  // ceil(cols / 256)
+  int super;       // blocks per unit
   uint8_t* q_row;
   uint8_t* s_row;
   uint8_t* q_col;
@@ -47,16 +82,170 @@ struct MxParams {
 };
 
 // Clamped group boundary: offsets outside [0, rows] are pulled back in, so
-// tiles never leave the tensor whatever the caller passes.
+// blocks never leave the tensor whatever the caller passes.
 __device__ __forceinline__ int64_t grp_row(const MxParams& p, int g) {
   if (p.off == nullptr) return g == 0 ? 0 : p.rows;
   int64_t v = __ldg(p.off + g);
   return v < 0 ? 0 : (v > p.rows ? p.rows : v);
 }
 
-// Write the first n (<= 32) bytes of d[0..7] to dst (any alignment).
-__device__ __forceinline__ void store_col32(uint8_t* dst, const uint32_t (&d)[8], int n) {
+// ---------------------------------------------------------------------------
+// Units and blocks
+// ---------------------------------------------------------------------------
+// blk[g] = sum_{h<g} ceil(n_h / 32), sup[g] = sum_{h<g} ceil(ceil(n_h / 32) / super),
+// for g = 0..G (block-wide scan; ends with __syncthreads).
+template <int NT>
+__device__ void build_prefix(const MxParams& p, int* blk, int* sup) {
+  __shared__ int tot_b[NT / 32], tot_s[NT / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (p.G + NT - 1) / NT;
+  const int g_lo = tid * per, g_hi = min(p.G, g_lo + per);
+  auto nblocks = [&](int g) {
+    const int64_t n = grp_row(p, g + 1) - grp_row(p, g);
+    return n > 0 ? (int)((n + 31) / 32) : 0;
+  };
+  int sb = 0, ss = 0;
+  for (int g = g_lo; g < g_hi; g++) {
+    const int nb = nblocks(g);
+    sb += nb;
+    ss += (nb + p.super - 1) / p.super;
+  }
+  int ib = sb, is = ss;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int vb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+    const int vs = __shfl_up_sync(0xFFFFFFFFu, is, o);
+    if (lane >= o) {
+      ib += vb;
+      is += vs;
+    }
+  }
+  if (lane == 31) {
+    tot_b[warp] = ib;
+    tot_s[warp] = is;
+  }
+  __syncthreads();
+  int bb = 0, bs = 0;
+  for (int w = 0; w < warp; w++) {
+    bb += tot_b[w];
+    bs += tot_s[w];
+  }
+  int rb = bb + ib - sb, rs = bs + is - ss;
+  for (int g = g_lo; g < g_hi; g++) {
+    blk[g] = rb;
+    sup[g] = rs;
+    const int nb = nblocks(g);
+    rb += nb;
+    rs += (nb + p.super - 1) / p.super;
+  }
+  if (tid == NT - 1) {
+    blk[p.G] = bb + ib;
+    sup[p.G] = bs + is;
+  }
+  __syncthreads();
+}
+
+struct Unit {
+  int g;
+  int nblk;          // blocks in this unit (1..super)
+  int64_t rg1;       // end row of the group
+  int64_t r_first;   // first row of the unit
+  int64_t gb0;       // s_col index of the unit's first block
+  int64_t c0;        // first column
+  int nc;            // columns in the strip (multiple of 32)
+};
+
+struct Tile {
+  int64_t r0;  // first row
+  int nr;      // rows of the block (1..32)
+  int64_t c0;
+  int nc;
+};
+
+__device__ __forceinline__ Unit unit_of(const MxParams& p, const int* blk, const int* sup, int64_t u) {
+  Unit t;
+  const int ti = (int)(u / p.strips);
+  t.c0 = (u - (int64_t)ti * p.strips) * kTileCols;
+  t.nc = (int)min((int64_t)kTileCols, p.cols - t.c0);
+  int lo = 0, hi = p.G;  // last g with sup[g] <= ti
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sup[mid] <= ti) lo = mid; else hi = mid;
+  }
+  t.g = lo;
+  const int b0 = p.super * (ti - sup[lo]);
+  t.nblk = min(p.super, blk[lo + 1] - blk[lo] - b0);
+  t.rg1 = grp_row(p, lo + 1);
+  t.r_first = grp_row(p, lo) + 32LL * b0;
+  t.gb0 = blk[lo] + b0;
+  return t;
+}
+
+__device__ __forceinline__ Tile block_of(const Unit& U, int j) {
+  Tile t;
+  t.r0 = U.r_first + 32LL * j;
+  t.nr = (int)min((int64_t)kTileRows, U.rg1 - t.r0);
+  t.c0 = U.c0;
+  t.nc = U.nc;
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// Stores
+// ---------------------------------------------------------------------------
+struct StorePolicy {
+  uint64_t data, scale;
+};
+
+__device__ __forceinline__ StorePolicy make_policy() {
+  StorePolicy sp{0, 0};
+#if FP8Q_MX_HINTS
+  sp.data = policy_evict_first();
+  sp.scale = policy_evict_last();
+#endif
+  return sp;
+}
+
+__device__ __forceinline__ void st_data32(void* p, const uint32_t (&d)[8], const StorePolicy& sp) {
+#if FP8Q_MX_HINTS
+  st32B_hint(p, d, sp.data);
+#else
+  (void)sp;
+  st32B(p, d);
+#endif
+}
+__device__ __forceinline__ void st_scale8(uint8_t* p, uint32_t v, const StorePolicy& sp) {
+#if FP8Q_MX_HINTS
+  st_u8_hint(p, v, sp.scale);
+#else
+  (void)sp;
+  *p = (uint8_t)v;
+#endif
+}
+__device__ __forceinline__ void st_scale32(uint8_t* p, uint32_t v, const StorePolicy& sp) {
+#if FP8Q_MX_HINTS
+  st_u32_hint(p, v, sp.scale);
+#else
+  (void)sp;
+  *(uint32_t*)p = v;
+#endif
+}
+__device__ __forceinline__ void st_scale64(uint8_t* p, uint64_t v, const StorePolicy& sp) {
+#if FP8Q_MX_HINTS
+  st_u64_hint(p, v, sp.scale);
+#else
+  (void)sp;
+  *(uint64_t*)p = v;
+#endif
+}
+
+// First n (<= 32) bytes of d[0..7] to dst, at any alignment.
+__device__ __forceinline__ void store_col32(uint8_t* dst, const uint32_t (&d)[8], int n, const StorePolicy& sp) {
   const uintptr_t a = (uintptr_t)dst;
+  if (n == 32 && (a & 31u) == 0) {
+    st_data32(dst, d, sp);
+    return;
+  }
   if (n == 32 && (a & 15u) == 0) {
     st_stream(dst, make_uint4(d[0], d[1], d[2], d[3]));
     st_stream(dst + 16, make_uint4(d[4], d[5], d[6], d[7]));
@@ -80,194 +269,365 @@ __device__ __forceinline__ void store_col32(uint8_t* dst, const uint32_t (&d)[8]
   }
 }
 
+// Scale bytes of column c for blocks gb0 .. gb0+n-1 (byte j of v).
+__device__ __forceinline__ void store_scales(const MxParams& p, int64_t c, int64_t gb0, int n, uint64_t v,
+                                             const StorePolicy& sp) {
+  uint8_t* dst = p.s_col + c * p.s_col_ld + gb0;
+  if (n == 8 && gb0 + 8 <= p.s_col_ld && ((uintptr_t)dst & 7u) == 0) {
+    st_scale64(dst, v, sp);
+    return;
+  }
+  if (n == 4 && gb0 + 4 <= p.s_col_ld && ((uintptr_t)dst & 3u) == 0) {
+    st_scale32(dst, (uint32_t)v, sp);
+    return;
+  }
+  for (int j = 0; j < n; j++)
+    if (gb0 + j < p.s_col_ld) st_scale8(dst + j, (uint32_t)(v >> (8 * j)), sp);
+}
+
+// ---------------------------------------------------------------------------
+// Element conversion
+// ---------------------------------------------------------------------------
+// The two BF16 values of word w scaled by (m_lo, m_hi) with one packed
+// multiply, as two floats ready for the packed conversion.
+__device__ __forceinline__ void scale_pair(uint32_t w, float m_lo, float m_hi, float& lo, float& hi) {
+  lo = bf16_lo(w);
+  hi = bf16_hi(w);
+  mul2(lo, hi, m_lo, m_hi);
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t row_codes4(uint32_t w0, uint32_t w1, float mult) {
+  float a, b, c, d;
+  scale_pair(w0, mult, mult, a, b);
+  scale_pair(w1, mult, mult, c, d);
+  return cvt4<FMT>(a, b, c, d);
+}
+
 template <int FMT>
 __device__ __forceinline__ uint32_t mx_codes4(float a, float b, float c, float d, float mult) {
   return cvt4<FMT>(__fmul_rn(a, mult), __fmul_rn(b, mult), __fmul_rn(c, mult), __fmul_rn(d, mult));
 }
 
-// Final code word for a block: NaN block -> 0x7F..., zero block -> 0.
+// Final code word of a block: Inf/NaN block -> 0x7F codes, zero block -> 0.
 __device__ __forceinline__ uint32_t mx_fix(uint32_t w, uint32_t byte, uint32_t amax_bits) {
   w = byte == 0xFFu ? 0x7F7F7F7Fu : w;
   return amax_bits == 0u ? 0u : w;
 }
 
-template <int DT, int FMT, int DIR>
-__global__ void __launch_bounds__(kMxThreads) mx_kernel(MxParams p) {
-  constexpr int kElt = DT == kBF16 ? 2 : 4;
-  constexpr int kRowBytes = kTileCols * kElt;
-  extern __shared__ __align__(16) unsigned char smem[];
-  unsigned char* tile = smem;                                      // [32][kRowBytes]
-  int* prefix = (int*)(smem + kTileRows * kRowBytes);              // [G + 1]
+// ---------------------------------------------------------------------------
+// BF16: TMA-fed, warp-specialised persistent kernel
+// ---------------------------------------------------------------------------
+// Stage layout: four 64-column boxes of 32 rows x 128 B, each written by one
+// TMA load with the 128-byte swizzle: 16-byte chunk c of row r sits at chunk
+// c ^ (r % 8).  Logical byte b of row r is therefore at
+//   (b / 128) * 4096 + r * 128 + (((b % 128) / 16) ^ (r % 8)) * 16 + b % 16.
+
+// Rowwise, one lane per 1x32 block: row r, block b (of the 8 in the strip).
+// Writes the 32 codes; returns the scale byte (0 if the block is not ours).
+template <int FMT>
+__device__ __forceinline__ uint32_t row_block_bf16(const MxParams& p, const Tile& t, const unsigned char* stage,
+                                                   int r, int b, const StorePolicy& sp) {
+  if (r >= t.nr || 32 * b >= t.nc) return 0u;
+  const unsigned char* line = stage + (b >> 1) * kSubBytes + r * 128;
+  const int c0 = (b & 1) * 4;
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+    const uint4 v = *(const uint4*)(line + (((c0 + j) ^ (r & 7)) << 4));
+    w[4 * j] = v.x;
+    w[4 * j + 1] = v.y;
+    w[4 * j + 2] = v.z;
+    w[4 * j + 3] = v.w;
+  }
+  uint32_t m4[4];
+#pragma unroll
+  for (int j = 0; j < 4; j++)
+    m4[j] = absmax_nan_bf16x2(absmax_nan_bf16x2(w[4 * j], w[4 * j + 1]), absmax_nan_bf16x2(w[4 * j + 2], w[4 * j + 3]));
+  const uint32_t m = absmax_nan_bf16x2(absmax_nan_bf16x2(m4[0], m4[1]), absmax_nan_bf16x2(m4[2], m4[3]));
+  const uint32_t am = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu) << 16;
+  const uint32_t byte = e8m0_from_amax<FMT>(am);
+  uint32_t d[8];
+  if (byte == 0xFFu || am == 0u) {  // Inf/NaN block: 0x7F codes; zero block: +0 codes
+    const uint32_t fill = am == 0u ? 0u : 0x7F7F7F7Fu;
+#pragma unroll
+    for (int k = 0; k < 8; k++) d[k] = fill;
+  } else {
+    const float mult = e8m0_multiplier(byte);
+#pragma unroll
+    for (int k = 0; k < 8; k++) d[k] = row_codes4<FMT>(w[2 * k], w[2 * k + 1], mult);
+  }
+  st_data32(p.q_row + (t.r0 + r) * p.cols + t.c0 + 32 * b, d, sp);
+  return byte;
+}
+
+// s_row bytes of one warp's 8 rows: lane l holds row 8w + l % 8, blocks
+// l / 8 (byte0) and 4 + l / 8 (byte1).  All 32 lanes must call.
+__device__ __forceinline__ void store_row_scales(const MxParams& p, const Tile& t, int warp, int lane,
+                                                 uint32_t byte0, uint32_t byte1, const StorePolicy& sp) {
+  const int r = 8 * warp + (lane & 7);
+  const int64_t sld = p.cols / 32;
+  uint8_t* dst = p.s_row + (t.r0 + r) * sld + t.c0 / 32;
+#if FP8Q_MX_SROW8
+  // gather the row's 8 bytes into lane r % 8 and store them at once
+  const uint32_t v = byte0 | (byte1 << 8);
+  const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 8);
+  const uint32_t v2 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 16);
+  const uint32_t v3 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 24);
+  if (r >= t.nr) return;
+  if (t.nc == kTileCols && ((uintptr_t)dst & 7u) == 0) {
+    if (lane < 8) {
+      const uint64_t lo = (v & 0xFFu) | ((v1 & 0xFFu) << 8) | ((v2 & 0xFFu) << 16) | ((v3 & 0xFFu) << 24);
+      const uint64_t hi = (v >> 8) | ((v1 >> 8) << 8) | ((v2 >> 8) << 16) | ((v3 >> 8) << 24);
+      st_scale64(dst, lo | (hi << 32), sp);
+    }
+    return;
+  }
+#endif
+  if (r < t.nr) {  // one byte per block
+    const int b = lane >> 3;
+    if (32 * b < t.nc) st_scale8(dst + b, byte0, sp);
+    if (32 * (b + 4) < t.nc) st_scale8(dst + b + 4, byte1, sp);
+  }
+}
+
+// Columnwise: thread t owns columns 2t, 2t+1 (one 32-bit word per row).
+// Returns the two scale bytes (column 2t in bits 0-7).
+template <int FMT>
+__device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Tile& t, const unsigned char* stage,
+                                                  int tid, const StorePolicy& sp) {
+  const unsigned char* seg = stage + (tid >> 5) * kSubBytes + 4 * (tid & 3);
+  const int c = (tid & 31) >> 2;  // 16-byte chunk of the word within the 128-byte line
+  uint32_t off[8];
+#pragma unroll
+  for (int k = 0; k < 8; k++) off[k] = (uint32_t)((c ^ k) << 4);
+  uint32_t w[kTileRows];
+  if (t.nr == kTileRows) {
+#pragma unroll
+    for (int r = 0; r < kTileRows; r++) w[r] = *(const uint32_t*)(seg + r * 128 + off[r & 7]);
+  } else {
+#pragma unroll
+    for (int r = 0; r < kTileRows; r++) w[r] = r < t.nr ? *(const uint32_t*)(seg + r * 128 + off[r & 7]) : 0u;
+  }
+  uint32_t m8[8];
+#pragma unroll
+  for (int k = 0; k < 8; k++)
+    m8[k] = absmax_nan_bf16x2(absmax_nan_bf16x2(w[4 * k], w[4 * k + 1]), absmax_nan_bf16x2(w[4 * k + 2], w[4 * k + 3]));
+  const uint32_t m = absmax_nan_bf16x2(absmax_nan_bf16x2(absmax_nan_bf16x2(m8[0], m8[1]), absmax_nan_bf16x2(m8[2], m8[3])),
+                                       absmax_nan_bf16x2(absmax_nan_bf16x2(m8[4], m8[5]), absmax_nan_bf16x2(m8[6], m8[7])));
+  const uint32_t a0 = (m & 0x7FFFu) << 16, a1 = m & 0x7FFF0000u;
+  const uint32_t b0 = e8m0_from_amax<FMT>(a0), b1 = e8m0_from_amax<FMT>(a1);
+  const float m0 = e8m0_multiplier(b0), m1 = e8m0_multiplier(b1);
+  uint32_t d0[8], d1[8];
+  if (b0 == 0xFFu || a0 == 0u || b1 == 0xFFu || a1 == 0u) {
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      float l[4], h[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) scale_pair(w[4 * k + i], m0, m1, l[i], h[i]);
+      d0[k] = mx_fix(cvt4<FMT>(l[0], l[1], l[2], l[3]), b0, a0);
+      d1[k] = mx_fix(cvt4<FMT>(h[0], h[1], h[2], h[3]), b1, a1);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      float l[4], h[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) scale_pair(w[4 * k + i], m0, m1, l[i], h[i]);
+      d0[k] = cvt4<FMT>(l[0], l[1], l[2], l[3]);
+      d1[k] = cvt4<FMT>(h[0], h[1], h[2], h[3]);
+    }
+  }
+  const int64_t col = t.c0 + 2 * tid;
+  store_col32(p.q_col + col * p.rows + t.r0, d0, t.nr, sp);
+  store_col32(p.q_col + (col + 1) * p.rows + t.r0, d1, t.nr, sp);
+  return b0 | (b1 << 8);
+}
+
+template <int FMT, int DIR>
+__global__ void __launch_bounds__(kTmaThreads, 4) mx_tma_kernel(const __grid_constant__ CUtensorMap tmap, MxParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t full[kStages], empty[kStages];
+  __shared__ volatile int abort_flag;
+  // stages start on a 1 KB boundary (required by the 128-byte swizzle)
+  unsigned char* stages = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  int* blk = (int*)(stages + kStages * kStageBytes);
+  int* sup = blk + (p.G + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // ---- tile index -> (group, block): exclusive scan of ceil(n_g / 32) ----
-  {
-    __shared__ int warp_tot[kMxThreads / 32];
-    const int per = (p.G + kMxThreads - 1) / kMxThreads;
-    const int g_lo = tid * per, g_hi = min(p.G, g_lo + per);
-    int sum = 0;
-    for (int g = g_lo; g < g_hi; g++) {
-      const int64_t n = grp_row(p, g + 1) - grp_row(p, g);
-      sum += n > 0 ? (int)((n + 31) / 32) : 0;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers / 32);
     }
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; w++) base += warp_tot[w];
-    int run = base + incl - sum;
-    for (int g = g_lo; g < g_hi; g++) {
-      prefix[g] = run;
-      const int64_t n = grp_row(p, g + 1) - grp_row(p, g);
-      run += n > 0 ? (int)((n + 31) / 32) : 0;
-    }
-    if (tid == kMxThreads - 1) prefix[p.G] = base + incl;
-    __syncthreads();
+    abort_flag = 0;
+    fence_barrier_init();
   }
-  const int total_tiles = prefix[p.G];
-  const int64_t units = (int64_t)total_tiles * p.strips;
-  const int64_t sblocks = p.cols / 32;
+  if (tid == kConsumers) prefetch_tensormap(&tmap);
+  build_prefix<kTmaThreads>(p, blk, sup);
+  const int64_t units = (int64_t)sup[p.G] * p.strips;
+  const uint64_t budget = g_wait_budget_ns;
+
+  if (warp == kConsumers / 32) {
+    // ---------------- producer ----------------
+    if (lane != 0) return;
+    int64_t k = 0;
+    for (int64_t u = blockIdx.x; u < units && !abort_flag; u += gridDim.x) {
+      const Unit U = unit_of(p, blk, sup, u);
+      for (int j = 0; j < U.nblk; j++, ++k) {
+        const int s = (int)(k % kStages);
+        const uint32_t round = (uint32_t)(k / kStages);
+        if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, budget)) {
+          atomicOr(&g_mx_error, 1u);
+          abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        unsigned char* dst = stages + s * kStageBytes;
+        const int row = (int)(U.r_first + 32 * j);
+#pragma unroll
+        for (int q = 0; q < kTileCols / kSubCols; q++)
+          tma_load_2d(dst + q * kSubBytes, &tmap, (int)U.c0 + q * kSubCols, row, &full[s]);
+      }
+    }
+    // every issued copy lands before the CTA can exit (fixed 2 s bound)
+    const int64_t first = k > kStages ? k - kStages : 0;
+    for (int64_t j = first; j < k; j++)
+      mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1), 2000000000ull);
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const StorePolicy sp = make_policy();
+  int64_t k = 0;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const Unit U = unit_of(p, blk, sup, u);
+    uint64_t sc0 = 0, sc1 = 0;  // scale bytes of this thread's two columns
+    for (int j = 0; j < U.nblk; j++, ++k) {
+      const int s = (int)(k % kStages);
+      const uint32_t round = (uint32_t)(k / kStages);
+      if (!mbar_wait(&full[s], round & 1u, budget)) {
+        atomicOr(&g_mx_error, 1u);
+        abort_flag = 1;
+        return;
+      }
+      const Tile t = block_of(U, j);
+      const unsigned char* stage = stages + s * kStageBytes;
+      if constexpr (DIR & MXFP8_ROW) {
+        const int r = 8 * warp + (lane & 7);
+        const uint32_t y0 = row_block_bf16<FMT>(p, t, stage, r, lane >> 3, sp);
+        const uint32_t y1 = row_block_bf16<FMT>(p, t, stage, r, 4 + (lane >> 3), sp);
+        store_row_scales(p, t, warp, lane, y0, y1, sp);
+      }
+      if constexpr (DIR & MXFP8_COL) {
+        if (2 * tid < t.nc) {
+          constexpr int F = FP8Q_MX_SCOL_FLUSH;
+          const uint32_t b = col_pair_bf16<FMT>(p, t, stage, tid, sp);
+          sc0 |= (uint64_t)(b & 0xFFu) << (8 * (j % F));
+          sc1 |= (uint64_t)(b >> 8) << (8 * (j % F));
+          if (j % F == F - 1 || j == U.nblk - 1) {
+            const int j0 = j - j % F;
+            store_scales(p, U.c0 + 2 * tid, U.gb0 + j0, j - j0 + 1, sc0, sp);
+            store_scales(p, U.c0 + 2 * tid + 1, U.gb0 + j0, j - j0 + 1, sc1, sp);
+            sc0 = sc1 = 0;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (abort_flag) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// FP32: loads into registers, rowwise from registers, columnwise via smem
+// ---------------------------------------------------------------------------
+template <int FMT, int DIR>
+__global__ void __launch_bounds__(kConsumers) mx_f32_kernel(MxParams p) {
+  constexpr int kRowBytes = kTileCols * 4;
+  constexpr int kRowSlots = kTileRows / (kConsumers / 32);
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* tile = smem;                           // [32][1024 B]
+  int* blk = (int*)(smem + kTileRows * kRowBytes);     // [G + 1]
+  int* sup = blk + (p.G + 1);                           // [G + 1] (super = 1)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const StorePolicy sp = make_policy();
+  build_prefix<kConsumers>(p, blk, sup);
+  const int64_t units = (int64_t)sup[p.G] * p.strips;
 
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    const int t = (int)(u / p.strips);
-    const int64_t c0 = (u - (int64_t)t * p.strips) * kTileCols;
-    const int nc = (int)min((int64_t)kTileCols, p.cols - c0);
-    // group of tile t: last g with prefix[g] <= t
-    int lo = 0, hi = p.G;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (prefix[mid] <= t) lo = mid; else hi = mid;
-    }
-    const int g = lo;
-    const int b = t - prefix[g];
-    const int64_t r0 = grp_row(p, g) + 32LL * b;
-    const int nr = (int)min((int64_t)kTileRows, grp_row(p, g + 1) - r0);
-
-    // ---- 1. loads: warp w covers rows w, w+4, ..; lane l covers 8 columns ----
-    const bool col_ok = lane * 8 < nc;
-    uint4 v[kRowSlots][kElt / 2];
+    const Unit U = unit_of(p, blk, sup, u);
+    const Tile t = block_of(U, 0);
+    const bool col_ok = lane * 8 < t.nc;
+    uint4 v[kRowSlots][2];
 #pragma unroll
     for (int i = 0; i < kRowSlots; i++) {
       const int r = warp + 4 * i;
-      const bool ok = col_ok && r < nr;
-      const char* src = (const char*)p.x + ((r0 + r) * p.cols + c0 + lane * 8) * kElt;
-#pragma unroll
-      for (int h = 0; h < kElt / 2; h++) v[i][h] = ok ? ld_stream(src + 16 * h) : make_uint4(0, 0, 0, 0);
+      const bool ok = col_ok && r < t.nr;
+      const char* src = (const char*)p.x + ((t.r0 + r) * p.cols + t.c0 + lane * 8) * 4;
+      v[i][0] = ok ? ld_stream(src) : make_uint4(0, 0, 0, 0);
+      v[i][1] = ok ? ld_stream(src + 16) : make_uint4(0, 0, 0, 0);
     }
-
-    // ---- 2. rowwise pass + 3. stage the tile ----
 #pragma unroll
     for (int i = 0; i < kRowSlots; i++) {
       const int r = warp + 4 * i;
       if constexpr (DIR & MXFP8_ROW) {
-        uint32_t am;
-        if constexpr (DT == kBF16) {
-          uint32_t m = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(0u, v[i][0].x), v[i][0].y),
-                                                   v[i][0].z), v[i][0].w);
-          am = max(m << 16, m & 0xFFFF0000u);
-        } else {
-          am = max(max(max(v[i][0].x & 0x7FFFFFFFu, v[i][0].y & 0x7FFFFFFFu),
-                       max(v[i][0].z & 0x7FFFFFFFu, v[i][0].w & 0x7FFFFFFFu)),
-                   max(max(v[i][1].x & 0x7FFFFFFFu, v[i][1].y & 0x7FFFFFFFu),
-                       max(v[i][1].z & 0x7FFFFFFFu, v[i][1].w & 0x7FFFFFFFu)));
-        }
+        uint32_t am = max(max(max(v[i][0].x & 0x7FFFFFFFu, v[i][0].y & 0x7FFFFFFFu),
+                              max(v[i][0].z & 0x7FFFFFFFu, v[i][0].w & 0x7FFFFFFFu)),
+                          max(max(v[i][1].x & 0x7FFFFFFFu, v[i][1].y & 0x7FFFFFFFu),
+                              max(v[i][1].z & 0x7FFFFFFFu, v[i][1].w & 0x7FFFFFFFu)));
         am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
         am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-        if (col_ok && r < nr) {
+        if (col_ok && r < t.nr) {
           const uint32_t byte = e8m0_from_amax<FMT>(am);
           const float mult = e8m0_multiplier(byte);
           uint2 o;
-          if constexpr (DT == kBF16) {
-            o.x = mx_codes4<FMT>(bf16_lo(v[i][0].x), bf16_hi(v[i][0].x), bf16_lo(v[i][0].y), bf16_hi(v[i][0].y), mult);
-            o.y = mx_codes4<FMT>(bf16_lo(v[i][0].z), bf16_hi(v[i][0].z), bf16_lo(v[i][0].w), bf16_hi(v[i][0].w), mult);
-          } else {
-            o.x = mx_codes4<FMT>(__uint_as_float(v[i][0].x), __uint_as_float(v[i][0].y),
-                                 __uint_as_float(v[i][0].z), __uint_as_float(v[i][0].w), mult);
-            o.y = mx_codes4<FMT>(__uint_as_float(v[i][1].x), __uint_as_float(v[i][1].y),
-                                 __uint_as_float(v[i][1].z), __uint_as_float(v[i][1].w), mult);
-          }
-          o.x = mx_fix(o.x, byte, am);
-          o.y = mx_fix(o.y, byte, am);
-          const int64_t row = r0 + r;
-          st_stream(p.q_row + row * p.cols + c0 + lane * 8, o);
-          if ((lane & 3) == 0) p.s_row[row * sblocks + (c0 + lane * 8) / 32] = (uint8_t)byte;
+          o.x = mx_fix(mx_codes4<FMT>(__uint_as_float(v[i][0].x), __uint_as_float(v[i][0].y),
+                                      __uint_as_float(v[i][0].z), __uint_as_float(v[i][0].w), mult), byte, am);
+          o.y = mx_fix(mx_codes4<FMT>(__uint_as_float(v[i][1].x), __uint_as_float(v[i][1].y),
+                                      __uint_as_float(v[i][1].z), __uint_as_float(v[i][1].w), mult), byte, am);
+          const int64_t row = t.r0 + r;
+          st_stream(p.q_row + row * p.cols + t.c0 + lane * 8, o);
+          if ((lane & 3) == 0) p.s_row[row * (p.cols / 32) + (t.c0 + lane * 8) / 32] = (uint8_t)byte;
         }
       }
       if constexpr (DIR & MXFP8_COL) {
-#pragma unroll
-        for (int h = 0; h < kElt / 2; h++)
-          *(uint4*)(tile + r * kRowBytes + lane * 8 * kElt + 16 * h) = v[i][h];
+        *(uint4*)(tile + r * kRowBytes + lane * 32) = v[i][0];
+        *(uint4*)(tile + r * kRowBytes + lane * 32 + 16) = v[i][1];
       }
     }
-
-    // ---- 4. columnwise pass ----
     if constexpr (DIR & MXFP8_COL) {
       __syncthreads();
-      const int cl = 2 * tid;  // this thread's first column within the tile
-      if (cl < nc) {
-        const int64_t gb = prefix[g] + b;  // block index within s_col rows
-        const int64_t c = c0 + cl;
+      const int cl = 2 * tid;
+      if (cl < t.nc) {
+        uint32_t a0 = 0, a1 = 0;
+#pragma unroll
+        for (int r = 0; r < kTileRows; r++) {
+          const uint2 w = *(const uint2*)(tile + r * kRowBytes + cl * 4);
+          a0 = max(a0, w.x & 0x7FFFFFFFu);
+          a1 = max(a1, w.y & 0x7FFFFFFFu);
+        }
+        const uint32_t b0 = e8m0_from_amax<FMT>(a0), b1 = e8m0_from_amax<FMT>(a1);
+        const float m0 = e8m0_multiplier(b0), m1 = e8m0_multiplier(b1);
         uint32_t d0[8], d1[8];
-        uint32_t a0, a1;
-        if constexpr (DT == kBF16) {
-          uint32_t w[kTileRows];
-          uint32_t m = 0;
 #pragma unroll
-          for (int r = 0; r < kTileRows; r++) {
-            w[r] = *(const uint32_t*)(tile + r * kRowBytes + cl * 2);
-            m = absmax_bf16x2(m, w[r]);
-          }
-          a0 = m << 16;
-          a1 = m & 0xFFFF0000u;
-          const uint32_t b0 = e8m0_from_amax<FMT>(a0), b1 = e8m0_from_amax<FMT>(a1);
-          const float m0 = e8m0_multiplier(b0), m1 = e8m0_multiplier(b1);
-#pragma unroll
-          for (int k = 0; k < 8; k++) {
-            d0[k] = mx_fix(mx_codes4<FMT>(bf16_lo(w[4 * k]), bf16_lo(w[4 * k + 1]), bf16_lo(w[4 * k + 2]),
-                                          bf16_lo(w[4 * k + 3]), m0), b0, a0);
-            d1[k] = mx_fix(mx_codes4<FMT>(bf16_hi(w[4 * k]), bf16_hi(w[4 * k + 1]), bf16_hi(w[4 * k + 2]),
-                                          bf16_hi(w[4 * k + 3]), m1), b1, a1);
-          }
-          store_col32(p.q_col + c * p.rows + r0, d0, nr);
-          if (cl + 1 < nc) store_col32(p.q_col + (c + 1) * p.rows + r0, d1, nr);
-          if (gb < p.s_col_ld) {
-            p.s_col[c * p.s_col_ld + gb] = (uint8_t)b0;
-            p.s_col[(c + 1) * p.s_col_ld + gb] = (uint8_t)b1;
-          }
-        } else {
-          a0 = 0;
-          a1 = 0;
-#pragma unroll
-          for (int r = 0; r < kTileRows; r++) {
-            const uint2 w = *(const uint2*)(tile + r * kRowBytes + cl * 4);
-            a0 = max(a0, w.x & 0x7FFFFFFFu);
-            a1 = max(a1, w.y & 0x7FFFFFFFu);
-          }
-          const uint32_t b0 = e8m0_from_amax<FMT>(a0), b1 = e8m0_from_amax<FMT>(a1);
-          const float m0 = e8m0_multiplier(b0), m1 = e8m0_multiplier(b1);
-#pragma unroll
-          for (int k = 0; k < 8; k++) {
-            uint2 w0 = *(const uint2*)(tile + (4 * k) * kRowBytes + cl * 4);
-            uint2 w1 = *(const uint2*)(tile + (4 * k + 1) * kRowBytes + cl * 4);
-            uint2 w2 = *(const uint2*)(tile + (4 * k + 2) * kRowBytes + cl * 4);
-            uint2 w3 = *(const uint2*)(tile + (4 * k + 3) * kRowBytes + cl * 4);
-            d0[k] = mx_fix(mx_codes4<FMT>(__uint_as_float(w0.x), __uint_as_float(w1.x), __uint_as_float(w2.x),
-                                          __uint_as_float(w3.x), m0), b0, a0);
-            d1[k] = mx_fix(mx_codes4<FMT>(__uint_as_float(w0.y), __uint_as_float(w1.y), __uint_as_float(w2.y),
-                                          __uint_as_float(w3.y), m1), b1, a1);
-          }
-          store_col32(p.q_col + c * p.rows + r0, d0, nr);
-          if (cl + 1 < nc) store_col32(p.q_col + (c + 1) * p.rows + r0, d1, nr);
-          if (gb < p.s_col_ld) {
-            p.s_col[c * p.s_col_ld + gb] = (uint8_t)b0;
-            p.s_col[(c + 1) * p.s_col_ld + gb] = (uint8_t)b1;
-          }
+        for (int k = 0; k < 8; k++) {
+          const uint2 w0 = *(const uint2*)(tile + (4 * k) * kRowBytes + cl * 4);
+          const uint2 w1 = *(const uint2*)(tile + (4 * k + 1) * kRowBytes + cl * 4);
+          const uint2 w2 = *(const uint2*)(tile + (4 * k + 2) * kRowBytes + cl * 4);
+          const uint2 w3 = *(const uint2*)(tile + (4 * k + 3) * kRowBytes + cl * 4);
+          d0[k] = mx_fix(mx_codes4<FMT>(__uint_as_float(w0.x), __uint_as_float(w1.x), __uint_as_float(w2.x),
+                                        __uint_as_float(w3.x), m0), b0, a0);
+          d1[k] = mx_fix(mx_codes4<FMT>(__uint_as_float(w0.y), __uint_as_float(w1.y), __uint_as_float(w2.y),
+                                        __uint_as_float(w3.y), m1), b1, a1);
+        }
+        const int64_t c = t.c0 + cl;
+        store_col32(p.q_col + c * p.rows + t.r0, d0, t.nr, sp);
+        store_col32(p.q_col + (c + 1) * p.rows + t.r0, d1, t.nr, sp);
+        if (U.gb0 < p.s_col_ld) {
+          p.s_col[c * p.s_col_ld + U.gb0] = (uint8_t)b0;
+          p.s_col[(c + 1) * p.s_col_ld + U.gb0] = (uint8_t)b1;
         }
       }
       __syncthreads();  // the tile is rewritten by the next unit
@@ -278,42 +638,102 @@ __global__ void __launch_bounds__(kMxThreads) mx_kernel(MxParams p) {
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-template <int DT, int FMT, int DIR>
-static fp8q_status launch_mx_t(const MxParams& p, cudaStream_t s) {
-  constexpr int kElt = DT == kBF16 ? 2 : 4;
-  const size_t smem = (size_t)kTileRows * kTileCols * kElt + sizeof(int) * (p.G + 1);
-  static int per_sm = -1;
-  static size_t attr_smem = 0;
-  if (smem > attr_smem) {
-    cudaError_t e = cudaFuncSetAttribute(mx_kernel<DT, FMT, DIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(mx_kernel)");
-    attr_smem = smem;
-    per_sm = -1;
-  }
-  if (per_sm < 0) {
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  });
+  return fn;
+}
+
+// Resident CTAs per SM for `kernel` with `smem` dynamic bytes (cached per
+// instantiation; recomputed when a call needs more shared memory).
+template <typename K>
+static fp8q_status ctas_per_sm(K kernel, int threads, size_t smem, size_t* attr, int* per_sm, std::mutex* mu,
+                               int* out) {
+  std::lock_guard<std::mutex> lock(*mu);
+  if (smem > *attr) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(mxfp8)");
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mx_kernel<DT, FMT, DIR>, kMxThreads, smem) != cudaSuccess || n < 1)
-      n = 1;
-    per_sm = n;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
+    *per_sm = n;
+    *attr = smem;
   }
+  *out = *per_sm;
+  return FP8Q_OK;
+}
+
+template <int FMT, int DIR>
+static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FP8Q_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  CUtensorMap map;
+  cuuint64_t dims[2] = {(cuuint64_t)p.cols, (cuuint64_t)p.rows};
+  cuuint64_t strides[1] = {(cuuint64_t)p.cols * 2};
+  cuuint32_t box[2] = {kSubCols, kTileRows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FP8Q_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  MxParams q = p;
+  q.super = FP8Q_MX_SUPER;
+  const size_t smem = 1024 + (size_t)kStages * kStageBytes + 2 * sizeof(int) * (p.G + 1);
+  static size_t attr = 0;
+  static int per_sm_cache = 0;
+  static std::mutex mu;
+  int per_sm = 0;
+  fp8q_status st = ctas_per_sm(mx_tma_kernel<FMT, DIR>, kTmaThreads, smem, &attr, &per_sm_cache, &mu, &per_sm);
+  if (st != FP8Q_OK) return st;
+  // units over any valid offsets: blocks per group rounded up to `super`
+  const int64_t max_units = ((p.rows + 31) / 32 / q.super + 1 + p.G) * p.strips;
   int64_t grid = (int64_t)per_sm * sm_count();
-  if (p.units < grid) grid = p.units;
+  if (max_units < grid) grid = max_units;
   if (grid < 1) grid = 1;
-  mx_kernel<DT, FMT, DIR><<<(unsigned)grid, kMxThreads, smem, s>>>(p);
-  return check_launch("mxfp8 kernel");
+  mx_tma_kernel<FMT, DIR><<<(unsigned)grid, kTmaThreads, smem, s>>>(map, q);
+  return check_launch("mxfp8 tma kernel");
 }
 
-template <int DT, int FMT>
-static fp8q_status launch_mx_dir(const MxParams& p, int dir, cudaStream_t s) {
-  if (dir == MXFP8_ROW) return launch_mx_t<DT, FMT, MXFP8_ROW>(p, s);
-  if (dir == MXFP8_COL) return launch_mx_t<DT, FMT, MXFP8_COL>(p, s);
-  return launch_mx_t<DT, FMT, MXFP8_BOTH>(p, s);
+template <int FMT, int DIR>
+static fp8q_status launch_f32(const MxParams& p, cudaStream_t s) {
+  MxParams q = p;
+  q.super = 1;
+  const size_t smem = (size_t)kTileRows * kTileCols * 4 + 2 * sizeof(int) * (p.G + 1);
+  static size_t attr = 0;
+  static int per_sm_cache = 0;
+  static std::mutex mu;
+  int per_sm = 0;
+  fp8q_status st = ctas_per_sm(mx_f32_kernel<FMT, DIR>, kConsumers, smem, &attr, &per_sm_cache, &mu, &per_sm);
+  if (st != FP8Q_OK) return st;
+  const int64_t max_units = ((p.rows + 31) / 32 + p.G) * p.strips;
+  int64_t grid = (int64_t)per_sm * sm_count();
+  if (max_units < grid) grid = max_units;
+  if (grid < 1) grid = 1;
+  mx_f32_kernel<FMT, DIR><<<(unsigned)grid, kConsumers, smem, s>>>(q);
+  return check_launch("mxfp8 fp32 kernel");
 }
 
-fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* off, int G,
-                      int fmt, int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
-                      int64_t s_col_ld, cudaStream_t stream) {
+template <int FMT>
+static fp8q_status launch_fmt(const MxParams& p, int dt, int dir, cudaStream_t s) {
+  if (dt == kBF16) {
+    if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW>(p, s);
+    if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL>(p, s);
+    return launch_tma<FMT, MXFP8_BOTH>(p, s);
+  }
+  if (dir == MXFP8_ROW) return launch_f32<FMT, MXFP8_ROW>(p, s);
+  if (dir == MXFP8_COL) return launch_f32<FMT, MXFP8_COL>(p, s);
+  return launch_f32<FMT, MXFP8_BOTH>(p, s);
+}
+
+fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* off, int G, int fmt,
+                      int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int64_t s_col_ld,
+                      cudaStream_t stream) {
   MxParams p{};
   p.x = x;
   p.rows = rows;
@@ -321,16 +741,33 @@ fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const i
   p.off = off;
   p.G = off ? G : 1;
   p.strips = (cols + kTileCols - 1) / kTileCols;
-  p.units = ((rows + 31) / 32 + p.G) * p.strips;
+  p.super = 1;
   p.q_row = q_row;
   p.s_row = s_row;
   p.q_col = q_col;
   p.s_col = s_col;
   p.s_col_ld = s_col_ld;
-  if (dt == kBF16) {
-    return fmt == kE4M3 ? launch_mx_dir<kBF16, kE4M3>(p, dir, stream) : launch_mx_dir<kBF16, kE5M2>(p, dir, stream);
+  return fmt == kE4M3 ? launch_fmt<kE4M3>(p, dt, dir, stream) : launch_fmt<kE5M2>(p, dt, dir, stream);
+}
+
+fp8q_status mx_device_status(cudaStream_t stream, bool clear, unsigned* word) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_mx_error, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+  if (clear && v) {
+    const unsigned z = 0;
+    e = cudaMemcpyToSymbol(g_mx_error, &z, sizeof(z));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
   }
-  return fmt == kE4M3 ? launch_mx_dir<kFP32, kE4M3>(p, dir, stream) : launch_mx_dir<kFP32, kE5M2>(p, dir, stream);
+  *word = v;
+  return FP8Q_OK;
+}
+
+fp8q_status mx_set_wait_budget(unsigned long long ns) {
+  cudaError_t e = cudaMemcpyToSymbol(g_wait_budget_ns, &ns, sizeof(ns));
+  return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, "cudaMemcpyToSymbol(wait budget)");
 }
 
 }  // namespace fp8q

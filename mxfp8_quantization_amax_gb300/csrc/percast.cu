@@ -340,9 +340,12 @@ __global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
   }
   if (cur_g >= 0) flush();
 
-  if (do_amax || do_sat) {
+  // The last CTA publishes per-group results and returns the scratch it used
+  // (accumulators, counters, the current-scaling scales) to zero.
+  if (do_amax || do_sat || p.src == kSrcWorkspace) {
     if (arrive_last(p.counter)) {
       for (int g = threadIdx.x; g < p.G; g += kPtThreads) {
+        if (p.src == kSrcWorkspace) p.ws_scale[g] = 0.0f;
         if (do_amax) {
           const uint32_t a = *(volatile unsigned*)(p.acc + g);
           if (p.amax_out) p.amax_out[g] = __uint_as_float(a);
