@@ -138,6 +138,31 @@ FP8Q_API fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t row
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fp8q_cast_per_tensor without a caller workspace.  The source pages have
+ * no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory where they quantize (a plugin inside a host
+ * application whose allocator owns all device memory, or a step where a
+ * cudaMalloc / cudaFree would synchronize the device).  It allocates
+ * nothing: the workspace is a fixed 8 KB array in the library's device
+ * memory, present on every GPU that loads the library until the process
+ * exits.
+ *   - Arguments and results are those of fp8q_cast_per_tensor, minus the
+ *     workspace; num_groups must be at most 256 (FP8Q_ERR_INVALID_ARG
+ *     otherwise).
+ *   - The first call on each device looks up the array's device address;
+ *     make that first call before any stream capture.
+ *   - All calls on a device share the array; each clears the part it uses
+ *     at its start (one cudaMemsetAsync on `stream`).  Calls whose work
+ *     may overlap on the GPU race on it: order them on one stream.
+ */
+FP8Q_API fp8q_status fp8q_cast_per_tensor_static_ws(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                                    const int64_t* group_offsets, int32_t num_groups,
+                                                    int32_t fmt, int32_t margin, const float* scale_in,
+                                                    uint8_t* q, float* amax_out, float* scale_out,
+                                                    float* scale_inv_out, unsigned long long* sat_count_out,
+                                                    void* stream);
+
+/*
  * Delayed scaling ("HiFloat8：高性能训练之路" 1.2 eqs. 3-4 and section 3;
  * "混合精度与 FP8 训练" 8.2): a library-owned state holds an amax history
  * ring of history_len entries.  Step t:

@@ -46,6 +46,8 @@ _SIGS = {
     "fp8q_cast_per_tensor": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32,
                                         _c.c_int32, _c.c_int32, _P, _P, _P, _P, _P, _P, _P,
                                         _c.c_size_t, _P]),
+    "fp8q_cast_per_tensor_static_ws": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32,
+                                                  _c.c_int32, _c.c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "fp8q_delayed_create": (_c.c_int, [_c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
                                        _c.POINTER(_P)]),
     "fp8q_delayed_destroy": (_c.c_int, [_P]),
