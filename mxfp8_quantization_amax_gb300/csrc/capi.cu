@@ -101,16 +101,19 @@ const char* fp8q_last_error_string(void) { return g_err; }
 
 fp8q_status fp8q_check_device(void* stream) {
   g_err[0] = 0;
-  unsigned word = 0;
-  fp8q_status r = mx_device_status((cudaStream_t)stream, true, &word);
+  unsigned mx = 0, pt = 0;
+  fp8q_status r = mx_device_status((cudaStream_t)stream, true, &mx);
   if (r != FP8Q_OK) return r;
-  if (word & 1u) return fail(FP8Q_ERR_TIMEOUT, "a bounded device-side wait gave up; the outputs of that call are incomplete");
+  if ((r = pt_device_status(true, &pt)) != FP8Q_OK) return r;
+  if ((mx | pt) & 1u)
+    return fail(FP8Q_ERR_TIMEOUT, "a bounded device-side wait gave up; the outputs of that call are incomplete");
   return FP8Q_OK;
 }
 
 fp8q_status fp8q_set_wait_budget_ns(uint64_t ns) {
   g_err[0] = 0;
-  return mx_set_wait_budget((unsigned long long)ns);
+  fp8q_status r = mx_set_wait_budget((unsigned long long)ns);
+  return r != FP8Q_OK ? r : pt_set_wait_budget((unsigned long long)ns);
 }
 
 fp8q_status fp8q_amax(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
@@ -177,15 +180,19 @@ fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t rows, int64_
   L.sat_out = sat_count_out;
   L.stream = (cudaStream_t)stream;
   if (scale_in == nullptr) {
-    // current scaling: amax pass (publishes scales), then the cast
+    // current scaling: amax pass (publishes scales), then the cast; a tensor
+    // that fits comfortably in L2 is kept there for the second pass
+    const bool keep = rows * cols * (dt == FP8Q_IN_BF16 ? 2 : 4) <= kL2KeepBytes;
     PtLaunch A = L;
     A.acc = ws.acc;
     A.amax_out = amax_out;
     A.scale_out = scale_out;
     A.scale_inv_out = scale_inv_out;
     A.sat_acc = nullptr;
+    A.l2_hint = keep ? 1 : 0;
     if ((r = launch_amax(A, true)) != FP8Q_OK) return r;
     L.src = kSrcWorkspace;
+    L.l2_hint = keep ? 2 : 0;
     return launch_cast(L);
   }
   L.src = kSrcGiven;

@@ -41,9 +41,31 @@ __device__ __forceinline__ uint32_t cvt2(float a, float b) {
 }
 
 // Four FP32 values -> four codes in one word (v0 in the low byte).
+#ifndef FP8Q_CVT4_MOV
+#define FP8Q_CVT4_MOV 0
+#endif
 template <int FMT>
 __device__ __forceinline__ uint32_t cvt4(float v0, float v1, float v2, float v3) {
+#if FP8Q_CVT4_MOV
+  uint32_t r;
+  if constexpr (FMT == kE4M3)
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  else
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  return r;
+#else
   return __byte_perm(cvt2<FMT>(v0, v1), cvt2<FMT>(v2, v3), 0x5410);
+#endif
 }
 
 // Every NaN code becomes 0x7F (positive, all mantissa bits set) in both
@@ -94,6 +116,17 @@ __device__ __forceinline__ void mul2(float& a, float& b, float sa, float sb) {
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// Emits nothing; marks v as rewritten here.  A run of volatile loads
+// followed by one of these per loaded vector keeps every load issued before
+// the first use of any of them, so a thread has all its loads in flight.
+__device__ __forceinline__ void reg_fence(uint4& v) {
+  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 __device__ __forceinline__ uint64_t policy_evict_last() {

@@ -60,8 +60,15 @@ struct PtLaunch {
   // non-finite one sets *flag
   float* hist_slot;
   unsigned* flag;
+  // L2 policy for reading x: 0 default, 1 keep (a second pass follows),
+  // 2 last use
+  int l2_hint;
   cudaStream_t stream;
 };
+
+// Tensors up to this size stay in L2 between the amax and the cast pass of
+// current scaling.
+constexpr int64_t kL2KeepBytes = 48ll << 20;
 
 // Amax pass.  finalize_scales: the last CTA turns acc[] into ws_scale[] and
 // the scale outputs, writes amax_out / hist_slot / flag and zeroes acc[].
@@ -75,8 +82,11 @@ fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const i
                       int fmt, int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                       uint8_t* s_col, int64_t s_col_ld, cudaStream_t stream);
 
-// Device failure word of the MXFP8 pipeline (synchronizes `stream`).
+// Device failure words of the MXFP8 pipeline (synchronizes `stream`) and
+// of the per-tensor pipeline, and their wait budgets.
 fp8q_status mx_device_status(cudaStream_t stream, bool clear, unsigned* word);
 fp8q_status mx_set_wait_budget(unsigned long long ns);
+fp8q_status pt_device_status(bool clear, unsigned* word);
+fp8q_status pt_set_wait_budget(unsigned long long ns);
 
 }  // namespace fp8q

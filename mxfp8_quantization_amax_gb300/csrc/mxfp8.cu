@@ -41,6 +41,9 @@
 #ifndef FP8Q_MX_SUPER  // 32-row blocks per unit of the BF16 kernel
 #define FP8Q_MX_SUPER 4
 #endif
+#ifndef FP8Q_MX_SUPER_GROUPED  // the same for grouped calls (fewer unit boundaries inside a group)
+#define FP8Q_MX_SUPER_GROUPED 16
+#endif
 #ifndef FP8Q_MX_SCOL_FLUSH  // scale bytes per s_col store (4 or 8)
 #define FP8Q_MX_SCOL_FLUSH 4
 #endif
@@ -259,13 +262,95 @@ __device__ __forceinline__ void store_col32(uint8_t* dst, const uint32_t (&d)[8]
     const uint32_t hi = k < 8 ? d[k] : 0u;
     const uint32_t w = mis ? __funnelshift_r(lo, hi, 8 * (4 - mis)) : hi;
     const int s = 4 * k - mis;  // index of this word's first byte in the column run
+    // partial sectors are completed by another unit: keep them in L2 until then
     if (s >= 0 && s + 4 <= n) {
-      *(uint32_t*)(base + 4 * k) = w;
+      st_scale32(base + 4 * k, w, sp);
     } else {
 #pragma unroll
       for (int i = 0; i < 4; i++)
-        if (s + i >= 0 && s + i < n) base[4 * k + i] = (uint8_t)(w >> (8 * i));
+        if (s + i >= 0 && s + i < n) st_scale8(base + 4 * k + i, w >> (8 * i), sp);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Byte ranges of an aligned window as naturally aligned chunks.  The range
+// bounds are compile-time, so every chunk reads registers at static
+// indices; run-time bounds dispatch through a switch (they are the same for
+// every column of a unit, so the branch is uniform).
+// ---------------------------------------------------------------------------
+template <int POS, int SZ>
+__device__ __forceinline__ void store_chunk(uint8_t* base, const uint32_t (&o)[8], uint64_t pol) {
+  uint8_t* p = base + POS;
+  if constexpr (SZ == 16) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(o[POS / 4]),
+                 "r"(o[POS / 4 + 1]), "r"(o[POS / 4 + 2]), "r"(o[POS / 4 + 3]), "l"(pol)
+                 : "memory");
+  } else if constexpr (SZ == 8) {
+    asm volatile("st.global.L2::cache_hint.v2.b32 [%0], {%1,%2}, %3;" ::"l"(p), "r"(o[POS / 4]), "r"(o[POS / 4 + 1]),
+                 "l"(pol)
+                 : "memory");
+  } else if constexpr (SZ == 4) {
+    st_u32_hint(p, o[POS / 4], pol);
+  } else if constexpr (SZ == 2) {
+    st_u16_hint(p, o[POS / 4] >> (8 * (POS % 4)), pol);
+  } else {
+    st_u8_hint(p, o[POS / 4] >> (8 * (POS % 4)), pol);
+  }
+}
+
+__host__ __device__ constexpr int chunk_for(int from, int to) {
+  int sz = 16;
+  while (sz > 1 && (from % sz != 0 || from + sz > to)) sz >>= 1;
+  return sz;
+}
+
+template <int FROM, int TO>
+__device__ __forceinline__ void store_range(uint8_t* base, const uint32_t (&o)[8], uint64_t pol) {
+  if constexpr (FROM < TO) {
+    constexpr int SZ = chunk_for(FROM, TO);
+    store_chunk<FROM, SZ>(base, o, pol);
+    store_range<FROM + SZ, TO>(base, o, pol);
+  }
+}
+
+// bytes [from, 32) of the 32-byte aligned window at base (from in 1..31)
+template <int F = 1>
+__device__ __forceinline__ void store_suffix32(uint8_t* base, const uint32_t (&o)[8], int from, uint64_t pol) {
+  if constexpr (F < 32) {
+    if (from == F) store_range<F, 32>(base, o, pol);
+    else store_suffix32<F + 1>(base, o, from, pol);
+  }
+}
+// bytes [0, to) of the 32-byte aligned window at base (to in 1..31)
+template <int T = 1>
+__device__ __forceinline__ void store_prefix32(uint8_t* base, const uint32_t (&o)[8], int to, uint64_t pol) {
+  if constexpr (T < 32) {
+    if (to == T) store_range<0, T>(base, o, pol);
+    else store_prefix32<T + 1>(base, o, to, pol);
+  }
+}
+// bytes [from, 8) of the 8-byte aligned window at base (from in 0..7)
+template <int F = 0>
+__device__ __forceinline__ void store_suffix8(uint8_t* base, const uint32_t (&o)[8], int from, uint64_t pol) {
+  if constexpr (F < 8) {
+    if (from == F) store_range<F, 8>(base, o, pol);
+    else store_suffix8<F + 1>(base, o, from, pol);
+  }
+}
+// bytes [from, to) of the 8-byte aligned window at base (0 <= from < to <= 8)
+template <int F, int T = F + 1>
+__device__ __forceinline__ void store_range8_to(uint8_t* base, const uint32_t (&o)[8], int to, uint64_t pol) {
+  if constexpr (T <= 8) {
+    if (to == T) store_range<F, T>(base, o, pol);
+    else store_range8_to<F, T + 1>(base, o, to, pol);
+  }
+}
+template <int F = 0>
+__device__ __forceinline__ void store_range8(uint8_t* base, const uint32_t (&o)[8], int from, int to, uint64_t pol) {
+  if constexpr (F < 8) {
+    if (from == F) store_range8_to<F>(base, o, to, pol);
+    else store_range8<F + 1>(base, o, from, to, pol);
   }
 }
 
@@ -285,15 +370,34 @@ __device__ __forceinline__ void store_scales(const MxParams& p, int64_t c, int64
     if (gb0 + j < p.s_col_ld) st_scale8(dst + j, (uint32_t)(v >> (8 * j)), sp);
 }
 
+// Scale bytes [from, to) of the 8-byte aligned window at `win`, whose first
+// byte is s_col block index `gbw` of its column (blocks past s_col_ld are
+// not written).
+__device__ __forceinline__ void flush_scales8(const MxParams& p, uint8_t* win, int from, int to, int64_t gbw,
+                                              uint64_t v, const StorePolicy& sp) {
+  if (gbw + to > p.s_col_ld) to = (int)(p.s_col_ld - gbw);
+  if (from >= to) return;
+  const uint32_t o[8] = {(uint32_t)v, (uint32_t)(v >> 32), 0, 0, 0, 0, 0, 0};
+  store_range8(win, o, from, to, sp.scale);
+}
+
 // ---------------------------------------------------------------------------
 // Element conversion
 // ---------------------------------------------------------------------------
 // The two BF16 values of word w scaled by (m_lo, m_hi) with one packed
 // multiply, as two floats ready for the packed conversion.
+#ifndef FP8Q_MX_MUL2  // packed f32x2 multiply (1) or two scalar multiplies (0)
+#define FP8Q_MX_MUL2 1
+#endif
 __device__ __forceinline__ void scale_pair(uint32_t w, float m_lo, float m_hi, float& lo, float& hi) {
+#if FP8Q_MX_MUL2
   lo = bf16_lo(w);
   hi = bf16_hi(w);
   mul2(lo, hi, m_lo, m_hi);
+#else
+  lo = __fmul_rn(bf16_lo(w), m_lo);
+  hi = __fmul_rn(bf16_hi(w), m_hi);
+#endif
 }
 
 template <int FMT>
@@ -391,11 +495,77 @@ __device__ __forceinline__ void store_row_scales(const MxParams& p, const Tile& 
   }
 }
 
+// The 32 bytes starting `off` bytes into the 64-byte concatenation a ++ b
+// (0 < off < 32), for an offset known only at run time.
+__device__ __forceinline__ void window32(const uint32_t (&a)[8], const uint32_t (&b)[8], int off, uint32_t (&o)[8]) {
+  const int sh = 8 * (off & 3);
+  uint32_t c[16];
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    c[i] = a[i];
+    c[8 + i] = b[i];
+  }
+  switch (off >> 2) {  // whole words; each case indexes registers statically
+#define FP8Q_WINDOW_CASE(Q)                                                           \
+  case Q:                                                                             \
+    _Pragma("unroll") for (int i = 0; i < 8; i++) o[i] =                              \
+        sh ? __funnelshift_r(c[Q + i], (Q + i + 1 < 16 ? c[Q + i + 1] : 0u), sh) : c[Q + i]; \
+    break;
+    FP8Q_WINDOW_CASE(0)
+    FP8Q_WINDOW_CASE(1)
+    FP8Q_WINDOW_CASE(2)
+    FP8Q_WINDOW_CASE(3)
+    FP8Q_WINDOW_CASE(4)
+    FP8Q_WINDOW_CASE(5)
+    FP8Q_WINDOW_CASE(6)
+    default:
+    FP8Q_WINDOW_CASE(7)
+#undef FP8Q_WINDOW_CASE
+  }
+}
+
+// Columnwise output of one column, block j of a unit whose codes form one
+// run of `len` bytes starting at `run` (any alignment).  Every block of the
+// run has the same offset `mis` inside its 32-byte sector, so after block j
+// the sector holding the tail of block j-1 and the head of block j is
+// complete and leaves with one 32-byte store; only the two ends of the run
+// are partial.  `prev` carries block j-1's codes.
+__device__ __forceinline__ void emit_col_block(uint8_t* run, int len, int j, int nblk, const uint32_t (&d)[8],
+                                               uint32_t (&prev)[8], const StorePolicy& sp) {
+  const int mis = (int)((uintptr_t)run & 31u);
+  const int lo = 32 * j;  // run bytes of this block: [lo, lo + 32)
+  if (mis == 0) {
+    store_col32(run + lo, d, min(32, len - lo), sp);
+    return;
+  }
+  const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (j == 0) {
+    // head: run bytes [0, 32 - mis) fill window bytes [mis, 32) of the first sector
+    uint32_t o[8];
+    window32(z, d, 32 - mis, o);
+    if (len >= 32 - mis) store_suffix32(run - mis, o, mis, sp.scale);
+    else store_col32(run, d, len, sp);  // the whole run ends inside the first sector
+  } else {
+    uint32_t o[8];
+    window32(prev, d, 32 - mis, o);  // run bytes [lo - mis, lo + 32 - mis)
+    store_col32(run + lo - mis, o, min(32, len - (lo - mis)), sp);
+  }
+  if (j == nblk - 1 && len > lo + 32 - mis) {  // tail after the last sector boundary
+    uint32_t o[8];
+    window32(d, z, 32 - mis, o);
+    const int n = len - (lo + 32 - mis);  // 1 .. mis bytes
+    store_prefix32(run + lo + 32 - mis, o, n, sp.scale);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i++) prev[i] = d[i];
+}
+
 // Columnwise: thread t owns columns 2t, 2t+1 (one 32-bit word per row).
 // Returns the two scale bytes (column 2t in bits 0-7).
 template <int FMT>
-__device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Tile& t, const unsigned char* stage,
-                                                  int tid, const StorePolicy& sp) {
+__device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit& U, const Tile& t,
+                                                  const unsigned char* stage, int tid, const StorePolicy& sp, int j,
+                                                  uint32_t (&prev0)[8], uint32_t (&prev1)[8]) {
   const unsigned char* seg = stage + (tid >> 5) * kSubBytes + 4 * (tid & 3);
   const int c = (tid & 31) >> 2;  // 16-byte chunk of the word within the 128-byte line
   uint32_t off[8];
@@ -439,8 +609,9 @@ __device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Tile&
     }
   }
   const int64_t col = t.c0 + 2 * tid;
-  store_col32(p.q_col + col * p.rows + t.r0, d0, t.nr, sp);
-  store_col32(p.q_col + (col + 1) * p.rows + t.r0, d1, t.nr, sp);
+  const int len = (int)min((int64_t)(32 * U.nblk), U.rg1 - U.r_first);
+  emit_col_block(p.q_col + col * p.rows + U.r_first, len, j, U.nblk, d0, prev0, sp);
+  emit_col_block(p.q_col + (col + 1) * p.rows + U.r_first, len, j, U.nblk, d1, prev1, sp);
   return b0 | (b1 << 8);
 }
 
@@ -503,13 +674,17 @@ __global__ void __launch_bounds__(kTmaThreads, 4) mx_tma_kernel(const __grid_con
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const Unit U = unit_of(p, blk, sup, u);
     uint64_t sc0 = 0, sc1 = 0;  // scale bytes of this thread's two columns
+    uint32_t prev0[8], prev1[8];  // previous block's column codes (sector carry)
+    bool gave_up = false;
     for (int j = 0; j < U.nblk; j++, ++k) {
       const int s = (int)(k % kStages);
       const uint32_t round = (uint32_t)(k / kStages);
-      if (!mbar_wait(&full[s], round & 1u, budget)) {
+      // every lane waits; the warp acts on one voted answer so it never splits
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], round & 1u, budget))) {
         atomicOr(&g_mx_error, 1u);
         abort_flag = 1;
-        return;
+        gave_up = true;
+        break;
       }
       const Tile t = block_of(U, j);
       const unsigned char* stage = stages + s * kStageBytes;
@@ -521,22 +696,32 @@ __global__ void __launch_bounds__(kTmaThreads, 4) mx_tma_kernel(const __grid_con
       }
       if constexpr (DIR & MXFP8_COL) {
         if (2 * tid < t.nc) {
-          constexpr int F = FP8Q_MX_SCOL_FLUSH;
-          const uint32_t b = col_pair_bf16<FMT>(p, t, stage, tid, sp);
-          sc0 |= (uint64_t)(b & 0xFFu) << (8 * (j % F));
-          sc1 |= (uint64_t)(b >> 8) << (8 * (j % F));
-          if (j % F == F - 1 || j == U.nblk - 1) {
-            const int j0 = j - j % F;
-            store_scales(p, U.c0 + 2 * tid, U.gb0 + j0, j - j0 + 1, sc0, sp);
-            store_scales(p, U.c0 + 2 * tid + 1, U.gb0 + j0, j - j0 + 1, sc1, sp);
-            sc0 = sc1 = 0;
+          const uint32_t b = col_pair_bf16<FMT>(p, U, t, stage, tid, sp, j, prev0, prev1);
+          // scale bytes go to s_col[c][gb0 + j]; they are gathered in the
+          // 8-byte aligned window of the destination and leave when the
+          // window is complete or the unit ends
+          uint8_t* d0 = p.s_col + (U.c0 + 2 * tid) * p.s_col_ld + U.gb0 + j;
+          uint8_t* d1 = d0 + p.s_col_ld;
+          const int q0 = (int)((uintptr_t)d0 & 7u), q1 = (int)((uintptr_t)d1 & 7u);
+          sc0 |= (uint64_t)(b & 0xFFu) << (8 * q0);
+          sc1 |= (uint64_t)(b >> 8) << (8 * q1);
+          const bool last = j == U.nblk - 1;
+          if (q0 == 7 || last) {
+            const int from = j < q0 ? q0 - j : 0;  // window bytes before the unit's first block
+            flush_scales8(p, d0 - q0, from, q0 + 1, U.gb0 + j - q0, sc0, sp);
+            sc0 = 0;
+          }
+          if (q1 == 7 || last) {
+            const int from = j < q1 ? q1 - j : 0;
+            flush_scales8(p, d1 - q1, from, q1 + 1, U.gb0 + j - q1, sc1, sp);
+            sc1 = 0;
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    if (abort_flag) return;
+    if (gave_up || abort_flag) return;
   }
 }
 
@@ -683,7 +868,7 @@ static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FP8Q_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   MxParams q = p;
-  q.super = FP8Q_MX_SUPER;
+  q.super = p.off != nullptr ? FP8Q_MX_SUPER_GROUPED : FP8Q_MX_SUPER;
   const size_t smem = 1024 + (size_t)kStages * kStageBytes + 2 * sizeof(int) * (p.G + 1);
   static size_t attr = 0;
   static int per_sm_cache = 0;

@@ -22,21 +22,29 @@
 namespace fp8q {
 
 constexpr int kPtThreads = 256;
-constexpr int kChunk = 8192;  // elements per chunk: 32 per thread
+#ifndef FP8Q_PT_VECS
+#define FP8Q_PT_VECS 8
+#endif
+constexpr int kVecs = FP8Q_PT_VECS;  // 16-byte vectors per thread per chunk (bytes in flight per thread / 16)
 
 template <int DT> struct InT;
 template <> struct InT<kBF16> {
   static constexpr int kPerVec = 8;  // elements per 16-byte vector
+  static constexpr int kChunk = kPtThreads * kVecs * kPerVec;  // elements per chunk
   static __device__ __forceinline__ uint32_t bits(const void* x, int64_t i) {
     return (uint32_t)__ldg((const unsigned short*)x + i) << 16;
   }
 };
 template <> struct InT<kFP32> {
   static constexpr int kPerVec = 4;
+  static constexpr int kChunk = kPtThreads * kVecs * kPerVec;
   static __device__ __forceinline__ uint32_t bits(const void* x, int64_t i) {
     return __ldg((const unsigned*)x + i);
   }
 };
+
+// The kernels in this file wait on nothing; their failure word stays zero.
+__device__ unsigned int g_pt_error;
 
 struct KParams {
   const void* x;
@@ -61,7 +69,23 @@ struct KParams {
   unsigned long long* sat_out;
   float* hist_slot;
   unsigned* flag;
+  int l2_hint;  // 0: default, 1: keep the input in L2 (a second pass follows), 2: last use
 };
+
+// 16-byte read-only load with an L2 eviction policy (createpolicy value).
+__device__ __forceinline__ uint4 ld_hint(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
+__device__ __forceinline__ uint64_t load_policy(int hint) {
+  if (hint == 1) return policy_evict_last();
+  if (hint == 2) return policy_evict_first();
+  return policy_evict_normal();
+}
 
 __device__ __forceinline__ int group_of_elem(const KParams& p, int64_t e) {
   if (p.off == nullptr || p.G <= 1) return 0;
@@ -111,6 +135,7 @@ __global__ void __launch_bounds__(kPtThreads) amax_kernel(KParams p) {
   __shared__ uint32_t sh_max[kPtThreads / 32];
   const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
   const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
+  const uint64_t pol = load_policy(p.l2_hint);
   int cur_g = -1;
   uint32_t cur = 0;
 
@@ -121,20 +146,22 @@ __global__ void __launch_bounds__(kPtThreads) amax_kernel(KParams p) {
   };
 
   for (int64_t c = c_begin; c < c_end; ++c) {
-    const int64_t e0 = c * kChunk;
-    const int64_t e1 = min(e0 + (int64_t)kChunk, p.n);
+    const int64_t e0 = c * InT<DT>::kChunk;
+    const int64_t e1 = min(e0 + (int64_t)InT<DT>::kChunk, p.n);
     const int g0 = group_of_elem(p, e0), g1 = group_of_elem(p, e1 - 1);
     if (g0 == g1) {
       if (g0 != cur_g) {
         if (cur_g >= 0) flush();
         cur_g = g0;
       }
-      if (e1 - e0 == kChunk) {
-        constexpr int V = kChunk / InT<DT>::kPerVec / kPtThreads;
+      if (e1 - e0 == InT<DT>::kChunk) {
+        constexpr int V = kVecs;
         uint4 v[V];
 #pragma unroll
         for (int k = 0; k < V; k++)
-          v[k] = ld_stream((const char*)p.x + (e0 + (int64_t)(k * kPtThreads + threadIdx.x) * InT<DT>::kPerVec) * (DT == kBF16 ? 2 : 4));
+          v[k] = ld_hint((const char*)p.x + (e0 + (int64_t)(k * kPtThreads + threadIdx.x) * InT<DT>::kPerVec) * (DT == kBF16 ? 2 : 4), pol);
+#pragma unroll
+        for (int k = 0; k < V; k++) reg_fence(v[k]);
         if constexpr (DT == kBF16) {
           uint32_t m = 0;
 #pragma unroll
@@ -229,6 +256,7 @@ __global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
 
   const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
   const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
+  const uint64_t pol = load_policy(p.l2_hint);
   int cur_g = -1;
   uint32_t cur = 0;
   unsigned long long nsat = 0;
@@ -247,8 +275,8 @@ __global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
   };
 
   for (int64_t c = c_begin; c < c_end; ++c) {
-    const int64_t e0 = c * kChunk;
-    const int64_t e1 = min(e0 + (int64_t)kChunk, p.n);
+    const int64_t e0 = c * InT<DT>::kChunk;
+    const int64_t e1 = min(e0 + (int64_t)InT<DT>::kChunk, p.n);
     const int g0 = group_of_elem(p, e0), g1 = group_of_elem(p, e1 - 1);
     if (g0 == g1) {
       if (g0 != cur_g) {
@@ -256,13 +284,15 @@ __global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
         cur_g = g0;
       }
       const float s = group_scale(p, g0, hist_scale);
-      if (e1 - e0 == kChunk) {
+      if (e1 - e0 == InT<DT>::kChunk) {
         constexpr int PV = InT<DT>::kPerVec;
-        constexpr int V = kChunk / PV / kPtThreads;
+        constexpr int V = kVecs;
         uint4 v[V];
 #pragma unroll
         for (int k = 0; k < V; k++)
-          v[k] = ld_stream((const char*)p.x + (e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV) * (DT == kBF16 ? 2 : 4));
+          v[k] = ld_hint((const char*)p.x + (e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV) * (DT == kBF16 ? 2 : 4), pol);
+#pragma unroll
+        for (int k = 0; k < V; k++) reg_fence(v[k]);
 #pragma unroll
         for (int k = 0; k < V; k++) {
           const int64_t e = e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV;
@@ -377,7 +407,8 @@ static KParams make_params(const PtLaunch& L) {
   p.n = L.rows * L.cols;
   p.off = L.off;
   p.G = L.G;
-  p.n_chunks = (p.n + kChunk - 1) / kChunk;
+  const int64_t chunk = L.dt == kBF16 ? InT<kBF16>::kChunk : InT<kFP32>::kChunk;
+  p.n_chunks = (p.n + chunk - 1) / chunk;
   p.f8max = fmt_max(L.fmt);
   p.margin = L.margin;
   p.src = L.src;
@@ -395,6 +426,7 @@ static KParams make_params(const PtLaunch& L) {
   p.sat_out = L.sat_out;
   p.hist_slot = L.hist_slot;
   p.flag = L.flag;
+  p.l2_hint = L.l2_hint;
   return p;
 }
 
@@ -451,5 +483,20 @@ fp8q_status launch_cast(const PtLaunch& L) {
   }
   return check_launch("cast kernel");
 }
+
+fp8q_status pt_device_status(bool clear, unsigned* word) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_pt_error, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+  if (clear && v) {
+    const unsigned z = 0;
+    e = cudaMemcpyToSymbol(g_pt_error, &z, sizeof(z));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+  }
+  *word = v;
+  return FP8Q_OK;
+}
+
+fp8q_status pt_set_wait_budget(unsigned long long) { return FP8Q_OK; }
 
 }  // namespace fp8q
