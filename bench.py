@@ -182,21 +182,52 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_traffic(peak_key):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel
-    source it was taken from is unchanged."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+MX_SOURCES = ("mxfp8_quantization_amax_gb300/csrc/mxfp8.cu", "mxfp8_quantization_amax_gb300/csrc/fp8q_device.cuh",
+              "mxfp8_quantization_amax_gb300/csrc/tma.cuh", "mxfp8_quantization_amax_gb300/csrc/internal.h")
+
+
+def sources_sha(paths=MX_SOURCES):
+    """First 16 hex digits of the sha256 of the kernel's source files, in order."""
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(workload):
+    """DRAM bytes per launch of the MXFP8 kernel from the committed ncu
+    summary (profiles/traffic.txt: one `key=value ...` line per workload),
+    or None if there is none or the kernel's sources changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
-            d = json.load(f)[peak_key]
-    except (OSError, KeyError, ValueError):
-        return None
-    src = os.path.join(ROOT, d["source"])
-    try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            lines = [ln.split() for ln in f if ln.startswith("workload=")]
+        sha = sources_sha()
     except OSError:
         return None
-    return d["bytes_per_launch"] if h == d.get("source_sha") else None
+    for toks in lines:
+        d = dict(t.split("=", 1) for t in toks if "=" in t)
+        if d.get("workload") == workload and d.get("sha") == sha:
+            return int(d["bytes_per_launch"])
+    return None
+
+
+def max_over_ranks(value, world, device=None):
+    """The largest of every rank's `value` (a float); itself when world == 1."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_step, world, ms_per_step):
+    """Whole-job GB/s: every rank moves bytes_per_step each step; the job's
+    step time is the slowest rank's."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -249,6 +280,8 @@ def run_ours(args):
             b = {"x": x}
             if op["kind"] in ("mx", "mx_grouped"):
                 ld = fq.mxfp8_col_blocks(r, None if offsets_host is None else list(offsets_host))
+                if offsets_host is not None:
+                    ld = (ld + 15) // 16 * 16  # the library's default layout for grouped scales
                 b["out"] = {"q_row": torch.empty((r, c), dtype=torch.uint8, device=dev),
                             "s_row": torch.empty((r, c // 32), dtype=torch.uint8, device=dev),
                             "q_col": torch.empty((c, r), dtype=torch.uint8, device=dev),
@@ -343,10 +376,7 @@ def run_ours(args):
         dist.barrier()
     clocks = sampler.stop()
     mx_ms = [a.elapsed_time(b) for a, b in mx_events]
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
     # end-to-end: host inputs -> device, the step, device -> host outputs
     e2e = None
@@ -389,11 +419,8 @@ def run_ours(args):
         z.record()
         torch.cuda.synchronize()
         e2e_ms = a.elapsed_time(z) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(world * bytes_per_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
+        e2e = {"value": round(job_gbs(bytes_per_step, world, e2e_ms), 2), "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 4)}
 
     if rank != 0:
@@ -402,7 +429,7 @@ def run_ours(args):
         return None
 
     ms_per_step = elapsed_ms / args.steps
-    value = world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(bytes_per_step, world, ms_per_step)
     peak, peak_src = hbm_peak()
     mx_op = next((op for op in ops if op["kind"] in ("mx", "mx_grouped")), None)
     roofline = None

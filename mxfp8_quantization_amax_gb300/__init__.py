@@ -319,7 +319,9 @@ def mxfp8_quantize(x: torch.Tensor, fmt: int = E4M3, direction: int = BOTH, grou
     """MXFP8 rowwise and/or columnwise quantization of a 2-D tensor.
 
     Returns dict(q_row [rows, cols], s_row [rows, cols/32], q_col [cols, rows],
-    s_col [cols, s_col_ld]) (uint8; unused direction -> None).
+    s_col [cols, s_col_ld]) (uint8; unused direction -> None).  The default
+    s_col_ld is ceil(rows / 32) without groups, and the column-block count
+    rounded up to a multiple of 16 with groups (the padding is not written).
     """
     _check_input(x)
     rows, cols = _as_2d(x)
@@ -330,7 +332,9 @@ def mxfp8_quantize(x: torch.Tensor, fmt: int = E4M3, direction: int = BOTH, grou
             s_col_ld = (rows + 31) // 32
         else:
             host = group_offsets.cpu() if isinstance(group_offsets, torch.Tensor) else group_offsets
-            s_col_ld = mxfp8_col_blocks(rows, host)
+            # padded to 16 bytes: scale rows then start aligned, which lets
+            # the kernel store a column's scales in whole 8-byte words
+            s_col_ld = (mxfp8_col_blocks(rows, host) + 15) // 16 * 16
     o = out or {}
 
     def buf(name, shape):
