@@ -118,6 +118,33 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+#ifndef FP8Q_PDL  // programmatic dependent launch between the library's kernels
+#define FP8Q_PDL 1
+#endif
+
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialization allowed, so it may start while the
+// kernel before it on the stream is still finishing.  pdl_wait() blocks
+// until the grids this one depends on have completed and their memory
+// operations are visible; every kernel calls it before its first access to
+// global memory (reads of its inputs and writes of its outputs alike).
+// pdl_launch_dependents() lets the next kernel on the stream be scheduled
+// early; that kernel waits in its own pdl_wait() for this grid to finish.
+// Kernels call it once a CTA's main loop is done, not at their start: the
+// next grid's CTAs then take the slots of CTAs that have finished instead
+// of crowding onto whichever SMs had room first, which would unbalance a
+// persistent grid whose work is dealt out by CTA index.
+__device__ __forceinline__ void pdl_wait() {
+#if FP8Q_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+#if FP8Q_PDL
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
 // Emits nothing; marks v as rewritten here.  A run of volatile loads
 // followed by one of these per loaded vector keeps every load issued before
 // the first use of any of them, so a thread has all its loads in flight.

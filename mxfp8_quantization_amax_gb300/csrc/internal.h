@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/fp8q.h"
 
 namespace fp8q {
@@ -18,6 +20,29 @@ fp8q_status cuda_fail(cudaError_t e, const char* what);
 fp8q_status check_launch(const char* what);
 
 int sm_count();
+
+#ifndef FP8Q_PDL
+#define FP8Q_PDL 1
+#endif
+
+// Launches kernel<<<grid, block, smem, stream>>>(args...) with programmatic
+// stream serialization allowed (the kernel calls pdl_wait() before touching
+// global memory), so its launch overlaps the end of the previous kernel.
+template <typename... P, typename... A>
+cudaError_t launch_kernel(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = FP8Q_PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // Per-tensor workspace layout (bytes from the start of the workspace).
 struct CastWorkspace {

@@ -635,6 +635,7 @@ __global__ void __launch_bounds__(kTmaThreads, 4) mx_tma_kernel(const __grid_con
     fence_barrier_init();
   }
   if (tid == kConsumers) prefetch_tensormap(&tmap);
+  pdl_wait();
   build_prefix<kTmaThreads>(p, blk, sup);
   const int64_t units = (int64_t)sup[p.G] * p.strips;
   const uint64_t budget = g_wait_budget_ns;
@@ -661,6 +662,7 @@ __global__ void __launch_bounds__(kTmaThreads, 4) mx_tma_kernel(const __grid_con
           tma_load_2d(dst + q * kSubBytes, &tmap, (int)U.c0 + q * kSubCols, row, &full[s]);
       }
     }
+    pdl_launch_dependents();  // all loads issued: the next kernel may launch
     // every issued copy lands before the CTA can exit (fixed 2 s bound)
     const int64_t first = k > kStages ? k - kStages : 0;
     for (int64_t j = first; j < k; j++)
@@ -723,6 +725,7 @@ __global__ void __launch_bounds__(kTmaThreads, 4) mx_tma_kernel(const __grid_con
     }
     if (gave_up || abort_flag) return;
   }
+  pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -738,6 +741,7 @@ __global__ void __launch_bounds__(kConsumers) mx_f32_kernel(MxParams p) {
   int* sup = blk + (p.G + 1);                           // [G + 1] (super = 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const StorePolicy sp = make_policy();
+  pdl_wait();
   build_prefix<kConsumers>(p, blk, sup);
   const int64_t units = (int64_t)sup[p.G] * p.strips;
 
@@ -818,6 +822,7 @@ __global__ void __launch_bounds__(kConsumers) mx_f32_kernel(MxParams p) {
       __syncthreads();  // the tile is rewritten by the next unit
     }
   }
+  pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -881,7 +886,8 @@ static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
   int64_t grid = (int64_t)per_sm * sm_count();
   if (max_units < grid) grid = max_units;
   if (grid < 1) grid = 1;
-  mx_tma_kernel<FMT, DIR><<<(unsigned)grid, kTmaThreads, smem, s>>>(map, q);
+  const cudaError_t e = launch_kernel(mx_tma_kernel<FMT, DIR>, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, map, q);
+  if (e != cudaSuccess) return cuda_fail(e, "mxfp8 tma kernel launch");
   return check_launch("mxfp8 tma kernel");
 }
 
@@ -900,7 +906,8 @@ static fp8q_status launch_f32(const MxParams& p, cudaStream_t s) {
   int64_t grid = (int64_t)per_sm * sm_count();
   if (max_units < grid) grid = max_units;
   if (grid < 1) grid = 1;
-  mx_f32_kernel<FMT, DIR><<<(unsigned)grid, kConsumers, smem, s>>>(q);
+  const cudaError_t e = launch_kernel(mx_f32_kernel<FMT, DIR>, dim3((unsigned)grid), dim3(kConsumers), smem, s, q);
+  if (e != cudaSuccess) return cuda_fail(e, "mxfp8 fp32 kernel launch");
   return check_launch("mxfp8 fp32 kernel");
 }
 

@@ -133,6 +133,7 @@ __device__ __forceinline__ bool arrive_last(unsigned* counter) {
 template <int DT, bool FINALIZE>
 __global__ void __launch_bounds__(kPtThreads) amax_kernel(KParams p) {
   __shared__ uint32_t sh_max[kPtThreads / 32];
+  pdl_wait();
   const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
   const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
   const uint64_t pol = load_policy(p.l2_hint);
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(kPtThreads) amax_kernel(KParams p) {
     }
   }
   if (cur_g >= 0) flush();
+  pdl_launch_dependents();  // main work done: the next kernel may launch
 
   if constexpr (FINALIZE) {
     if (arrive_last(p.counter)) {
@@ -238,6 +240,7 @@ __global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
   constexpr float kMax = Fmt<FMT>::kMax;
   const bool do_amax = p.acc != nullptr;
   const bool do_sat = p.sat_acc != nullptr;
+  pdl_wait();
 
   float hist_scale = 1.0f;
   if (p.src == kSrcHistory) {  // max over the filled history entries
@@ -369,6 +372,7 @@ __global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
     }
   }
   if (cur_g >= 0) flush();
+  pdl_launch_dependents();  // main work done: the next kernel may launch
 
   // The last CTA publishes per-group results and returns the scratch it used
   // (accumulators, counters, the current-scaling scales) to zero.
@@ -446,41 +450,45 @@ static int grid_for(int64_t n_chunks, int per_sm) {
 
 fp8q_status launch_amax(const PtLaunch& L, bool finalize_scales) {
   KParams p = make_params(L);
+  cudaError_t e;
   if (L.dt == kBF16) {
     if (finalize_scales) {
       static int r = ctas_per_sm(amax_kernel<kBF16, true>);
-      amax_kernel<kBF16, true><<<grid_for(p.n_chunks, r), kPtThreads, 0, L.stream>>>(p);
+      e = launch_kernel(amax_kernel<kBF16, true>, dim3(grid_for(p.n_chunks, r)), dim3(kPtThreads), 0, L.stream, p);
     } else {
       static int r = ctas_per_sm(amax_kernel<kBF16, false>);
-      amax_kernel<kBF16, false><<<grid_for(p.n_chunks, r), kPtThreads, 0, L.stream>>>(p);
+      e = launch_kernel(amax_kernel<kBF16, false>, dim3(grid_for(p.n_chunks, r)), dim3(kPtThreads), 0, L.stream, p);
     }
   } else {
     if (finalize_scales) {
       static int r = ctas_per_sm(amax_kernel<kFP32, true>);
-      amax_kernel<kFP32, true><<<grid_for(p.n_chunks, r), kPtThreads, 0, L.stream>>>(p);
+      e = launch_kernel(amax_kernel<kFP32, true>, dim3(grid_for(p.n_chunks, r)), dim3(kPtThreads), 0, L.stream, p);
     } else {
       static int r = ctas_per_sm(amax_kernel<kFP32, false>);
-      amax_kernel<kFP32, false><<<grid_for(p.n_chunks, r), kPtThreads, 0, L.stream>>>(p);
+      e = launch_kernel(amax_kernel<kFP32, false>, dim3(grid_for(p.n_chunks, r)), dim3(kPtThreads), 0, L.stream, p);
     }
   }
+  if (e != cudaSuccess) return cuda_fail(e, "amax kernel launch");
   return check_launch("amax kernel");
 }
 
 template <int DT, int FMT>
-static void launch_cast_t(const KParams& p, cudaStream_t s) {
+static cudaError_t launch_cast_t(const KParams& p, cudaStream_t s) {
   static int r = ctas_per_sm(cast_kernel<DT, FMT>);
-  cast_kernel<DT, FMT><<<grid_for(p.n_chunks, r), kPtThreads, 0, s>>>(p);
+  return launch_kernel(cast_kernel<DT, FMT>, dim3(grid_for(p.n_chunks, r)), dim3(kPtThreads), 0, s, p);
 }
 
 fp8q_status launch_cast(const PtLaunch& L) {
   KParams p = make_params(L);
+  cudaError_t e;
   if (L.dt == kBF16) {
-    if (L.fmt == kE4M3) launch_cast_t<kBF16, kE4M3>(p, L.stream);
-    else launch_cast_t<kBF16, kE5M2>(p, L.stream);
+    if (L.fmt == kE4M3) e = launch_cast_t<kBF16, kE4M3>(p, L.stream);
+    else e = launch_cast_t<kBF16, kE5M2>(p, L.stream);
   } else {
-    if (L.fmt == kE4M3) launch_cast_t<kFP32, kE4M3>(p, L.stream);
-    else launch_cast_t<kFP32, kE5M2>(p, L.stream);
+    if (L.fmt == kE4M3) e = launch_cast_t<kFP32, kE4M3>(p, L.stream);
+    else e = launch_cast_t<kFP32, kE5M2>(p, L.stream);
   }
+  if (e != cudaSuccess) return cuda_fail(e, "cast kernel launch");
   return check_launch("cast kernel");
 }
 
