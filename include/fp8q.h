@@ -88,6 +88,17 @@ FP8Q_API fp8q_status fp8q_check_device(void* stream);
 FP8Q_API fp8q_status fp8q_set_wait_budget_ns(uint64_t ns);
 
 /*
+ * Test hook for the failure path above (the pages have no counterpart).
+ * While `on` is nonzero, the BF16 MXFP8 kernel's producer warp issues no
+ * loads, so its consumers' waits for data can never complete: each gives up
+ * after the wait budget, the call's outputs are left unwritten and
+ * fp8q_check_device reports FP8Q_ERR_TIMEOUT.  No copy is in flight when
+ * the kernel ends.  Applies to kernels launched afterwards on the current
+ * device; leave it off (the default) outside such tests.
+ */
+FP8Q_API fp8q_status fp8q_debug_stall_mx_producer(int32_t on);
+
+/*
  * amax_out[g] = max |x| over group g, bit-exact: the FP32 value whose bits
  * are the largest magnitude bits in the group (BF16 widened exactly), so a
  * NaN makes the result NaN and an empty group gives 0.

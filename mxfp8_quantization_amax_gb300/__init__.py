@@ -40,6 +40,7 @@ _SIGS = {
     "fp8q_version": (_c.c_int32, []),
     "fp8q_last_error_string": (_c.c_char_p, []),
     "fp8q_check_device": (_c.c_int, [_P]),
+    "fp8q_debug_stall_mx_producer": (_c.c_int, [_c.c_int32]),
     "fp8q_set_wait_budget_ns": (_c.c_int, [_c.c_uint64]),
     "fp8q_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _P, _P]),
     "fp8q_cast_workspace_bytes": (_c.c_size_t, [_c.c_int32]),
@@ -154,6 +155,12 @@ def check_device():
 
 def set_wait_budget_ns(ns: int):
     _check(lib().fp8q_set_wait_budget_ns(int(ns)), "fp8q_set_wait_budget_ns")
+
+
+def debug_stall_mx_producer(on: bool):
+    """Test hook: the BF16 MXFP8 kernel's producer issues no loads while on,
+    so its consumers' bounded waits expire (reported by check_device)."""
+    _check(lib().fp8q_debug_stall_mx_producer(1 if on else 0), "fp8q_debug_stall_mx_producer")
 
 
 # ---------------------------------------------------------------------------

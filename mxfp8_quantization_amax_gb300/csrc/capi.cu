@@ -116,6 +116,11 @@ fp8q_status fp8q_set_wait_budget_ns(uint64_t ns) {
   return r != FP8Q_OK ? r : pt_set_wait_budget((unsigned long long)ns);
 }
 
+fp8q_status fp8q_debug_stall_mx_producer(int32_t on) {
+  g_err[0] = 0;
+  return mx_set_stall_producer(on != 0);
+}
+
 fp8q_status fp8q_amax(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
                       int32_t num_groups, float* amax_out, void* stream) {
   g_err[0] = 0;

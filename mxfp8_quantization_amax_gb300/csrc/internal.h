@@ -111,6 +111,7 @@ fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const i
 // of the per-tensor pipeline, and their wait budgets.
 fp8q_status mx_device_status(cudaStream_t stream, bool clear, unsigned* word);
 fp8q_status mx_set_wait_budget(unsigned long long ns);
+fp8q_status mx_set_stall_producer(bool on);
 fp8q_status pt_device_status(bool clear, unsigned* word);
 fp8q_status pt_set_wait_budget(unsigned long long ns);
 

@@ -68,6 +68,9 @@ constexpr int kSubBytes = kTileRows * 128;    // one box in shared memory
 // Device-side failure word (bit 0: a bounded wait gave up) and the wait
 // budget in ns.  Read and cleared by fp8q_check_device().
 __device__ unsigned int g_mx_error;
+// Failure-detection test hook: while nonzero, the BF16 kernel's producer
+// issues no loads, so every consumer wait runs out its budget.
+__device__ unsigned int g_mx_stall_producer;
 __device__ unsigned long long g_wait_budget_ns = 1000000000ull;
 
 struct MxParams {
@@ -644,7 +647,8 @@ __global__ void __launch_bounds__(kTmaThreads, 4) mx_tma_kernel(const __grid_con
     // ---------------- producer ----------------
     if (lane != 0) return;
     int64_t k = 0;
-    for (int64_t u = blockIdx.x; u < units && !abort_flag; u += gridDim.x) {
+    const bool stall = *(volatile unsigned*)&g_mx_stall_producer != 0;
+    for (int64_t u = blockIdx.x; u < units && !abort_flag && !stall; u += gridDim.x) {
       const Unit U = unit_of(p, blk, sup, u);
       for (int j = 0; j < U.nblk; j++, ++k) {
         const int s = (int)(k % kStages);
@@ -955,6 +959,12 @@ fp8q_status mx_device_status(cudaStream_t stream, bool clear, unsigned* word) {
   }
   *word = v;
   return FP8Q_OK;
+}
+
+fp8q_status mx_set_stall_producer(bool on) {
+  const unsigned v = on ? 1u : 0u;
+  cudaError_t e = cudaMemcpyToSymbol(g_mx_stall_producer, &v, sizeof(v));
+  return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, "cudaMemcpyToSymbol(stall hook)");
 }
 
 fp8q_status mx_set_wait_budget(unsigned long long ns) {
