@@ -112,6 +112,24 @@ FP8Q_API fp8q_status fp8q_amax(const void* x, int32_t dt, int64_t rows, int64_t 
                       void* stream);
 
 /*
+ * scale_out[g] = fl32(fl32(F8max / amax[g]) * 2^-margin) and
+ * scale_inv_out[g] = fl32(1 / scale_out[g]), with the same special cases as
+ * current scaling (amax 0 or non-finite -> scale 1; a quotient above FLT_MAX
+ * -> FLT_MAX).  ("HiFloat8：高性能训练之路" 1.2, eqs. 1 and 3; "混合精度与 FP8
+ * 训练" 8.2, the margin.)  It is the scale step of current scaling on its
+ * own, for a tensor split across devices: each device takes fp8q_amax of
+ * its part, the amaxes are combined with a MAX all-reduce (on the FP32 bit
+ * patterns as int32, which keeps NaN), and each device casts its part with
+ * fp8q_cast_per_tensor(scale_in = scale_out).
+ *   amax           device float[num_groups] (taken by magnitude)
+ *   scale_out      device float[num_groups]
+ *   scale_inv_out  device float[num_groups] or NULL
+ */
+FP8Q_API fp8q_status fp8q_scale_from_amax(const float* amax, int32_t num_groups, int32_t fmt,
+                                          int32_t margin, float* scale_out, float* scale_inv_out,
+                                          void* stream);
+
+/*
  * Bytes of workspace fp8q_cast_per_tensor needs for num_groups groups.
  */
 FP8Q_API size_t fp8q_cast_workspace_bytes(int32_t num_groups);

@@ -25,6 +25,7 @@ __all__ = [
     "E4M3", "E5M2", "ROW", "COL", "BOTH", "build", "library_path", "lib",
     "fp8q_amax", "fp8q_cast_per_tensor", "fp8q_cast_workspace_bytes", "DelayedScaling",
     "mxfp8_quantize", "mxfp8_col_blocks", "Fp8qError", "check_device", "set_wait_budget_ns",
+    "fp8q_scale_from_amax", "debug_stall_mx_producer",
 ]
 
 E4M3 = 0
@@ -41,6 +42,7 @@ _SIGS = {
     "fp8q_last_error_string": (_c.c_char_p, []),
     "fp8q_check_device": (_c.c_int, [_P]),
     "fp8q_debug_stall_mx_producer": (_c.c_int, [_c.c_int32]),
+    "fp8q_scale_from_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int32, _c.c_int32, _P, _P, _P]),
     "fp8q_set_wait_budget_ns": (_c.c_int, [_c.c_uint64]),
     "fp8q_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _P, _P]),
     "fp8q_cast_workspace_bytes": (_c.c_size_t, [_c.c_int32]),
@@ -175,6 +177,21 @@ def fp8q_amax(x: torch.Tensor, group_offsets=None, out: torch.Tensor | None = No
         out = torch.empty(G, dtype=torch.float32, device=x.device)
     _check(lib().fp8q_amax(_ptr(x), _dt(x), rows, cols, _ptr(off), G, _ptr(out), _stream()), "fp8q_amax")
     return out
+
+
+def fp8q_scale_from_amax(amax: torch.Tensor, fmt: int = E4M3, margin: int = 0, out: dict | None = None) -> dict:
+    """Per-group scale and its reciprocal from given amaxes (device float32 [G])."""
+    if not amax.is_cuda or amax.dtype != torch.float32 or not amax.is_contiguous():
+        raise ValueError("amax must be a contiguous float32 CUDA tensor")
+    G = amax.numel()
+    o = out or {}
+    scale = o.get("scale")
+    scale = torch.empty(G, dtype=torch.float32, device=amax.device) if scale is None else scale
+    scale_inv = o.get("scale_inv")
+    scale_inv = torch.empty(G, dtype=torch.float32, device=amax.device) if scale_inv is None else scale_inv
+    _check(lib().fp8q_scale_from_amax(_ptr(amax), G, fmt, margin, _ptr(scale), _ptr(scale_inv), _stream()),
+           "fp8q_scale_from_amax")
+    return {"scale": scale, "scale_inv": scale_inv}
 
 
 # ---------------------------------------------------------------------------

@@ -144,6 +144,19 @@ fp8q_status fp8q_amax(const void* x, int32_t dt, int64_t rows, int64_t cols, con
   return launch_amax(L, false);
 }
 
+fp8q_status fp8q_scale_from_amax(const float* amax, int32_t num_groups, int32_t fmt, int32_t margin,
+                                 float* scale_out, float* scale_inv_out, void* stream) {
+  g_err[0] = 0;
+  if (num_groups < 1 || num_groups > FP8Q_MAX_GROUPS)
+    return fail(FP8Q_ERR_INVALID_ARG, "num_groups must be in [1, %d]", FP8Q_MAX_GROUPS);
+  if (!fmt_ok(fmt)) return fail(FP8Q_ERR_INVALID_ARG, "fmt must be FP8Q_E4M3 or FP8Q_E5M2");
+  if (margin < 0 || margin > 63) return fail(FP8Q_ERR_INVALID_ARG, "margin must be in [0, 63]");
+  if (!amax || !scale_out) return fail(FP8Q_ERR_INVALID_ARG, "amax and scale_out must not be NULL");
+  if (!aligned(amax, 4) || !aligned(scale_out, 4) || !aligned(scale_inv_out, 4))
+    return fail(FP8Q_ERR_INVALID_ARG, "misaligned pointer");
+  return launch_scale(amax, num_groups, fmt, margin, scale_out, scale_inv_out, (cudaStream_t)stream);
+}
+
 size_t fp8q_cast_workspace_bytes(int32_t num_groups) {
   if (num_groups < 1) num_groups = 1;
   return cast_workspace_bytes(num_groups);

@@ -112,6 +112,8 @@ fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const i
 fp8q_status mx_device_status(cudaStream_t stream, bool clear, unsigned* word);
 fp8q_status mx_set_wait_budget(unsigned long long ns);
 fp8q_status mx_set_stall_producer(bool on);
+fp8q_status launch_scale(const float* amax, int G, int fmt, int margin, float* scale_out, float* scale_inv_out,
+                         cudaStream_t s);
 fp8q_status pt_device_status(bool clear, unsigned* word);
 fp8q_status pt_set_wait_budget(unsigned long long ns);
 

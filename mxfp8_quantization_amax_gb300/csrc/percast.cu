@@ -401,6 +401,21 @@ __global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Scales from given amaxes (the cast pass of a tensor split across devices,
+// after the per-device amaxes were combined)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPtThreads) scale_kernel(const float* amax, int G, float f8max, int margin,
+                                                           float* scale_out, float* scale_inv_out) {
+  pdl_wait();
+  for (int g = blockIdx.x * kPtThreads + threadIdx.x; g < G; g += gridDim.x * kPtThreads) {
+    const float s = scale_from_amax(__float_as_uint(amax[g]) & 0x7FFFFFFFu, f8max, margin);
+    scale_out[g] = s;
+    if (scale_inv_out) scale_inv_out[g] = __frcp_rn(s);
+  }
+  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 static KParams make_params(const PtLaunch& L) {
@@ -490,6 +505,15 @@ fp8q_status launch_cast(const PtLaunch& L) {
   }
   if (e != cudaSuccess) return cuda_fail(e, "cast kernel launch");
   return check_launch("cast kernel");
+}
+
+fp8q_status launch_scale(const float* amax, int G, int fmt, int margin, float* scale_out, float* scale_inv_out,
+                         cudaStream_t s) {
+  const int blocks = (G + kPtThreads - 1) / kPtThreads;
+  const cudaError_t e = launch_kernel(scale_kernel, dim3(blocks), dim3(kPtThreads), 0, s, amax, G, fmt_max(fmt),
+                                      margin, scale_out, scale_inv_out);
+  if (e != cudaSuccess) return cuda_fail(e, "scale kernel launch");
+  return check_launch("scale kernel");
 }
 
 fp8q_status pt_device_status(bool clear, unsigned* word) {
