@@ -230,7 +230,7 @@ class DelayedScaling:
     Section 5.2 (and "昇腾 950" 3.2): the first step after a (re)start has
     no history, so it uses current scaling.
 
-    Readings (the design doc lists them): a step records iff step % interval == 0,
+    Readings where the pages are silent: a step records iff step % interval == 0,
     counting from creation or reset; the first step uses margin 0; the max
     runs over the filled entries only.
     """

@@ -25,7 +25,7 @@
  * two floats, rounding the double result to float gives the correctly
  * rounded float result (53 >= 2*24 + 2), so this is IEEE single arithmetic.
  *
- * Readings where the pages are silent (documented again in the design doc):
+ * Readings where the pages are silent:
  *   - any NaN input encodes to byte 0x7F in both formats;
  *   - +-Inf saturates to +-max like any other overflow;
  *   - the sign of zero is kept (0x80), except in an all-zero MX block;
