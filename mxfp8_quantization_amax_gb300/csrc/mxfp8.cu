@@ -36,13 +36,16 @@
 #include "tma.cuh"
 
 #ifndef FP8Q_MX_STAGES  // shared-memory ring depth (16 KB per stage)
-#define FP8Q_MX_STAGES 3
+#define FP8Q_MX_STAGES 2
 #endif
 #ifndef FP8Q_MX_SUPER  // 32-row blocks per unit of the BF16 kernel
 #define FP8Q_MX_SUPER 4
 #endif
 #ifndef FP8Q_MX_SUPER_GROUPED  // the same for grouped calls (fewer unit boundaries inside a group)
 #define FP8Q_MX_SUPER_GROUPED 16
+#endif
+#ifndef FP8Q_MX_MIN_CTAS  // CTAs per SM the register budget is sized for
+#define FP8Q_MX_MIN_CTAS 4
 #endif
 #ifndef FP8Q_MX_SCOL_FLUSH  // scale bytes per s_col store (4 or 8)
 #define FP8Q_MX_SCOL_FLUSH 4
@@ -619,7 +622,7 @@ __device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit&
 }
 
 template <int FMT, int DIR>
-__global__ void __launch_bounds__(kTmaThreads, 4) mx_tma_kernel(const __grid_constant__ CUtensorMap tmap, MxParams p) {
+__global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(const __grid_constant__ CUtensorMap tmap, MxParams p) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t full[kStages], empty[kStages];
   __shared__ volatile int abort_flag;
