@@ -130,13 +130,11 @@ __device__ __forceinline__ bool arrive_last(unsigned* counter) {
 // ---------------------------------------------------------------------------
 // Amax pass
 // ---------------------------------------------------------------------------
-template <int DT, bool FINALIZE>
-__global__ void __launch_bounds__(kPtThreads) amax_kernel(KParams p) {
-  __shared__ uint32_t sh_max[kPtThreads / 32];
-  pdl_wait();
-  const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
-  const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
-  const uint64_t pol = load_policy(p.l2_hint);
+// Amax of the CTA's chunks [c_begin, c_end), merged into p.acc[group] with
+// one atomic per CTA and group.  Block-uniform: every thread calls it.
+template <int DT>
+__device__ __forceinline__ void amax_pass(const KParams& p, int64_t c_begin, int64_t c_end, uint64_t pol,
+                                          uint32_t* sh_max) {
   int cur_g = -1;
   uint32_t cur = 0;
 
@@ -202,23 +200,38 @@ __global__ void __launch_bounds__(kPtThreads) amax_kernel(KParams p) {
     }
   }
   if (cur_g >= 0) flush();
+}
+
+// Turns the merged amaxes into the scales (current scaling) and publishes
+// them; returns the accumulators to zero.  Run by the last CTA.
+__device__ __forceinline__ void publish_scales(const KParams& p) {
+  for (int g = threadIdx.x; g < p.G; g += kPtThreads) {
+    const uint32_t a = *(volatile unsigned*)(p.acc + g);
+    const float s = scale_from_amax(a, p.f8max, p.margin);
+    p.ws_scale[g] = s;
+    if (p.amax_out) p.amax_out[g] = __uint_as_float(a);
+    if (p.scale_out) p.scale_out[g] = s;
+    if (p.scale_inv_out) p.scale_inv_out[g] = __frcp_rn(s);
+    if (g == 0) {
+      if (p.hist_slot) *p.hist_slot = __uint_as_float(a);
+      if (p.flag && a >= 0x7F800000u) atomicOr(p.flag, 1u);
+    }
+    p.acc[g] = 0;
+  }
+}
+
+template <int DT, bool FINALIZE>
+__global__ void __launch_bounds__(kPtThreads) amax_kernel(KParams p) {
+  __shared__ uint32_t sh_max[kPtThreads / 32];
+  pdl_wait();
+  const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
+  const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
+  amax_pass<DT>(p, c_begin, c_end, load_policy(p.l2_hint), sh_max);
   pdl_launch_dependents();  // main work done: the next kernel may launch
 
   if constexpr (FINALIZE) {
     if (arrive_last(p.counter)) {
-      for (int g = threadIdx.x; g < p.G; g += kPtThreads) {
-        const uint32_t a = *(volatile unsigned*)(p.acc + g);
-        const float s = scale_from_amax(a, p.f8max, p.margin);
-        p.ws_scale[g] = s;
-        if (p.amax_out) p.amax_out[g] = __uint_as_float(a);
-        if (p.scale_out) p.scale_out[g] = s;
-        if (p.scale_inv_out) p.scale_inv_out[g] = __frcp_rn(s);
-        if (g == 0) {
-          if (p.hist_slot) *p.hist_slot = __uint_as_float(a);
-          if (p.flag && a >= 0x7F800000u) atomicOr(p.flag, 1u);
-        }
-        p.acc[g] = 0;
-      }
+      publish_scales(p);
       if (threadIdx.x == 0) *p.counter = 0;
     }
   }
@@ -233,33 +246,15 @@ __device__ __forceinline__ float group_scale(const KParams& p, int g, float hist
   return hist_scale;
 }
 
+// Cast of the CTA's chunks [c_begin, c_end) with the per-group scale of
+// `p.src`; optional fused amax (p.acc) and saturation count (p.sat_acc).
+// Block-uniform: every thread calls it.
 template <int DT, int FMT>
-__global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
-  __shared__ uint32_t sh_max[kPtThreads / 32];
-  __shared__ unsigned long long sh_sum[kPtThreads / 32];
+__device__ __forceinline__ void cast_pass(const KParams& p, int64_t c_begin, int64_t c_end, uint64_t pol,
+                                          float hist_scale, uint32_t* sh_max, unsigned long long* sh_sum) {
   constexpr float kMax = Fmt<FMT>::kMax;
   const bool do_amax = p.acc != nullptr;
   const bool do_sat = p.sat_acc != nullptr;
-  pdl_wait();
-
-  float hist_scale = 1.0f;
-  if (p.src == kSrcHistory) {  // max over the filled history entries
-    uint32_t hm = 0;
-    for (int i = threadIdx.x; i < p.hist_count; i += kPtThreads)
-      hm = max(hm, __float_as_uint(p.hist[i]) & 0x7FFFFFFFu);
-    hist_scale = scale_from_amax(block_max(hm, sh_max), kMax, p.margin);
-  }
-  if (blockIdx.x == 0 && p.src != kSrcWorkspace) {
-    for (int g = threadIdx.x; g < p.G; g += kPtThreads) {
-      const float s = group_scale(p, g, hist_scale);
-      if (p.scale_out) p.scale_out[g] = s;
-      if (p.scale_inv_out) p.scale_inv_out[g] = __frcp_rn(s);
-    }
-  }
-
-  const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
-  const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
-  const uint64_t pol = load_policy(p.l2_hint);
   int cur_g = -1;
   uint32_t cur = 0;
   unsigned long long nsat = 0;
@@ -372,29 +367,64 @@ __global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
     }
   }
   if (cur_g >= 0) flush();
+}
+
+// Publishes the fused amax / saturation results and returns the scratch
+// (accumulators, the current-scaling scales) to zero.  Run by the last CTA.
+__device__ __forceinline__ void publish_cast_results(const KParams& p) {
+  const bool do_amax = p.acc != nullptr;
+  const bool do_sat = p.sat_acc != nullptr;
+  for (int g = threadIdx.x; g < p.G; g += kPtThreads) {
+    if (p.src == kSrcWorkspace) p.ws_scale[g] = 0.0f;
+    if (do_amax) {
+      const uint32_t a = *(volatile unsigned*)(p.acc + g);
+      if (p.amax_out) p.amax_out[g] = __uint_as_float(a);
+      if (p.hist_slot && g == 0) {
+        *p.hist_slot = __uint_as_float(a);
+        if (a >= 0x7F800000u) atomicOr(p.flag, 1u);
+      }
+      p.acc[g] = 0;
+    }
+    if (do_sat) {
+      const unsigned long long s = *(volatile unsigned long long*)(p.sat_acc + g);
+      if (p.sat_out) p.sat_out[g] = s;
+      p.sat_acc[g] = 0;
+    }
+  }
+}
+
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
+  __shared__ uint32_t sh_max[kPtThreads / 32];
+  __shared__ unsigned long long sh_sum[kPtThreads / 32];
+  constexpr float kMax = Fmt<FMT>::kMax;
+  pdl_wait();
+
+  float hist_scale = 1.0f;
+  if (p.src == kSrcHistory) {  // max over the filled history entries
+    uint32_t hm = 0;
+    for (int i = threadIdx.x; i < p.hist_count; i += kPtThreads)
+      hm = max(hm, __float_as_uint(p.hist[i]) & 0x7FFFFFFFu);
+    hist_scale = scale_from_amax(block_max(hm, sh_max), kMax, p.margin);
+  }
+  if (blockIdx.x == 0 && p.src != kSrcWorkspace) {
+    for (int g = threadIdx.x; g < p.G; g += kPtThreads) {
+      const float s = group_scale(p, g, hist_scale);
+      if (p.scale_out) p.scale_out[g] = s;
+      if (p.scale_inv_out) p.scale_inv_out[g] = __frcp_rn(s);
+    }
+  }
+
+  const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
+  const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
+  cast_pass<DT, FMT>(p, c_begin, c_end, load_policy(p.l2_hint), hist_scale, sh_max, sh_sum);
   pdl_launch_dependents();  // main work done: the next kernel may launch
 
   // The last CTA publishes per-group results and returns the scratch it used
   // (accumulators, counters, the current-scaling scales) to zero.
-  if (do_amax || do_sat || p.src == kSrcWorkspace) {
+  if (p.acc != nullptr || p.sat_acc != nullptr || p.src == kSrcWorkspace) {
     if (arrive_last(p.counter)) {
-      for (int g = threadIdx.x; g < p.G; g += kPtThreads) {
-        if (p.src == kSrcWorkspace) p.ws_scale[g] = 0.0f;
-        if (do_amax) {
-          const uint32_t a = *(volatile unsigned*)(p.acc + g);
-          if (p.amax_out) p.amax_out[g] = __uint_as_float(a);
-          if (p.hist_slot && g == 0) {
-            *p.hist_slot = __uint_as_float(a);
-            if (a >= 0x7F800000u) atomicOr(p.flag, 1u);
-          }
-          p.acc[g] = 0;
-        }
-        if (do_sat) {
-          const unsigned long long s = *(volatile unsigned long long*)(p.sat_acc + g);
-          if (p.sat_out) p.sat_out[g] = s;
-          p.sat_acc[g] = 0;
-        }
-      }
+      publish_cast_results(p);
       if (threadIdx.x == 0) *p.counter = 0;
     }
   }
