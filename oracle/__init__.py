@@ -79,6 +79,12 @@ def _load():
         "orc_encode_array": (None, [c.c_int, P, c.c_int64, P, c.c_int]),
         "orc_encode_f32_range": (None, [c.c_int, c.c_uint64, c.c_int64, P, c.c_int]),
         "orc_max_threads": (c.c_int, []),
+        "orc_bf16_round": (c.c_uint16, [c.c_float]),
+        "orc_bf16_round_array": (None, [P, c.c_int64, P, c.c_int]),
+        "orc_dequant_per_tensor": (None, [P, c.c_int64, c.c_int64, P, c.c_int, c.c_int, P, c.c_int, P,
+                                          c.c_int]),
+        "orc_mx_dequantize": (None, [P, P, c.c_int64, c.c_int64, P, c.c_int, c.c_int, c.c_int, c.c_int64,
+                                     c.c_int, P, c.c_int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -322,3 +328,55 @@ def mx_quantize(x: np.ndarray, fmt: int, direction: int = 3, offsets=None,
         _ptr(q_col if q_col is not None else dummy), _ptr(s_col if s_col is not None else dummy),
         ld, nthreads or max_threads())
     return {"q_row": q_row, "s_row": s_row, "q_col": q_col, "s_col": s_col, "col_blocks": T}
+
+
+# --------------------------------------------------------------------------
+# Dequantization
+# --------------------------------------------------------------------------
+def bf16_round(f) -> np.ndarray:
+    """Nearest BF16 bit patterns (ties to even, NaN -> 0x7FC0) of float32 values."""
+    f = np.ascontiguousarray(np.asarray(f, dtype=np.float32).reshape(-1))
+    out = np.zeros(f.size, dtype=np.uint16)
+    _load().orc_bf16_round_array(_ptr(f), f.size, _ptr(out), max_threads())
+    return out
+
+
+def _out_array(n: int, out_dt: int) -> np.ndarray:
+    return np.zeros(n, dtype=np.uint16 if out_dt == 0 else np.uint32)
+
+
+def dequant_per_tensor(q: np.ndarray, fmt: int, scale_inv, out_dt: int = 0, offsets=None,
+                       nthreads: int = 0) -> np.ndarray:
+    """y = round_out(fl32(value(q) * scale_inv[g])) over a 2-D code array.
+
+    out_dt 0: BF16 bit patterns (uint16), 1: FP32 bit patterns (uint32);
+    the result has q's shape.
+    """
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    rows, cols = q.shape
+    o = None if offsets is None else np.ascontiguousarray(offsets, dtype=np.int64)
+    G = 1 if o is None else o.size - 1
+    si = np.ascontiguousarray(np.asarray(scale_inv, dtype=np.float32).reshape(-1))
+    assert si.size == G
+    y = _out_array(q.size, out_dt)
+    _load().orc_dequant_per_tensor(_ptr(q), rows, cols, _ptr(o) if o is not None else None, G, fmt, _ptr(si),
+                                   out_dt, _ptr(y), nthreads or max_threads())
+    return y.reshape(rows, cols)
+
+
+def mx_dequantize(q: np.ndarray, s: np.ndarray, fmt: int, direction: int, rows: int, cols: int,
+                  out_dt: int = 0, offsets=None, nthreads: int = 0) -> np.ndarray:
+    """MX dequantization of one copy: value(q) * 2^(s - 127), byte 0xFF -> NaN.
+
+    direction 1: q [rows, cols], s [rows, cols/32] -> y [rows, cols].
+    direction 2: q [cols, rows], s [cols, s_ld] -> y [cols, rows].
+    """
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    o = None if offsets is None else np.ascontiguousarray(offsets, dtype=np.int64)
+    G = 1 if o is None else o.size - 1
+    s_ld = s.shape[1]
+    y = _out_array(q.size, out_dt)
+    _load().orc_mx_dequantize(_ptr(q), _ptr(s), rows, cols, _ptr(o) if o is not None else None, G, fmt,
+                              direction, s_ld, out_dt, _ptr(y), nthreads or max_threads())
+    return y.reshape(q.shape)

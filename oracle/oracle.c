@@ -35,7 +35,12 @@
  *     elements 0x7F;
  *   - per-tensor: amax = 0 gives scale 1, a non-finite amax gives scale 1
  *     and raises the non-finite flag, and an overflowing F8max/amax gives
- *     FLT_MAX.
+ *     FLT_MAX;
+ *   - dequantization: a per-tensor product value * scale_inv is rounded to
+ *     FP32 first and then to the output type; an MX product value * 2^X is
+ *     exact in FP32 except for overflow to Inf; BF16 output rounds to
+ *     nearest, ties to even; every NaN result is the canonical quiet NaN
+ *     (BF16 0x7FC0, FP32 0x7FC00000).
  * Those readings are pinned only by their own definition ("parity unpinned"
  * by the pages); everything else is pinned by page values, closed forms and
  * library routines in tests/test_oracle_pins.py.
@@ -376,4 +381,116 @@ void orc_encode_f32_range(int fmt, uint64_t first, int64_t n, uint8_t* q, int nt
 #endif
     for (int64_t i = 0; i < n; i++)
         q[i] = (uint8_t)orc_fp8_encode(fmt, (double)bits_to_float((uint32_t)(first + (uint64_t)i)));
+}
+
+/* ------------------------------------------------------------------ */
+/* Dequantization: the inverse step that de-scales an FP8 value for   */
+/* use in higher precision ("HiFloat8：高性能训练之路" 1.1-1.2: the     */
+/* matmul result is multiplied back by scale_inv = 1/Scale;           */
+/* "Blackwell GPU MXFP8 预训练最佳实践" 4.3: without MX hardware the     */
+/* blocks are dequantized and a BF16 matmul runs).                    */
+/* ------------------------------------------------------------------ */
+
+/* Nearest BF16 (ties to the even code) of a float, from the values of   */
+/* the two BF16 neighbours: BF16 keeps FP32's sign and exponent and the */
+/* top 7 fraction bits ("混合精度与 FP8 训练" 2.2).  Magnitudes at or    */
+/* beyond the midpoint above the largest finite BF16 round to Inf (IEEE */
+/* rounding with an unbounded exponent).  NaN -> 0x7FC0.                */
+uint16_t orc_bf16_round(float f)
+{
+    uint32_t b = float_to_bits(f);
+    uint32_t sign = b & 0x80000000u, mag = b & 0x7FFFFFFFu;
+    if (mag > 0x7F800000u) return 0x7FC0;                  /* NaN */
+    if (mag == 0x7F800000u) return (uint16_t)((sign | mag) >> 16);
+    uint32_t lo = mag & 0xFFFF0000u;                       /* toward zero */
+    if (lo == mag) return (uint16_t)((sign | mag) >> 16);  /* exact */
+    uint32_t hi = lo + 0x10000u;                           /* next away from zero */
+    double v = (double)bits_to_float(mag);
+    double vlo = (double)bits_to_float(lo);
+    double vhi = hi == 0x7F800000u ? ldexp(1.0, 128) : (double)bits_to_float(hi);
+    uint32_t pick;
+    if (v - vlo < vhi - v) pick = lo;
+    else if (v - vlo > vhi - v) pick = hi;
+    else pick = ((lo >> 16) & 1u) ? hi : lo;               /* tie: even code */
+    return (uint16_t)((sign | pick) >> 16);
+}
+
+/* One dequantized value in the output type (out_dt: 0 BF16, 1 FP32):    */
+/* v is the exact real result, rounded once to float, then to BF16.      */
+static void put_out(void* y, int out_dt, int64_t i, double v)
+{
+    float f = isnan(v) ? bits_to_float(0x7FC00000u) : to_float(v);
+    if (out_dt == 0) ((uint16_t*)y)[i] = orc_bf16_round(f);
+    else ((uint32_t*)y)[i] = isnan(f) ? 0x7FC00000u : float_to_bits(f);
+}
+
+/* Per-tensor (per-group) dequantization of a rows x cols code array:    */
+/* y = fl32(value(q) * scale_inv[g]) for the rows of group g, then the   */
+/* output rounding above.  value(q) * scale_inv is exact in double.     */
+void orc_dequant_per_tensor(const uint8_t* q, int64_t rows, int64_t cols, const int64_t* offs, int G,
+                            int fmt, const float* scale_inv, int out_dt, void* y, int nthreads)
+{
+    int ng = offs ? G : 1;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#endif
+    for (int g = 0; g < ng; g++) {
+        int64_t r0 = grp_off(offs, ng, rows, g), r1 = grp_off(offs, ng, rows, g + 1);
+        double si = (double)scale_inv[g];
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+        for (int64_t i = r0 * cols; i < r1 * cols; i++)
+            put_out(y, out_dt, i, orc_fp8_value(fmt, q[i]) * si);
+    }
+}
+
+/* MX dequantization ("Blackwell GPU MXFP8 预训练最佳实践" 4.1: element   */
+/* value times 2^X, X = byte - 127; byte 0xFF is NaN).  dir 1: rowwise   */
+/* copy, q [rows][cols], s [rows][cols/32], y [rows][cols].  dir 2:      */
+/* columnwise copy, q [cols][rows], s [cols][s_ld] with blocks counted   */
+/* over the groups in order, y [cols][rows] (the copy's own layout).     */
+void orc_mx_dequantize(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t cols, const int64_t* offs,
+                       int G, int fmt, int dir, int64_t s_ld, int out_dt, void* y, int nthreads)
+{
+    int ng = offs ? G : 1;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#endif
+    if (dir == 1) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+        for (int64_t r = 0; r < rows; r++)
+            for (int64_t c = 0; c < cols; c++) {
+                unsigned byte = s[r * (cols / 32) + c / 32];
+                double v = byte == 0xFFu ? NAN : ldexp(orc_fp8_value(fmt, q[r * cols + c]), (int)byte - 127);
+                put_out(y, out_dt, r * cols + c, v);
+            }
+        return;
+    }
+    int64_t base = 0;
+    for (int g = 0; g < ng; g++) {
+        int64_t r0 = grp_off(offs, ng, rows, g), r1 = grp_off(offs, ng, rows, g + 1);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+        for (int64_t c = 0; c < cols; c++)
+            for (int64_t r = r0; r < r1; r++) {
+                unsigned byte = s[c * s_ld + base + (r - r0) / 32];
+                double v = byte == 0xFFu ? NAN : ldexp(orc_fp8_value(fmt, q[c * rows + r]), (int)byte - 127);
+                put_out(y, out_dt, c * rows + r, v);
+            }
+        base += (r1 - r0 + 31) / 32;
+    }
+}
+
+/* Array form of orc_bf16_round, for the tests' sweeps. */
+void orc_bf16_round_array(const float* f, int64_t n, uint16_t* out, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t i = 0; i < n; i++) out[i] = orc_bf16_round(f[i]);
 }

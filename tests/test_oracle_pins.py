@@ -446,3 +446,121 @@ def test_scaled_cast_overflow_matches_ieee_single():
             np.testing.assert_array_equal(q, torch_encode(fmt, prod.astype(np.float64)))
             assert sat == int((np.abs(prod) > oracle.fp8_max(fmt)).sum())
     assert oracle.reciprocal(np.float32(1e-45)) == np.inf
+
+
+# --------------------------------------------------------------------------
+# Dequantization ("HiFloat8：高性能训练之路" 1.1-1.2: de-scaling by
+# scale_inv; "Blackwell GPU MXFP8 预训练最佳实践" 4.1, 4.3: value * 2^X)
+# --------------------------------------------------------------------------
+F8_TORCH = {oracle.E4M3: torch.float8_e4m3fn, oracle.E5M2: torch.float8_e5m2}
+
+
+def _torch_bf16_bits(f32: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(f32, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_bf16_rounding_matches_torch():
+    """The oracle's nearest-BF16 against torch's float32 -> bfloat16 (RNE)."""
+    rng = np.random.default_rng(21)
+    bits = rng.integers(0, 1 << 32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    # exact midpoints and their neighbours, the top binade, subnormals
+    mids = (rng.integers(0, 1 << 16, size=4096, dtype=np.uint64).astype(np.uint32) << 16) | 0x8000
+    edge = np.array([0x7F7F7FFF, 0x7F7F8000, 0x7F7F8001, 0x7F7FFFFF, 0xFF7F8000, 0x00008000,
+                     0x00018000, 0x00000001, 0x80000001, 0x3DCCCCCD], np.uint32)
+    bits = np.concatenate([bits, mids, mids + 1, mids - 1, edge])
+    f = bits.view(np.float32)
+    got = oracle.bf16_round(f)
+    want = _torch_bf16_bits(f)
+    ok = ~np.isnan(f)
+    np.testing.assert_array_equal(got[ok], want[ok])
+    assert (got[~ok] == 0x7FC0).all()
+
+
+def test_bf16_rounding_page_example():
+    """BF16(0.1) = 0.10009765625 ("混合精度与 FP8 训练" 2.2)."""
+    b = int(oracle.bf16_round([np.float32(0.1)])[0])
+    assert np.array([b << 16], np.uint32).view(np.float32)[0] == np.float32(0.10009765625)
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_dequant_decode_matches_torch(fmt):
+    """All 256 codes at scale_inv 1 (FP32 out) against torch's float8 -> float32."""
+    codes = np.arange(256, dtype=np.uint8).reshape(1, 256)
+    y = oracle.dequant_per_tensor(codes, fmt, [1.0], out_dt=1).view(np.float32).reshape(-1)
+    want = torch.from_numpy(codes.reshape(-1)).view(F8_TORCH[fmt]).to(torch.float32).numpy()
+    nan = np.isnan(want)
+    np.testing.assert_array_equal(y[~nan], want[~nan])
+    assert np.isnan(y[nan]).all() and (y[nan].view(np.uint32) == 0x7FC00000).all()
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+@pytest.mark.parametrize("out_dt", [0, 1])
+def test_dequant_per_tensor_matches_torch(fmt, out_dt):
+    """y = round_out(fl32(value * scale_inv)) against torch float32 arithmetic."""
+    rng = np.random.default_rng(22)
+    q = rng.integers(0, 256, size=(64, 256), dtype=np.uint64).astype(np.uint8)
+    offs = np.array([0, 5, 5, 40, 64], np.int64)
+    si = np.array([1.0 / 448, 3.7e-3, 1.0, 2.0 ** 100], np.float32)
+    y = oracle.dequant_per_tensor(q, fmt, si, out_dt=out_dt, offsets=offs)
+    v = torch.from_numpy(q.reshape(-1)).view(F8_TORCH[fmt]).to(torch.float32).reshape(64, 256)
+    srow = torch.from_numpy(np.repeat(si, np.diff(offs)).astype(np.float32)).reshape(64, 1)
+    prod = (v * srow).numpy()
+    want = _torch_bf16_bits(prod) if out_dt == 0 else prod.view(np.uint32)
+    nan = np.isnan(prod)
+    np.testing.assert_array_equal(y[~nan], want[~nan])
+    assert (y[nan] == (0x7FC0 if out_dt == 0 else 0x7FC00000)).all()
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_mx_dequant_then_quantize_round_trips(fmt):
+    """Every finite code under every scale byte: a block holding
+    value(c) * 2^X next to the format's maximum times 2^X quantizes back to
+    byte X + 127 and code c, so the dequantizer applies exactly the
+    exponent the quantizer chose."""
+    fin = [c for c in range(256) if np.isfinite(oracle.fp8_value(fmt, c))]
+    maxc = oracle.fp8_max_code(fmt)
+    for byte in range(0, 255, 1):
+        X = byte - 127
+        if X > 127 - 16:  # max * 2^X would overflow FP32
+            continue
+        q = np.zeros((len(fin), 32), np.uint8)
+        q[:, 0] = fin
+        q[:, 1] = maxc
+        s = np.full((len(fin), 1), byte, np.uint8)
+        y = oracle.mx_dequantize(q, s, fmt, 1, len(fin), 32, out_dt=1).view(np.float32)
+        r = oracle.mx_quantize(y, fmt, 1)
+        assert (r["s_row"][:, 0] == byte).all(), byte
+        np.testing.assert_array_equal(r["q_row"][:, 0], np.array(fin, np.uint8))
+
+
+def test_mx_dequant_special_bytes_and_codes():
+    q = np.array([[0x00, 0x80, 0x7F, 0x01] * 8], np.uint8)
+    y = oracle.mx_dequantize(q, np.array([[0xFF]], np.uint8), oracle.E4M3, 1, 1, 32, out_dt=1).view(np.uint32)
+    assert (y == 0x7FC00000).all()  # scale byte 0xFF: every element NaN
+    y = oracle.mx_dequantize(q, np.array([[0]], np.uint8), oracle.E4M3, 1, 1, 32, out_dt=1).view(np.float32)
+    assert y[0, 0] == 0.0 and np.signbit(y[0, 1]) and np.isnan(y[0, 2])
+    assert y[0, 3] == np.float32(2.0 ** -9 * 2.0 ** -127)  # smallest subnormal code at X = -127, exact
+    big = oracle.mx_dequantize(np.array([[0x7E] * 32], np.uint8), np.array([[254]], np.uint8), oracle.E4M3, 1, 1,
+                               32, out_dt=0)
+    assert (big == 0x7F80).all()  # 448 * 2^127 overflows to +Inf
+
+
+def test_mx_dequant_columnwise_is_rowwise_of_transpose():
+    """The columnwise copy dequantizes in its own [cols][rows] layout exactly
+    as the rowwise copy of x^T does; with groups, as each group's slice."""
+    rng = np.random.default_rng(23)
+    x = _bf16_from_f32(rng.standard_normal((96, 64)) * np.exp(rng.standard_normal((96, 1)) * 3))
+    both = oracle.mx_quantize(x, oracle.E4M3, 3)
+    yc = oracle.mx_dequantize(both["q_col"], both["s_col"], oracle.E4M3, 2, 96, 64)
+    rt = oracle.mx_quantize(np.ascontiguousarray(x.T), oracle.E4M3, 1)
+    yr = oracle.mx_dequantize(rt["q_row"], rt["s_row"], oracle.E4M3, 1, 64, 96)
+    np.testing.assert_array_equal(yc, yr)
+    offs = np.array([0, 7, 7, 45, 96], np.int64)
+    g = oracle.mx_quantize(x, oracle.E5M2, 2, offsets=offs)
+    yg = oracle.mx_dequantize(g["q_col"], g["s_col"], oracle.E5M2, 2, 96, 64, offsets=offs)
+    for a, b in zip(offs[:-1], offs[1:]):
+        if a == b:
+            continue
+        sl = oracle.mx_quantize(np.ascontiguousarray(x[a:b]), oracle.E5M2, 2)
+        ys = oracle.mx_dequantize(sl["q_col"], sl["s_col"], oracle.E5M2, 2, b - a, 64)
+        np.testing.assert_array_equal(yg[:, a:b], ys)
