@@ -65,6 +65,9 @@ typedef enum { FP8Q_E4M3 = 0, FP8Q_E5M2 = 1 } fp8q_format;
 
 typedef enum { MXFP8_ROW = 1, MXFP8_COL = 2, MXFP8_BOTH = 3 } mxfp8_dir;
 
+/* Output type of the dequantizers. */
+typedef enum { FP8Q_OUT_BF16 = 0, FP8Q_OUT_FP32 = 1 } fp8q_out_dtype;
+
 /* Library version (major * 10000 + minor * 100 + patch). */
 FP8Q_API int32_t fp8q_version(void);
 
@@ -270,6 +273,43 @@ FP8Q_API fp8q_status mxfp8_quantize(const void* x, int32_t dt, int64_t rows, int
                            const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
                            int32_t dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                            uint8_t* s_col, int64_t s_col_ld, void* stream);
+
+/*
+ * Dequantization.  ("HiFloat8：高性能训练之路" 1.1-1.2: a quantized tensor is
+ * de-scaled by scale_inv = 1 / Scale; "Blackwell GPU MXFP8 预训练最佳实践"
+ * 4.1 and 4.3: an MX element stands for value * 2^X, X = byte - 127, and
+ * without MX hardware the blocks are dequantized to BF16 for a BF16
+ * matmul.)  Codes are decoded exactly.  BF16 output rounds to nearest, ties
+ * to even; every NaN result is the canonical quiet NaN (BF16 0x7FC0, FP32
+ * 0x7FC00000).  q and y must be 16-byte aligned; out_dt is FP8Q_OUT_BF16
+ * (2 bytes per element) or FP8Q_OUT_FP32 (4 bytes).
+ */
+
+/*
+ * y[i] = fl_out(fl32(value(q[i]) * scale_inv[g])) for the rows of group g.
+ *   q          device uint8[rows*cols], the codes of fp8q_cast_per_tensor
+ *   scale_inv  device float[num_groups]
+ *   y          device BF16 or FP32 [rows*cols]
+ */
+FP8Q_API fp8q_status fp8q_dequantize_per_tensor(const uint8_t* q, int64_t rows, int64_t cols,
+                                                const int64_t* group_offsets, int32_t num_groups,
+                                                int32_t fmt, const float* scale_inv, int32_t out_dt,
+                                                void* y, void* stream);
+
+/*
+ * One MX copy back to high precision: y = fl_out(value(q) * 2^(s - 127)),
+ * scale byte 0xFF -> NaN.  rows x cols is the original tensor (cols % 32 ==
+ * 0).
+ *   dir MXFP8_ROW: q = q_row [rows][cols], s = s_row [rows][cols/32]
+ *                  (s_ld ignored), y [rows][cols].
+ *   dir MXFP8_COL: q = q_col [cols][rows], s = s_col [cols][s_ld] with the
+ *                  column blocks of all groups in order, as mxfp8_quantize
+ *                  wrote them; y [cols][rows], the copy's own (transposed)
+ *                  layout.  Blocks past s_ld dequantize to NaN.
+ */
+FP8Q_API fp8q_status mxfp8_dequantize(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t cols,
+                                      const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
+                                      int32_t dir, int64_t s_ld, int32_t out_dt, void* y, void* stream);
 
 #ifdef __cplusplus
 }

@@ -25,7 +25,7 @@ __all__ = [
     "E4M3", "E5M2", "ROW", "COL", "BOTH", "build", "library_path", "lib",
     "fp8q_amax", "fp8q_cast_per_tensor", "fp8q_cast_workspace_bytes", "DelayedScaling",
     "mxfp8_quantize", "mxfp8_col_blocks", "Fp8qError", "check_device", "set_wait_budget_ns",
-    "fp8q_scale_from_amax", "debug_stall_mx_producer",
+    "fp8q_scale_from_amax", "debug_stall_mx_producer", "fp8q_dequantize_per_tensor", "mxfp8_dequantize",
 ]
 
 E4M3 = 0
@@ -43,6 +43,10 @@ _SIGS = {
     "fp8q_check_device": (_c.c_int, [_P]),
     "fp8q_debug_stall_mx_producer": (_c.c_int, [_c.c_int32]),
     "fp8q_scale_from_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int32, _c.c_int32, _P, _P, _P]),
+    "fp8q_dequantize_per_tensor": (_c.c_int, [_P, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _P,
+                                              _c.c_int32, _P, _P]),
+    "mxfp8_dequantize": (_c.c_int, [_P, _P, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _c.c_int32,
+                                    _c.c_int64, _c.c_int32, _P, _P]),
     "fp8q_set_wait_budget_ns": (_c.c_int, [_c.c_uint64]),
     "fp8q_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _P, _P]),
     "fp8q_cast_workspace_bytes": (_c.c_size_t, [_c.c_int32]),
@@ -376,3 +380,49 @@ def mxfp8_quantize(x: torch.Tensor, fmt: int = E4M3, direction: int = BOTH, grou
                                 _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), s_col_ld, _stream()),
            "mxfp8_quantize")
     return {"q_row": q_row, "s_row": s_row, "q_col": q_col, "s_col": s_col, "s_col_ld": s_col_ld}
+
+
+# ---------------------------------------------------------------------------
+# dequantization
+# ---------------------------------------------------------------------------
+def _out_dtype(out_dtype) -> int:
+    if out_dtype == torch.bfloat16:
+        return 0
+    if out_dtype == torch.float32:
+        return 1
+    raise TypeError("out_dtype must be torch.bfloat16 or torch.float32")
+
+
+def fp8q_dequantize_per_tensor(q: torch.Tensor, scale_inv: torch.Tensor, fmt: int = E4M3, group_offsets=None,
+                               out_dtype=torch.bfloat16, out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = round_out(fl32(value(q) * scale_inv[g])), shaped like q (uint8 codes)."""
+    if not q.is_cuda or q.dtype != torch.uint8 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous uint8 CUDA tensor")
+    rows, cols = _as_2d(q)
+    off, G = _offsets(group_offsets, q.device)
+    si = scale_inv.to(device=q.device, dtype=torch.float32).reshape(-1).contiguous()
+    if si.numel() != G:
+        raise ValueError("scale_inv must hold one value per group")
+    y = torch.empty(q.shape, dtype=out_dtype, device=q.device) if out is None else out
+    _check(lib().fp8q_dequantize_per_tensor(_ptr(q), rows, cols, _ptr(off), G, fmt, _ptr(si),
+                                            _out_dtype(out_dtype), _ptr(y), _stream()),
+           "fp8q_dequantize_per_tensor")
+    return y
+
+
+def mxfp8_dequantize(q: torch.Tensor, s: torch.Tensor, rows: int, cols: int, fmt: int = E4M3,
+                     direction: int = ROW, group_offsets=None, out_dtype=torch.bfloat16,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """One MX copy back to high precision, in the copy's own layout.
+
+    direction ROW: q [rows, cols], s [rows, cols/32] -> y [rows, cols].
+    direction COL: q [cols, rows], s [cols, s_ld] -> y [cols, rows].
+    """
+    if not q.is_cuda or q.dtype != torch.uint8 or not q.is_contiguous() or not s.is_contiguous():
+        raise ValueError("q and s must be contiguous uint8 CUDA tensors")
+    off, G = _offsets(group_offsets, q.device)
+    s_ld = s.shape[-1] if s.dim() == 2 else 0
+    y = torch.empty(q.shape, dtype=out_dtype, device=q.device) if out is None else out
+    _check(lib().mxfp8_dequantize(_ptr(q), _ptr(s), rows, cols, _ptr(off), G, fmt, direction, s_ld,
+                                  _out_dtype(out_dtype), _ptr(y), _stream()), "mxfp8_dequantize")
+    return y

@@ -317,4 +317,46 @@ fp8q_status mxfp8_quantize(const void* x, int32_t dt, int64_t rows, int64_t cols
                    (cudaStream_t)stream);
 }
 
+static fp8q_status check_dequant_common(const uint8_t* q, int64_t rows, int64_t cols, const int64_t* off, int G,
+                                        int32_t fmt, int32_t out_dt, const void* y) {
+  if (rows < 0 || cols < 0) return fail(FP8Q_ERR_INVALID_ARG, "rows and cols must be >= 0");
+  if (G < 1 || G > FP8Q_MAX_GROUPS) return fail(FP8Q_ERR_INVALID_ARG, "num_groups must be in [1, %d]", FP8Q_MAX_GROUPS);
+  if (off != nullptr && !aligned(off, 8)) return fail(FP8Q_ERR_INVALID_ARG, "group_offsets must be 8-byte aligned");
+  if (!fmt_ok(fmt)) return fail(FP8Q_ERR_INVALID_ARG, "fmt must be FP8Q_E4M3 or FP8Q_E5M2");
+  if (out_dt != FP8Q_OUT_BF16 && out_dt != FP8Q_OUT_FP32)
+    return fail(FP8Q_ERR_INVALID_ARG, "out_dt must be FP8Q_OUT_BF16 or FP8Q_OUT_FP32");
+  if (rows * cols > 0 && (!q || !y)) return fail(FP8Q_ERR_INVALID_ARG, "q and y must not be NULL");
+  if (!aligned(q, 16) || !aligned(y, 16)) return fail(FP8Q_ERR_INVALID_ARG, "q and y must be 16-byte aligned");
+  return FP8Q_OK;
+}
+
+fp8q_status fp8q_dequantize_per_tensor(const uint8_t* q, int64_t rows, int64_t cols, const int64_t* group_offsets,
+                                       int32_t num_groups, int32_t fmt, const float* scale_inv, int32_t out_dt,
+                                       void* y, void* stream) {
+  g_err[0] = 0;
+  fp8q_status r = check_dequant_common(q, rows, cols, group_offsets, num_groups, fmt, out_dt, y);
+  if (r != FP8Q_OK) return r;
+  if (!scale_inv || !aligned(scale_inv, 4)) return fail(FP8Q_ERR_INVALID_ARG, "scale_inv must be a 4-byte aligned device pointer");
+  if (rows * cols == 0) return FP8Q_OK;
+  return launch_dequant(0, q, nullptr, scale_inv, group_offsets, num_groups, rows, cols, 0, fmt, out_dt, y,
+                        (cudaStream_t)stream);
+}
+
+fp8q_status mxfp8_dequantize(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t cols,
+                             const int64_t* group_offsets, int32_t num_groups, int32_t fmt, int32_t dir,
+                             int64_t s_ld, int32_t out_dt, void* y, void* stream) {
+  g_err[0] = 0;
+  fp8q_status r = check_dequant_common(q, rows, cols, group_offsets, num_groups, fmt, out_dt, y);
+  if (r != FP8Q_OK) return r;
+  if (dir != MXFP8_ROW && dir != MXFP8_COL) return fail(FP8Q_ERR_INVALID_ARG, "dir must be MXFP8_ROW or MXFP8_COL");
+  if (cols % 32 != 0) return fail(FP8Q_ERR_UNSUPPORTED, "MXFP8 needs cols %% 32 == 0 (cols = %lld)", (long long)cols);
+  if (rows * cols > 0 && !s) return fail(FP8Q_ERR_INVALID_ARG, "s must not be NULL");
+  if (dir == MXFP8_COL && s_ld < (rows + 31) / 32)
+    return fail(FP8Q_ERR_INVALID_ARG, "s_ld (%lld) is below ceil(rows / 32) = %lld", (long long)s_ld,
+                (long long)((rows + 31) / 32));
+  if (rows * cols == 0) return FP8Q_OK;
+  return launch_dequant(dir == MXFP8_ROW ? 1 : 2, q, s, nullptr, group_offsets, num_groups, rows, cols, s_ld, fmt,
+                        out_dt, y, (cudaStream_t)stream);
+}
+
 }  // extern "C"

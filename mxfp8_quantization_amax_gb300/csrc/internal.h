@@ -102,6 +102,11 @@ fp8q_status launch_amax(const PtLaunch& p, bool finalize_scales);
 // Cast pass (optionally with fused amax into acc[] and saturation counts).
 fp8q_status launch_cast(const PtLaunch& p);
 
+// Dequantization; kind 0 per-tensor, 1 MX rowwise copy, 2 MX columnwise copy.
+fp8q_status launch_dequant(int kind, const uint8_t* q, const uint8_t* s, const float* scale_inv,
+                           const int64_t* off, int G, int64_t rows, int64_t cols, int64_t s_ld, int fmt,
+                           int out_dt, void* y, cudaStream_t stream);
+
 // MXFP8.
 fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* off, int G,
                       int fmt, int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,

@@ -111,6 +111,25 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.fp8q_delayed_step(None, aligned, 0, 4, aligned, None, None, None, None, None) == 1
 
 
+def test_dequantize_arguments_rejected_on_host(lib):
+    buf = ctypes.create_string_buffer(256)
+    aligned = (ctypes.addressof(buf) + 15) // 16 * 16
+    mis = aligned + 1
+    # per-tensor: bad out_dt, bad fmt, missing scale_inv, misaligned y
+    assert lib.fp8q_dequantize_per_tensor(aligned, 4, 4, None, 1, 0, aligned, 2, aligned, None) == 1
+    assert lib.fp8q_dequantize_per_tensor(aligned, 4, 4, None, 1, 7, aligned, 0, aligned, None) == 1
+    assert lib.fp8q_dequantize_per_tensor(aligned, 4, 4, None, 1, 0, None, 0, aligned, None) == 1
+    assert lib.fp8q_dequantize_per_tensor(aligned, 4, 4, None, 1, 0, aligned, 0, mis, None) == 1
+    # MX: both directions at once, cols % 32, s_ld too small, missing scales
+    assert lib.mxfp8_dequantize(aligned, aligned, 4, 64, None, 1, 0, 3, 1, 0, aligned, None) == 1
+    assert lib.mxfp8_dequantize(aligned, aligned, 4, 48, None, 1, 0, 1, 0, 0, aligned, None) == 2
+    assert lib.mxfp8_dequantize(aligned, aligned, 100, 64, None, 1, 0, 2, 3, 0, aligned, None) == 1
+    assert lib.mxfp8_dequantize(aligned, None, 4, 64, None, 1, 0, 1, 0, 0, aligned, None) == 1
+    # empty tensors return before any launch
+    assert lib.mxfp8_dequantize(None, None, 0, 64, None, 1, 0, 1, 0, 0, None, None) == 0
+    assert lib.fp8q_dequantize_per_tensor(None, 0, 4, None, 1, 0, aligned, 0, None, None) == 0
+
+
 def test_empty_mx_is_a_no_op(lib):
     # rows * cols == 0 returns before any launch
     assert lib.mxfp8_quantize(None, 0, 0, 64, None, 1, 0, 3, None, None, None, None, 0, None) == 0
