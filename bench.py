@@ -21,7 +21,8 @@ in every 8th timed step, against the measured HBM copy bandwidth.
   per_tensor_1024 (1024x1024 current scaling),
   delayed_8192 (8192x8192 delayed steps), linear_layer (A, W, E of an
   8B-class layer, MXFP8 both directions), moe (65536x7168, 64 experts:
-  grouped MXFP8 and grouped current scaling).
+  grouped MXFP8 and grouped current scaling), dequant_8192 (both MXFP8
+  copies and a per-tensor code array of 8192x8192 back to BF16).
 --impl reference: the CPU oracle on this host (a bounded sample per step).
 """
 from __future__ import annotations
@@ -53,7 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="activation",
-                   choices=["activation", "mx_8192", "per_tensor_1024", "delayed_8192", "linear_layer", "moe"])
+                   choices=["activation", "mx_8192", "per_tensor_1024", "delayed_8192", "linear_layer", "moe",
+                            "dequant_8192"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
@@ -103,7 +105,19 @@ def workload_spec(name):
         ops = [{"kind": "mx_grouped", "shape": (r, c), "fmt": E4M3, "bytes": None, "gen": ("c5", 0)},
                {"kind": "current_grouped", "shape": (r, c), "fmt": E4M3, "bytes": 5 * r * c, "gen": ("c5", 0)}]
         return {"workload": "moe_64_experts_65536x7168_bf16", "rows": r, "cols": c, "experts": 64}, ops
+    if name == "dequant_8192":
+        r = c = 8192
+        ops = [{"kind": "dq_mx_row", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + r * c // 32, "gen": ("c2", 0)},
+               {"kind": "dq_mx_col", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + c * (r // 32), "gen": ("c2", 0)},
+               {"kind": "dq_tensor", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + 4, "gen": ("c2", 1)}]
+        return {"workload": "dequantize_8192x8192_to_bf16", "rows": r, "cols": c,
+                "ops": ["mxfp8 e4m3 rowwise copy -> bf16", "mxfp8 e4m3 columnwise copy -> bf16",
+                        "per-tensor e4m3 -> bf16"]}, ops
     raise ValueError(name)
+
+
+DQ_KINDS = ("dq_mx_row", "dq_mx_col", "dq_tensor")
+ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row")
 
 
 def host_input(gen, shape):
@@ -278,7 +292,7 @@ def run_ours(args):
         for op, h in zip(ops, host):
             r, c = op["shape"]
             x = h.to(dev, non_blocking=True)
-            b = {"x": x}
+            b = {"x": x, "in": [x]}
             if op["kind"] in ("mx", "mx_grouped"):
                 ld = fq.mxfp8_col_blocks(r, None if offsets_host is None else list(offsets_host))
                 if offsets_host is not None:
@@ -288,6 +302,18 @@ def run_ours(args):
                             "q_col": torch.empty((c, r), dtype=torch.uint8, device=dev),
                             "s_col": torch.empty((c, ld), dtype=torch.uint8, device=dev)}
                 b["ld"] = ld
+            elif op["kind"] in DQ_KINDS:
+                # the codes to dequantize, made by the library's own quantizers
+                # before timing; the BF16 input is not kept
+                if op["kind"] == "dq_tensor":
+                    qr = fq.fp8q_cast_per_tensor(x, op["fmt"])
+                    b["in"] = [qr["q"], qr["scale_inv"]]
+                else:
+                    qr = fq.mxfp8_quantize(x, op["fmt"], 3)
+                    b["in"] = [qr["q_row"], qr["s_row"]] if op["kind"] == "dq_mx_row" else [qr["q_col"], qr["s_col"]]
+                b["y"] = torch.empty(b["in"][0].shape, dtype=torch.bfloat16, device=dev)
+                b["x"] = None
+                del x
             else:
                 b["q"] = torch.empty((r, c), dtype=torch.uint8, device=dev)
                 G = 64 if op["kind"] == "current_grouped" else 1
@@ -326,6 +352,16 @@ def run_ours(args):
                     pt["amax"].data_ptr(), pt["scale"].data_ptr(), pt["scale_inv"].data_ptr(), None,
                     b["ws"].data_ptr(), b["ws"].numel(), stream))
                 b["launches"] = 2
+            elif k == "dq_tensor":
+                b["call"] = (lib.fp8q_dequantize_per_tensor, (
+                    b["in"][0].data_ptr(), r, c, None, 1, op["fmt"], b["in"][1].data_ptr(), 0, b["y"].data_ptr(),
+                    stream))
+                b["launches"] = 1
+            elif k in ("dq_mx_row", "dq_mx_col"):
+                b["call"] = (lib.mxfp8_dequantize, (
+                    b["in"][0].data_ptr(), b["in"][1].data_ptr(), r, c, None, 1, op["fmt"],
+                    1 if k == "dq_mx_row" else 2, b["in"][1].shape[1], 0, b["y"].data_ptr(), stream))
+                b["launches"] = 1
             else:
                 dl = b["dl"]
                 b["call"] = (lib.fp8q_delayed_step, (
@@ -336,7 +372,7 @@ def run_ours(args):
     mx_events = []
     launches = {"n": 0}
 
-    mx_first = next((j for j, op in enumerate(ops) if op["kind"] in ("mx", "mx_grouped")), None)
+    mx_first = next((j for j, op in enumerate(ops) if op["kind"] in ROOFLINE_KINDS), None)
 
     def step(i, record_mx=False):
         bufs = sets[i % nsets]
@@ -387,30 +423,29 @@ def run_ours(args):
     # end-to-end: host inputs -> device, the step, device -> host outputs
     e2e = None
     if not args.no_e2e:
-        outs_host = []
-        for op in ops:
-            r, c = op["shape"]
+        # each op's step inputs as pinned host copies (the quantizers' BF16
+        # input, or the dequantizers' codes and scales) and its outputs
+        def outputs(op, b):
             if op["kind"] in ("mx", "mx_grouped"):
-                ld = sets[0][ops.index(op)]["ld"]
-                outs_host.append([torch.empty(n, dtype=torch.uint8).pin_memory()
-                                  for n in (r * c, r * (c // 32), c * r, c * ld)])
-            else:
-                outs_host.append([torch.empty(r * c, dtype=torch.uint8).pin_memory()])
-        bi = sum(h.numel() * 2 for h in host)
+                o = b["out"]
+                return [o["q_row"], o["s_row"], o["q_col"], o["s_col"]]
+            return [b["y"]] if op["kind"] in DQ_KINDS else [b["q"]]
+
+        ins_host = [[t.cpu().pin_memory() for t in sets[0][j]["in"]] for j in range(len(ops))]
+        outs_host = [[torch.empty(t.numel() * t.element_size(), dtype=torch.uint8).pin_memory()
+                      for t in outputs(op, sets[0][j])] for j, op in enumerate(ops)]
+        bi = sum(t.numel() * t.element_size() for lst in ins_host for t in lst)
         bo = sum(t.numel() for lst in outs_host for t in lst)
 
         def e2e_step(i):
             b = sets[i % nsets]
-            for j, op in enumerate(ops):
-                b[j]["x"].copy_(host[j], non_blocking=True)
+            for j in range(len(ops)):
+                for dst, src in zip(b[j]["in"], ins_host[j]):
+                    dst.copy_(src, non_blocking=True)
             step(i)
             for j, op in enumerate(ops):
-                if op["kind"] in ("mx", "mx_grouped"):
-                    o = b[j]["out"]
-                    for dst, src in zip(outs_host[j], (o["q_row"], o["s_row"], o["q_col"], o["s_col"])):
-                        dst.copy_(src.reshape(-1), non_blocking=True)
-                else:
-                    outs_host[j][0].copy_(b[j]["q"].reshape(-1), non_blocking=True)
+                for dst, src in zip(outs_host[j], outputs(op, b[j])):
+                    dst.copy_(src.reshape(-1).view(torch.uint8), non_blocking=True)
 
         for i in range(3):
             e2e_step(i)
@@ -437,7 +472,7 @@ def run_ours(args):
     ms_per_step = elapsed_ms / args.steps
     value = job_gbs(bytes_per_step, world, ms_per_step)
     peak, peak_src = hbm_peak()
-    mx_op = next((op for op in ops if op["kind"] in ("mx", "mx_grouped")), None)
+    mx_op = next((op for op in ops if op["kind"] in ROOFLINE_KINDS), None)
     roofline = None
     if mx_op is not None and mx_ms:
         # average over the sampled launches of the step's first MXFP8 op
@@ -445,7 +480,8 @@ def run_ours(args):
         achieved = mx_op["bytes"] / (avg_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                    "kernel": "mx_kernel<bf16,%s,both>" % ("e4m3" if mx_op["fmt"] == E4M3 else "e5m2"),
+                    "kernel": ("dequant_kernel<mx_row,%s,bf16>" if mx_op["kind"] == "dq_mx_row"
+                               else "mx_kernel<bf16,%s,both>") % ("e4m3" if mx_op["fmt"] == E4M3 else "e5m2"),
                     "algorithmic_bytes_per_launch": mx_op["bytes"], "avg_launch_us": round(avg_ms * 1e3, 3),
                     "launches_timed": len(mx_ms),
                     "traffic": kernel_traffic(args.workload)}
@@ -477,14 +513,21 @@ def oracle_sample_step(workload, sample_rows, inputs, states):
     cfg, ops = workload_spec(workload)
     total = 0
     for op, x, st in zip(ops, inputs, states):
-        r, c = x.shape
         k = op["kind"]
+        r, c = x["shape"] if k in DQ_KINDS else x.shape
         if k in ("mx", "mx_grouped"):
             oracle.mx_quantize(x, op["fmt"], 3)
             total += mx_bytes(r, c)
         elif k in ("current", "current_grouped"):
             oracle.current_scaling(x, op["fmt"])
             total += 5 * r * c
+        elif k == "dq_tensor":
+            oracle.dequant_per_tensor(x["q"], op["fmt"], x["scale_inv"])
+            total += 3 * r * c
+        elif k in ("dq_mx_row", "dq_mx_col"):
+            d = 1 if k == "dq_mx_row" else 2
+            oracle.mx_dequantize(x["q"], x["s"], op["fmt"], d, r, c)
+            total += 3 * r * c + x["s"].size
         else:
             st.step(x)
             total += 3 * r * c
@@ -498,14 +541,22 @@ def oracle_inputs(workload, sample_rows):
     for op in ops:
         r, c = op["shape"]
         rr = min(r, sample_rows)
-        xs.append(np.ascontiguousarray(host_input(op["gen"], (rr, c))))
+        x = np.ascontiguousarray(host_input(op["gen"], (rr, c)))
+        if op["kind"] == "dq_tensor":  # the codes to dequantize, made by the oracle before timing
+            cs = oracle.current_scaling(x, op["fmt"])
+            x = {"q": cs["q"].reshape(rr, c), "scale_inv": cs["scale_inv"], "shape": (rr, c)}
+        elif op["kind"] in ("dq_mx_row", "dq_mx_col"):
+            m = oracle.mx_quantize(x, op["fmt"], 3)
+            x = ({"q": m["q_row"], "s": m["s_row"], "shape": (rr, c)} if op["kind"] == "dq_mx_row"
+                 else {"q": m["q_col"], "s": m["s_col"], "shape": (rr, c)})
+        xs.append(x)
         states.append(oracle.DelayedScaling(16, 1, 3, op["fmt"]) if op["kind"] == "delayed" else None)
     return xs, states
 
 
 def sample_rows_for(workload):
     return {"activation": 256, "mx_8192": 128, "per_tensor_1024": 1024, "delayed_8192": 128, "linear_layer": 64,
-            "moe": 32}[workload]
+            "moe": 32, "dequant_8192": 128}[workload]
 
 
 def cpu_baseline(workload, budget_s=10.0):
