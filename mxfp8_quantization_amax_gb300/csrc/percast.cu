@@ -487,9 +487,16 @@ static int ctas_per_sm(K kernel) {
   return per_sm;
 }
 
+#ifndef FP8Q_PT_BALANCED_GRID  // 1: as few CTAs as give every CTA the same chunk count
+#define FP8Q_PT_BALANCED_GRID 1
+#endif
 static int grid_for(int64_t n_chunks, int per_sm) {
   const int64_t resident = (int64_t)per_sm * sm_count();
   int64_t g = n_chunks < resident ? n_chunks : resident;
+  if (FP8Q_PT_BALANCED_GRID && n_chunks > resident) {
+    const int64_t per_cta = (n_chunks + resident - 1) / resident;
+    g = (n_chunks + per_cta - 1) / per_cta;
+  }
   return (int)(g < 1 ? 1 : g);
 }
 
