@@ -80,6 +80,9 @@ def _load():
         "orc_encode_f32_range": (None, [c.c_int, c.c_uint64, c.c_int64, P, c.c_int]),
         "orc_max_threads": (c.c_int, []),
         "orc_bf16_round": (c.c_uint16, [c.c_float]),
+        "orc_mx_block_rule": (c.c_uint8, [P, c.c_int, c.c_int, c.c_int, P, c.POINTER(c.c_int64)]),
+        "orc_mx_quantize_rule": (None, [P, c.c_int, c.c_int64, c.c_int64, P, c.c_int, c.c_int, c.c_int, c.c_int,
+                                        P, P, P, P, c.c_int64, P, c.c_int]),
         "orc_bf16_round_array": (None, [P, c.c_int64, P, c.c_int]),
         "orc_dequant_per_tensor": (None, [P, c.c_int64, c.c_int64, P, c.c_int, c.c_int, P, c.c_int, P,
                                           c.c_int]),
@@ -293,6 +296,18 @@ def mx_block(values: np.ndarray, fmt: int) -> tuple[int, np.ndarray]:
     return int(b), q
 
 
+MX_RULE_UP, MX_RULE_OCP = 0, 1
+
+
+def mx_block_rule(values: np.ndarray, fmt: int, rule: int) -> tuple[int, np.ndarray, int]:
+    """One MX block under a scale rule -> (scale byte, codes, saturated count)."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    q = np.zeros(v.size, dtype=np.uint8)
+    n = ctypes.c_int64(0)
+    b = _load().orc_mx_block_rule(_ptr(v), v.size, fmt, rule, _ptr(q), ctypes.byref(n))
+    return int(b), q, int(n.value)
+
+
 def mx_col_blocks(rows: int, offsets=None) -> int:
     """sum over groups of ceil(n_g / 32) (one group when offsets is None)."""
     if offsets is None:
@@ -328,6 +343,32 @@ def mx_quantize(x: np.ndarray, fmt: int, direction: int = 3, offsets=None,
         _ptr(q_col if q_col is not None else dummy), _ptr(s_col if s_col is not None else dummy),
         ld, nthreads or max_threads())
     return {"q_row": q_row, "s_row": s_row, "q_col": q_col, "s_col": s_col, "col_blocks": T}
+
+
+def mx_quantize_rule(x: np.ndarray, fmt: int, direction: int, rule: int, offsets=None,
+                     s_col_ld: int | None = None, nthreads: int = 0) -> dict:
+    """mx_quantize under a scale rule (MX_RULE_UP or MX_RULE_OCP), plus
+    'sat': the saturated-element counts [rowwise, columnwise]."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    assert cols % 32 == 0
+    G = 1 if offsets is None else len(offsets) - 1
+    o = None if offsets is None else np.ascontiguousarray(offsets, dtype=np.int64)
+    T = mx_col_blocks(rows, o)
+    ld = T if s_col_ld is None else s_col_ld
+    q_row = np.zeros((rows, cols), np.uint8) if direction & 1 else None
+    s_row = np.zeros((rows, cols // 32), np.uint8) if direction & 1 else None
+    q_col = np.zeros((cols, rows), np.uint8) if direction & 2 else None
+    s_col = np.zeros((cols, max(ld, 1)), np.uint8) if direction & 2 else None
+    sat = np.zeros(2, np.int64)
+    dummy = np.zeros(1, np.uint8)
+    _load().orc_mx_quantize_rule(
+        _ptr(x), _dtype_code(x), rows, cols, _ptr(o) if o is not None else None, G, fmt, direction, rule,
+        _ptr(q_row if q_row is not None else dummy), _ptr(s_row if s_row is not None else dummy),
+        _ptr(q_col if q_col is not None else dummy), _ptr(s_col if s_col is not None else dummy),
+        ld, _ptr(sat), nthreads or max_threads())
+    return {"q_row": q_row, "s_row": s_row, "q_col": q_col, "s_col": s_col, "col_blocks": T,
+            "sat": [int(sat[0]), int(sat[1])]}
 
 
 # --------------------------------------------------------------------------

@@ -275,6 +275,53 @@ uint8_t orc_mx_block(const float* v, int k, int fmt, uint8_t* q)
     return (uint8_t)(X + 127);
 }
 
+/*
+ * The same block under a choice of scale rule, with a saturation count.
+ * rule 0: the round-up rule above.  rule 1: the OCP rule ("混合精度与 FP8
+ * 训练" 13.1; "Blackwell GPU MXFP8 预训练最佳实践" 4.1, its formula read as
+ * floor(log2 amax) - floor(log2 448)): X = floor(log2 amax) - e_max, e_max
+ * the exponent of the element format's largest value (8 for E4M3, 15 for
+ * E5M2), i.e. the largest integer X with 2^(X + e_max) <= amax, saturated to
+ * [-127, 127].  Elements are RNE_sat(v / 2^X) either way; *sat counts those
+ * whose scaled magnitude exceeds the format's maximum (the ones the
+ * conversion clamps; never under rule 0).
+ */
+uint8_t orc_mx_block_rule(const float* v, int k, int fmt, int rule, uint8_t* q, int64_t* sat)
+{
+    uint32_t amax = 0;
+    double destmax = orc_fp8_max(fmt);
+    int emax = (int)floor(log2(destmax));
+    int X, i;
+    *sat = 0;
+    if (rule == 0) {
+        uint8_t b = orc_mx_block(v, k, fmt, q);
+        if (b == 0xFF || b == 0) return b;
+        for (i = 0; i < k; i++)
+            if (fabs(ldexp((double)v[i], -((int)b - 127))) > destmax) (*sat)++;
+        return b;
+    }
+    for (i = 0; i < k; i++) {
+        uint32_t mag = float_to_bits(v[i]) & 0x7FFFFFFFu;
+        if (mag > amax) amax = mag;
+    }
+    if (amax >= 0x7F800000u) {
+        for (i = 0; i < k; i++) q[i] = 0x7F;
+        return 0xFF;
+    }
+    if (amax == 0) {
+        for (i = 0; i < k; i++) q[i] = 0x00;
+        return 0x00;
+    }
+    for (X = 127; X > -127; X--)
+        if (ldexp(1.0, X + emax) <= (double)bits_to_float(amax)) break;
+    for (i = 0; i < k; i++) {
+        double s = ldexp((double)v[i], -X);
+        if (fabs(s) > destmax) (*sat)++;
+        q[i] = (uint8_t)orc_fp8_encode(fmt, s);
+    }
+    return (uint8_t)(X + 127);
+}
+
 /* Group g covers rows [offs[g], offs[g+1]); offs == NULL means one group. */
 static int64_t grp_off(const int64_t* offs, int G, int64_t rows, int g)
 {
@@ -350,6 +397,59 @@ void orc_mx_quantize(const void* x, int dt, int64_t rows, int64_t cols, const in
             base += nb;
         }
     }
+}
+
+/* orc_mx_quantize under a scale rule (see orc_mx_block_rule), also
+ * returning the saturated-element counts of the rowwise (sat[0]) and
+ * columnwise (sat[1]) copies. */
+void orc_mx_quantize_rule(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* offs, int G,
+                          int fmt, int dir, int rule, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                          uint8_t* s_col, int64_t s_col_ld, int64_t* sat, int nthreads)
+{
+    int ng = offs ? G : 1;
+    int64_t sat_r = 0, sat_c = 0;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#endif
+    if (dir & 1) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads) reduction(+ : sat_r)
+#endif
+        for (int64_t r = 0; r < rows; r++) {
+            float v[32];
+            for (int64_t j = 0; j < cols / 32; j++) {
+                int64_t n = 0;
+                for (int i = 0; i < 32; i++) v[i] = orc_input_value(x, dt, r * cols + j * 32 + i);
+                s_row[r * (cols / 32) + j] = orc_mx_block_rule(v, 32, fmt, rule, q_row + r * cols + j * 32, &n);
+                sat_r += n;
+            }
+        }
+    }
+    if (dir & 2) {
+        int64_t base = 0;
+        for (int g = 0; g < ng; g++) {
+            int64_t r0 = grp_off(offs, ng, rows, g), r1 = grp_off(offs, ng, rows, g + 1);
+            int64_t nb = (r1 - r0 + 31) / 32;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads) reduction(+ : sat_c)
+#endif
+            for (int64_t c = 0; c < cols; c++) {
+                float v[32];
+                uint8_t qb[32];
+                for (int64_t b = 0; b < nb; b++) {
+                    int64_t rs = r0 + 32 * b, n = 0;
+                    int k = (int)((r1 - rs) < 32 ? (r1 - rs) : 32);
+                    for (int i = 0; i < k; i++) v[i] = orc_input_value(x, dt, (rs + i) * cols + c);
+                    s_col[c * s_col_ld + base + b] = orc_mx_block_rule(v, k, fmt, rule, qb, &n);
+                    sat_c += n;
+                    for (int i = 0; i < k; i++) q_col[c * rows + rs + i] = qb[i];
+                }
+            }
+            base += nb;
+        }
+    }
+    sat[0] = sat_r;
+    sat[1] = sat_c;
 }
 
 int orc_max_threads(void)

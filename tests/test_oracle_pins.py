@@ -564,3 +564,108 @@ def test_mx_dequant_columnwise_is_rowwise_of_transpose():
         sl = oracle.mx_quantize(np.ascontiguousarray(x[a:b]), oracle.E5M2, 2)
         ys = oracle.mx_dequantize(sl["q_col"], sl["s_col"], oracle.E5M2, 2, b - a, 64)
         np.testing.assert_array_equal(yg[:, a:b], ys)
+
+
+# --------------------------------------------------------------------------
+# MX scale rules: round-up (built) and the OCP round-down rule
+# ("混合精度与 FP8 训练" 13.1; "Blackwell GPU MXFP8 预训练最佳实践" 4.1)
+# --------------------------------------------------------------------------
+def _floor_log2_fraction(r: Fraction) -> int:
+    """Exact floor(log2 r) of a positive rational."""
+    e = r.numerator.bit_length() - r.denominator.bit_length()
+    while Fraction(2) ** e > r:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= r:
+        e += 1
+    return e
+
+
+def test_page_mx_ocp_examples():
+    """13.1's example: amax 5.3 in E4M3 -> shared exponent 2 - 8 = -6, the top
+    element becomes about 339 and nothing saturates; and the T8 case: amax 480
+    -> X_ocp = 0 saturates to 448 where the round-up rule's X = 1 does not."""
+    v = np.zeros(32, np.float32)
+    v[5], v[7] = 5.3, -5.3 / 3
+    b, q, n = oracle.mx_block_rule(v, oracle.E4M3, oracle.MX_RULE_OCP)
+    assert b - 127 == -6 and n == 0
+    assert abs(oracle.fp8_value(oracle.E4M3, int(q[5])) - 5.3 * 64) < 16
+    case = next(c for c in json.load(open(os.path.join(GOLD, "page_values.json")))["mx"] if c["id"] == "T8-ocp")
+    v[5], v[7] = case["amax"], -case["amax"] / 3
+    b, q, n = oracle.mx_block_rule(v, oracle.E4M3, oracle.MX_RULE_OCP)
+    assert b - 127 == case["X_ocp"] and n == 1 and q[5] == oracle.fp8_max_code(oracle.E4M3)
+    b, q, n = oracle.mx_block_rule(v, oracle.E4M3, oracle.MX_RULE_UP)
+    assert b - 127 == case["X_roundup"] and n == 0
+
+
+@pytest.mark.parametrize("fmt,emax", [(oracle.E4M3, 8), (oracle.E5M2, 15)])
+def test_mx_ocp_exponent_is_exact_floor_log2(fmt, emax):
+    """Over every positive finite BF16 value as the block amax, X equals
+    floor(log2 amax) - e_max in exact rational arithmetic, clamped to the
+    UE8M0 range."""
+    for bits in range(1, 0x7F80, 7):
+        a = float(np.array([bits << 16], np.uint32).view(np.float32)[0])
+        v = np.zeros(32, np.float32)
+        v[3] = a
+        b, _, _ = oracle.mx_block_rule(v, fmt, oracle.MX_RULE_OCP)
+        want = min(max(_floor_log2_fraction(Fraction(a)) - emax, -127), 127)
+        assert b - 127 == want, (hex(bits), b)
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_mx_rules_relation_and_saturation(fmt):
+    """On random blocks: the round-up exponent is the OCP one or one above
+    it; the round-up rule never saturates; the OCP rule saturates exactly the
+    elements the round-up rule keeps below the maximum only by choosing the
+    larger exponent; equal exponents give equal codes."""
+    rng = np.random.default_rng(31)
+    for _ in range(3000):
+        v = (rng.standard_normal(32) * np.exp(rng.standard_normal() * 8)).astype(np.float32)
+        bu, qu, nu = oracle.mx_block_rule(v, fmt, oracle.MX_RULE_UP)
+        bo, qo, no = oracle.mx_block_rule(v, fmt, oracle.MX_RULE_OCP)
+        assert bu - bo in (0, 1) and nu == 0
+        if bu == bo:
+            np.testing.assert_array_equal(qu, qo)
+            assert no == 0
+        else:
+            mx = oracle.fp8_max(fmt)
+            assert no == int(np.sum(np.abs(v.astype(np.float64)) * 2.0 ** -(bo - 127) > mx))
+
+
+def test_mx_quantize_rule_matches_blocks_and_transpose():
+    rng = np.random.default_rng(32)
+    x = _bf16_from_f32(rng.standard_normal((64, 96)) * np.exp(rng.standard_normal((64, 1)) * 3))
+    up = oracle.mx_quantize_rule(x, oracle.E4M3, 3, oracle.MX_RULE_UP)
+    base = oracle.mx_quantize(x, oracle.E4M3, 3)
+    for k in ("q_row", "s_row", "q_col", "s_col"):
+        np.testing.assert_array_equal(up[k], base[k])
+    assert up["sat"] == [0, 0]
+    ocp = oracle.mx_quantize_rule(x, oracle.E4M3, 3, oracle.MX_RULE_OCP)
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    nrow = 0
+    for i in range(64):
+        for j in range(3):
+            b, q, n = oracle.mx_block_rule(xf[i, 32 * j:32 * j + 32], oracle.E4M3, oracle.MX_RULE_OCP)
+            assert ocp["s_row"][i, j] == b
+            np.testing.assert_array_equal(ocp["q_row"][i, 32 * j:32 * j + 32], q)
+            nrow += n
+    assert ocp["sat"][0] == nrow
+    rt = oracle.mx_quantize_rule(np.ascontiguousarray(x.T), oracle.E4M3, 1, oracle.MX_RULE_OCP)
+    np.testing.assert_array_equal(ocp["q_col"], rt["q_row"])
+    np.testing.assert_array_equal(ocp["s_col"], rt["s_row"])
+    assert ocp["sat"][1] == rt["sat"][0]
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_mx_ocp_value_on_the_maximum_is_not_saturated(fmt):
+    """An element that scales exactly onto the format's maximum is
+    representable: it is not counted as saturated (|v * 2^-X| > max only)."""
+    mx = oracle.fp8_max(fmt)
+    for k in (-20, 0, 7):
+        v = np.zeros(32, np.float32)
+        v[0] = mx * 2.0 ** k
+        v[1] = -mx * 2.0 ** k
+        b, q, n = oracle.mx_block_rule(v, fmt, oracle.MX_RULE_OCP)
+        assert n == 0 and q[0] == oracle.fp8_max_code(fmt)
+        v[2] = np.float32(mx * 2.0 ** k * 1.0625)  # just above: saturates
+        b, q, n = oracle.mx_block_rule(v, fmt, oracle.MX_RULE_OCP)
+        assert n == 1
