@@ -65,6 +65,13 @@ typedef enum { FP8Q_E4M3 = 0, FP8Q_E5M2 = 1 } fp8q_format;
 
 typedef enum { MXFP8_ROW = 1, MXFP8_COL = 2, MXFP8_BOTH = 3 } mxfp8_dir;
 
+/* MX scale rule.  FP8Q_MX_RULE_UP: X = ceil(log2(amax / destmax)), the
+ * round-up rule ("Blackwell GPU MXFP8 预训练最佳实践" 4.1, Algorithm 1);
+ * FP8Q_MX_RULE_OCP: X = floor(log2(amax)) - e_max, the OCP rule ("混合精度与
+ * FP8 训练" 13.1; e_max = 8 for E4M3, 15 for E5M2), which can put elements
+ * above the format maximum (they saturate).  Both saturate X to [-127, 127]. */
+typedef enum { FP8Q_MX_RULE_UP = 0, FP8Q_MX_RULE_OCP = 1 } fp8q_mx_rule;
+
 /* Output type of the dequantizers. */
 typedef enum { FP8Q_OUT_BF16 = 0, FP8Q_OUT_FP32 = 1 } fp8q_out_dtype;
 
@@ -273,6 +280,21 @@ FP8Q_API fp8q_status mxfp8_quantize(const void* x, int32_t dt, int64_t rows, int
                            const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
                            int32_t dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                            uint8_t* s_col, int64_t s_col_ld, void* stream);
+
+/*
+ * mxfp8_quantize with a choice of scale rule (fp8q_mx_rule) and an optional
+ * count of saturated elements: those whose scaled magnitude |v / 2^X|
+ * exceeds the format maximum and are clamped to it ("Blackwell GPU MXFP8
+ * 预训练最佳实践" 4.1 compares the two rules by exactly this saturation).
+ *   sat_count  device uint64[2] or NULL: [0] rowwise copy, [1] columnwise
+ *              copy; zeroed by the call, then accumulated on the stream.
+ * Never saturates under FP8Q_MX_RULE_UP.  Other arguments as mxfp8_quantize.
+ */
+FP8Q_API fp8q_status mxfp8_quantize_rule(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                         const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
+                                         int32_t dir, int32_t scale_rule, uint8_t* q_row, uint8_t* s_row,
+                                         uint8_t* q_col, uint8_t* s_col, int64_t s_col_ld,
+                                         unsigned long long* sat_count, void* stream);
 
 /*
  * Dequantization.  ("HiFloat8：高性能训练之路" 1.1-1.2: a quantized tensor is

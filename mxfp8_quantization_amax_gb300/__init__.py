@@ -26,6 +26,7 @@ __all__ = [
     "fp8q_amax", "fp8q_cast_per_tensor", "fp8q_cast_workspace_bytes", "DelayedScaling",
     "mxfp8_quantize", "mxfp8_col_blocks", "Fp8qError", "check_device", "set_wait_budget_ns",
     "fp8q_scale_from_amax", "debug_stall_mx_producer", "fp8q_dequantize_per_tensor", "mxfp8_dequantize",
+    "RULE_UP", "RULE_OCP",
 ]
 
 E4M3 = 0
@@ -34,6 +35,8 @@ ROW = 1
 COL = 2
 BOTH = 3
 MAX_GROUPS = 4096
+RULE_UP = 0   # MX scale rule: X = ceil(log2(amax / destmax))
+RULE_OCP = 1  # MX scale rule: X = floor(log2(amax)) - e_max (can saturate)
 
 _c = ctypes
 _P = _c.c_void_p
@@ -43,6 +46,8 @@ _SIGS = {
     "fp8q_check_device": (_c.c_int, [_P]),
     "fp8q_debug_stall_mx_producer": (_c.c_int, [_c.c_int32]),
     "fp8q_scale_from_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int32, _c.c_int32, _P, _P, _P]),
+    "mxfp8_quantize_rule": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32,
+                                       _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_int64, _P, _P]),
     "fp8q_dequantize_per_tensor": (_c.c_int, [_P, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _P,
                                               _c.c_int32, _P, _P]),
     "mxfp8_dequantize": (_c.c_int, [_P, _P, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _c.c_int32,
@@ -343,7 +348,8 @@ def mxfp8_col_blocks(rows: int, group_offsets=None) -> int:
 
 
 def mxfp8_quantize(x: torch.Tensor, fmt: int = E4M3, direction: int = BOTH, group_offsets=None,
-                   s_col_ld: int | None = None, out: dict | None = None) -> dict:
+                   s_col_ld: int | None = None, out: dict | None = None, rule: int = RULE_UP,
+                   count_saturation: bool = False) -> dict:
     """MXFP8 rowwise and/or columnwise quantization of a 2-D tensor.
 
     Returns dict(q_row [rows, cols], s_row [rows, cols/32], q_col [cols, rows],
@@ -376,10 +382,20 @@ def mxfp8_quantize(x: torch.Tensor, fmt: int = E4M3, direction: int = BOTH, grou
     if direction & COL:
         q_col = buf("q_col", (cols, rows))
         s_col = buf("s_col", (cols, max(s_col_ld, 1)))
-    _check(lib().mxfp8_quantize(_ptr(x), _dt(x), rows, cols, _ptr(off), G, fmt, direction,
-                                _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), s_col_ld, _stream()),
-           "mxfp8_quantize")
-    return {"q_row": q_row, "s_row": s_row, "q_col": q_col, "s_col": s_col, "s_col_ld": s_col_ld}
+    sat = o.get("sat")
+    if count_saturation and sat is None:
+        sat = torch.empty(2, dtype=torch.int64, device=dev)
+    if rule == RULE_UP and not count_saturation:
+        _check(lib().mxfp8_quantize(_ptr(x), _dt(x), rows, cols, _ptr(off), G, fmt, direction,
+                                    _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), s_col_ld, _stream()),
+               "mxfp8_quantize")
+    else:
+        _check(lib().mxfp8_quantize_rule(_ptr(x), _dt(x), rows, cols, _ptr(off), G, fmt, direction, rule,
+                                         _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), s_col_ld,
+                                         _ptr(sat) if count_saturation else None, _stream()),
+               "mxfp8_quantize_rule")
+    return {"q_row": q_row, "s_row": s_row, "q_col": q_col, "s_col": s_col, "s_col_ld": s_col_ld,
+            "sat": sat if count_saturation else None}
 
 
 # ---------------------------------------------------------------------------

@@ -294,13 +294,28 @@ int64_t mxfp8_col_blocks(const int64_t* off, int32_t G, int64_t rows) {
 fp8q_status mxfp8_quantize(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
                            int32_t num_groups, int32_t fmt, int32_t dir, uint8_t* q_row, uint8_t* s_row,
                            uint8_t* q_col, uint8_t* s_col, int64_t s_col_ld, void* stream) {
+  return mxfp8_quantize_rule(x, dt, rows, cols, group_offsets, num_groups, fmt, dir, FP8Q_MX_RULE_UP, q_row,
+                             s_row, q_col, s_col, s_col_ld, nullptr, stream);
+}
+
+fp8q_status mxfp8_quantize_rule(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                const int64_t* group_offsets, int32_t num_groups, int32_t fmt, int32_t dir,
+                                int32_t scale_rule, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                                uint8_t* s_col, int64_t s_col_ld, unsigned long long* sat_count, void* stream) {
   g_err[0] = 0;
+  if (scale_rule != FP8Q_MX_RULE_UP && scale_rule != FP8Q_MX_RULE_OCP)
+    return fail(FP8Q_ERR_INVALID_ARG, "scale_rule must be FP8Q_MX_RULE_UP or FP8Q_MX_RULE_OCP");
+  if (!aligned(sat_count, 8)) return fail(FP8Q_ERR_INVALID_ARG, "sat_count must be 8-byte aligned");
   fp8q_status r = check_common(x, dt, rows, cols, group_offsets, num_groups);
   if (r != FP8Q_OK) return r;
   if (!fmt_ok(fmt)) return fail(FP8Q_ERR_INVALID_ARG, "fmt must be FP8Q_E4M3 or FP8Q_E5M2");
   if (dir != MXFP8_ROW && dir != MXFP8_COL && dir != MXFP8_BOTH)
     return fail(FP8Q_ERR_INVALID_ARG, "dir must be MXFP8_ROW, MXFP8_COL or MXFP8_BOTH");
   if (cols % 32 != 0) return fail(FP8Q_ERR_UNSUPPORTED, "MXFP8 needs cols %% 32 == 0 (cols = %lld)", (long long)cols);
+  if (sat_count) {  // zero even for an empty tensor
+    cudaError_t e = cudaMemsetAsync(sat_count, 0, 2 * sizeof(unsigned long long), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(sat_count)");
+  }
   if (rows * cols == 0) return FP8Q_OK;
   if (rows > INT32_MAX / 2) return fail(FP8Q_ERR_UNSUPPORTED, "rows too large");
   if (dir & MXFP8_ROW) {
@@ -314,7 +329,7 @@ fp8q_status mxfp8_quantize(const void* x, int32_t dt, int64_t rows, int64_t cols
                   (long long)((rows + 31) / 32));
   }
   return launch_mx(x, dt, rows, cols, group_offsets, num_groups, fmt, dir, q_row, s_row, q_col, s_col, s_col_ld,
-                   (cudaStream_t)stream);
+                   scale_rule == FP8Q_MX_RULE_UP ? 1 : 0, sat_count, (cudaStream_t)stream);
 }
 
 static fp8q_status check_dequant_common(const uint8_t* q, int64_t rows, int64_t cols, const int64_t* off, int G,

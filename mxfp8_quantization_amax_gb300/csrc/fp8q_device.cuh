@@ -201,9 +201,10 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
 // X = -127.  Inf/NaN amax gives 0xFF.  amax_bits: FP32 bits, sign clear.
 // ---------------------------------------------------------------------------
 template <int FMT>
-__device__ __forceinline__ uint32_t e8m0_from_amax(uint32_t amax_bits) {
+__device__ __forceinline__ uint32_t e8m0_from_amax(uint32_t amax_bits, int round_up = 1) {
   if (amax_bits >= 0x7F800000u) return 0xFFu;
-  const int b = (int)(amax_bits >> 23) - Fmt<FMT>::kEmax + ((amax_bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  // round_up 0: the OCP rule, X = floor(log2 amax) - e_max (no mantissa term)
+  const int b = (int)(amax_bits >> 23) - Fmt<FMT>::kEmax + ((round_up && (amax_bits & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
   return (uint32_t)min(max(b, 0), 254);
 }
 

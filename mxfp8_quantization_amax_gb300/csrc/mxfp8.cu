@@ -88,6 +88,8 @@ struct MxParams {
   uint8_t* q_col;
   uint8_t* s_col;
   int64_t s_col_ld;
+  int round_up;              // scale rule: 1 round-up (default), 0 OCP round-down
+  unsigned long long* sat;   // saturated-element counts [row, col], or nullptr
 };
 
 // Clamped group boundary: offsets outside [0, rows] are pulled back in, so
@@ -419,6 +421,21 @@ __device__ __forceinline__ uint32_t mx_codes4(float a, float b, float c, float d
   return cvt4<FMT>(__fmul_rn(a, mult), __fmul_rn(b, mult), __fmul_rn(c, mult), __fmul_rn(d, mult));
 }
 
+// Elements of a BF16 pair whose scaled magnitude exceeds the format maximum
+// (they clamp; only possible when the scale rule rounds X down).
+template <int FMT>
+__device__ __forceinline__ uint32_t sat_pair(uint32_t w, float m_lo, float m_hi) {
+  constexpr float kMax = Fmt<FMT>::kMax;
+  return (uint32_t)(fabsf(bf16_lo(w)) * m_lo > kMax) + (uint32_t)(fabsf(bf16_hi(w)) * m_hi > kMax);
+}
+
+// True when a finite, nonzero block's amax scaled by mult exceeds the
+// format maximum (then its elements are counted one by one).
+template <int FMT>
+__device__ __forceinline__ bool block_saturates(uint32_t amax_bits, uint32_t byte, float mult) {
+  return byte != 0xFFu && amax_bits != 0u && __uint_as_float(amax_bits) * mult > Fmt<FMT>::kMax;
+}
+
 // Final code word of a block: Inf/NaN block -> 0x7F codes, zero block -> 0.
 __device__ __forceinline__ uint32_t mx_fix(uint32_t w, uint32_t byte, uint32_t amax_bits) {
   w = byte == 0xFFu ? 0x7F7F7F7Fu : w;
@@ -435,9 +452,9 @@ __device__ __forceinline__ uint32_t mx_fix(uint32_t w, uint32_t byte, uint32_t a
 
 // Rowwise, one lane per 1x32 block: row r, block b (of the 8 in the strip).
 // Writes the 32 codes; returns the scale byte (0 if the block is not ours).
-template <int FMT>
+template <int FMT, bool EXT>
 __device__ __forceinline__ uint32_t row_block_bf16(const MxParams& p, const Tile& t, const unsigned char* stage,
-                                                   int r, int b, const StorePolicy& sp) {
+                                                   int r, int b, const StorePolicy& sp, uint32_t& nsat) {
   if (r >= t.nr || 32 * b >= t.nc) return 0u;
   const unsigned char* line = stage + (b >> 1) * kSubBytes + r * 128;
   const int c0 = (b & 1) * 4;
@@ -456,7 +473,7 @@ __device__ __forceinline__ uint32_t row_block_bf16(const MxParams& p, const Tile
     m4[j] = absmax_nan_bf16x2(absmax_nan_bf16x2(w[4 * j], w[4 * j + 1]), absmax_nan_bf16x2(w[4 * j + 2], w[4 * j + 3]));
   const uint32_t m = absmax_nan_bf16x2(absmax_nan_bf16x2(m4[0], m4[1]), absmax_nan_bf16x2(m4[2], m4[3]));
   const uint32_t am = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu) << 16;
-  const uint32_t byte = e8m0_from_amax<FMT>(am);
+  const uint32_t byte = e8m0_from_amax<FMT>(am, EXT ? p.round_up : 1);
   uint32_t d[8];
   if (byte == 0xFFu || am == 0u) {  // Inf/NaN block: 0x7F codes; zero block: +0 codes
     const uint32_t fill = am == 0u ? 0u : 0x7F7F7F7Fu;
@@ -466,6 +483,12 @@ __device__ __forceinline__ uint32_t row_block_bf16(const MxParams& p, const Tile
     const float mult = e8m0_multiplier(byte);
 #pragma unroll
     for (int k = 0; k < 8; k++) d[k] = row_codes4<FMT>(w[2 * k], w[2 * k + 1], mult);
+    if constexpr (EXT) {
+      if (p.sat != nullptr && block_saturates<FMT>(am, byte, mult)) {
+#pragma unroll
+        for (int k = 0; k < 16; k++) nsat += sat_pair<FMT>(w[k], mult, mult);
+      }
+    }
   }
   st_data32(p.q_row + (t.r0 + r) * p.cols + t.c0 + 32 * b, d, sp);
   return byte;
@@ -568,10 +591,10 @@ __device__ __forceinline__ void emit_col_block(uint8_t* run, int len, int j, int
 
 // Columnwise: thread t owns columns 2t, 2t+1 (one 32-bit word per row).
 // Returns the two scale bytes (column 2t in bits 0-7).
-template <int FMT>
+template <int FMT, bool EXT>
 __device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit& U, const Tile& t,
                                                   const unsigned char* stage, int tid, const StorePolicy& sp, int j,
-                                                  uint32_t (&prev0)[8], uint32_t (&prev1)[8]) {
+                                                  uint32_t (&prev0)[8], uint32_t (&prev1)[8], uint32_t& nsat) {
   const unsigned char* seg = stage + (tid >> 5) * kSubBytes + 4 * (tid & 3);
   const int c = (tid & 31) >> 2;  // 16-byte chunk of the word within the 128-byte line
   uint32_t off[8];
@@ -592,8 +615,18 @@ __device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit&
   const uint32_t m = absmax_nan_bf16x2(absmax_nan_bf16x2(absmax_nan_bf16x2(m8[0], m8[1]), absmax_nan_bf16x2(m8[2], m8[3])),
                                        absmax_nan_bf16x2(absmax_nan_bf16x2(m8[4], m8[5]), absmax_nan_bf16x2(m8[6], m8[7])));
   const uint32_t a0 = (m & 0x7FFFu) << 16, a1 = m & 0x7FFF0000u;
-  const uint32_t b0 = e8m0_from_amax<FMT>(a0), b1 = e8m0_from_amax<FMT>(a1);
+  const int up = EXT ? p.round_up : 1;
+  const uint32_t b0 = e8m0_from_amax<FMT>(a0, up), b1 = e8m0_from_amax<FMT>(a1, up);
   const float m0 = e8m0_multiplier(b0), m1 = e8m0_multiplier(b1);
+  if constexpr (EXT) {
+    if (p.sat != nullptr) {
+      const bool s0 = block_saturates<FMT>(a0, b0, m0), s1 = block_saturates<FMT>(a1, b1, m1);
+      if (s0 || s1) {
+#pragma unroll
+        for (int r = 0; r < kTileRows; r++) nsat += sat_pair<FMT>(w[r], s0 ? m0 : 0.0f, s1 ? m1 : 0.0f);
+      }
+    }
+  }
   uint32_t d0[8], d1[8];
   if (b0 == 0xFFu || a0 == 0u || b1 == 0xFFu || a1 == 0u) {
 #pragma unroll
@@ -621,7 +654,9 @@ __device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit&
   return b0 | (b1 << 8);
 }
 
-template <int FMT, int DIR>
+// EXT: the scale rule and saturation counting of mxfp8_quantize_rule; the
+// plain instantiation (round-up rule, no counting) carries none of that code.
+template <int FMT, int DIR, bool EXT>
 __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(const __grid_constant__ CUtensorMap tmap, MxParams p) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t full[kStages], empty[kStages];
@@ -679,6 +714,7 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(c
 
   // ---------------- consumers ----------------
   const StorePolicy sp = make_policy();
+  uint32_t nsat_r = 0, nsat_c = 0;  // saturated elements (counted when p.sat is set)
   int64_t k = 0;
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const Unit U = unit_of(p, blk, sup, u);
@@ -699,13 +735,13 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(c
       const unsigned char* stage = stages + s * kStageBytes;
       if constexpr (DIR & MXFP8_ROW) {
         const int r = 8 * warp + (lane & 7);
-        const uint32_t y0 = row_block_bf16<FMT>(p, t, stage, r, lane >> 3, sp);
-        const uint32_t y1 = row_block_bf16<FMT>(p, t, stage, r, 4 + (lane >> 3), sp);
+        const uint32_t y0 = row_block_bf16<FMT, EXT>(p, t, stage, r, lane >> 3, sp, nsat_r);
+        const uint32_t y1 = row_block_bf16<FMT, EXT>(p, t, stage, r, 4 + (lane >> 3), sp, nsat_r);
         store_row_scales(p, t, warp, lane, y0, y1, sp);
       }
       if constexpr (DIR & MXFP8_COL) {
         if (2 * tid < t.nc) {
-          const uint32_t b = col_pair_bf16<FMT>(p, U, t, stage, tid, sp, j, prev0, prev1);
+          const uint32_t b = col_pair_bf16<FMT, EXT>(p, U, t, stage, tid, sp, j, prev0, prev1, nsat_c);
           // scale bytes go to s_col[c][gb0 + j]; they are gathered in the
           // 8-byte aligned window of the destination and leave when the
           // window is complete or the unit ends
@@ -732,6 +768,13 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(c
     }
     if (gave_up || abort_flag) return;
   }
+  if constexpr (EXT) {
+    if (p.sat != nullptr) {  // one atomic per warp and direction
+      const uint32_t a = __reduce_add_sync(0xFFFFFFFFu, nsat_r), c = __reduce_add_sync(0xFFFFFFFFu, nsat_c);
+      if (lane == 0 && a) atomicAdd(p.sat, (unsigned long long)a);
+      if (lane == 0 && c) atomicAdd(p.sat + 1, (unsigned long long)c);
+    }
+  }
   pdl_launch_dependents();
 }
 
@@ -748,6 +791,7 @@ __global__ void __launch_bounds__(kConsumers) mx_f32_kernel(MxParams p) {
   int* sup = blk + (p.G + 1);                           // [G + 1] (super = 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const StorePolicy sp = make_policy();
+  uint32_t nsat_r = 0, nsat_c = 0;
   pdl_wait();
   build_prefix<kConsumers>(p, blk, sup);
   const int64_t units = (int64_t)sup[p.G] * p.strips;
@@ -776,8 +820,14 @@ __global__ void __launch_bounds__(kConsumers) mx_f32_kernel(MxParams p) {
         am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
         am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
         if (col_ok && r < t.nr) {
-          const uint32_t byte = e8m0_from_amax<FMT>(am);
+          const uint32_t byte = e8m0_from_amax<FMT>(am, p.round_up);
           const float mult = e8m0_multiplier(byte);
+          if (p.sat != nullptr && block_saturates<FMT>(am, byte, mult)) {
+            const uint32_t e[8] = {v[i][0].x, v[i][0].y, v[i][0].z, v[i][0].w,
+                                   v[i][1].x, v[i][1].y, v[i][1].z, v[i][1].w};
+#pragma unroll
+            for (int q = 0; q < 8; q++) nsat_r += fabsf(__uint_as_float(e[q])) * mult > Fmt<FMT>::kMax;
+          }
           uint2 o;
           o.x = mx_fix(mx_codes4<FMT>(__uint_as_float(v[i][0].x), __uint_as_float(v[i][0].y),
                                       __uint_as_float(v[i][0].z), __uint_as_float(v[i][0].w), mult), byte, am);
@@ -804,8 +854,18 @@ __global__ void __launch_bounds__(kConsumers) mx_f32_kernel(MxParams p) {
           a0 = max(a0, w.x & 0x7FFFFFFFu);
           a1 = max(a1, w.y & 0x7FFFFFFFu);
         }
-        const uint32_t b0 = e8m0_from_amax<FMT>(a0), b1 = e8m0_from_amax<FMT>(a1);
+        const uint32_t b0 = e8m0_from_amax<FMT>(a0, p.round_up), b1 = e8m0_from_amax<FMT>(a1, p.round_up);
         const float m0 = e8m0_multiplier(b0), m1 = e8m0_multiplier(b1);
+        if (p.sat != nullptr) {
+          const bool s0 = block_saturates<FMT>(a0, b0, m0), s1 = block_saturates<FMT>(a1, b1, m1);
+          if (s0 || s1) {
+            for (int r = 0; r < t.nr; r++) {
+              const uint2 w = *(const uint2*)(tile + r * kRowBytes + cl * 4);
+              if (s0) nsat_c += fabsf(__uint_as_float(w.x)) * m0 > Fmt<FMT>::kMax;
+              if (s1) nsat_c += fabsf(__uint_as_float(w.y)) * m1 > Fmt<FMT>::kMax;
+            }
+          }
+        }
         uint32_t d0[8], d1[8];
 #pragma unroll
         for (int k = 0; k < 8; k++) {
@@ -828,6 +888,11 @@ __global__ void __launch_bounds__(kConsumers) mx_f32_kernel(MxParams p) {
       }
       __syncthreads();  // the tile is rewritten by the next unit
     }
+  }
+  if (p.sat != nullptr) {
+    const uint32_t a = __reduce_add_sync(0xFFFFFFFFu, nsat_r), c = __reduce_add_sync(0xFFFFFFFFu, nsat_c);
+    if (lane == 0 && a) atomicAdd(p.sat, (unsigned long long)a);
+    if (lane == 0 && c) atomicAdd(p.sat + 1, (unsigned long long)c);
   }
   pdl_launch_dependents();
 }
@@ -866,7 +931,7 @@ static fp8q_status ctas_per_sm(K kernel, int threads, size_t smem, size_t* attr,
   return FP8Q_OK;
 }
 
-template <int FMT, int DIR>
+template <int FMT, int DIR, bool EXT>
 static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
   auto enc = encode_fn();
   if (!enc) return fail(FP8Q_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -886,14 +951,14 @@ static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
   static int per_sm_cache = 0;
   static std::mutex mu;
   int per_sm = 0;
-  fp8q_status st = ctas_per_sm(mx_tma_kernel<FMT, DIR>, kTmaThreads, smem, &attr, &per_sm_cache, &mu, &per_sm);
+  fp8q_status st = ctas_per_sm(mx_tma_kernel<FMT, DIR, EXT>, kTmaThreads, smem, &attr, &per_sm_cache, &mu, &per_sm);
   if (st != FP8Q_OK) return st;
   // units over any valid offsets: blocks per group rounded up to `super`
   const int64_t max_units = ((p.rows + 31) / 32 / q.super + 1 + p.G) * p.strips;
   int64_t grid = (int64_t)per_sm * sm_count();
   if (max_units < grid) grid = max_units;
   if (grid < 1) grid = 1;
-  const cudaError_t e = launch_kernel(mx_tma_kernel<FMT, DIR>, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, map, q);
+  const cudaError_t e = launch_kernel(mx_tma_kernel<FMT, DIR, EXT>, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, map, q);
   if (e != cudaSuccess) return cuda_fail(e, "mxfp8 tma kernel launch");
   return check_launch("mxfp8 tma kernel");
 }
@@ -921,9 +986,14 @@ static fp8q_status launch_f32(const MxParams& p, cudaStream_t s) {
 template <int FMT>
 static fp8q_status launch_fmt(const MxParams& p, int dt, int dir, cudaStream_t s) {
   if (dt == kBF16) {
-    if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW>(p, s);
-    if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL>(p, s);
-    return launch_tma<FMT, MXFP8_BOTH>(p, s);
+    if (p.round_up == 0 || p.sat != nullptr) {
+      if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW, true>(p, s);
+      if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL, true>(p, s);
+      return launch_tma<FMT, MXFP8_BOTH, true>(p, s);
+    }
+    if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW, false>(p, s);
+    if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL, false>(p, s);
+    return launch_tma<FMT, MXFP8_BOTH, false>(p, s);
   }
   if (dir == MXFP8_ROW) return launch_f32<FMT, MXFP8_ROW>(p, s);
   if (dir == MXFP8_COL) return launch_f32<FMT, MXFP8_COL>(p, s);
@@ -932,7 +1002,7 @@ static fp8q_status launch_fmt(const MxParams& p, int dt, int dir, cudaStream_t s
 
 fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* off, int G, int fmt,
                       int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int64_t s_col_ld,
-                      cudaStream_t stream) {
+                      int round_up, unsigned long long* sat, cudaStream_t stream) {
   MxParams p{};
   p.x = x;
   p.rows = rows;
@@ -946,6 +1016,8 @@ fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const i
   p.q_col = q_col;
   p.s_col = s_col;
   p.s_col_ld = s_col_ld;
+  p.round_up = round_up;
+  p.sat = sat;
   return fmt == kE4M3 ? launch_fmt<kE4M3>(p, dt, dir, stream) : launch_fmt<kE5M2>(p, dt, dir, stream);
 }
 

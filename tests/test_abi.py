@@ -130,6 +130,16 @@ def test_dequantize_arguments_rejected_on_host(lib):
     assert lib.fp8q_dequantize_per_tensor(None, 0, 4, None, 1, 0, aligned, 0, None, None) == 0
 
 
+def test_mx_rule_arguments_rejected_on_host(lib):
+    buf = ctypes.create_string_buffer(256)
+    aligned = (ctypes.addressof(buf) + 15) // 16 * 16
+    # unknown rule, misaligned saturation counter
+    assert lib.mxfp8_quantize_rule(aligned, 0, 4, 64, None, 1, 0, 3, 2, aligned, aligned, aligned, aligned, 1,
+                                   None, None) == 1
+    assert lib.mxfp8_quantize_rule(aligned, 0, 4, 64, None, 1, 0, 3, 1, aligned, aligned, aligned, aligned, 1,
+                                   aligned + 4, None) == 1
+
+
 def test_empty_mx_is_a_no_op(lib):
     # rows * cols == 0 returns before any launch
     assert lib.mxfp8_quantize(None, 0, 0, 64, None, 1, 0, 3, None, None, None, None, 0, None) == 0
