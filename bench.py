@@ -22,7 +22,9 @@ in every 8th timed step, against the measured HBM copy bandwidth.
   delayed_8192 (8192x8192 delayed steps), linear_layer (A, W, E of an
   8B-class layer, MXFP8 both directions), moe (65536x7168, 64 experts:
   grouped MXFP8 and grouped current scaling), dequant_8192 (both MXFP8
-  copies and a per-tensor code array of 8192x8192 back to BF16).
+  copies and a per-tensor code array of 8192x8192 back to BF16),
+  mx_rules_4096 (MXFP8 of the activation under the round-up and the OCP
+  scale rule, saturated elements counted and reported).
 --impl reference: the CPU oracle on this host (a bounded sample per step).
 """
 from __future__ import annotations
@@ -55,7 +57,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="activation",
                    choices=["activation", "mx_8192", "per_tensor_1024", "delayed_8192", "linear_layer", "moe",
-                            "dequant_8192"])
+                            "dequant_8192", "mx_rules_4096"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
@@ -105,6 +107,13 @@ def workload_spec(name):
         ops = [{"kind": "mx_grouped", "shape": (r, c), "fmt": E4M3, "bytes": None, "gen": ("c5", 0)},
                {"kind": "current_grouped", "shape": (r, c), "fmt": E4M3, "bytes": 5 * r * c, "gen": ("c5", 0)}]
         return {"workload": "moe_64_experts_65536x7168_bf16", "rows": r, "cols": c, "experts": 64}, ops
+    if name == "mx_rules_4096":
+        r = c = 4096
+        ops = [{"kind": "mx_rule", "rule": 0, "shape": (r, c), "fmt": E4M3, "bytes": mx_bytes(r, c), "gen": ("c2", 0)},
+               {"kind": "mx_rule", "rule": 1, "shape": (r, c), "fmt": E4M3, "bytes": mx_bytes(r, c), "gen": ("c2", 0)}]
+        return {"workload": "mxfp8_scale_rules_4096x4096_bf16", "rows": r, "cols": c,
+                "ops": ["mxfp8 e4m3 row+col, round-up rule, saturation counted",
+                        "mxfp8 e4m3 row+col, OCP rule, saturation counted"]}, ops
     if name == "dequant_8192":
         r = c = 8192
         ops = [{"kind": "dq_mx_row", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + r * c // 32, "gen": ("c2", 0)},
@@ -117,7 +126,7 @@ def workload_spec(name):
 
 
 DQ_KINDS = ("dq_mx_row", "dq_mx_col", "dq_tensor")
-ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row")
+ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule")
 
 
 def host_input(gen, shape):
@@ -293,7 +302,7 @@ def run_ours(args):
             r, c = op["shape"]
             x = h.to(dev, non_blocking=True)
             b = {"x": x, "in": [x]}
-            if op["kind"] in ("mx", "mx_grouped"):
+            if op["kind"] in ("mx", "mx_grouped", "mx_rule"):
                 ld = fq.mxfp8_col_blocks(r, None if offsets_host is None else list(offsets_host))
                 if offsets_host is not None:
                     ld = (ld + 15) // 16 * 16  # the library's default layout for grouped scales
@@ -302,6 +311,8 @@ def run_ours(args):
                             "q_col": torch.empty((c, r), dtype=torch.uint8, device=dev),
                             "s_col": torch.empty((c, ld), dtype=torch.uint8, device=dev)}
                 b["ld"] = ld
+                if op["kind"] == "mx_rule":
+                    b["sat"] = torch.zeros(2, dtype=torch.int64, device=dev)
             elif op["kind"] in DQ_KINDS:
                 # the codes to dequantize, made by the library's own quantizers
                 # before timing; the BF16 input is not kept
@@ -352,6 +363,13 @@ def run_ours(args):
                     pt["amax"].data_ptr(), pt["scale"].data_ptr(), pt["scale_inv"].data_ptr(), None,
                     b["ws"].data_ptr(), b["ws"].numel(), stream))
                 b["launches"] = 2
+            elif k == "mx_rule":
+                o = b["out"]
+                b["call"] = (lib.mxfp8_quantize_rule, (
+                    b["x"].data_ptr(), 0, r, c, None, 1, op["fmt"], 3, op["rule"], o["q_row"].data_ptr(),
+                    o["s_row"].data_ptr(), o["q_col"].data_ptr(), o["s_col"].data_ptr(), b["ld"],
+                    b["sat"].data_ptr(), stream))
+                b["launches"] = 1  # (plus the driver's memset of the two counters)
             elif k == "dq_tensor":
                 b["call"] = (lib.fp8q_dequantize_per_tensor, (
                     b["in"][0].data_ptr(), r, c, None, 1, op["fmt"], b["in"][1].data_ptr(), 0, b["y"].data_ptr(),
@@ -426,7 +444,7 @@ def run_ours(args):
         # each op's step inputs as pinned host copies (the quantizers' BF16
         # input, or the dequantizers' codes and scales) and its outputs
         def outputs(op, b):
-            if op["kind"] in ("mx", "mx_grouped"):
+            if op["kind"] in ("mx", "mx_grouped", "mx_rule"):
                 o = b["out"]
                 return [o["q_row"], o["s_row"], o["q_col"], o["s_col"]]
             return [b["y"]] if op["kind"] in DQ_KINDS else [b["q"]]
@@ -480,8 +498,10 @@ def run_ours(args):
         achieved = mx_op["bytes"] / (avg_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                    "kernel": ("dequant_kernel<mx_row,%s,bf16>" if mx_op["kind"] == "dq_mx_row"
-                               else "mx_kernel<bf16,%s,both>") % ("e4m3" if mx_op["fmt"] == E4M3 else "e5m2"),
+                    "kernel": ({"dq_mx_row": "dequant_kernel<mx_row,%s,bf16>",
+                                "mx_rule": "mx_kernel<bf16,%s,both,rule+counts>"}.get(mx_op["kind"],
+                                                                                     "mx_kernel<bf16,%s,both>")
+                               % ("e4m3" if mx_op["fmt"] == E4M3 else "e5m2")),
                     "algorithmic_bytes_per_launch": mx_op["bytes"], "avg_launch_us": round(avg_ms * 1e3, 3),
                     "launches_timed": len(mx_ms),
                     "traffic": kernel_traffic(args.workload)}
@@ -493,6 +513,9 @@ def run_ours(args):
             "config": cfg, "frac_of_hbm_peak": round(value / world / peak, 4), "roofline": roofline,
             "e2e": e2e, "gpu_launches": launches["n"], "clocks": clocks,
             "bytes_per_step": bytes_per_step}
+    if any(op["kind"] == "mx_rule" for op in ops):
+        line["saturated_elements"] = {("round_up" if op["rule"] == 0 else "ocp"): sets[0][j]["sat"].cpu().tolist()
+                                      for j, op in enumerate(ops) if op["kind"] == "mx_rule"}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload)
     for st in states:
@@ -517,6 +540,9 @@ def oracle_sample_step(workload, sample_rows, inputs, states):
         r, c = x["shape"] if k in DQ_KINDS else x.shape
         if k in ("mx", "mx_grouped"):
             oracle.mx_quantize(x, op["fmt"], 3)
+            total += mx_bytes(r, c)
+        elif k == "mx_rule":
+            oracle.mx_quantize_rule(x, op["fmt"], 3, op["rule"])
             total += mx_bytes(r, c)
         elif k in ("current", "current_grouped"):
             oracle.current_scaling(x, op["fmt"])
@@ -556,7 +582,7 @@ def oracle_inputs(workload, sample_rows):
 
 def sample_rows_for(workload):
     return {"activation": 256, "mx_8192": 128, "per_tensor_1024": 1024, "delayed_8192": 128, "linear_layer": 64,
-            "moe": 32, "dequant_8192": 128}[workload]
+            "moe": 32, "dequant_8192": 128, "mx_rules_4096": 256}[workload]
 
 
 def cpu_baseline(workload, budget_s=10.0):
