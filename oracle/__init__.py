@@ -80,6 +80,9 @@ def _load():
         "orc_encode_f32_range": (None, [c.c_int, c.c_uint64, c.c_int64, P, c.c_int]),
         "orc_max_threads": (c.c_int, []),
         "orc_bf16_round": (c.c_uint16, [c.c_float]),
+        "orc_pow2_floor": (c.c_float, [c.c_float]),
+        "orc_blockwise": (None, [P, c.c_int, c.c_int64, c.c_int64, c.c_int, c.c_int, c.c_int, c.c_int, P, P,
+                                 c.c_int]),
         "orc_mx_block_rule": (c.c_uint8, [P, c.c_int, c.c_int, c.c_int, P, c.POINTER(c.c_int64)]),
         "orc_mx_quantize_rule": (None, [P, c.c_int, c.c_int64, c.c_int64, P, c.c_int, c.c_int, c.c_int, c.c_int,
                                         P, P, P, P, c.c_int64, P, c.c_int]),
@@ -421,3 +424,28 @@ def mx_dequantize(q: np.ndarray, s: np.ndarray, fmt: int, direction: int, rows: 
     _load().orc_mx_dequantize(_ptr(q), _ptr(s), rows, cols, _ptr(o) if o is not None else None, G, fmt,
                               direction, s_ld, out_dt, _ptr(y), nthreads or max_threads())
     return y.reshape(q.shape)
+
+
+# --------------------------------------------------------------------------
+# Blockwise FP8 (1x128, 128x1, 128x128 groups with FP32 scales)
+# --------------------------------------------------------------------------
+def pow2_floor(s: float) -> np.float32:
+    """The largest power of two not above a positive float."""
+    return np.float32(_load().orc_pow2_floor(float(s)))
+
+
+def blockwise(x: np.ndarray, fmt: int, group: tuple[int, int], pow2: bool = False,
+              nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """Blockwise quantization of a 2-D tensor with (gr, gc) groups.
+
+    Returns (q [rows, cols] uint8 in x's layout, scale_inv float32
+    [ceil(rows/gr), ceil(cols/gc)]).
+    """
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    gr, gc = group
+    q = np.zeros((rows, cols), np.uint8)
+    si = np.zeros(((rows + gr - 1) // gr, (cols + gc - 1) // gc), np.float32)
+    _load().orc_blockwise(_ptr(x), _dtype_code(x), rows, cols, fmt, gr, gc, int(pow2), _ptr(q), _ptr(si),
+                          nthreads or max_threads())
+    return q, si

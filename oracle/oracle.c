@@ -40,7 +40,10 @@
  *     FP32 first and then to the output type; an MX product value * 2^X is
  *     exact in FP32 except for overflow to Inf; BF16 output rounds to
  *     nearest, ties to even; every NaN result is the canonical quiet NaN
- *     (BF16 0x7FC0, FP32 0x7FC00000).
+ *     (BF16 0x7FC0, FP32 0x7FC00000);
+ *   - blockwise groups use the current-scaling scale of the group (the
+ *     per-tensor special cases included); power-of-two scales round it
+ *     down to the largest power of two not above it.
  * Those readings are pinned only by their own definition ("parity unpinned"
  * by the pages); everything else is pinned by page values, closed forms and
  * library routines in tests/test_oracle_pins.py.
@@ -593,4 +596,54 @@ void orc_bf16_round_array(const float* f, int64_t n, uint16_t* out, int nthreads
 #pragma omp parallel for schedule(static) num_threads(nthreads)
 #endif
     for (int64_t i = 0; i < n; i++) out[i] = orc_bf16_round(f[i]);
+}
+
+/* ------------------------------------------------------------------ */
+/* Blockwise FP8 ("混合精度与 FP8 训练" 10.2-10.5): one FP32 scale per    */
+/* group of gr rows x gc columns -- 1x128 for activations (128 channels */
+/* of one token), 128x128 for weights, 128x1 for the transposed copy of */
+/* an activation.  The scale is the current-scaling scale of the group  */
+/* (Scale = F8max / amax, eq. 1 of "HiFloat8：高性能训练之路" 1.2, taken  */
+/* online per group, 10.3), optionally rounded down to a power of two   */
+/* (10.4: scales that are integer powers of 2).                         */
+/* q = RNE_sat(fl32(x * scale)); the stored scale is scale_inv =        */
+/* fl32(1 / scale), one per group, row-major over the group grid        */
+/* [ceil(rows / gr)][ceil(cols / gc)].  Codes keep x's layout.          */
+/* ------------------------------------------------------------------ */
+float orc_pow2_floor(float s)
+{
+    int e;
+    double m = frexp((double)s, &e); /* s = m * 2^e, m in [0.5, 1) */
+    (void)m;
+    return to_float(ldexp(1.0, e - 1));
+}
+
+void orc_blockwise(const void* x, int dt, int64_t rows, int64_t cols, int fmt, int gr, int gc, int pow2,
+                   uint8_t* q, float* scale_inv, int nthreads)
+{
+    int64_t nbr = (rows + gr - 1) / gr, nbc = (cols + gc - 1) / gc;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t b = 0; b < nbr * nbc; b++) {
+        int64_t br = b / nbc, bc = b % nbc;
+        int64_t r0 = br * gr, r1 = r0 + gr < rows ? r0 + gr : rows;
+        int64_t c0 = bc * gc, c1 = c0 + gc < cols ? c0 + gc : cols;
+        uint32_t amax = 0;
+        for (int64_t r = r0; r < r1; r++)
+            for (int64_t c = c0; c < c1; c++) {
+                uint32_t mag = input_bits(x, dt, r * cols + c) & 0x7FFFFFFFu;
+                if (mag > amax) amax = mag;
+            }
+        int nf;
+        float s = orc_per_tensor_scale(amax, fmt, 0, &nf);
+        if (pow2) s = orc_pow2_floor(s);
+        for (int64_t r = r0; r < r1; r++)
+            for (int64_t c = c0; c < c1; c++) {
+                double v = (double)orc_input_value(x, dt, r * cols + c);
+                q[r * cols + c] = (uint8_t)orc_fp8_encode(fmt, (double)to_float(v * (double)s));
+            }
+        scale_inv[b] = orc_reciprocal(s);
+    }
 }

@@ -669,3 +669,78 @@ def test_mx_ocp_value_on_the_maximum_is_not_saturated(fmt):
         v[2] = np.float32(mx * 2.0 ** k * 1.0625)  # just above: saturates
         b, q, n = oracle.mx_block_rule(v, fmt, oracle.MX_RULE_OCP)
         assert n == 1
+
+
+# --------------------------------------------------------------------------
+# Blockwise FP8 ("混合精度与 FP8 训练" 10.2-10.5)
+# --------------------------------------------------------------------------
+def _act(rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    return _bf16_from_f32(rng.standard_normal((rows, cols)) * np.exp(rng.standard_normal((rows, 1)) * 2))
+
+
+@pytest.mark.parametrize("group", [(1, 128), (128, 128)])
+def test_blockwise_groups_are_current_scaling_of_each_slice(group):
+    """Each group is quantized exactly as current scaling of that slice alone
+    (its amax, Scale = F8max / amax, the saturating cast)."""
+    x = _act(200, 300, 41)
+    q, si = oracle.blockwise(x, oracle.E4M3, group)
+    gr, gc = group
+    for br in range(si.shape[0]):
+        for bc in range(si.shape[1]):
+            sl = np.ascontiguousarray(x[br * gr:(br + 1) * gr, bc * gc:(bc + 1) * gc])
+            ref = oracle.current_scaling(sl, oracle.E4M3)
+            np.testing.assert_array_equal(q[br * gr:(br + 1) * gr, bc * gc:(bc + 1) * gc].reshape(-1), ref["q"])
+            assert si[br, bc].view(np.uint32) == ref["scale_inv"][0].view(np.uint32)
+
+
+def test_blockwise_128x1_is_1x128_of_the_transpose():
+    """The transposed copy's 128x1 groups are the 1x128 groups of x^T (10.5:
+    a 1x128 result cannot simply be transposed, so both come from x)."""
+    x = _act(300, 160, 42)
+    q, si = oracle.blockwise(x, oracle.E4M3, (128, 1))
+    qt, sit = oracle.blockwise(np.ascontiguousarray(x.T), oracle.E4M3, (1, 128))
+    np.testing.assert_array_equal(q.T, qt)
+    np.testing.assert_array_equal(si.T, sit)
+
+
+def test_pow2_floor_closed_form():
+    rng = np.random.default_rng(43)
+    for s in np.concatenate([rng.lognormal(0, 20, 2000), [1.0, 2.0, 0.5, 3.4e38, 1e-30]]).astype(np.float32):
+        p = float(oracle.pow2_floor(s))
+        assert math.frexp(p)[0] == 0.5 and p <= float(s) < 2 * p, s
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_blockwise_power_of_two_scales(fmt):
+    """10.4's power-of-two scales: the largest power of two that keeps the
+    group's amax at or below the format maximum; codes are the cast with it."""
+    x = _act(64, 256, 44)
+    q, si = oracle.blockwise(x, fmt, (1, 128), pow2=True)
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    mx = oracle.fp8_max(fmt)
+    for r in range(64):
+        for b in range(2):
+            s = 1.0 / float(si[r, b])
+            assert math.frexp(s)[0] == 0.5
+            amax = float(np.max(np.abs(xf[r, 128 * b:128 * b + 128])))
+            assert amax * s <= mx < 2 * amax * s
+            qc, _ = oracle.cast(np.ascontiguousarray(x[r, 128 * b:128 * b + 128]), np.float32(s), fmt)
+            np.testing.assert_array_equal(q[r, 128 * b:128 * b + 128], qc)
+
+
+def test_page_outlier_demo_only_touches_its_groups():
+    """Section 9's demo: a 128x256 activation with two outlier channels in the
+    first 128 columns.  Every 1x128 group that holds them gets a larger
+    scale_inv; the right half is exactly what it is without the outliers."""
+    rng = np.random.default_rng(45)
+    base = rng.standard_normal((128, 256)).astype(np.float32)
+    out = base.copy()
+    out[:, 7] *= 1000.0
+    out[:, 100] *= 300.0
+    xb, xo = _bf16_from_f32(base), _bf16_from_f32(out)
+    qb, sb = oracle.blockwise(xb, oracle.E4M3, (1, 128))
+    qo, so = oracle.blockwise(xo, oracle.E4M3, (1, 128))
+    assert (so[:, 0] > sb[:, 0]).all()
+    np.testing.assert_array_equal(qo[:, 128:], qb[:, 128:])
+    np.testing.assert_array_equal(so[:, 1], sb[:, 1])
