@@ -72,6 +72,12 @@ typedef enum { MXFP8_ROW = 1, MXFP8_COL = 2, MXFP8_BOTH = 3 } mxfp8_dir;
  * above the format maximum (they saturate).  Both saturate X to [-127, 127]. */
 typedef enum { FP8Q_MX_RULE_UP = 0, FP8Q_MX_RULE_OCP = 1 } fp8q_mx_rule;
 
+/* Blockwise group shapes.  FP8Q_BLOCK_1X128: 1x128 groups (one token's 128
+ * channels) for the rowwise copy, 128x1 groups for the transposed copy;
+ * FP8Q_BLOCK_128X128: 128x128 blocks, whose transposed copy is the same
+ * blocks transposed. */
+typedef enum { FP8Q_BLOCK_1X128 = 1, FP8Q_BLOCK_128X128 = 128 } fp8q_block;
+
 /* Output type of the dequantizers. */
 typedef enum { FP8Q_OUT_BF16 = 0, FP8Q_OUT_FP32 = 1 } fp8q_out_dtype;
 
@@ -84,8 +90,9 @@ FP8Q_API const char* fp8q_last_error_string(void);
 /*
  * Synchronizes `stream`, then reports and clears device-side failures that
  * earlier calls on this device recorded: FP8Q_ERR_TIMEOUT when a bounded
- * wait inside a kernel (the MXFP8 pipeline's shared-memory barriers) gave
- * up, in which case that call's outputs are incomplete.  FP8Q_OK otherwise.
+ * wait inside a kernel (the shared-memory barriers of the MXFP8 and the
+ * blockwise pipelines) gave up, in which case that call's outputs are
+ * incomplete.  FP8Q_OK otherwise.
  */
 FP8Q_API fp8q_status fp8q_check_device(void* stream);
 
@@ -295,6 +302,32 @@ FP8Q_API fp8q_status mxfp8_quantize_rule(const void* x, int32_t dt, int64_t rows
                                          int32_t dir, int32_t scale_rule, uint8_t* q_row, uint8_t* s_row,
                                          uint8_t* q_col, uint8_t* s_col, int64_t s_col_ld,
                                          unsigned long long* sat_count, void* stream);
+
+/*
+ * Blockwise FP8 with one FP32 scale per group ("混合精度与 FP8 训练" 10.2:
+ * activations in 1x128 groups, weights in 128x128 blocks, along the GEMM
+ * reduction dimension; 10.3: scales taken online from each group's amax;
+ * 10.4: optionally integer powers of two; 10.5: the transposed copy of a
+ * 1x128-grouped tensor is quantized from x in 128x1 groups, never from the
+ * rowwise codes).  Per group: scale = fl32(F8max / amax) with the
+ * per-tensor special cases (amax 0 or non-finite -> 1, overflow -> FLT_MAX),
+ * rounded down to a power of two when pow2_scales is set; q =
+ * RNE_sat(fl32(x * scale)); scale_inv = fl32(1 / scale) is stored.
+ *   x            device BF16 [rows][cols]; rows % 16 == 0, cols % 16 == 0
+ *                (FP8Q_ERR_UNSUPPORTED otherwise, and for FP32 input)
+ *   block        fp8q_block
+ *   dir          MXFP8_ROW, MXFP8_COL or MXFP8_BOTH
+ *   q            device uint8 [rows][cols] (rowwise copy)
+ *   scale_inv    device float: 1x128 -> [rows][ceil(cols/128)];
+ *                128x128 -> [ceil(rows/128)][ceil(cols/128)]
+ *   q_t          device uint8 [cols][rows] (transposed copy)
+ *   scale_inv_t  device float: 128x1 -> [cols][ceil(rows/128)];
+ *                128x128 -> [ceil(cols/128)][ceil(rows/128)]
+ * Pointers of the unused copy may be NULL; x, q and q_t 16-byte aligned.
+ */
+FP8Q_API fp8q_status fp8q_quantize_blockwise(const void* x, int32_t dt, int64_t rows, int64_t cols, int32_t fmt,
+                                             int32_t block, int32_t pow2_scales, int32_t dir, uint8_t* q,
+                                             float* scale_inv, uint8_t* q_t, float* scale_inv_t, void* stream);
 
 /*
  * Dequantization.  ("HiFloat8：高性能训练之路" 1.1-1.2: a quantized tensor is

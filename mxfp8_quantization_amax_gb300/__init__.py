@@ -26,7 +26,7 @@ __all__ = [
     "fp8q_amax", "fp8q_cast_per_tensor", "fp8q_cast_workspace_bytes", "DelayedScaling",
     "mxfp8_quantize", "mxfp8_col_blocks", "Fp8qError", "check_device", "set_wait_budget_ns",
     "fp8q_scale_from_amax", "debug_stall_mx_producer", "fp8q_dequantize_per_tensor", "mxfp8_dequantize",
-    "RULE_UP", "RULE_OCP",
+    "RULE_UP", "RULE_OCP", "BLOCK_1X128", "BLOCK_128X128", "fp8q_quantize_blockwise",
 ]
 
 E4M3 = 0
@@ -37,6 +37,8 @@ BOTH = 3
 MAX_GROUPS = 4096
 RULE_UP = 0   # MX scale rule: X = ceil(log2(amax / destmax))
 RULE_OCP = 1  # MX scale rule: X = floor(log2(amax)) - e_max (can saturate)
+BLOCK_1X128 = 1      # blockwise groups: 1x128 (rowwise copy) / 128x1 (transposed copy)
+BLOCK_128X128 = 128  # blockwise groups: 128x128 blocks
 
 _c = ctypes
 _P = _c.c_void_p
@@ -48,6 +50,8 @@ _SIGS = {
     "fp8q_scale_from_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int32, _c.c_int32, _P, _P, _P]),
     "mxfp8_quantize_rule": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32,
                                        _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_int64, _P, _P]),
+    "fp8q_quantize_blockwise": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.c_int32,
+                                           _c.c_int32, _c.c_int32, _P, _P, _P, _P, _P]),
     "fp8q_dequantize_per_tensor": (_c.c_int, [_P, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _P,
                                               _c.c_int32, _P, _P]),
     "mxfp8_dequantize": (_c.c_int, [_P, _P, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _c.c_int32,
@@ -442,3 +446,35 @@ def mxfp8_dequantize(q: torch.Tensor, s: torch.Tensor, rows: int, cols: int, fmt
     _check(lib().mxfp8_dequantize(_ptr(q), _ptr(s), rows, cols, _ptr(off), G, fmt, direction, s_ld,
                                   _out_dtype(out_dtype), _ptr(y), _stream()), "mxfp8_dequantize")
     return y
+
+
+# ---------------------------------------------------------------------------
+# blockwise FP8
+# ---------------------------------------------------------------------------
+def fp8q_quantize_blockwise(x: torch.Tensor, fmt: int = E4M3, block: int = BLOCK_1X128, pow2_scales: bool = False,
+                            direction: int = ROW, out: dict | None = None) -> dict:
+    """Blockwise FP8 of a 2-D BF16 tensor with FP32 scales (see the C header).
+
+    Returns dict(q [rows, cols], scale_inv, q_t [cols, rows], scale_inv_t);
+    the unused copy is None.
+    """
+    _check_input(x)
+    rows, cols = _as_2d(x)
+    tr, tc = (rows + 127) // 128, (cols + 127) // 128
+    o = out or {}
+
+    def buf(name, shape, dtype):
+        t = o.get(name)
+        return t if t is not None else torch.empty(shape, dtype=dtype, device=x.device)
+
+    q = si = q_t = si_t = None
+    if direction & ROW:
+        q = buf("q", (rows, cols), torch.uint8)
+        si = buf("scale_inv", (rows, tc) if block == BLOCK_1X128 else (tr, tc), torch.float32)
+    if direction & COL:
+        q_t = buf("q_t", (cols, rows), torch.uint8)
+        si_t = buf("scale_inv_t", (cols, tr) if block == BLOCK_1X128 else (tc, tr), torch.float32)
+    _check(lib().fp8q_quantize_blockwise(_ptr(x), _dt(x), rows, cols, fmt, block, 1 if pow2_scales else 0,
+                                         direction, _ptr(q), _ptr(si), _ptr(q_t), _ptr(si_t), _stream()),
+           "fp8q_quantize_blockwise")
+    return {"q": q, "scale_inv": si, "q_t": q_t, "scale_inv_t": si_t}

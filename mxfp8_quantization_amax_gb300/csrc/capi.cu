@@ -101,11 +101,12 @@ const char* fp8q_last_error_string(void) { return g_err; }
 
 fp8q_status fp8q_check_device(void* stream) {
   g_err[0] = 0;
-  unsigned mx = 0, pt = 0;
+  unsigned mx = 0, pt = 0, bw = 0;
   fp8q_status r = mx_device_status((cudaStream_t)stream, true, &mx);
   if (r != FP8Q_OK) return r;
   if ((r = pt_device_status(true, &pt)) != FP8Q_OK) return r;
-  if ((mx | pt) & 1u)
+  if ((r = bw_device_status(true, &bw)) != FP8Q_OK) return r;
+  if ((mx | pt | bw) & 1u)
     return fail(FP8Q_ERR_TIMEOUT, "a bounded device-side wait gave up; the outputs of that call are incomplete");
   return FP8Q_OK;
 }
@@ -113,7 +114,8 @@ fp8q_status fp8q_check_device(void* stream) {
 fp8q_status fp8q_set_wait_budget_ns(uint64_t ns) {
   g_err[0] = 0;
   fp8q_status r = mx_set_wait_budget((unsigned long long)ns);
-  return r != FP8Q_OK ? r : pt_set_wait_budget((unsigned long long)ns);
+  if (r == FP8Q_OK) r = pt_set_wait_budget((unsigned long long)ns);
+  return r != FP8Q_OK ? r : bw_set_wait_budget((unsigned long long)ns);
 }
 
 fp8q_status fp8q_debug_stall_mx_producer(int32_t on) {
@@ -330,6 +332,36 @@ fp8q_status mxfp8_quantize_rule(const void* x, int32_t dt, int64_t rows, int64_t
   }
   return launch_mx(x, dt, rows, cols, group_offsets, num_groups, fmt, dir, q_row, s_row, q_col, s_col, s_col_ld,
                    scale_rule == FP8Q_MX_RULE_UP ? 1 : 0, sat_count, (cudaStream_t)stream);
+}
+
+fp8q_status fp8q_quantize_blockwise(const void* x, int32_t dt, int64_t rows, int64_t cols, int32_t fmt,
+                                    int32_t block, int32_t pow2_scales, int32_t dir, uint8_t* q, float* scale_inv,
+                                    uint8_t* q_t, float* scale_inv_t, void* stream) {
+  g_err[0] = 0;
+  if (dt != FP8Q_IN_BF16 && dt != FP8Q_IN_FP32) return fail(FP8Q_ERR_INVALID_ARG, "dt must be FP8Q_IN_BF16 or FP8Q_IN_FP32");
+  if (dt != FP8Q_IN_BF16) return fail(FP8Q_ERR_UNSUPPORTED, "blockwise quantization takes BF16 input");
+  if (!fmt_ok(fmt)) return fail(FP8Q_ERR_INVALID_ARG, "fmt must be FP8Q_E4M3 or FP8Q_E5M2");
+  if (block != FP8Q_BLOCK_1X128 && block != FP8Q_BLOCK_128X128)
+    return fail(FP8Q_ERR_INVALID_ARG, "block must be FP8Q_BLOCK_1X128 or FP8Q_BLOCK_128X128");
+  if (dir != MXFP8_ROW && dir != MXFP8_COL && dir != MXFP8_BOTH)
+    return fail(FP8Q_ERR_INVALID_ARG, "dir must be MXFP8_ROW, MXFP8_COL or MXFP8_BOTH");
+  if (rows < 0 || cols < 0) return fail(FP8Q_ERR_INVALID_ARG, "rows and cols must be >= 0");
+  if (rows % 16 != 0 || cols % 16 != 0)
+    return fail(FP8Q_ERR_UNSUPPORTED, "blockwise quantization needs rows %% 16 == 0 and cols %% 16 == 0");
+  if (rows > INT32_MAX / 2 || cols > INT32_MAX / 2) return fail(FP8Q_ERR_UNSUPPORTED, "rows or cols too large");
+  if (rows * cols == 0) return FP8Q_OK;
+  if (!x || !aligned(x, 16)) return fail(FP8Q_ERR_INVALID_ARG, "x must be a 16-byte aligned device pointer");
+  if (dir & MXFP8_ROW) {
+    if (!q || !scale_inv) return fail(FP8Q_ERR_INVALID_ARG, "q and scale_inv are required for the rowwise copy");
+    if (!aligned(q, 16) || !aligned(scale_inv, 4)) return fail(FP8Q_ERR_INVALID_ARG, "misaligned q or scale_inv");
+  }
+  if (dir & MXFP8_COL) {
+    if (!q_t || !scale_inv_t)
+      return fail(FP8Q_ERR_INVALID_ARG, "q_t and scale_inv_t are required for the transposed copy");
+    if (!aligned(q_t, 16) || !aligned(scale_inv_t, 4)) return fail(FP8Q_ERR_INVALID_ARG, "misaligned q_t or scale_inv_t");
+  }
+  return launch_blockwise(x, rows, cols, fmt, block, pow2_scales ? 1 : 0, dir, q, scale_inv, q_t, scale_inv_t,
+                          (cudaStream_t)stream);
 }
 
 static fp8q_status check_dequant_common(const uint8_t* q, int64_t rows, int64_t cols, const int64_t* off, int G,

@@ -107,6 +107,12 @@ fp8q_status launch_dequant(int kind, const uint8_t* q, const uint8_t* s, const f
                            const int64_t* off, int G, int64_t rows, int64_t cols, int64_t s_ld, int fmt,
                            int out_dt, void* y, cudaStream_t stream);
 
+// Blockwise FP8 (BF16 input; block 1: 1x128 / 128x1 groups, 128: 128x128).
+fp8q_status launch_blockwise(const void* x, int64_t rows, int64_t cols, int fmt, int block, int pow2, int dir,
+                             uint8_t* q, float* s, uint8_t* q_t, float* s_t, cudaStream_t stream);
+fp8q_status bw_device_status(bool clear, unsigned* word);
+fp8q_status bw_set_wait_budget(unsigned long long ns);
+
 // MXFP8.
 fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* off, int G,
                       int fmt, int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,

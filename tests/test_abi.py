@@ -140,6 +140,20 @@ def test_mx_rule_arguments_rejected_on_host(lib):
                                    aligned + 4, None) == 1
 
 
+def test_blockwise_arguments_rejected_on_host(lib):
+    buf = ctypes.create_string_buffer(256)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    # FP32 input and shapes off the 16 grid are unsupported; bad block / dir
+    assert lib.fp8q_quantize_blockwise(a, 1, 128, 128, 0, 1, 0, 3, a, a, a, a, None) == 2
+    assert lib.fp8q_quantize_blockwise(a, 0, 130, 128, 0, 1, 0, 3, a, a, a, a, None) == 2
+    assert lib.fp8q_quantize_blockwise(a, 0, 128, 128, 0, 64, 0, 3, a, a, a, a, None) == 1
+    assert lib.fp8q_quantize_blockwise(a, 0, 128, 128, 0, 1, 0, 0, a, a, a, a, None) == 1
+    # missing outputs of a requested copy, misaligned input
+    assert lib.fp8q_quantize_blockwise(a, 0, 128, 128, 0, 1, 0, 2, a, a, None, a, None) == 1
+    assert lib.fp8q_quantize_blockwise(a + 2, 0, 128, 128, 0, 1, 0, 1, a, a, None, None, None) == 1
+    assert lib.fp8q_quantize_blockwise(None, 0, 0, 128, 0, 1, 0, 3, None, None, None, None, None) == 0
+
+
 def test_empty_mx_is_a_no_op(lib):
     # rows * cols == 0 returns before any launch
     assert lib.mxfp8_quantize(None, 0, 0, 64, None, 1, 0, 3, None, None, None, None, 0, None) == 0
