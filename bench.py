@@ -24,7 +24,9 @@ in every 8th timed step, against the measured HBM copy bandwidth.
   grouped MXFP8 and grouped current scaling), dequant_8192 (both MXFP8
   copies and a per-tensor code array of 8192x8192 back to BF16),
   mx_rules_4096 (MXFP8 of the activation under the round-up and the OCP
-  scale rule, saturated elements counted and reported).
+  scale rule, saturated elements counted and reported), blockwise_8192
+  (blockwise FP8 of an activation in 1x128/128x1 groups and of a weight in
+  128x128 blocks, both copies each).
 --impl reference: the CPU oracle on this host (a bounded sample per step).
 """
 from __future__ import annotations
@@ -57,7 +59,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="activation",
                    choices=["activation", "mx_8192", "per_tensor_1024", "delayed_8192", "linear_layer", "moe",
-                            "dequant_8192", "mx_rules_4096"])
+                            "dequant_8192", "mx_rules_4096", "blockwise_8192"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
@@ -114,6 +116,14 @@ def workload_spec(name):
         return {"workload": "mxfp8_scale_rules_4096x4096_bf16", "rows": r, "cols": c,
                 "ops": ["mxfp8 e4m3 row+col, round-up rule, saturation counted",
                         "mxfp8 e4m3 row+col, OCP rule, saturation counted"]}, ops
+    if name == "blockwise_8192":
+        r = c = 8192
+        ops = [{"kind": "bw", "block": 1, "shape": (r, c), "fmt": E4M3, "bytes": 4 * r * c + 4 * (r * (c // 128) + c * (r // 128)),
+                "gen": ("c2", 0)},
+               {"kind": "bw", "block": 128, "shape": (r, c), "fmt": E4M3, "bytes": 4 * r * c + 8 * (r // 128) * (c // 128),
+                "gen": ("c4", "W")}]
+        return {"workload": "blockwise_fp8_8192x8192_bf16", "rows": r, "cols": c,
+                "ops": ["1x128 + 128x1 groups (activation), both copies", "128x128 blocks (weight), both copies"]}, ops
     if name == "dequant_8192":
         r = c = 8192
         ops = [{"kind": "dq_mx_row", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + r * c // 32, "gen": ("c2", 0)},
@@ -126,7 +136,7 @@ def workload_spec(name):
 
 
 DQ_KINDS = ("dq_mx_row", "dq_mx_col", "dq_tensor")
-ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule")
+ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule", "bw")
 
 
 def host_input(gen, shape):
@@ -313,6 +323,13 @@ def run_ours(args):
                 b["ld"] = ld
                 if op["kind"] == "mx_rule":
                     b["sat"] = torch.zeros(2, dtype=torch.int64, device=dev)
+            elif op["kind"] == "bw":
+                tr, tc = (r + 127) // 128, (c + 127) // 128
+                b["bw"] = {"q": torch.empty((r, c), dtype=torch.uint8, device=dev),
+                           "s": torch.empty((r, tc) if op["block"] == 1 else (tr, tc), dtype=torch.float32, device=dev),
+                           "q_t": torch.empty((c, r), dtype=torch.uint8, device=dev),
+                           "s_t": torch.empty((c, tr) if op["block"] == 1 else (tc, tr), dtype=torch.float32,
+                                              device=dev)}
             elif op["kind"] in DQ_KINDS:
                 # the codes to dequantize, made by the library's own quantizers
                 # before timing; the BF16 input is not kept
@@ -370,6 +387,12 @@ def run_ours(args):
                     o["s_row"].data_ptr(), o["q_col"].data_ptr(), o["s_col"].data_ptr(), b["ld"],
                     b["sat"].data_ptr(), stream))
                 b["launches"] = 1  # (plus the driver's memset of the two counters)
+            elif k == "bw":
+                o = b["bw"]
+                b["call"] = (lib.fp8q_quantize_blockwise, (
+                    b["x"].data_ptr(), 0, r, c, op["fmt"], op["block"], 0, 3, o["q"].data_ptr(), o["s"].data_ptr(),
+                    o["q_t"].data_ptr(), o["s_t"].data_ptr(), stream))
+                b["launches"] = 1
             elif k == "dq_tensor":
                 b["call"] = (lib.fp8q_dequantize_per_tensor, (
                     b["in"][0].data_ptr(), r, c, None, 1, op["fmt"], b["in"][1].data_ptr(), 0, b["y"].data_ptr(),
@@ -447,6 +470,8 @@ def run_ours(args):
             if op["kind"] in ("mx", "mx_grouped", "mx_rule"):
                 o = b["out"]
                 return [o["q_row"], o["s_row"], o["q_col"], o["s_col"]]
+            if op["kind"] == "bw":
+                return [b["bw"][k] for k in ("q", "s", "q_t", "s_t")]
             return [b["y"]] if op["kind"] in DQ_KINDS else [b["q"]]
 
         ins_host = [[t.cpu().pin_memory() for t in sets[0][j]["in"]] for j in range(len(ops))]
@@ -499,7 +524,8 @@ def run_ours(args):
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
                     "kernel": ({"dq_mx_row": "dequant_kernel<mx_row,%s,bf16>",
-                                "mx_rule": "mx_kernel<bf16,%s,both,rule+counts>"}.get(mx_op["kind"],
+                                "mx_rule": "mx_kernel<bf16,%s,both,rule+counts>",
+                                "bw": "blockwise_kernel<%s,1x128,both>"}.get(mx_op["kind"],
                                                                                      "mx_kernel<bf16,%s,both>")
                                % ("e4m3" if mx_op["fmt"] == E4M3 else "e5m2")),
                     "algorithmic_bytes_per_launch": mx_op["bytes"], "avg_launch_us": round(avg_ms * 1e3, 3),
@@ -544,6 +570,11 @@ def oracle_sample_step(workload, sample_rows, inputs, states):
         elif k == "mx_rule":
             oracle.mx_quantize_rule(x, op["fmt"], 3, op["rule"])
             total += mx_bytes(r, c)
+        elif k == "bw":
+            g = (1, 128) if op["block"] == 1 else (128, 128)
+            oracle.blockwise(x, op["fmt"], g)
+            oracle.blockwise(x, op["fmt"], (128, 1) if op["block"] == 1 else g)
+            total += 4 * r * c
         elif k in ("current", "current_grouped"):
             oracle.current_scaling(x, op["fmt"])
             total += 5 * r * c
@@ -582,7 +613,7 @@ def oracle_inputs(workload, sample_rows):
 
 def sample_rows_for(workload):
     return {"activation": 256, "mx_8192": 128, "per_tensor_1024": 1024, "delayed_8192": 128, "linear_layer": 64,
-            "moe": 32, "dequant_8192": 128, "mx_rules_4096": 256}[workload]
+            "moe": 32, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128}[workload]
 
 
 def cpu_baseline(workload, budget_s=10.0):
