@@ -81,6 +81,11 @@ def _load():
         "orc_max_threads": (c.c_int, []),
         "orc_bf16_round": (c.c_uint16, [c.c_float]),
         "orc_pow2_floor": (c.c_float, [c.c_float]),
+        "orc_e2m1_value": (c.c_double, [c.c_uint]),
+        "orc_e2m1_encode": (c.c_uint, [c.c_double]),
+        "orc_nvfp4_tensor_scale": (c.c_float, [c.c_uint32]),
+        "orc_nvfp4_block": (c.c_uint8, [P, c.c_int, c.c_float, P]),
+        "orc_nvfp4": (None, [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int]),
         "orc_blockwise": (None, [P, c.c_int, c.c_int64, c.c_int64, c.c_int, c.c_int, c.c_int, c.c_int, P, P,
                                  c.c_int]),
         "orc_mx_block_rule": (c.c_uint8, [P, c.c_int, c.c_int, c.c_int, P, c.POINTER(c.c_int64)]),
@@ -449,3 +454,39 @@ def blockwise(x: np.ndarray, fmt: int, group: tuple[int, int], pow2: bool = Fals
     _load().orc_blockwise(_ptr(x), _dtype_code(x), rows, cols, fmt, gr, gc, int(pow2), _ptr(q), _ptr(si),
                           nthreads or max_threads())
     return q, si
+
+
+# --------------------------------------------------------------------------
+# NVFP4 (E2M1 elements, E4M3 scale per 16, FP32 tensor scale)
+# --------------------------------------------------------------------------
+def e2m1_value(code: int) -> float:
+    return float(_load().orc_e2m1_value(code))
+
+
+def e2m1_encode(a: float) -> int:
+    return int(_load().orc_e2m1_encode(float(a)))
+
+
+def nvfp4_tensor_scale(amax_value_bits: int) -> np.float32:
+    return np.float32(_load().orc_nvfp4_tensor_scale(amax_value_bits))
+
+
+def nvfp4_block(values: np.ndarray, S: float) -> tuple[int, np.ndarray]:
+    """One block (k <= 16 float32 values) under tensor scale S -> (E4M3 scale code, E2M1 codes)."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    q = np.zeros(v.size, dtype=np.uint8)
+    c = _load().orc_nvfp4_block(_ptr(v), v.size, float(np.float32(S)), _ptr(q))
+    return int(c), q
+
+
+def nvfp4(x: np.ndarray, nthreads: int = 0) -> dict:
+    """NVFP4 of a 2-D tensor (cols % 16 == 0): q [rows, cols/2] (packed, even
+    element in the low nibble), s [rows, cols/16] E4M3 codes, S the tensor scale."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    assert cols % 16 == 0
+    q = np.zeros((rows, cols // 2), np.uint8)
+    s = np.zeros((rows, cols // 16), np.uint8)
+    S = ctypes.c_float(0)
+    _load().orc_nvfp4(_ptr(x), _dtype_code(x), rows, cols, _ptr(q), _ptr(s), ctypes.byref(S), nthreads or max_threads())
+    return {"q": q, "s": s, "S": np.float32(S.value)}

@@ -43,7 +43,12 @@
  *     (BF16 0x7FC0, FP32 0x7FC00000);
  *   - blockwise groups use the current-scaling scale of the group (the
  *     per-tensor special cases included); power-of-two scales round it
- *     down to the largest power of two not above it.
+ *     down to the largest power of two not above it;
+ *   - NVFP4: tensor scale S = fl32(448 * 6 / amax); block scale code
+ *     RNE_sat_E4M3(fl32(amax_b * fl32(S / 6))); elements
+ *     RNE_sat_E2M1(fl32(x * fl32(S / d))) with d the block scale's value
+ *     (all zero when d = 0); a NaN element encodes as the largest code 0x7;
+ *     two codes per byte, the even element in the low nibble.
  * Those readings are pinned only by their own definition ("parity unpinned"
  * by the pages); everything else is pinned by page values, closed forms and
  * library routines in tests/test_oracle_pins.py.
@@ -645,5 +650,91 @@ void orc_blockwise(const void* x, int dt, int64_t rows, int64_t cols, int fmt, i
                 q[r * cols + c] = (uint8_t)orc_fp8_encode(fmt, (double)to_float(v * (double)s));
             }
         scale_inv[b] = orc_reciprocal(s);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* NVFP4 ("混合精度与 FP8 训练" 13.2): E2M1 elements (1 sign, 2 exponent  */
+/* bits with bias 1, 1 mantissa bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6), one    */
+/* E4M3 scale per 16 elements, and one FP32 scale for the tensor (the    */
+/* second level, because E4M3 alone lacks the range).                    */
+/* ------------------------------------------------------------------ */
+double orc_e2m1_value(unsigned code)
+{
+    unsigned sign = (code >> 3) & 1u, e = (code >> 1) & 3u, m = code & 1u;
+    double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, (int)e - 1);
+    return sign ? -mag : mag;
+}
+
+/* Nearest E2M1 code (ties to the even code), saturating at 6; a NaN
+ * encodes as the largest code 0x7. */
+unsigned orc_e2m1_encode(double a)
+{
+    if (isnan(a)) return 0x7u;
+    unsigned sign = signbit(a) ? 0x8u : 0u;
+    double m = fabs(a);
+    if (m >= 6.0) return sign | 0x7u;
+    unsigned lo = 0;
+    while (lo < 7u && orc_e2m1_value(lo + 1) <= m) lo++;
+    if (orc_e2m1_value(lo) == m || lo == 7u) return sign | lo;
+    double dl = m - orc_e2m1_value(lo), dh = orc_e2m1_value(lo + 1) - m;
+    unsigned c = dl < dh ? lo : dh < dl ? lo + 1 : ((lo & 1u) ? lo + 1 : lo);
+    return sign | c;
+}
+
+/* The tensor-level scale S = fl32(448 * 6 / amax) (the E4M3 maximum times
+ * the E2M1 maximum over the tensor's amax), with the per-tensor special
+ * cases: amax 0 or non-finite -> 1, a quotient above FLT_MAX -> FLT_MAX. */
+float orc_nvfp4_tensor_scale(uint32_t amax_bits)
+{
+    if (amax_bits == 0 || amax_bits >= 0x7F800000u) return 1.0f;
+    double q = 448.0 * 6.0 / (double)bits_to_float(amax_bits);
+    float s = to_float(q);
+    return isinf(s) ? FLT_MAX : s;
+}
+
+/* One block of k <= 16 values under tensor scale S: block scale code
+ * RNE_sat_E4M3(fl32(amax_b * fl32(S / 6))), its value d; elements
+ * RNE_sat_E2M1(fl32(x * fl32(S / d))), or all +0 when d = 0.  Returns the
+ * scale code. */
+uint8_t orc_nvfp4_block(const float* v, int k, float S, uint8_t* q)
+{
+    uint32_t amax = 0;
+    for (int i = 0; i < k; i++) {
+        uint32_t mag = float_to_bits(v[i]) & 0x7FFFFFFFu;
+        if (mag > amax) amax = mag;
+    }
+    float t = to_float((double)S / 6.0);
+    float sval = to_float((double)bits_to_float(amax) * (double)t);
+    uint8_t code = (uint8_t)orc_fp8_encode(ORC_E4M3, (double)sval);
+    double d = orc_fp8_value(ORC_E4M3, code);
+    if (d == 0.0 || isnan(d)) {
+        for (int i = 0; i < k; i++) q[i] = 0;
+        return code;
+    }
+    float r = to_float((double)S / d);
+    for (int i = 0; i < k; i++) q[i] = (uint8_t)orc_e2m1_encode((double)to_float((double)v[i] * (double)r));
+    return code;
+}
+
+/* NVFP4 of a rows x cols tensor (cols % 16 == 0), rowwise 1x16 blocks:
+ * q [rows][cols / 2] with element 2i in the low nibble, s [rows][cols / 16]
+ * E4M3 codes, *S_out the tensor scale. */
+void orc_nvfp4(const void* x, int dt, int64_t rows, int64_t cols, uint8_t* q, uint8_t* s, float* S_out, int nthreads)
+{
+    float S = orc_nvfp4_tensor_scale(orc_amax_bits(x, dt, 0, rows * cols));
+    *S_out = S;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t r = 0; r < rows; r++) {
+        float v[16];
+        uint8_t qb[16];
+        for (int64_t j = 0; j < cols / 16; j++) {
+            for (int i = 0; i < 16; i++) v[i] = orc_input_value(x, dt, r * cols + 16 * j + i);
+            s[r * (cols / 16) + j] = orc_nvfp4_block(v, 16, S, qb);
+            for (int i = 0; i < 8; i++) q[r * (cols / 2) + 8 * j + i] = (uint8_t)(qb[2 * i] | (qb[2 * i + 1] << 4));
+        }
     }
 }

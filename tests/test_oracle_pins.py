@@ -744,3 +744,78 @@ def test_page_outlier_demo_only_touches_its_groups():
     assert (so[:, 0] > sb[:, 0]).all()
     np.testing.assert_array_equal(qo[:, 128:], qb[:, 128:])
     np.testing.assert_array_equal(so[:, 1], sb[:, 1])
+
+
+# --------------------------------------------------------------------------
+# NVFP4 ("混合精度与 FP8 训练" 13.2)
+# --------------------------------------------------------------------------
+def test_page_e2m1_values():
+    """E2M1 represents 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives."""
+    vals = [oracle.e2m1_value(c) for c in range(16)]
+    assert vals[:8] == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    assert vals[8:] == [-v for v in vals[:8]]
+
+
+def test_page_nvfp4_example():
+    """The amax-5.3 block: block scale 5.3/6 ~ 0.883 stored in E4M3 as
+    0.875; 5.3/0.875 ~ 6.06 rounds to 6; dequantized 5.25, under 1% off."""
+    v = np.zeros(16, np.float32)
+    v[3] = 5.3
+    code, q = oracle.nvfp4_block(v, 1.0)
+    d = oracle.fp8_value(oracle.E4M3, code)
+    assert d == 0.875 and abs(5.3 / 6 - 0.883) < 1e-3
+    assert oracle.e2m1_value(int(q[3])) == 6.0
+    assert oracle.e2m1_value(int(q[3])) * d == 5.25 and abs(5.25 - 5.3) / 5.3 < 0.01
+
+
+def test_e2m1_encoding_brute_force():
+    """Nearest E2M1 value with ties to the even code, saturating at 6, over a
+    fine grid and every midpoint (the rounding of "混合精度与 FP8 训练" 4.1)."""
+    mags = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    grid = np.concatenate([np.linspace(-8, 8, 4097), [(a + b) / 2 for a, b in zip(mags, mags[1:])]])
+    for a in grid:
+        m = abs(a)
+        best = min(range(8), key=lambda c: (abs(mags[c] - m), c & 1))
+        if m >= 6:
+            best = 7
+        want = best | (8 if a < 0 or (a == 0 and math.copysign(1, a) < 0) else 0)
+        assert oracle.e2m1_encode(a) == want, a
+
+
+def test_nvfp4_tensor_scale_and_blocks():
+    """S = 448 * 6 / amax puts the block holding the tensor's amax on the
+    E4M3 maximum (no block scale overflows); every block is the block rule
+    under S; codes pack two per byte, the even element low."""
+    rng = np.random.default_rng(51)
+    x = _bf16_from_f32(rng.standard_normal((8, 64)) * np.exp(rng.standard_normal((8, 1)) * 3))
+    r = oracle.nvfp4(x)
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    amax = float(np.max(np.abs(xf)))
+    assert r["S"] == np.float32(448.0 * 6.0 / amax)
+    assert max(oracle.fp8_value(oracle.E4M3, int(c)) for c in r["s"].reshape(-1)) == 448.0
+    for i in range(8):
+        for j in range(4):
+            code, q = oracle.nvfp4_block(xf[i, 16 * j:16 * j + 16], r["S"])
+            assert r["s"][i, j] == code
+            packed = r["q"][i, 8 * j:8 * j + 8]
+            np.testing.assert_array_equal(packed & 0xF, q[0::2])
+            np.testing.assert_array_equal(packed >> 4, q[1::2])
+
+
+def test_nvfp4_zero_block_and_dequant_error():
+    """An all-zero block gets scale 0 and zero codes; on random blocks the
+    dequantized values (code * scale / S) stay within half an E2M1 step of x
+    except where the element saturates."""
+    code, q = oracle.nvfp4_block(np.zeros(16, np.float32), 1.0)
+    assert code == 0 and not q.any()
+    rng = np.random.default_rng(52)
+    for _ in range(500):
+        v = (rng.standard_normal(16) * np.exp(rng.standard_normal() * 4)).astype(np.float32)
+        S = np.float32(448 * 6 / np.max(np.abs(v)) * rng.uniform(0.5, 1.0))
+        code, q = oracle.nvfp4_block(v, S)
+        d = oracle.fp8_value(oracle.E4M3, code)
+        for i in range(16):
+            y = oracle.e2m1_value(int(q[i])) * d / float(S)
+            scaled = abs(float(v[i])) * float(S) / d
+            if scaled < 6:
+                assert abs(y - float(v[i])) <= 1.0 * d / float(S) + 1e-12 * abs(float(v[i]))
