@@ -330,6 +330,26 @@ FP8Q_API fp8q_status fp8q_quantize_blockwise(const void* x, int32_t dt, int64_t 
                                              float* scale_inv, uint8_t* q_t, float* scale_inv_t, void* stream);
 
 /*
+ * NVFP4 ("混合精度与 FP8 训练" 13.2): E2M1 elements (0, 0.5, 1, 1.5, 2, 3,
+ * 4, 6 and negatives), one E4M3 scale per 16 elements along a row, and one
+ * FP32 scale for the tensor.  Each step is one IEEE single operation:
+ *   S = 448 * 6 / amax(tensor)   (amax 0 or non-finite -> 1; overflow -> FLT_MAX)
+ *   block code = RNE_sat_E4M3(amax_b * fl32(S / 6)), d = its value
+ *   element = RNE_sat_E2M1(x * fl32(S / d)), all +0 when d is 0 or NaN
+ * The value a code stands for is e2m1(q) * d / S.
+ *   x          device BF16 or FP32 [rows][cols], cols % 16 == 0
+ *   q          device uint8 [rows][cols / 2], two codes per byte, the even
+ *              element in the low nibble (8-byte aligned)
+ *   s          device uint8 [rows][cols / 16], E4M3 codes
+ *   amax_out   device float[1], required: receives the tensor amax (it is
+ *              the reduction's accumulator, zeroed by the call)
+ *   scale_out  device float[1] or NULL: receives S
+ * Two passes over x: the amax, then the quantization.
+ */
+FP8Q_API fp8q_status fp8q_quantize_nvfp4(const void* x, int32_t dt, int64_t rows, int64_t cols, uint8_t* q,
+                                         uint8_t* s, float* amax_out, float* scale_out, void* stream);
+
+/*
  * Dequantization.  ("HiFloat8：高性能训练之路" 1.1-1.2: a quantized tensor is
  * de-scaled by scale_inv = 1 / Scale; "Blackwell GPU MXFP8 预训练最佳实践"
  * 4.1 and 4.3: an MX element stands for value * 2^X, X = byte - 127, and

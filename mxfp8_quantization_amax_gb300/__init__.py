@@ -26,7 +26,7 @@ __all__ = [
     "fp8q_amax", "fp8q_cast_per_tensor", "fp8q_cast_workspace_bytes", "DelayedScaling",
     "mxfp8_quantize", "mxfp8_col_blocks", "Fp8qError", "check_device", "set_wait_budget_ns",
     "fp8q_scale_from_amax", "debug_stall_mx_producer", "fp8q_dequantize_per_tensor", "mxfp8_dequantize",
-    "RULE_UP", "RULE_OCP", "BLOCK_1X128", "BLOCK_128X128", "fp8q_quantize_blockwise",
+    "RULE_UP", "RULE_OCP", "BLOCK_1X128", "BLOCK_128X128", "fp8q_quantize_blockwise", "fp8q_quantize_nvfp4",
 ]
 
 E4M3 = 0
@@ -52,6 +52,7 @@ _SIGS = {
                                        _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_int64, _P, _P]),
     "fp8q_quantize_blockwise": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.c_int32,
                                            _c.c_int32, _c.c_int32, _P, _P, _P, _P, _P]),
+    "fp8q_quantize_nvfp4": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _P, _P, _P, _P]),
     "fp8q_dequantize_per_tensor": (_c.c_int, [_P, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _P,
                                               _c.c_int32, _P, _P]),
     "mxfp8_dequantize": (_c.c_int, [_P, _P, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _c.c_int32,
@@ -478,3 +479,26 @@ def fp8q_quantize_blockwise(x: torch.Tensor, fmt: int = E4M3, block: int = BLOCK
                                          direction, _ptr(q), _ptr(si), _ptr(q_t), _ptr(si_t), _stream()),
            "fp8q_quantize_blockwise")
     return {"q": q, "scale_inv": si, "q_t": q_t, "scale_inv_t": si_t}
+
+
+# ---------------------------------------------------------------------------
+# NVFP4
+# ---------------------------------------------------------------------------
+def fp8q_quantize_nvfp4(x: torch.Tensor, out: dict | None = None) -> dict:
+    """NVFP4 of a 2-D tensor: dict(q [rows, cols/2] packed E2M1, s [rows, cols/16]
+    E4M3 codes, amax [1], scale [1] = the tensor scale S)."""
+    _check_input(x)
+    rows, cols = _as_2d(x)
+    o = out or {}
+
+    def buf(name, shape, dtype):
+        t = o.get(name)
+        return t if t is not None else torch.empty(shape, dtype=dtype, device=x.device)
+
+    q = buf("q", (rows, cols // 2), torch.uint8)
+    s = buf("s", (rows, cols // 16), torch.uint8)
+    amax = buf("amax", (1,), torch.float32)
+    scale = buf("scale", (1,), torch.float32)
+    _check(lib().fp8q_quantize_nvfp4(_ptr(x), _dt(x), rows, cols, _ptr(q), _ptr(s), _ptr(amax), _ptr(scale),
+                                     _stream()), "fp8q_quantize_nvfp4")
+    return {"q": q, "s": s, "amax": amax, "scale": scale}

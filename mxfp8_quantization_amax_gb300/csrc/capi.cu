@@ -364,6 +364,34 @@ fp8q_status fp8q_quantize_blockwise(const void* x, int32_t dt, int64_t rows, int
                           (cudaStream_t)stream);
 }
 
+fp8q_status fp8q_quantize_nvfp4(const void* x, int32_t dt, int64_t rows, int64_t cols, uint8_t* q, uint8_t* s,
+                                float* amax_out, float* scale_out, void* stream) {
+  g_err[0] = 0;
+  fp8q_status r = check_common(x, dt, rows, cols, nullptr, 1);
+  if (r != FP8Q_OK) return r;
+  if (cols % 16 != 0) return fail(FP8Q_ERR_UNSUPPORTED, "NVFP4 needs cols %% 16 == 0 (cols = %lld)", (long long)cols);
+  if (!amax_out || !aligned(amax_out, 4)) return fail(FP8Q_ERR_INVALID_ARG, "amax_out must be a 4-byte aligned device pointer");
+  if (!aligned(scale_out, 4)) return fail(FP8Q_ERR_INVALID_ARG, "scale_out must be 4-byte aligned");
+  if (rows * cols > 0 && (!q || !s)) return fail(FP8Q_ERR_INVALID_ARG, "q and s must not be NULL");
+  if (!aligned(q, 8)) return fail(FP8Q_ERR_INVALID_ARG, "q must be 8-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(amax_out)");
+  if (rows * cols > 0) {
+    PtLaunch L{};
+    L.x = x;
+    L.dt = dt;
+    L.rows = rows;
+    L.cols = cols;
+    L.G = 1;
+    L.fmt = FP8Q_E4M3;
+    L.acc = (unsigned*)amax_out;
+    L.stream = st;
+    if ((r = launch_amax(L, false)) != FP8Q_OK) return r;
+  }
+  return launch_nvfp4(x, dt, rows, cols, (const unsigned*)amax_out, q, s, scale_out, st);
+}
+
 static fp8q_status check_dequant_common(const uint8_t* q, int64_t rows, int64_t cols, const int64_t* off, int G,
                                         int32_t fmt, int32_t out_dt, const void* y) {
   if (rows < 0 || cols < 0) return fail(FP8Q_ERR_INVALID_ARG, "rows and cols must be >= 0");

@@ -113,6 +113,10 @@ fp8q_status launch_blockwise(const void* x, int64_t rows, int64_t cols, int fmt,
 fp8q_status bw_device_status(bool clear, unsigned* word);
 fp8q_status bw_set_wait_budget(unsigned long long ns);
 
+// NVFP4 quantization pass (the tensor amax, FP32 bits, is already in amax).
+fp8q_status launch_nvfp4(const void* x, int dt, int64_t rows, int64_t cols, const unsigned* amax, uint8_t* q,
+                         uint8_t* s, float* scale_out, cudaStream_t stream);
+
 // MXFP8.
 fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* off, int G,
                       int fmt, int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,

@@ -154,6 +154,14 @@ def test_blockwise_arguments_rejected_on_host(lib):
     assert lib.fp8q_quantize_blockwise(None, 0, 0, 128, 0, 1, 0, 3, None, None, None, None, None) == 0
 
 
+def test_nvfp4_arguments_rejected_on_host(lib):
+    buf = ctypes.create_string_buffer(256)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert lib.fp8q_quantize_nvfp4(a, 0, 4, 24, a, a, a, None, None) == 2   # cols % 16
+    assert lib.fp8q_quantize_nvfp4(a, 0, 4, 32, a, a, None, None, None) == 1  # amax_out required
+    assert lib.fp8q_quantize_nvfp4(a, 0, 4, 32, a + 4, a, a, None, None) == 1  # q alignment
+
+
 def test_empty_mx_is_a_no_op(lib):
     # rows * cols == 0 returns before any launch
     assert lib.mxfp8_quantize(None, 0, 0, 64, None, 1, 0, 3, None, None, None, None, 0, None) == 0
