@@ -26,7 +26,8 @@ in every 8th timed step, against the measured HBM copy bandwidth.
   mx_rules_4096 (MXFP8 of the activation under the round-up and the OCP
   scale rule, saturated elements counted and reported), blockwise_8192
   (blockwise FP8 of an activation in 1x128/128x1 groups and of a weight in
-  128x128 blocks, both copies each).
+  128x128 blocks, both copies each), nvfp4_8192 (NVFP4 of the activation:
+  tensor amax, then E2M1 codes with E4M3 scales per 16).
 --impl reference: the CPU oracle on this host (a bounded sample per step).
 """
 from __future__ import annotations
@@ -59,7 +60,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="activation",
                    choices=["activation", "mx_8192", "per_tensor_1024", "delayed_8192", "linear_layer", "moe",
-                            "dequant_8192", "mx_rules_4096", "blockwise_8192"])
+                            "dequant_8192", "mx_rules_4096", "blockwise_8192", "nvfp4_8192"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
@@ -124,6 +125,12 @@ def workload_spec(name):
                 "gen": ("c4", "W")}]
         return {"workload": "blockwise_fp8_8192x8192_bf16", "rows": r, "cols": c,
                 "ops": ["1x128 + 128x1 groups (activation), both copies", "128x128 blocks (weight), both copies"]}, ops
+    if name == "nvfp4_8192":
+        r = c = 8192
+        ops = [{"kind": "nvfp4", "shape": (r, c), "fmt": E4M3, "bytes": 4 * r * c + r * c // 2 + r * c // 16 + 8,
+                "gen": ("c2", 0)}]
+        return {"workload": "nvfp4_8192x8192_bf16", "rows": r, "cols": c,
+                "ops": ["nvfp4: tensor amax, then E2M1 codes and E4M3 scales per 16"]}, ops
     if name == "dequant_8192":
         r = c = 8192
         ops = [{"kind": "dq_mx_row", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + r * c // 32, "gen": ("c2", 0)},
@@ -136,7 +143,7 @@ def workload_spec(name):
 
 
 DQ_KINDS = ("dq_mx_row", "dq_mx_col", "dq_tensor")
-ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule", "bw")
+ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule", "bw", "nvfp4")
 
 
 def host_input(gen, shape):
@@ -323,6 +330,11 @@ def run_ours(args):
                 b["ld"] = ld
                 if op["kind"] == "mx_rule":
                     b["sat"] = torch.zeros(2, dtype=torch.int64, device=dev)
+            elif op["kind"] == "nvfp4":
+                b["nv"] = {"q": torch.empty((r, c // 2), dtype=torch.uint8, device=dev),
+                           "s": torch.empty((r, c // 16), dtype=torch.uint8, device=dev),
+                           "amax": torch.empty(1, dtype=torch.float32, device=dev),
+                           "scale": torch.empty(1, dtype=torch.float32, device=dev)}
             elif op["kind"] == "bw":
                 tr, tc = (r + 127) // 128, (c + 127) // 128
                 b["bw"] = {"q": torch.empty((r, c), dtype=torch.uint8, device=dev),
@@ -387,6 +399,12 @@ def run_ours(args):
                     o["s_row"].data_ptr(), o["q_col"].data_ptr(), o["s_col"].data_ptr(), b["ld"],
                     b["sat"].data_ptr(), stream))
                 b["launches"] = 1  # (plus the driver's memset of the two counters)
+            elif k == "nvfp4":
+                o = b["nv"]
+                b["call"] = (lib.fp8q_quantize_nvfp4, (
+                    b["x"].data_ptr(), 0, r, c, o["q"].data_ptr(), o["s"].data_ptr(), o["amax"].data_ptr(),
+                    o["scale"].data_ptr(), stream))
+                b["launches"] = 2  # amax, then the quantization (plus the driver's memset of amax)
             elif k == "bw":
                 o = b["bw"]
                 b["call"] = (lib.fp8q_quantize_blockwise, (
@@ -472,6 +490,8 @@ def run_ours(args):
                 return [o["q_row"], o["s_row"], o["q_col"], o["s_col"]]
             if op["kind"] == "bw":
                 return [b["bw"][k] for k in ("q", "s", "q_t", "s_t")]
+            if op["kind"] == "nvfp4":
+                return [b["nv"][k] for k in ("q", "s", "scale")]
             return [b["y"]] if op["kind"] in DQ_KINDS else [b["q"]]
 
         ins_host = [[t.cpu().pin_memory() for t in sets[0][j]["in"]] for j in range(len(ops))]
@@ -525,7 +545,8 @@ def run_ours(args):
                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
                     "kernel": ({"dq_mx_row": "dequant_kernel<mx_row,%s,bf16>",
                                 "mx_rule": "mx_kernel<bf16,%s,both,rule+counts>",
-                                "bw": "blockwise_kernel<%s,1x128,both>"}.get(mx_op["kind"],
+                                "bw": "blockwise_kernel<%s,1x128,both>",
+                                "nvfp4": "amax_kernel+nvfp4_kernel<bf16> (%s block scales)"}.get(mx_op["kind"],
                                                                                      "mx_kernel<bf16,%s,both>")
                                % ("e4m3" if mx_op["fmt"] == E4M3 else "e5m2")),
                     "algorithmic_bytes_per_launch": mx_op["bytes"], "avg_launch_us": round(avg_ms * 1e3, 3),
@@ -570,6 +591,9 @@ def oracle_sample_step(workload, sample_rows, inputs, states):
         elif k == "mx_rule":
             oracle.mx_quantize_rule(x, op["fmt"], 3, op["rule"])
             total += mx_bytes(r, c)
+        elif k == "nvfp4":
+            oracle.nvfp4(x)
+            total += 4 * r * c + r * c // 2 + r * c // 16
         elif k == "bw":
             g = (1, 128) if op["block"] == 1 else (128, 128)
             oracle.blockwise(x, op["fmt"], g)
@@ -613,7 +637,7 @@ def oracle_inputs(workload, sample_rows):
 
 def sample_rows_for(workload):
     return {"activation": 256, "mx_8192": 128, "per_tensor_1024": 1024, "delayed_8192": 128, "linear_layer": 64,
-            "moe": 32, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128}[workload]
+            "moe": 32, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128, "nvfp4_8192": 128}[workload]
 
 
 def cpu_baseline(workload, budget_s=10.0):
