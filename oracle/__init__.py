@@ -96,6 +96,9 @@ def _load():
                                           c.c_int]),
         "orc_mx_dequantize": (None, [P, P, c.c_int64, c.c_int64, P, c.c_int, c.c_int, c.c_int, c.c_int64,
                                      c.c_int, P, c.c_int]),
+        "orc_qstats_per_tensor": (None, [P, c.c_int, c.c_int64, c.c_int64, P, c.c_int, c.c_int, P, P, P, P]),
+        "orc_qstats_mx": (None, [P, c.c_int, c.c_int64, c.c_int64, P, c.c_int, c.c_int, c.c_int, P, P,
+                                 c.c_int64, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -429,6 +432,59 @@ def mx_dequantize(q: np.ndarray, s: np.ndarray, fmt: int, direction: int, rows: 
     _load().orc_mx_dequantize(_ptr(q), _ptr(s), rows, cols, _ptr(o) if o is not None else None, G, fmt,
                               direction, s_ld, out_dt, _ptr(y), nthreads or max_threads())
     return y.reshape(q.shape)
+
+
+# --------------------------------------------------------------------------
+# Quantization-error statistics (SQNR, zero-rate)
+# --------------------------------------------------------------------------
+def _stats_dict(sums: np.ndarray, counts: np.ndarray) -> dict:
+    return {"signal": float(sums[0]), "noise": float(sums[1]), "n": int(counts[0]), "n_zero": int(counts[1]),
+            "n_flushed": int(counts[2]), "n_nonfinite": int(counts[3])}
+
+
+def qstats_per_tensor(x: np.ndarray, q: np.ndarray, fmt: int, scale_inv, offsets=None) -> dict:
+    """Statistics of a per-tensor (per-group) copy q of x against x, with
+    xh = fl32(value(q) * scale_inv[g]): signal = sum x^2 and noise =
+    sum (x - xh)^2 over the elements where both are finite (double sums),
+    n, n_zero (xh == 0), n_flushed (xh == 0, x != 0), n_nonfinite."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    q = np.ascontiguousarray(q, dtype=np.uint8).reshape(-1)
+    assert q.size == x.size
+    o = None if offsets is None else np.ascontiguousarray(offsets, dtype=np.int64)
+    G = 1 if o is None else o.size - 1
+    si = np.ascontiguousarray(np.asarray(scale_inv, dtype=np.float32).reshape(-1))
+    assert si.size == G
+    sums = np.zeros(2, dtype=np.float64)
+    counts = np.zeros(4, dtype=np.int64)
+    _load().orc_qstats_per_tensor(_ptr(x), _dtype_code(x), rows, cols, _ptr(o) if o is not None else None, G, fmt,
+                                  _ptr(q), _ptr(si), _ptr(sums), _ptr(counts))
+    return _stats_dict(sums, counts)
+
+
+def qstats_mx(x: np.ndarray, q: np.ndarray, s: np.ndarray, fmt: int, direction: int, offsets=None) -> dict:
+    """The statistics of qstats_per_tensor for one MX copy of x, xh =
+    value(q) * 2^(s - 127) rounded to FP32 (byte 0xFF: NaN).  direction 1:
+    q [rows, cols], s [rows, cols/32]; direction 2: q [cols, rows], s
+    [cols, s_ld] with the column blocks of all groups in order."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    o = None if offsets is None else np.ascontiguousarray(offsets, dtype=np.int64)
+    G = 1 if o is None else o.size - 1
+    sums = np.zeros(2, dtype=np.float64)
+    counts = np.zeros(4, dtype=np.int64)
+    _load().orc_qstats_mx(_ptr(x), _dtype_code(x), rows, cols, _ptr(o) if o is not None else None, G, fmt,
+                          direction, _ptr(q), _ptr(s), s.shape[1] if s.ndim == 2 else 0, _ptr(sums), _ptr(counts))
+    return _stats_dict(sums, counts)
+
+
+def sqnr_db(stats: dict) -> float:
+    """10 log10(signal / noise); +inf for an exact copy of a nonzero signal."""
+    if stats["noise"] == 0.0:
+        return float("inf") if stats["signal"] > 0 else float("nan")
+    return 10.0 * np.log10(stats["signal"] / stats["noise"])
 
 
 # --------------------------------------------------------------------------

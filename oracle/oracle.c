@@ -48,7 +48,12 @@
  *     RNE_sat_E4M3(fl32(amax_b * fl32(S / 6))); elements
  *     RNE_sat_E2M1(fl32(x * fl32(S / d))) with d the block scale's value
  *     (all zero when d = 0); a NaN element encodes as the largest code 0x7;
- *     two codes per byte, the even element in the low nibble.
+ *     two codes per byte, the even element in the low nibble;
+ *   - quantization statistics: SQNR = 10 log10(sum x^2 / sum (x - xh)^2)
+ *     with xh the FP32 value the code stands for, both sums over the
+ *     elements where x and xh are finite (the rest counted apart); the
+ *     zero-rate counts elements with xh = 0 and x != 0 (values that
+ *     quantization flushed), next to the plain count of xh = 0.
  * Those readings are pinned only by their own definition ("parity unpinned"
  * by the pages); everything else is pinned by page values, closed forms and
  * library routines in tests/test_oracle_pins.py.
@@ -736,5 +741,88 @@ void orc_nvfp4(const void* x, int dt, int64_t rows, int64_t cols, uint8_t* q, ui
             s[r * (cols / 16) + j] = orc_nvfp4_block(v, 16, S, qb);
             for (int i = 0; i < 8; i++) q[r * (cols / 2) + 8 * j + i] = (uint8_t)(qb[2 * i] | (qb[2 * i + 1] << 4));
         }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Quantization-error statistics ("昇腾 Ascend 950 低精度格式", appendix */
+/* 3.4: the SQNR and the zero-rate of quantized weights, activations   */
+/* and KV cache, compared between formats).  For input x and the FP32  */
+/* value xh its code stands for, over the elements where both are      */
+/* finite: signal = sum x^2 and noise = sum (x - xh)^2 (SQNR = 10      */
+/* log10(signal / noise) dB); the other elements are counted as        */
+/* non-finite.  n_zero counts xh == 0; n_flushed counts xh == 0 with   */
+/* x != 0 (a NaN x is not zero): the values quantization set to zero.  */
+/* Plain double sums in element order.                                 */
+/* sums[0] signal, sums[1] noise; counts[0] n, [1] n_zero,             */
+/* [2] n_flushed, [3] n_nonfinite.                                     */
+/* ------------------------------------------------------------------ */
+static void stats_add(double* sums, int64_t* counts, float x, float xh)
+{
+    counts[0]++;
+    if (xh == 0.0f) {
+        counts[1]++;
+        if (!(x == 0.0f)) counts[2]++;
+    }
+    if (!isfinite(x) || !isfinite(xh)) {
+        counts[3]++;
+        return;
+    }
+    double e = (double)x - (double)xh;
+    sums[0] += (double)x * (double)x;
+    sums[1] += e * e;
+}
+
+/* The FP32 value an MX code stands for: value(q) * 2^X, exact in double,
+ * rounded once to float (so only a product of 2^128 or more changes: it
+ * becomes Inf); scale byte 0xFF is NaN. */
+static float mx_value_f32(int fmt, unsigned code, unsigned byte)
+{
+    if (byte == 0xFFu) return NAN;
+    double v = orc_fp8_value(fmt, code);
+    return isnan(v) ? NAN : to_float(ldexp(v, (int)byte - 127));
+}
+
+/* Statistics of the per-tensor (per-group) copy q of x: xh =
+ * fl32(value(q) * scale_inv[g]) for the rows of group g. */
+void orc_qstats_per_tensor(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* offs, int G,
+                           int fmt, const uint8_t* q, const float* scale_inv, double* sums, int64_t* counts)
+{
+    int ng = offs ? G : 1;
+    sums[0] = sums[1] = 0.0;
+    counts[0] = counts[1] = counts[2] = counts[3] = 0;
+    for (int g = 0; g < ng; g++) {
+        int64_t r0 = grp_off(offs, ng, rows, g), r1 = grp_off(offs, ng, rows, g + 1);
+        double si = (double)scale_inv[g];
+        for (int64_t i = r0 * cols; i < r1 * cols; i++) {
+            double v = orc_fp8_value(fmt, q[i]);
+            float xh = isnan(v) || isnan(si) ? NAN : to_float(v * si);
+            stats_add(sums, counts, orc_input_value(x, dt, i), xh);
+        }
+    }
+}
+
+/* Statistics of one MX copy of x (layouts as orc_mx_dequantize): dir 1
+ * the rowwise copy, dir 2 the columnwise copy, whose element (c, r)
+ * pairs with x[r][c].  Elements are visited in x's row-major order. */
+void orc_qstats_mx(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* offs, int G, int fmt,
+                   int dir, const uint8_t* q, const uint8_t* s, int64_t s_ld, double* sums, int64_t* counts)
+{
+    int ng = offs ? G : 1;
+    sums[0] = sums[1] = 0.0;
+    counts[0] = counts[1] = counts[2] = counts[3] = 0;
+    int64_t base = 0;
+    for (int g = 0; g < ng; g++) {
+        int64_t r0 = grp_off(offs, ng, rows, g), r1 = grp_off(offs, ng, rows, g + 1);
+        for (int64_t r = r0; r < r1; r++)
+            for (int64_t c = 0; c < cols; c++) {
+                float xh;
+                if (dir == 1)
+                    xh = mx_value_f32(fmt, q[r * cols + c], s[r * (cols / 32) + c / 32]);
+                else
+                    xh = mx_value_f32(fmt, q[c * rows + r], s[c * s_ld + base + (r - r0) / 32]);
+                stats_add(sums, counts, orc_input_value(x, dt, r * cols + c), xh);
+            }
+        base += (r1 - r0 + 31) / 32;
     }
 }

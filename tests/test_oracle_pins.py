@@ -819,3 +819,113 @@ def test_nvfp4_zero_block_and_dequant_error():
             scaled = abs(float(v[i])) * float(S) / d
             if scaled < 6:
                 assert abs(y - float(v[i])) <= 1.0 * d / float(S) + 1e-12 * abs(float(v[i]))
+
+
+# --------------------------------------------------------------------------
+# Quantization-error statistics ("昇腾 Ascend 950 低精度格式", appendix 3.4:
+# SQNR and zero-rate of quantized tensors)
+# --------------------------------------------------------------------------
+def _uniform_sqnr_db(man_bits):
+    """x uniform on [1, 2) rounded to a grid of step h = 2^-m: the error is
+    uniform on [-h/2, h/2], so E[e^2] = h^2 / 12 and E[x^2] = 7/3."""
+    return 10.0 * math.log10(7.0 / 3.0 * 12.0 * 4.0 ** man_bits)
+
+
+def test_qstats_exact_copy_closed_form():
+    """Powers of two are exact in both formats: noise 0 and signal the
+    geometric sum; zeros count as zero but not as flushed."""
+    for fmt in (oracle.E4M3, oracle.E5M2):
+        ks = np.arange(-6, 9)
+        x = np.zeros((1, 64), np.float32)
+        x[0, :ks.size] = 2.0 ** ks
+        x[0, 32:32 + ks.size] = -(2.0 ** ks)
+        want_signal = 2 * sum(Fraction(4) ** int(k) for k in ks)
+        q, _ = oracle.cast(x, 1.0, fmt)
+        st = oracle.qstats_per_tensor(x, q.reshape(1, 64), fmt, [1.0])
+        assert st["noise"] == 0.0 and Fraction(st["signal"]) == want_signal
+        assert (st["n"], st["n_zero"], st["n_flushed"], st["n_nonfinite"]) == (64, 64 - 2 * ks.size, 0, 0)
+        r = oracle.mx_quantize(x, fmt, 3)
+        for d, (qq, ss) in ((1, ("q_row", "s_row")), (2, ("q_col", "s_col"))):
+            st = oracle.qstats_mx(x, r[qq], r[ss], fmt, d)
+            assert st["noise"] == 0.0 and Fraction(st["signal"]) == want_signal
+
+
+def test_qstats_worked_elements():
+    """Hand-computed elements under E4M3 with scale 1: 1 + 2^-5 rounds to 1;
+    2^-11 is below half the smallest subnormal 2^-9 and is flushed; 0 is
+    zero but not flushed; 500 saturates to 448; +Inf (cast to 448) and NaN
+    (code 0x7F) are non-finite and left out of both sums."""
+    vals = [1 + 2 ** -5, 2 ** -11, 0.0, 500.0, np.inf, np.nan]
+    x = np.array([vals], np.float32)
+    q, _ = oracle.cast(x, 1.0, oracle.E4M3)
+    st = oracle.qstats_per_tensor(x, q.reshape(x.shape), oracle.E4M3, [1.0])
+    F = Fraction
+    assert F(st["signal"]) == (1 + F(1, 32)) ** 2 + F(1, 2 ** 22) + 500 ** 2
+    assert F(st["noise"]) == F(1, 2 ** 10) + F(1, 2 ** 22) + 52 ** 2
+    assert (st["n"], st["n_zero"], st["n_flushed"], st["n_nonfinite"]) == (6, 2, 1, 2)
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_qstats_uniform_per_tensor_sqnr(fmt):
+    """Per-tensor copy of x = 2^-5 * U[1, 2) under scale 2^5: the SQNR of
+    uniform rounding error (3 mantissa bits: 32.53 dB, 2 bits: 26.51 dB)
+    to within sampling noise."""
+    rng = np.random.default_rng(61)
+    x = ((1.0 + rng.random((512, 1024))) / 32.0).astype(np.float32)
+    q, _ = oracle.cast(x, 32.0, fmt)
+    st = oracle.qstats_per_tensor(x, q.reshape(x.shape), fmt, [1.0 / 32.0])
+    assert abs(oracle.sqnr_db(st) - _uniform_sqnr_db(3 if fmt == oracle.E4M3 else 2)) < 0.03
+    assert st["n_zero"] == 0
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_qstats_mx_uniform_rows_of_any_magnitude(fmt):
+    """MX copies of U[1, 2) * 2^k, k constant along each block (per row for
+    the rowwise copy, per column for the columnwise one): every block
+    scales its binade onto the format's, so both copies (grouped
+    columnwise too) keep the uniform-rounding SQNR and flush nothing; a
+    scale paired with the wrong block would not."""
+    rng = np.random.default_rng(62)
+    rows, cols = 600, 512
+    u = 1.0 + rng.random((rows, cols))
+    want = _uniform_sqnr_db(3 if fmt == oracle.E4M3 else 2)
+    for K, offs in ((-40, None), (0, np.array([0, 0, 45, 46, 130, 600])), (40, None)):
+        x_by = {1: (u * 2.0 ** (K + rng.integers(-2, 3, size=(rows, 1)))).astype(np.float32),
+                2: (u * 2.0 ** (K + rng.integers(-2, 3, size=(1, cols)))).astype(np.float32)}
+        for d, (qq, ss) in ((1, ("q_row", "s_row")), (2, ("q_col", "s_col"))):
+            r = oracle.mx_quantize(x_by[d], fmt, d, offsets=offs)
+            st = oracle.qstats_mx(x_by[d], r[qq], r[ss], fmt, d, offsets=offs)
+            assert abs(oracle.sqnr_db(st) - want) < 0.06, (d, K)
+            assert st["n_flushed"] == 0 and st["n"] == rows * cols
+
+
+def test_page_mxfp8_sqnr_band():
+    """Gaussian weights under MXFP8 E4M3 land in the SQNR band the page
+    measured for MXFP8 activations (30.5-33.5 dB), within 0.5 dB of the
+    highest weight SQNR it reports (31.4 dB)."""
+    act = next(c for c in PAGES["sqnr"] if c["id"] == "SQNR-act")
+    wt = next(c for c in PAGES["sqnr"] if c["id"] == "SQNR-weight")
+    x = np.random.default_rng(63).standard_normal((512, 1024)).astype(np.float32)
+    r = oracle.mx_quantize(x, oracle.E4M3, 1)
+    db = oracle.sqnr_db(oracle.qstats_mx(x, r["q_row"], r["s_row"], oracle.E4M3, 1))
+    lo, hi = act["sqnr_db_band"]
+    assert lo <= db <= hi and abs(db - wt["sqnr_db_max"]) < 0.5
+
+
+def test_qstats_nonfinite_elements_leave_the_sums():
+    """Inf and NaN inputs, and a block whose scale byte is 0xFF, change only
+    n_nonfinite: the sums are those of the finite elements alone."""
+    rng = np.random.default_rng(64)
+    x = rng.standard_normal((4, 64)).astype(np.float32)
+    r = oracle.mx_quantize(x, oracle.E4M3, 1)
+    base = oracle.qstats_mx(x, r["q_row"], r["s_row"], oracle.E4M3, 1)
+    s = r["s_row"].copy()
+    s[2, 1] = 0xFF
+    st = oracle.qstats_mx(x, r["q_row"], s, oracle.E4M3, 1)
+    keep = np.ones_like(x, bool)
+    keep[2, 32:] = False
+    xs, qs = x[keep].reshape(-1, 32), r["q_row"][keep].reshape(-1, 32)
+    part = oracle.qstats_mx(xs, qs, np.delete(r["s_row"].reshape(-1), 5).reshape(-1, 1), oracle.E4M3, 1)
+    assert st["n_nonfinite"] == 32 and st["n"] == base["n"]
+    assert st["signal"] == pytest.approx(part["signal"], rel=1e-15)
+    assert st["noise"] == pytest.approx(part["noise"], rel=1e-15)
