@@ -6,7 +6,9 @@
  *   - per-tensor amax, current scaling and delayed scaling, each followed by
  *     a saturating round-to-nearest-even cast to E4M3 or E5M2;
  *   - MXFP8: 1x32 blocks with one E8M0 scale each (exponent rounded up),
- *     rowwise and columnwise (transposed), optionally per ragged group.
+ *     rowwise and columnwise (transposed), optionally per ragged group;
+ * and the steps around it: dequantization, blockwise FP8, NVFP4, and the
+ * SQNR / zero-rate statistics of a quantized copy.
  *
  * Conventions for every entry point:
  *   - Pointers documented as "device" are CUDA device pointers owned by the
@@ -385,6 +387,64 @@ FP8Q_API fp8q_status fp8q_dequantize_per_tensor(const uint8_t* q, int64_t rows, 
 FP8Q_API fp8q_status mxfp8_dequantize(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t cols,
                                       const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
                                       int32_t dir, int64_t s_ld, int32_t out_dt, void* y, void* stream);
+
+/*
+ * Quantization-error statistics of a quantized copy against the tensor it
+ * was made from ("昇腾 Ascend 950 低精度格式", appendix 3.4: formats are
+ * compared by the per-layer SQNR and zero-rate of weights, activations and
+ * KV cache).  xh is the FP32 value a code stands for: per-tensor
+ * fl32(value(q) * scale_inv[g]); MX value(q) * 2^X rounded to FP32 (exact
+ * unless it reaches 2^128, which gives Inf; scale byte 0xFF gives NaN).
+ * Over the elements where x and xh are both finite:
+ *   SQNR = 10 log10(signal / noise) dB,  zero-rate = n_flushed / n.
+ * Sums are exact to about 2e-6 relative (FP32 sums of 32 elements added in
+ * FP64) and repeat exactly from run to run on one GPU.
+ */
+typedef struct fp8q_qstats {
+    double signal;                   /* sum of x^2 over the finite pairs */
+    double noise;                    /* sum of (x - xh)^2 over the finite pairs */
+    unsigned long long n;            /* elements compared */
+    unsigned long long n_zero;       /* elements with xh == 0 */
+    unsigned long long n_flushed;    /* xh == 0 while x != 0 (a NaN x is not 0) */
+    unsigned long long n_nonfinite;  /* x or xh Inf or NaN: left out of the sums */
+} fp8q_qstats;
+
+/* Bytes of workspace the statistics calls need (a constant, under 100 KB). */
+FP8Q_API size_t fp8q_qstats_workspace_bytes(void);
+
+/*
+ * Statistics of a per-tensor (per-group) copy, one pass over x and q.
+ *   x          device BF16 or FP32 [rows][cols] (16-byte aligned)
+ *   q          device uint8 [rows][cols], 16-byte aligned (the codes of
+ *              fp8q_cast_per_tensor)
+ *   scale_inv  device float[num_groups]
+ *   out        device fp8q_qstats, 8-byte aligned: written by the call
+ *   workspace  device, >= fp8q_qstats_workspace_bytes() bytes, 16-byte
+ *              aligned, zero-filled before its first use; every call leaves
+ *              it ready for the next.  Calls that may overlap on the GPU
+ *              need separate workspaces.
+ * Rows outside every group are not compared.
+ */
+FP8Q_API fp8q_status fp8q_qstats_per_tensor(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                            const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
+                                            const uint8_t* q, const float* scale_inv, fp8q_qstats* out,
+                                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Statistics of one MX copy of x (cols % 32 == 0), one pass over x and the
+ * copy.  Layouts as mxfp8_quantize wrote them:
+ *   dir MXFP8_ROW: q = q_row [rows][cols] (16-byte aligned), s = s_row
+ *                  [rows][cols/32]; group_offsets and s_ld are not used.
+ *   dir MXFP8_COL: q = q_col [cols][rows], s = s_col [cols][s_ld] with the
+ *                  column blocks of all groups in order; element (c, r) of
+ *                  the copy is compared with x[r][c].  Blocks past s_ld
+ *                  count as NaN scales.
+ * Other arguments as fp8q_qstats_per_tensor.
+ */
+FP8Q_API fp8q_status mxfp8_qstats(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                  const int64_t* group_offsets, int32_t num_groups, int32_t fmt, int32_t dir,
+                                  const uint8_t* q, const uint8_t* s, int64_t s_ld, fp8q_qstats* out,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -14,6 +14,7 @@ reinterprets them for torch.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import threading
 
@@ -27,6 +28,7 @@ __all__ = [
     "mxfp8_quantize", "mxfp8_col_blocks", "Fp8qError", "check_device", "set_wait_budget_ns",
     "fp8q_scale_from_amax", "debug_stall_mx_producer", "fp8q_dequantize_per_tensor", "mxfp8_dequantize",
     "RULE_UP", "RULE_OCP", "BLOCK_1X128", "BLOCK_128X128", "fp8q_quantize_blockwise", "fp8q_quantize_nvfp4",
+    "fp8q_qstats_workspace_bytes", "fp8q_qstats_per_tensor", "mxfp8_qstats", "qstats_dict",
 ]
 
 E4M3 = 0
@@ -57,6 +59,11 @@ _SIGS = {
                                               _c.c_int32, _P, _P]),
     "mxfp8_dequantize": (_c.c_int, [_P, _P, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _c.c_int32,
                                     _c.c_int64, _c.c_int32, _P, _P]),
+    "fp8q_qstats_workspace_bytes": (_c.c_size_t, []),
+    "fp8q_qstats_per_tensor": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32,
+                                          _P, _P, _P, _P, _c.c_size_t, _P]),
+    "mxfp8_qstats": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _c.c_int32,
+                                _P, _P, _c.c_int64, _P, _P, _c.c_size_t, _P]),
     "fp8q_set_wait_budget_ns": (_c.c_int, [_c.c_uint64]),
     "fp8q_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _P, _P]),
     "fp8q_cast_workspace_bytes": (_c.c_size_t, [_c.c_int32]),
@@ -447,6 +454,89 @@ def mxfp8_dequantize(q: torch.Tensor, s: torch.Tensor, rows: int, cols: int, fmt
     _check(lib().mxfp8_dequantize(_ptr(q), _ptr(s), rows, cols, _ptr(off), G, fmt, direction, s_ld,
                                   _out_dtype(out_dtype), _ptr(y), _stream()), "mxfp8_dequantize")
     return y
+
+
+# ---------------------------------------------------------------------------
+# quantization-error statistics (SQNR, zero-rate)
+# ---------------------------------------------------------------------------
+QSTATS_BYTES = 48  # fp8q_qstats: 2 doubles, 4 uint64
+
+
+def fp8q_qstats_workspace_bytes() -> int:
+    return int(lib().fp8q_qstats_workspace_bytes())
+
+
+_qs_ws_cache: dict = {}
+
+
+def _qstats_workspace(device, stream_id: int) -> torch.Tensor:
+    key = (device.index, stream_id)
+    ws = _qs_ws_cache.get(key)
+    if ws is None:
+        ws = torch.zeros(fp8q_qstats_workspace_bytes(), dtype=torch.uint8, device=device)
+        _qs_ws_cache[key] = ws
+    return ws
+
+
+def _qstats_out(x: torch.Tensor, out):
+    if out is None:
+        return torch.empty(QSTATS_BYTES // 8, dtype=torch.float64, device=x.device)
+    if not out.is_cuda or out.numel() * out.element_size() < QSTATS_BYTES or out.data_ptr() % 8:
+        raise ValueError("out must be an 8-byte aligned CUDA tensor of at least 48 bytes")
+    return out
+
+
+def fp8q_qstats_per_tensor(x: torch.Tensor, q: torch.Tensor, scale_inv: torch.Tensor, fmt: int = E4M3,
+                           group_offsets=None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Statistics of a per-tensor (per-group) copy q of x, as a device
+    tensor holding an fp8q_qstats (read it with qstats_dict)."""
+    _check_input(x)
+    rows, cols = _as_2d(x)
+    if not q.is_cuda or q.dtype != torch.uint8 or not q.is_contiguous() or q.numel() != x.numel():
+        raise ValueError("q must be a contiguous uint8 CUDA tensor with x's element count")
+    off, G = _offsets(group_offsets, x.device)
+    si = scale_inv.to(device=x.device, dtype=torch.float32).reshape(-1).contiguous()
+    if si.numel() != G:
+        raise ValueError("scale_inv must hold one value per group")
+    o = _qstats_out(x, out)
+    stream = torch.cuda.current_stream(x.device)
+    ws = _qstats_workspace(x.device, stream.cuda_stream)
+    _check(lib().fp8q_qstats_per_tensor(_ptr(x), _dt(x), rows, cols, _ptr(off), G, fmt, _ptr(q), _ptr(si), _ptr(o),
+                                        _ptr(ws), ws.numel(), _stream()), "fp8q_qstats_per_tensor")
+    return o
+
+
+def mxfp8_qstats(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, fmt: int = E4M3, direction: int = ROW,
+                 group_offsets=None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Statistics of one MX copy of x (direction ROW: q_row/s_row; COL:
+    q_col/s_col), as a device tensor holding an fp8q_qstats."""
+    _check_input(x)
+    rows, cols = _as_2d(x)
+    if not q.is_cuda or q.dtype != torch.uint8 or not q.is_contiguous() or not s.is_contiguous():
+        raise ValueError("q and s must be contiguous uint8 CUDA tensors")
+    off, G = _offsets(group_offsets, x.device)
+    s_ld = s.shape[-1] if s.dim() == 2 else 0
+    o = _qstats_out(x, out)
+    stream = torch.cuda.current_stream(x.device)
+    ws = _qstats_workspace(x.device, stream.cuda_stream)
+    _check(lib().mxfp8_qstats(_ptr(x), _dt(x), rows, cols, _ptr(off), G, fmt, direction, _ptr(q), _ptr(s), s_ld,
+                              _ptr(o), _ptr(ws), ws.numel(), _stream()), "mxfp8_qstats")
+    return o
+
+
+def qstats_dict(t: torch.Tensor) -> dict:
+    """The fp8q_qstats in a device tensor as a dict, with the SQNR in dB
+    (10 log10(signal / noise)) and the zero-rate (n_flushed / n)."""
+    raw = t.reshape(-1).view(torch.uint8)[:QSTATS_BYTES].cpu()
+    f = raw[:16].view(torch.float64).tolist()
+    c = raw[16:].view(torch.int64).tolist()
+    d = {"signal": f[0], "noise": f[1], "n": c[0], "n_zero": c[1], "n_flushed": c[2], "n_nonfinite": c[3]}
+    if d["noise"] > 0:
+        d["sqnr_db"] = 10.0 * math.log10(d["signal"] / d["noise"]) if d["signal"] > 0 else float("-inf")
+    else:
+        d["sqnr_db"] = float("inf") if d["signal"] > 0 else float("nan")
+    d["zero_rate"] = d["n_flushed"] / d["n"] if d["n"] else 0.0
+    return d
 
 
 # ---------------------------------------------------------------------------

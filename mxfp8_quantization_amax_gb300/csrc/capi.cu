@@ -89,6 +89,12 @@ static fp8q_status check_common(const void* x, int32_t dt, int64_t rows, int64_t
 
 static bool fmt_ok(int32_t fmt) { return fmt == FP8Q_E4M3 || fmt == FP8Q_E5M2; }
 
+// Quantization statistics (qstats.cu).
+size_t qstats_workspace_bytes();
+fp8q_status launch_qstats(int kind, const void* x, int dt, const uint8_t* q, const uint8_t* s, const float* scale_inv,
+                          const int64_t* off, int G, int64_t rows, int64_t cols, int64_t s_ld, int fmt,
+                          fp8q_qstats* out, void* workspace, cudaStream_t stream);
+
 }  // namespace fp8q
 
 using namespace fp8q;
@@ -392,6 +398,23 @@ fp8q_status fp8q_quantize_nvfp4(const void* x, int32_t dt, int64_t rows, int64_t
   return launch_nvfp4(x, dt, rows, cols, (const unsigned*)amax_out, q, s, scale_out, st);
 }
 
+size_t fp8q_qstats_workspace_bytes(void) { return qstats_workspace_bytes(); }
+
+static fp8q_status check_qstats_common(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* off,
+                                       int32_t G, int32_t fmt, const uint8_t* q, const fp8q_qstats* out,
+                                       const void* ws, size_t ws_bytes) {
+  fp8q_status r = check_common(x, dt, rows, cols, off, G);
+  if (r != FP8Q_OK) return r;
+  if (!fmt_ok(fmt)) return fail(FP8Q_ERR_INVALID_ARG, "fmt must be FP8Q_E4M3 or FP8Q_E5M2");
+  if (rows * cols > 0 && !q) return fail(FP8Q_ERR_INVALID_ARG, "q must not be NULL");
+  if (!out || !aligned(out, 8)) return fail(FP8Q_ERR_INVALID_ARG, "out must be an 8-byte aligned device pointer");
+  if (!ws || !aligned(ws, 16)) return fail(FP8Q_ERR_INVALID_ARG, "workspace must be a 16-byte aligned device pointer");
+  if (ws_bytes < qstats_workspace_bytes())
+    return fail(FP8Q_ERR_INVALID_ARG, "workspace_bytes (%zu) is below fp8q_qstats_workspace_bytes() = %zu", ws_bytes,
+                qstats_workspace_bytes());
+  return FP8Q_OK;
+}
+
 static fp8q_status check_dequant_common(const uint8_t* q, int64_t rows, int64_t cols, const int64_t* off, int G,
                                         int32_t fmt, int32_t out_dt, const void* y) {
   if (rows < 0 || cols < 0) return fail(FP8Q_ERR_INVALID_ARG, "rows and cols must be >= 0");
@@ -432,6 +455,38 @@ fp8q_status mxfp8_dequantize(const uint8_t* q, const uint8_t* s, int64_t rows, i
   if (rows * cols == 0) return FP8Q_OK;
   return launch_dequant(dir == MXFP8_ROW ? 1 : 2, q, s, nullptr, group_offsets, num_groups, rows, cols, s_ld, fmt,
                         out_dt, y, (cudaStream_t)stream);
+}
+
+fp8q_status fp8q_qstats_per_tensor(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                   const int64_t* group_offsets, int32_t num_groups, int32_t fmt, const uint8_t* q,
+                                   const float* scale_inv, fp8q_qstats* out, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  fp8q_status r = check_qstats_common(x, dt, rows, cols, group_offsets, num_groups, fmt, q, out, workspace,
+                                      workspace_bytes);
+  if (r != FP8Q_OK) return r;
+  if (!aligned(q, 16)) return fail(FP8Q_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (!scale_inv || !aligned(scale_inv, 4)) return fail(FP8Q_ERR_INVALID_ARG, "scale_inv must be a 4-byte aligned device pointer");
+  return launch_qstats(0, x, dt, q, nullptr, scale_inv, group_offsets, num_groups, rows, cols, 0, fmt, out, workspace,
+                       (cudaStream_t)stream);
+}
+
+fp8q_status mxfp8_qstats(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
+                         int32_t num_groups, int32_t fmt, int32_t dir, const uint8_t* q, const uint8_t* s,
+                         int64_t s_ld, fp8q_qstats* out, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  fp8q_status r = check_qstats_common(x, dt, rows, cols, group_offsets, num_groups, fmt, q, out, workspace,
+                                      workspace_bytes);
+  if (r != FP8Q_OK) return r;
+  if (dir != MXFP8_ROW && dir != MXFP8_COL) return fail(FP8Q_ERR_INVALID_ARG, "dir must be MXFP8_ROW or MXFP8_COL");
+  if (cols % 32 != 0) return fail(FP8Q_ERR_UNSUPPORTED, "MXFP8 needs cols %% 32 == 0 (cols = %lld)", (long long)cols);
+  if (rows * cols > 0 && !s) return fail(FP8Q_ERR_INVALID_ARG, "s must not be NULL");
+  if (dir == MXFP8_ROW && !aligned(q, 16)) return fail(FP8Q_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (dir == MXFP8_COL && s_ld < (rows + 31) / 32)
+    return fail(FP8Q_ERR_INVALID_ARG, "s_ld (%lld) is below ceil(rows / 32) = %lld", (long long)s_ld,
+                (long long)((rows + 31) / 32));
+  return launch_qstats(dir, x, dt, q, s, nullptr, group_offsets, num_groups, rows, cols, s_ld, fmt, out, workspace,
+                       (cudaStream_t)stream);
 }
 
 }  // extern "C"

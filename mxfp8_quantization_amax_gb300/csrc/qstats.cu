@@ -1,0 +1,558 @@
+// qstats.cu -- quantization-error statistics of a quantized copy against the
+// tensor it was made from: the signal and noise energies behind the SQNR, and
+// the counts behind the zero-rate.
+//
+// "昇腾 Ascend 950 低精度格式", appendix 3.4: weights, activations and KV
+// cache are compared between formats by their per-layer SQNR and by their
+// zero-rate (how many values quantization set to zero).  The pages define
+// neither; the library takes the plain reading.  xh is the FP32 value a code
+// stands for: per-tensor fl32(value(q) * scale_inv[g]), MX value(q) * 2^X
+// rounded to FP32 (exact unless it reaches 2^128, which gives Inf; scale
+// byte 0xFF gives NaN).  Over the elements where x and xh are both finite,
+//   signal = sum x^2,   noise = sum (x - xh)^2,   SQNR = 10 log10(signal / noise);
+// n_zero counts xh == 0, n_flushed counts xh == 0 with x != 0 (a NaN x is
+// not zero) and n_nonfinite the pairs left out of the sums.
+//
+// Arithmetic.  A thread takes 32 elements at a time (a chunk: one rowwise MX
+// block, 32 consecutive per-tensor elements, or a 32-row strip of one column
+// of a columnwise copy).  Under one multiplier per chunk it sums x^2 and
+// e^2 = (x - xh)^2 in FP32 with fused multiply-adds, two lanes at a time in
+// Blackwell's packed f32x2 arithmetic, and adds the chunk sums to FP64
+// accumulators.  Each FP32 chunk sum is within 17 units of 2^-24 (relative)
+// of the exact sum of its (at most twice rounded) terms when it is finite and
+// at least 2^-100 (subnormal roundings then weigh below 2^-45), or is exactly
+// a sum of zeros.  Zero values are found on the code words (a code of zero
+// magnitude is the only way to a zero value when value * m cannot underflow)
+// and counted element by element only in chunks that hold one.  Any other
+// chunk -- non-finite or tiny sums, a multiplier that changes inside it (a
+// group boundary, the ragged end) -- is summed again element by element in
+// FP64, as the oracle does.
+//
+// Totals.  Each CTA writes its partial sums to the workspace; the last CTA
+// to finish (atomic ticket) adds them in a fixed order, so results repeat
+// exactly from run to run on one GPU.
+#include "fp8q_device.cuh"
+#include "internal.h"
+
+namespace fp8q {
+
+constexpr int kQsThreads = 256;
+constexpr int kQsMaxGrid = 2048;
+constexpr int kQsTileCols = 2 * kQsThreads;  // columnwise: a column pair per thread
+
+struct QsPartial {
+  double signal, noise;
+  unsigned long long n, n_zero, n_flushed, n_nonfinite;
+};
+
+size_t qstats_workspace_bytes() { return 16 + sizeof(QsPartial) * kQsMaxGrid; }
+
+struct QsParams {
+  const void* x;
+  const uint8_t* q;
+  const uint8_t* s;         // MX scale bytes
+  const float* scale_inv;   // per-tensor [G]
+  const int64_t* off;       // device row offsets [G + 1] or nullptr
+  int G;
+  int64_t rows, cols;
+  int64_t s_ld;             // columnwise: scale bytes per column
+  QsPartial* part;          // [gridDim.x]
+  unsigned* counter;        // last-CTA ticket, zero between calls
+  fp8q_qstats* out;
+};
+
+struct QsAcc {
+  double signal = 0.0, noise = 0.0;
+  unsigned n = 0, nz = 0, nf = 0, nn = 0;
+};
+
+// 2^(byte - 127) as an FP32 value (byte 0: 2^-127, subnormal; 0xFF: NaN).
+__device__ __forceinline__ float qs_e8m0(uint32_t byte) {
+  if (byte == 0xFFu) return __uint_as_float(0x7FC00000u);
+  return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
+}
+
+// Two codes (bits 0-7 and 8-15) -> their exact values.
+template <int FMT>
+__device__ __forceinline__ void qs_decode2(uint32_t two, float& lo, float& hi) {
+  uint32_t h2;
+  const unsigned short c = (unsigned short)two;
+  if constexpr (FMT == kE4M3)
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  else
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(c));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((unsigned short)(h2 & 0xFFFFu)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((unsigned short)(h2 >> 16)));
+}
+
+template <int FMT>
+__device__ __forceinline__ float qs_value(uint32_t code) {
+  float lo, hi;
+  qs_decode2<FMT>(code & 0xFFu, lo, hi);
+  return lo;
+}
+
+template <int DT>
+__device__ __forceinline__ float qs_x(const void* x, int64_t i) {
+  if constexpr (DT == kBF16)
+    return __uint_as_float((uint32_t)__ldg((const unsigned short*)x + i) << 16);
+  else
+    return __ldg((const float*)x + i);
+}
+
+// One element in FP64 (the oracle's own arithmetic); the caller counts n.
+__device__ __forceinline__ void qs_elem(QsAcc& a, float x, float xh) {
+  if (xh == 0.0f) {
+    a.nz++;
+    if (!(x == 0.0f)) a.nf++;
+  }
+  if (!isfinite(x) || !isfinite(xh)) {
+    a.nn++;
+    return;
+  }
+  const double e = (double)x - (double)xh;
+  a.signal = fma((double)x, (double)x, a.signal);
+  a.noise = fma(e, e, a.noise);
+}
+
+// Two FP32 lanes in one 64-bit register (Blackwell's packed f32x2 ops).
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2_make(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(f32x2 v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(f32x2 v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// One pair step: x = X, codes decode to V, multiplier M; S += x^2, N += e^2
+// lane by lane, e = x - fl32(v * m).
+__device__ __forceinline__ void qs_pair(f32x2 X, f32x2 V, f32x2 M, f32x2& S, f32x2& N) {
+  const f32x2 E = f2_sub(X, f2_mul(V, M));
+  S = f2_fma(X, X, S);
+  N = f2_fma(E, E, N);
+}
+
+// Bit 7 of each byte of the result: that code's magnitude bits are nonzero.
+__device__ __forceinline__ uint32_t qs_nonzero_codes(uint32_t w) { return (w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu; }
+
+constexpr float kQsSmall = 7.88860905221011805e-31f;  // 2^-100
+
+// Settles one chunk of 32 elements whose FP32 sums s and n the caller took
+// under the single multiplier m.  code_nz: AND of qs_nonzero_codes over its
+// code words.  m_exact_zero: a code of magnitude zero is the only way to get
+// xh == 0 (no FP32 underflow of value * m) -- true for MX scales, and for a
+// finite per-tensor multiplier of magnitude at least 2^-100.  xat(i) and
+// code(i) re-read element i from memory (rare paths only).
+// The FP32 sums are kept when they are finite (then every pair is finite)
+// and each is either at least 2^-100 or exactly the sum of zeros;
+// otherwise the chunk is summed again in FP64.
+template <int FMT, class XF, class CF>
+__device__ __forceinline__ void qs_settle(QsAcc& a, float s, float n, uint32_t code_nz, bool m_exact_zero, float m,
+                                          XF xat, CF code) {
+  a.n += 32;
+  bool ok = isfinite(s) && isfinite(n) && m_exact_zero;
+  if (ok && s < kQsSmall) {
+    for (int i = 0; i < 32; i++) ok = ok && xat(i) == 0.0f;
+  }
+  if (ok && n < kQsSmall) {
+    for (int i = 0; i < 32; i++) ok = ok && __fsub_rn(xat(i), __fmul_rn(qs_value<FMT>(code(i)), m)) == 0.0f;
+  }
+  if (!ok) {
+    for (int i = 0; i < 32; i++) qs_elem(a, xat(i), __fmul_rn(qs_value<FMT>(code(i)), m));
+    return;
+  }
+  a.signal += (double)s;
+  a.noise += (double)n;
+  if ((code_nz & 0x80808080u) != 0x80808080u) {  // some codes are zero: count them
+    for (int i = 0; i < 32; i++) {
+      if ((code(i) & 0x7Fu) == 0u) {
+        a.nz++;
+        if (!(xat(i) == 0.0f)) a.nf++;
+      }
+    }
+  }
+}
+
+// Group boundary g, clamped into [0, rows].
+__device__ __forceinline__ int64_t qs_row(const QsParams& p, int g) {
+  if (p.off == nullptr) return g == 0 ? 0 : p.rows;
+  const int64_t v = __ldg(p.off + g);
+  return v < 0 ? 0 : (v > p.rows ? p.rows : v);
+}
+
+// Last group g with (clamped) off[g] <= r.
+__device__ __forceinline__ int qs_group(const QsParams& p, int64_t r) {
+  if (p.off == nullptr || p.G <= 1) return 0;
+  int lo = 0, hi = p.G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (qs_row(p, mid) <= r) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Per-tensor: the multiplier of row r, or false for a row in no group.
+__device__ __forceinline__ bool qs_tensor_scale(const QsParams& p, int64_t r, float& si) {
+  const int g = qs_group(p, r);
+  if (r < qs_row(p, g) || r >= qs_row(p, g + 1)) return false;
+  si = __ldg(p.scale_inv + g);
+  return true;
+}
+
+// Columnwise: index of the column block holding row r (blocks of 32 rows
+// from each group's first row, numbered over the groups in order), or -1
+// for a row in no group.  blk[g]: blocks before group g.
+__device__ __forceinline__ int64_t qs_col_block(const QsParams& p, const int* blk, int64_t r) {
+  if (p.off == nullptr || p.G <= 1) return r / 32;
+  const int g = qs_group(p, r);
+  const int64_t r0 = qs_row(p, g);
+  if (r < r0 || r >= qs_row(p, g + 1)) return -1;
+  return blk[g] + (r - r0) / 32;
+}
+
+// blk[g] = sum over h < g of ceil(n_h / 32) (clamped group sizes), g <= G.
+__device__ void qs_build_blk(const QsParams& p, int* blk) {
+  __shared__ int tot[kQsThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (p.G + kQsThreads - 1) / kQsThreads;
+  const int g_lo = tid * per, g_hi = min(p.G, g_lo + per);
+  int sum = 0;
+  for (int g = g_lo; g < g_hi; g++) {
+    const int64_t n = qs_row(p, g + 1) - qs_row(p, g);
+    sum += n > 0 ? (int)((n + 31) / 32) : 0;
+  }
+  int inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) tot[warp] = inc;
+  __syncthreads();
+  int run = inc - sum;
+  for (int w = 0; w < warp; w++) run += tot[w];
+  for (int g = g_lo; g < g_hi; g++) {
+    blk[g] = run;
+    const int64_t n = qs_row(p, g + 1) - qs_row(p, g);
+    run += n > 0 ? (int)((n + 31) / 32) : 0;
+  }
+  if (tid == kQsThreads - 1) blk[p.G] = run;
+  __syncthreads();
+}
+
+// Block sum of the six totals; thread 0 gets the result.
+__device__ __forceinline__ void qs_block_sum(double& s, double& n, unsigned long long (&c)[4]) {
+  __shared__ double sd[2][kQsThreads / 32];
+  __shared__ unsigned long long sc[4][kQsThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
+#pragma unroll
+    for (int j = 0; j < 4; j++) c[j] += __shfl_xor_sync(0xFFFFFFFFu, c[j], o);
+  }
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    sd[0][w] = s;
+    sd[1][w] = n;
+#pragma unroll
+    for (int j = 0; j < 4; j++) sc[j][w] = c[j];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s = n = 0.0;
+    for (int j = 0; j < 4; j++) c[j] = 0;
+    for (int i = 0; i < kQsThreads / 32; i++) {
+      s += sd[0][i];
+      n += sd[1][i];
+      for (int j = 0; j < 4; j++) c[j] += sc[j][i];
+    }
+  }
+}
+
+// The CTA's partial into the workspace; the last CTA adds all partials in
+// index order, writes the result and re-arms the ticket.
+__device__ void qs_finish(const QsParams& p, const QsAcc& a) {
+  double s = a.signal, n = a.noise;
+  unsigned long long c[4] = {a.n, a.nz, a.nf, a.nn};
+  qs_block_sum(s, n, c);
+  if (threadIdx.x == 0) {
+    QsPartial& d = p.part[blockIdx.x];
+    d.signal = s;
+    d.noise = n;
+    d.n = c[0];
+    d.n_zero = c[1];
+    d.n_flushed = c[2];
+    d.n_nonfinite = c[3];
+  }
+  __shared__ bool last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  s = n = 0.0;
+  for (int j = 0; j < 4; j++) c[j] = 0;
+  for (int i = threadIdx.x; i < (int)gridDim.x; i += kQsThreads) {
+    const QsPartial* d = p.part + i;
+    s += __ldcg(&d->signal);
+    n += __ldcg(&d->noise);
+    c[0] += __ldcg(&d->n);
+    c[1] += __ldcg(&d->n_zero);
+    c[2] += __ldcg(&d->n_flushed);
+    c[3] += __ldcg(&d->n_nonfinite);
+  }
+  qs_block_sum(s, n, c);
+  if (threadIdx.x == 0) {
+    p.out->signal = s;
+    p.out->noise = n;
+    p.out->n = c[0];
+    p.out->n_zero = c[1];
+    p.out->n_flushed = c[2];
+    p.out->n_nonfinite = c[3];
+    *p.counter = 0;
+  }
+}
+
+// Rowwise MX copy (MX = true: q [rows][cols], s [rows][cols / 32]) or
+// per-tensor copy (q [rows][cols], scale_inv [G]), in x's own order.
+template <int DT, int FMT, bool MX>
+__global__ void __launch_bounds__(kQsThreads) qstats_lin_kernel(QsParams p) {
+  pdl_wait();
+  QsAcc a;
+  const int64_t n = p.rows * p.cols;
+  const int64_t nchunk = n / 32;
+  const int64_t stride = (int64_t)gridDim.x * kQsThreads;
+  const int64_t tid = (int64_t)blockIdx.x * kQsThreads + threadIdx.x;
+  constexpr int kXw = DT == kBF16 ? 16 : 32;
+  const bool one_scale = MX || p.off == nullptr || p.G <= 1;
+  for (int64_t b = tid; b < nchunk; b += stride) {
+    uint32_t xw[kXw];
+    const char* xp = (const char*)p.x + b * (32 * (DT == kBF16 ? 2 : 4));
+#pragma unroll
+    for (int j = 0; j < kXw / 4; j++) {
+      const uint4 v = ld_stream(xp + 16 * j);
+      xw[4 * j] = v.x;
+      xw[4 * j + 1] = v.y;
+      xw[4 * j + 2] = v.z;
+      xw[4 * j + 3] = v.w;
+    }
+    const uint4 q0 = ld_stream(p.q + 32 * b), q1 = ld_stream(p.q + 32 * b + 16);
+    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    float m;
+    bool uniform = true;
+    if constexpr (MX) {
+      m = qs_e8m0(__ldg(p.s + b));
+    } else if (one_scale) {
+      m = __ldg(p.scale_inv);
+    } else {
+      const int64_t r0 = 32 * b / p.cols, r1 = (32 * b + 31) / p.cols;
+      const int g = qs_group(p, r0);
+      uniform = r0 >= qs_row(p, g) && r1 < qs_row(p, g + 1);
+      m = __ldg(p.scale_inv + g);
+    }
+    const int64_t e0 = 32 * b;
+    auto xg = [&](int i) { return qs_x<DT>(p.x, e0 + i); };
+    auto cg = [&](int i) { return (uint32_t)__ldg(p.q + e0 + i); };
+    if (uniform) {
+      f32x2 S = f2_make(0.0f, 0.0f), N = S;
+      const f32x2 M = f2_make(m, m);
+#pragma unroll
+      for (int k = 0; k < 16; k++) {
+        float v0, v1;
+        qs_decode2<FMT>(qw[k >> 1] >> (16 * (k & 1)), v0, v1);
+        f32x2 X;
+        if constexpr (DT == kBF16) X = f2_make(bf16_lo(xw[k]), bf16_hi(xw[k]));
+        else X = f2_make(__uint_as_float(xw[2 * k]), __uint_as_float(xw[2 * k + 1]));
+        qs_pair(X, f2_make(v0, v1), M, S, N);
+      }
+      uint32_t nzc = 0xFFFFFFFFu;
+#pragma unroll
+      for (int j = 0; j < 8; j++) nzc &= qs_nonzero_codes(qw[j]);
+      const bool m_exact_zero = MX || (isfinite(m) && fabsf(m) >= kQsSmall);
+      qs_settle<FMT>(a, __fadd_rn(f2_lo(S), f2_hi(S)), __fadd_rn(f2_lo(N), f2_hi(N)), nzc, m_exact_zero, m, xg, cg);
+    } else {
+      for (int i = 0; i < 32; i++) {
+        float si;
+        if (qs_tensor_scale(p, (e0 + i) / p.cols, si)) {
+          a.n++;
+          qs_elem(a, xg(i), __fmul_rn(qs_value<FMT>(cg(i)), si));
+        }
+      }
+    }
+  }
+  pdl_launch_dependents();
+  if (tid == 0) {  // the ragged end (per-tensor only: MX rows are whole blocks)
+    for (int64_t e = 32 * nchunk; e < n; e++) {
+      float si;
+      if (qs_tensor_scale(p, e / p.cols, si)) {
+        a.n++;
+        qs_elem(a, qs_x<DT>(p.x, e), __fmul_rn(qs_value<FMT>(__ldg(p.q + e)), si));
+      }
+    }
+  }
+  qs_finish(p, a);
+}
+
+// Columnwise MX copy: q [cols][rows], s [cols][s_ld].  Tiles of 32 rows x
+// 512 columns, a thread per column pair (c, c + 1): the two columns' codes
+// are contiguous in q, the warp's x reads are contiguous along each row,
+// and the pair rides the two lanes of the packed FP32 arithmetic.
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kQsThreads) qstats_col_kernel(QsParams p) {
+  extern __shared__ int blk[];  // [G + 1], grouped tensors only
+  pdl_wait();
+  if (p.off != nullptr && p.G > 1) qs_build_blk(p, blk);
+  QsAcc a;
+  const int64_t ntr = (p.rows + 31) / 32, ntc = (p.cols + kQsTileCols - 1) / kQsTileCols;
+  const int64_t ntiles = ntr * ntc;
+  const bool qvec = (p.rows % 16) == 0 && ((uintptr_t)p.q & 15) == 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t tr = t / ntc, tc = t - tr * ntc;
+    const int64_t c = tc * kQsTileCols + 2 * threadIdx.x;  // cols % 32 == 0: c + 1 < cols too
+    if (c >= p.cols) continue;
+    const int64_t r0 = tr * 32;
+    const int nr = (int)min(p.rows - r0, (int64_t)32);
+    const int64_t sb0 = qs_col_block(p, blk, r0);
+    const int64_t sb1 = nr == 32 ? qs_col_block(p, blk, r0 + 31) : -2;
+    const uint8_t* qa = p.q + c * p.rows + r0;
+    const uint8_t* qb = qa + p.rows;
+    if (sb0 >= 0 && sb0 == sb1) {  // 32 rows under one scale per column
+      const float nan = __uint_as_float(0x7FC00000u);
+      const float ma = sb0 < p.s_ld ? qs_e8m0(__ldg(p.s + c * p.s_ld + sb0)) : nan;
+      const float mb = sb0 < p.s_ld ? qs_e8m0(__ldg(p.s + (c + 1) * p.s_ld + sb0)) : nan;
+      uint32_t wa[8], wb[8];
+      if (qvec) {
+        const uint4 a0 = ld_stream(qa), a1 = ld_stream(qa + 16), b0 = ld_stream(qb), b1 = ld_stream(qb + 16);
+        wa[0] = a0.x; wa[1] = a0.y; wa[2] = a0.z; wa[3] = a0.w; wa[4] = a1.x; wa[5] = a1.y; wa[6] = a1.z; wa[7] = a1.w;
+        wb[0] = b0.x; wb[1] = b0.y; wb[2] = b0.z; wb[3] = b0.w; wb[4] = b1.x; wb[5] = b1.y; wb[6] = b1.z; wb[7] = b1.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          wa[j] = (uint32_t)__ldg(qa + 4 * j) | ((uint32_t)__ldg(qa + 4 * j + 1) << 8) |
+                  ((uint32_t)__ldg(qa + 4 * j + 2) << 16) | ((uint32_t)__ldg(qa + 4 * j + 3) << 24);
+          wb[j] = (uint32_t)__ldg(qb + 4 * j) | ((uint32_t)__ldg(qb + 4 * j + 1) << 8) |
+                  ((uint32_t)__ldg(qb + 4 * j + 2) << 16) | ((uint32_t)__ldg(qb + 4 * j + 3) << 24);
+        }
+      }
+      f32x2 S = f2_make(0.0f, 0.0f), N = S;
+      const f32x2 M = f2_make(ma, mb);
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        f32x2 X;
+        if constexpr (DT == kBF16) {
+          const uint32_t w = __ldg((const unsigned*)((const uint16_t*)p.x + (r0 + i) * p.cols + c));
+          X = f2_make(bf16_lo(w), bf16_hi(w));
+        } else {
+          const float2 w = __ldg((const float2*)((const float*)p.x + (r0 + i) * p.cols + c));
+          X = f2_make(w.x, w.y);
+        }
+        const int j = i & 3;
+        float va, vb;  // row i's code of column c (low byte) and of column c + 1
+        qs_decode2<FMT>(__byte_perm(wa[i >> 2], wb[i >> 2], j | ((4 + j) << 4)), va, vb);
+        qs_pair(X, f2_make(va, vb), M, S, N);
+      }
+      uint32_t za = 0xFFFFFFFFu, zb = 0xFFFFFFFFu;
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        za &= qs_nonzero_codes(wa[j]);
+        zb &= qs_nonzero_codes(wb[j]);
+      }
+      for (int h = 0; h < 2; h++) {
+        const int64_t cc = c + h;
+        const uint8_t* qc = h ? qb : qa;
+        auto xg = [&](int i) { return qs_x<DT>(p.x, (r0 + i) * p.cols + cc); };
+        auto cg = [&](int i) { return (uint32_t)__ldg(qc + i); };
+        qs_settle<FMT>(a, h ? f2_hi(S) : f2_lo(S), h ? f2_hi(N) : f2_lo(N), h ? zb : za, true, h ? mb : ma, xg, cg);
+      }
+    } else {
+      for (int h = 0; h < 2; h++) {
+        const int64_t cc = c + h;
+        const uint8_t* qc = h ? qb : qa;
+        for (int i = 0; i < nr; i++) {
+          const int64_t sb = qs_col_block(p, blk, r0 + i);
+          if (sb < 0) continue;
+          const float m = sb < p.s_ld ? qs_e8m0(__ldg(p.s + cc * p.s_ld + sb)) : __uint_as_float(0x7FC00000u);
+          a.n++;
+          qs_elem(a, qs_x<DT>(p.x, (r0 + i) * p.cols + cc), __fmul_rn(qs_value<FMT>(__ldg(qc + i)), m));
+        }
+      }
+    }
+  }
+  pdl_launch_dependents();
+  qs_finish(p, a);
+}
+
+template <class K>
+static int qs_grid(K kernel, size_t smem, int64_t units) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kQsThreads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  int64_t g = (int64_t)per_sm * sm_count();
+  if (g > kQsMaxGrid) g = kQsMaxGrid;
+  if (units < g) g = units;
+  return g < 1 ? 1 : (int)g;
+}
+
+template <int DT, int FMT>
+static fp8q_status qs_launch_typed(int kind, QsParams p, cudaStream_t stream) {
+  cudaError_t e;
+  if (kind == 2) {
+    const size_t smem = (p.off != nullptr && p.G > 1) ? sizeof(int) * (size_t)(p.G + 1) : 0;
+    const int64_t tiles = ((p.rows + 31) / 32) * ((p.cols + kQsTileCols - 1) / kQsTileCols);
+    const int grid = qs_grid(qstats_col_kernel<DT, FMT>, smem, tiles);
+    e = launch_kernel(qstats_col_kernel<DT, FMT>, dim3(grid), dim3(kQsThreads), smem, stream, p);
+  } else {
+    const int64_t chunks = (p.rows * p.cols / 32 + kQsThreads - 1) / kQsThreads;
+    if (kind == 1) {
+      const int grid = qs_grid(qstats_lin_kernel<DT, FMT, true>, 0, chunks);
+      e = launch_kernel(qstats_lin_kernel<DT, FMT, true>, dim3(grid), dim3(kQsThreads), 0, stream, p);
+    } else {
+      const int grid = qs_grid(qstats_lin_kernel<DT, FMT, false>, 0, chunks);
+      e = launch_kernel(qstats_lin_kernel<DT, FMT, false>, dim3(grid), dim3(kQsThreads), 0, stream, p);
+    }
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "quantization statistics kernel launch");
+  return check_launch("quantization statistics kernel");
+}
+
+fp8q_status launch_qstats(int kind, const void* x, int dt, const uint8_t* q, const uint8_t* s, const float* scale_inv,
+                          const int64_t* off, int G, int64_t rows, int64_t cols, int64_t s_ld, int fmt,
+                          fp8q_qstats* out, void* workspace, cudaStream_t stream) {
+  QsParams p{};
+  p.x = x;
+  p.q = q;
+  p.s = s;
+  p.scale_inv = scale_inv;
+  p.off = off;
+  p.G = G;
+  p.rows = rows;
+  p.cols = cols;
+  p.s_ld = s_ld;
+  p.counter = (unsigned*)workspace;
+  p.part = (QsPartial*)((char*)workspace + 16);
+  p.out = out;
+  if (dt == kBF16)
+    return fmt == kE4M3 ? qs_launch_typed<kBF16, kE4M3>(kind, p, stream) : qs_launch_typed<kBF16, kE5M2>(kind, p, stream);
+  return fmt == kE4M3 ? qs_launch_typed<kFP32, kE4M3>(kind, p, stream) : qs_launch_typed<kFP32, kE5M2>(kind, p, stream);
+}
+
+}  // namespace fp8q

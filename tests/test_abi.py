@@ -165,3 +165,24 @@ def test_nvfp4_arguments_rejected_on_host(lib):
 def test_empty_mx_is_a_no_op(lib):
     # rows * cols == 0 returns before any launch
     assert lib.mxfp8_quantize(None, 0, 0, 64, None, 1, 0, 3, None, None, None, None, 0, None) == 0
+
+
+def test_qstats_arguments_rejected_on_host(lib):
+    buf = ctypes.create_string_buffer(256)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    wsb = lib.fp8q_qstats_workspace_bytes()
+    assert 16 + 48 <= wsb < 100 * 1024
+    # per-tensor: bad fmt, missing scale_inv, misaligned out, small workspace, misaligned q
+    assert lib.fp8q_qstats_per_tensor(a, 0, 4, 4, None, 1, 9, a, a, a, a, wsb, None) == 1
+    assert lib.fp8q_qstats_per_tensor(a, 0, 4, 4, None, 1, 0, a, None, a, a, wsb, None) == 1
+    assert lib.fp8q_qstats_per_tensor(a, 0, 4, 4, None, 1, 0, a, a, a + 4, a, wsb, None) == 1
+    assert lib.fp8q_qstats_per_tensor(a, 0, 4, 4, None, 1, 0, a, a, a, a, wsb - 1, None) == 1
+    assert lib.fp8q_qstats_per_tensor(a, 0, 4, 4, None, 1, 0, a + 1, a, a, a, wsb, None) == 1
+    # MX: both directions at once, cols % 32, s_ld too small, missing scales, no workspace
+    assert lib.mxfp8_qstats(a, 0, 4, 64, None, 1, 0, 3, a, a, 1, a, a, wsb, None) == 1
+    assert lib.mxfp8_qstats(a, 0, 4, 48, None, 1, 0, 1, a, a, 0, a, a, wsb, None) == 2
+    assert lib.mxfp8_qstats(a, 0, 100, 64, None, 1, 0, 2, a, a, 3, a, a, wsb, None) == 1
+    assert lib.mxfp8_qstats(a, 0, 4, 64, None, 1, 0, 1, a, None, 0, a, a, wsb, None) == 1
+    assert lib.mxfp8_qstats(a, 0, 4, 64, None, 1, 0, 1, a, a, 0, a, None, wsb, None) == 1
+    # a grouped call needs num_groups + 1 offsets; NULL offsets mean one group
+    assert lib.mxfp8_qstats(a, 0, 4, 64, None, 2, 0, 2, a, a, 1, a, a, wsb, None) == 1
