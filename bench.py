@@ -60,7 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="activation",
                    choices=["activation", "mx_8192", "per_tensor_1024", "delayed_8192", "linear_layer", "moe",
-                            "dequant_8192", "mx_rules_4096", "blockwise_8192", "nvfp4_8192"])
+                            "dequant_8192", "mx_rules_4096", "blockwise_8192", "nvfp4_8192",
+                            "qstats_8192"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
@@ -131,6 +132,14 @@ def workload_spec(name):
                 "gen": ("c2", 0)}]
         return {"workload": "nvfp4_8192x8192_bf16", "rows": r, "cols": c,
                 "ops": ["nvfp4: tensor amax, then E2M1 codes and E4M3 scales per 16"]}, ops
+    if name == "qstats_8192":
+        r = c = 8192
+        ops = [{"kind": "qs_mx_row", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + r * c // 32 + 48, "gen": ("c2", 0)},
+               {"kind": "qs_mx_col", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + c * (r // 32) + 48, "gen": ("c2", 0)},
+               {"kind": "qs_tensor", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + 4 + 48, "gen": ("c2", 0)}]
+        return {"workload": "qstats_8192x8192_bf16", "rows": r, "cols": c,
+                "ops": ["sqnr/zero-rate of the mxfp8 e4m3 rowwise copy", "... of the columnwise copy",
+                        "... of the per-tensor e4m3 copy"]}, ops
     if name == "dequant_8192":
         r = c = 8192
         ops = [{"kind": "dq_mx_row", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + r * c // 32, "gen": ("c2", 0)},
@@ -143,7 +152,8 @@ def workload_spec(name):
 
 
 DQ_KINDS = ("dq_mx_row", "dq_mx_col", "dq_tensor")
-ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule", "bw", "nvfp4")
+QS_KINDS = ("qs_mx_row", "qs_mx_col", "qs_tensor")
+ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule", "bw", "nvfp4", "qs_mx_row")
 
 
 def host_input(gen, shape):
@@ -342,6 +352,18 @@ def run_ours(args):
                            "q_t": torch.empty((c, r), dtype=torch.uint8, device=dev),
                            "s_t": torch.empty((c, tr) if op["block"] == 1 else (tc, tr), dtype=torch.float32,
                                               device=dev)}
+            elif op["kind"] in QS_KINDS:
+                # the copy to measure, made by the library's own quantizers
+                # before timing; x stays as the reference
+                if op["kind"] == "qs_tensor":
+                    qr = fq.fp8q_cast_per_tensor(x, op["fmt"])
+                    b["in"] = [x, qr["q"], qr["scale_inv"]]
+                else:
+                    qr = fq.mxfp8_quantize(x, op["fmt"], 3)
+                    b["in"] = [x, qr["q_row"], qr["s_row"]] if op["kind"] == "qs_mx_row" else \
+                        [x, qr["q_col"], qr["s_col"]]
+                b["st"] = torch.empty(6, dtype=torch.float64, device=dev)
+                b["ws"] = torch.zeros(fq.fp8q_qstats_workspace_bytes(), dtype=torch.uint8, device=dev)
             elif op["kind"] in DQ_KINDS:
                 # the codes to dequantize, made by the library's own quantizers
                 # before timing; the BF16 input is not kept
@@ -415,6 +437,17 @@ def run_ours(args):
                 b["call"] = (lib.fp8q_dequantize_per_tensor, (
                     b["in"][0].data_ptr(), r, c, None, 1, op["fmt"], b["in"][1].data_ptr(), 0, b["y"].data_ptr(),
                     stream))
+                b["launches"] = 1
+            elif k == "qs_tensor":
+                b["call"] = (lib.fp8q_qstats_per_tensor, (
+                    b["x"].data_ptr(), 0, r, c, None, 1, op["fmt"], b["in"][1].data_ptr(), b["in"][2].data_ptr(),
+                    b["st"].data_ptr(), b["ws"].data_ptr(), b["ws"].numel(), stream))
+                b["launches"] = 1
+            elif k in ("qs_mx_row", "qs_mx_col"):
+                b["call"] = (lib.mxfp8_qstats, (
+                    b["x"].data_ptr(), 0, r, c, None, 1, op["fmt"], 1 if k == "qs_mx_row" else 2,
+                    b["in"][1].data_ptr(), b["in"][2].data_ptr(), b["in"][2].shape[1], b["st"].data_ptr(),
+                    b["ws"].data_ptr(), b["ws"].numel(), stream))
                 b["launches"] = 1
             elif k in ("dq_mx_row", "dq_mx_col"):
                 b["call"] = (lib.mxfp8_dequantize, (
@@ -492,6 +525,8 @@ def run_ours(args):
                 return [b["bw"][k] for k in ("q", "s", "q_t", "s_t")]
             if op["kind"] == "nvfp4":
                 return [b["nv"][k] for k in ("q", "s", "scale")]
+            if op["kind"] in QS_KINDS:
+                return [b["st"]]
             return [b["y"]] if op["kind"] in DQ_KINDS else [b["q"]]
 
         ins_host = [[t.cpu().pin_memory() for t in sets[0][j]["in"]] for j in range(len(ops))]
@@ -546,7 +581,8 @@ def run_ours(args):
                     "kernel": ({"dq_mx_row": "dequant_kernel<mx_row,%s,bf16>",
                                 "mx_rule": "mx_kernel<bf16,%s,both,rule+counts>",
                                 "bw": "blockwise_kernel<%s,1x128,both>",
-                                "nvfp4": "amax_kernel+nvfp4_kernel<bf16> (%s block scales)"}.get(mx_op["kind"],
+                                "nvfp4": "amax_kernel+nvfp4_kernel<bf16> (%s block scales)",
+                                "qs_mx_row": "qstats_lin_kernel<bf16,%s,mx_row>"}.get(mx_op["kind"],
                                                                                      "mx_kernel<bf16,%s,both>")
                                % ("e4m3" if mx_op["fmt"] == E4M3 else "e5m2")),
                     "algorithmic_bytes_per_launch": mx_op["bytes"], "avg_launch_us": round(avg_ms * 1e3, 3),
@@ -563,6 +599,13 @@ def run_ours(args):
     if any(op["kind"] == "mx_rule" for op in ops):
         line["saturated_elements"] = {("round_up" if op["rule"] == 0 else "ocp"): sets[0][j]["sat"].cpu().tolist()
                                       for j, op in enumerate(ops) if op["kind"] == "mx_rule"}
+    if any(op["kind"] in QS_KINDS for op in ops):
+        line["qstats"] = {}
+        for j, op in enumerate(ops):
+            if op["kind"] in QS_KINDS:
+                d = fq.qstats_dict(sets[0][j]["st"])
+                line["qstats"][op["kind"]] = {"sqnr_db": round(d["sqnr_db"], 4), "zero_rate": d["zero_rate"],
+                                              "n_flushed": d["n_flushed"], "n_zero": d["n_zero"]}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload)
     for st in states:
@@ -584,7 +627,7 @@ def oracle_sample_step(workload, sample_rows, inputs, states):
     total = 0
     for op, x, st in zip(ops, inputs, states):
         k = op["kind"]
-        r, c = x["shape"] if k in DQ_KINDS else x.shape
+        r, c = x["shape"] if k in DQ_KINDS or k in QS_KINDS else x.shape
         if k in ("mx", "mx_grouped"):
             oracle.mx_quantize(x, op["fmt"], 3)
             total += mx_bytes(r, c)
@@ -609,6 +652,12 @@ def oracle_sample_step(workload, sample_rows, inputs, states):
             d = 1 if k == "dq_mx_row" else 2
             oracle.mx_dequantize(x["q"], x["s"], op["fmt"], d, r, c)
             total += 3 * r * c + x["s"].size
+        elif k == "qs_tensor":
+            oracle.qstats_per_tensor(x["x"], x["q"], op["fmt"], x["scale_inv"])
+            total += 3 * r * c + 4 + 48
+        elif k in ("qs_mx_row", "qs_mx_col"):
+            oracle.qstats_mx(x["x"], x["q"], x["s"], op["fmt"], 1 if k == "qs_mx_row" else 2)
+            total += 3 * r * c + x["s"].size + 48
         else:
             st.step(x)
             total += 3 * r * c
@@ -630,6 +679,13 @@ def oracle_inputs(workload, sample_rows):
             m = oracle.mx_quantize(x, op["fmt"], 3)
             x = ({"q": m["q_row"], "s": m["s_row"], "shape": (rr, c)} if op["kind"] == "dq_mx_row"
                  else {"q": m["q_col"], "s": m["s_col"], "shape": (rr, c)})
+        elif op["kind"] == "qs_tensor":  # the copy to measure, made by the oracle before timing
+            cs = oracle.current_scaling(x, op["fmt"])
+            x = {"x": x, "q": cs["q"].reshape(rr, c), "scale_inv": cs["scale_inv"], "shape": (rr, c)}
+        elif op["kind"] in ("qs_mx_row", "qs_mx_col"):
+            m = oracle.mx_quantize(x, op["fmt"], 3)
+            x = ({"x": x, "q": m["q_row"], "s": m["s_row"], "shape": (rr, c)} if op["kind"] == "qs_mx_row"
+                 else {"x": x, "q": m["q_col"], "s": m["s_col"], "shape": (rr, c)})
         xs.append(x)
         states.append(oracle.DelayedScaling(16, 1, 3, op["fmt"]) if op["kind"] == "delayed" else None)
     return xs, states
@@ -637,7 +693,8 @@ def oracle_inputs(workload, sample_rows):
 
 def sample_rows_for(workload):
     return {"activation": 256, "mx_8192": 128, "per_tensor_1024": 1024, "delayed_8192": 128, "linear_layer": 64,
-            "moe": 32, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128, "nvfp4_8192": 128}[workload]
+            "moe": 32, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128, "nvfp4_8192": 128,
+            "qstats_8192": 128}[workload]
 
 
 def cpu_baseline(workload, budget_s=10.0):

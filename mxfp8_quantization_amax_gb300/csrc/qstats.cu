@@ -153,40 +153,50 @@ __device__ __forceinline__ uint32_t qs_nonzero_codes(uint32_t w) { return (w & 0
 
 constexpr float kQsSmall = 7.88860905221011805e-31f;  // 2^-100
 
+// Bit 7 + 8k of the result: element k of four has a nonzero magnitude.
+// BF16: w0 holds elements 0 and 1, w1 elements 2 and 3 (low half first).
+__device__ __forceinline__ uint32_t qs_nonzero_bf16x4(uint32_t w0, uint32_t w1) {
+  const uint32_t t0 = (w0 & 0x7FFF7FFFu) + 0x7FFF7FFFu, t1 = (w1 & 0x7FFF7FFFu) + 0x7FFF7FFFu;
+  return __byte_perm(t0, t1, 0x7531);
+}
+// FP32: one element per word.
+__device__ __forceinline__ uint32_t qs_nonzero_f32x4(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+  const uint32_t t0 = (w0 & 0x7FFFFFFFu) + 0x7FFFFFFFu, t1 = (w1 & 0x7FFFFFFFu) + 0x7FFFFFFFu;
+  const uint32_t t2 = (w2 & 0x7FFFFFFFu) + 0x7FFFFFFFu, t3 = (w3 & 0x7FFFFFFFu) + 0x7FFFFFFFu;
+  return __byte_perm(__byte_perm(t0, t1, 0x0073), __byte_perm(t2, t3, 0x0073), 0x5410);
+}
+
+// Zero counts of four elements: code_nz from qs_nonzero_codes (bit 7 of a
+// byte: that code is nonzero), x_nz from qs_nonzero_* (the input is).
+__device__ __forceinline__ void qs_count4(QsAcc& a, uint32_t code_nz, uint32_t x_nz) {
+  a.nz += __popc(~code_nz & 0x80808080u);
+  a.nf += __popc(~code_nz & x_nz & 0x80808080u);
+}
+
 // Settles one chunk of 32 elements whose FP32 sums s and n the caller took
-// under the single multiplier m.  code_nz: AND of qs_nonzero_codes over its
-// code words.  m_exact_zero: a code of magnitude zero is the only way to get
-// xh == 0 (no FP32 underflow of value * m) -- true for MX scales, and for a
-// finite per-tensor multiplier of magnitude at least 2^-100.  xat(i) and
-// code(i) re-read element i from memory (rare paths only).
+// under the single multiplier m, from its registers:
+//   code_nz       AND of qs_nonzero_codes over the chunk's code words;
+//   x_zero        every x of the chunk is +-0;  codes_zero  every code is;
+//   m_exact_zero  xh == 0 exactly when the code is +-0 (value * m cannot
+//                 underflow): always for MX scales, and for a finite
+//                 per-tensor multiplier of magnitude at least 2^-100;
+//   count(a)      adds the chunk's zero counts (qs_count4 per code word).
 // The FP32 sums are kept when they are finite (then every pair is finite)
-// and each is either at least 2^-100 or exactly the sum of zeros;
-// otherwise the chunk is summed again in FP64.
-template <int FMT, class XF, class CF>
-__device__ __forceinline__ void qs_settle(QsAcc& a, float s, float n, uint32_t code_nz, bool m_exact_zero, float m,
-                                          XF xat, CF code) {
+// and each is either at least 2^-100 or exactly a sum of zeros; otherwise
+// the chunk is summed again in FP64 from memory (xat(i), code(i)).
+template <int FMT, class XF, class CF, class KF>
+__device__ __forceinline__ void qs_settle(QsAcc& a, float s, float n, uint32_t code_nz, bool x_zero, bool codes_zero,
+                                          bool m_exact_zero, float m, XF xat, CF code, KF count) {
   a.n += 32;
-  bool ok = isfinite(s) && isfinite(n) && m_exact_zero;
-  if (ok && s < kQsSmall) {
-    for (int i = 0; i < 32; i++) ok = ok && xat(i) == 0.0f;
-  }
-  if (ok && n < kQsSmall) {
-    for (int i = 0; i < 32; i++) ok = ok && __fsub_rn(xat(i), __fmul_rn(qs_value<FMT>(code(i)), m)) == 0.0f;
-  }
+  const bool ok = isfinite(s) && isfinite(n) && m_exact_zero && (s >= kQsSmall || x_zero) &&
+                  (n >= kQsSmall || (x_zero && codes_zero));
   if (!ok) {
     for (int i = 0; i < 32; i++) qs_elem(a, xat(i), __fmul_rn(qs_value<FMT>(code(i)), m));
     return;
   }
   a.signal += (double)s;
   a.noise += (double)n;
-  if ((code_nz & 0x80808080u) != 0x80808080u) {  // some codes are zero: count them
-    for (int i = 0; i < 32; i++) {
-      if ((code(i) & 0x7Fu) == 0u) {
-        a.nz++;
-        if (!(xat(i) == 0.0f)) a.nf++;
-      }
-    }
-  }
+  if ((code_nz & 0x80808080u) != 0x80808080u) count(a);
 }
 
 // Group boundary g, clamped into [0, rows].
@@ -384,11 +394,25 @@ __global__ void __launch_bounds__(kQsThreads) qstats_lin_kernel(QsParams p) {
         else X = f2_make(__uint_as_float(xw[2 * k]), __uint_as_float(xw[2 * k + 1]));
         qs_pair(X, f2_make(v0, v1), M, S, N);
       }
-      uint32_t nzc = 0xFFFFFFFFu;
+      uint32_t nzc = 0xFFFFFFFFu, cor = 0u, xor_ = 0u;
 #pragma unroll
-      for (int j = 0; j < 8; j++) nzc &= qs_nonzero_codes(qw[j]);
+      for (int j = 0; j < 8; j++) {
+        nzc &= qs_nonzero_codes(qw[j]);
+        cor |= qw[j] & 0x7F7F7F7Fu;
+      }
+#pragma unroll
+      for (int j = 0; j < kXw; j++) xor_ |= xw[j] & (DT == kBF16 ? 0x7FFF7FFFu : 0x7FFFFFFFu);
       const bool m_exact_zero = MX || (isfinite(m) && fabsf(m) >= kQsSmall);
-      qs_settle<FMT>(a, __fadd_rn(f2_lo(S), f2_hi(S)), __fadd_rn(f2_lo(N), f2_hi(N)), nzc, m_exact_zero, m, xg, cg);
+      auto count = [&](QsAcc& acc) {
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          const uint32_t xnz = DT == kBF16 ? qs_nonzero_bf16x4(xw[2 * j], xw[2 * j + 1])
+                                           : qs_nonzero_f32x4(xw[4 * j], xw[4 * j + 1], xw[4 * j + 2], xw[4 * j + 3]);
+          qs_count4(acc, qs_nonzero_codes(qw[j]), xnz);
+        }
+      };
+      qs_settle<FMT>(a, __fadd_rn(f2_lo(S), f2_hi(S)), __fadd_rn(f2_lo(N), f2_hi(N)), nzc, xor_ == 0u, cor == 0u,
+                     m_exact_zero, m, xg, cg, count);
     } else {
       for (int i = 0; i < 32; i++) {
         float si;
@@ -455,33 +479,69 @@ __global__ void __launch_bounds__(kQsThreads) qstats_col_kernel(QsParams p) {
       }
       f32x2 S = f2_make(0.0f, 0.0f), N = S;
       const f32x2 M = f2_make(ma, mb);
+      // row i of the pair: BF16 one word (column c low), FP32 two words
+      uint32_t xv[DT == kBF16 ? 32 : 64];
 #pragma unroll
       for (int i = 0; i < 32; i++) {
-        f32x2 X;
         if constexpr (DT == kBF16) {
-          const uint32_t w = __ldg((const unsigned*)((const uint16_t*)p.x + (r0 + i) * p.cols + c));
-          X = f2_make(bf16_lo(w), bf16_hi(w));
+          xv[i] = __ldg((const unsigned*)((const uint16_t*)p.x + (r0 + i) * p.cols + c));
         } else {
           const float2 w = __ldg((const float2*)((const float*)p.x + (r0 + i) * p.cols + c));
-          X = f2_make(w.x, w.y);
+          xv[2 * i] = __float_as_uint(w.x);
+          xv[2 * i + 1] = __float_as_uint(w.y);
         }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        const f32x2 X = DT == kBF16 ? f2_make(bf16_lo(xv[i]), bf16_hi(xv[i]))
+                                    : f2_make(__uint_as_float(xv[2 * i]), __uint_as_float(xv[2 * i + 1]));
         const int j = i & 3;
         float va, vb;  // row i's code of column c (low byte) and of column c + 1
         qs_decode2<FMT>(__byte_perm(wa[i >> 2], wb[i >> 2], j | ((4 + j) << 4)), va, vb);
         qs_pair(X, f2_make(va, vb), M, S, N);
       }
-      uint32_t za = 0xFFFFFFFFu, zb = 0xFFFFFFFFu;
+      uint32_t za = 0xFFFFFFFFu, zb = 0xFFFFFFFFu, ca = 0u, cb = 0u, xa = 0u, xb = 0u;
 #pragma unroll
       for (int j = 0; j < 8; j++) {
         za &= qs_nonzero_codes(wa[j]);
         zb &= qs_nonzero_codes(wb[j]);
+        ca |= wa[j] & 0x7F7F7F7Fu;
+        cb |= wb[j] & 0x7F7F7F7Fu;
       }
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        if constexpr (DT == kBF16) {
+          xa |= xv[i] & 0x7FFFu;
+          xb |= xv[i] & 0x7FFF0000u;
+        } else {
+          xa |= xv[2 * i] & 0x7FFFFFFFu;
+          xb |= xv[2 * i + 1] & 0x7FFFFFFFu;
+        }
+      }
+#pragma unroll
       for (int h = 0; h < 2; h++) {
         const int64_t cc = c + h;
         const uint8_t* qc = h ? qb : qa;
         auto xg = [&](int i) { return qs_x<DT>(p.x, (r0 + i) * p.cols + cc); };
         auto cg = [&](int i) { return (uint32_t)__ldg(qc + i); };
-        qs_settle<FMT>(a, h ? f2_hi(S) : f2_lo(S), h ? f2_hi(N) : f2_lo(N), h ? zb : za, true, h ? mb : ma, xg, cg);
+        auto count = [&](QsAcc& acc) {
+#pragma unroll
+          for (int j = 0; j < 8; j++) {
+            uint32_t t[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+              const int i = 4 * j + k;
+              t[k] = DT == kBF16 ? (xv[i] & 0x7FFF7FFFu) + 0x7FFF7FFFu
+                                 : (xv[2 * i + h] & 0x7FFFFFFFu) + 0x7FFFFFFFu;
+            }
+            // bit 15 (column c) or bit 31 (column c + 1, and FP32) of each row
+            const uint32_t sel = (DT == kBF16 && h == 0) ? 0x0051u : 0x0073u;
+            const uint32_t xnz = __byte_perm(__byte_perm(t[0], t[1], sel), __byte_perm(t[2], t[3], sel), 0x5410);
+            qs_count4(acc, qs_nonzero_codes(h ? wb[j] : wa[j]), xnz);
+          }
+        };
+        qs_settle<FMT>(a, h ? f2_hi(S) : f2_lo(S), h ? f2_hi(N) : f2_lo(N), h ? zb : za, (h ? xb : xa) == 0u,
+                       (h ? cb : ca) == 0u, true, h ? mb : ma, xg, cg, count);
       }
     } else {
       for (int h = 0; h < 2; h++) {
