@@ -30,6 +30,9 @@ import numpy as np
 
 E4M3 = 0
 E5M2 = 1
+E2M1 = 2  # MXFP4 elements
+E2M3 = 3  # MXFP6 elements (OCP reading)
+E3M2 = 4  # MXFP6 elements (OCP reading)
 BF16 = 0
 FP32 = 1
 
@@ -96,6 +99,10 @@ def _load():
                                           c.c_int]),
         "orc_mx_dequantize": (None, [P, P, c.c_int64, c.c_int64, P, c.c_int, c.c_int, c.c_int, c.c_int64,
                                      c.c_int, P, c.c_int]),
+        "orc_lp_value": (c.c_double, [c.c_int, c.c_uint]),
+        "orc_lp_encode": (c.c_uint, [c.c_int, c.c_double]),
+        "orc_mxlp_block": (c.c_uint8, [P, c.c_int, c.c_int, c.c_int, P, c.POINTER(c.c_int64)]),
+        "orc_mxlp_quantize": (None, [P, c.c_int, c.c_int64, c.c_int64, c.c_int, c.c_int, c.c_int, P, P, P, P, P]),
         "orc_qstats_per_tensor": (None, [P, c.c_int, c.c_int64, c.c_int64, P, c.c_int, c.c_int, P, P, P, P]),
         "orc_qstats_mx": (None, [P, c.c_int, c.c_int64, c.c_int64, P, c.c_int, c.c_int, c.c_int, P, P,
                                  c.c_int64, P, P]),
@@ -432,6 +439,46 @@ def mx_dequantize(q: np.ndarray, s: np.ndarray, fmt: int, direction: int, rows: 
     _load().orc_mx_dequantize(_ptr(q), _ptr(s), rows, cols, _ptr(o) if o is not None else None, G, fmt,
                               direction, s_ld, out_dt, _ptr(y), nthreads or max_threads())
     return y.reshape(q.shape)
+
+
+# --------------------------------------------------------------------------
+# MXFP4 / MXFP6 (E2M1, E2M3, E3M2 elements with E8M0 block scales)
+# --------------------------------------------------------------------------
+def lp_value(fmt: int, code: int) -> float:
+    """Value of an E2M1 / E2M3 / E3M2 code from its fields."""
+    return float(_load().orc_lp_value(fmt, code))
+
+
+def lp_encode(fmt: int, a: float) -> int:
+    """Nearest E2M1 / E2M3 / E3M2 code (ties to even), saturating."""
+    return int(_load().orc_lp_encode(fmt, float(a)))
+
+
+def mxlp_block(values: np.ndarray, fmt: int, rule: int) -> tuple[int, np.ndarray, int]:
+    """(scale byte, codes, saturated count) of one MX block of <= 32 values."""
+    v = np.ascontiguousarray(values, dtype=np.float32).reshape(-1)
+    q = np.zeros(v.size, dtype=np.uint8)
+    sat = ctypes.c_int64(0)
+    b = _load().orc_mxlp_block(_ptr(v), v.size, fmt, rule, _ptr(q), ctypes.byref(sat))
+    return int(b), q, int(sat.value)
+
+
+def mxlp_quantize(x: np.ndarray, fmt: int, direction: int = 3, rule: int = 0) -> dict:
+    """MXFP4 (E2M1, two codes per byte, even element low) or MXFP6 (E2M3 /
+    E3M2, one code per byte) of a 2-D tensor, rowwise and/or columnwise."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    fp4 = fmt == E2M1
+    nb = (rows + 31) // 32
+    out = {"q_row": np.zeros((rows, cols // 2 if fp4 else cols), np.uint8),
+           "s_row": np.zeros((rows, cols // 32), np.uint8),
+           "q_col": np.zeros((cols, rows // 2 if fp4 else rows), np.uint8),
+           "s_col": np.zeros((cols, nb), np.uint8)}
+    sat = np.zeros(2, dtype=np.int64)
+    _load().orc_mxlp_quantize(_ptr(x), _dtype_code(x), rows, cols, fmt, direction, rule, _ptr(out["q_row"]),
+                              _ptr(out["s_row"]), _ptr(out["q_col"]), _ptr(out["s_col"]), _ptr(sat))
+    out["sat"] = sat.tolist()
+    return out
 
 
 # --------------------------------------------------------------------------

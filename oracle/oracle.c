@@ -53,7 +53,16 @@
  *     with xh the FP32 value the code stands for, both sums over the
  *     elements where x and xh are finite (the rest counted apart); the
  *     zero-rate counts elements with xh = 0 and x != 0 (values that
- *     quantization flushed), next to the plain count of xh = 0.
+ *     quantization flushed), next to the plain count of xh = 0;
+ *   - MXFP6 elements are the OCP microscaling formats E2M3 (bias 1,
+ *     largest 7.5) and E3M2 (bias 3, largest 28) -- the pages name MXFP6
+ *     without defining them, so these two are parity unpinned by the
+ *     pages (pinned by a binade-by-binade construction only); MXFP4 /
+ *     MXFP6 blocks take destmax = the element format's largest value under
+ *     the round-up rule and its exponent as e_max under the OCP rule; a
+ *     non-finite block gets scale 0xFF and +0 codes (the formats have no
+ *     NaN); E2M1 codes are stored two per byte (even element low), FP6
+ *     codes one per byte (bits 0-5).
  * Those readings are pinned only by their own definition ("parity unpinned"
  * by the pages); everything else is pinned by page values, closed forms and
  * library routines in tests/test_oracle_pins.py.
@@ -68,6 +77,9 @@
 
 #define ORC_E4M3 0
 #define ORC_E5M2 1
+#define ORC_E2M1 2
+#define ORC_E2M3 3
+#define ORC_E3M2 4
 #define ORC_BF16 0
 #define ORC_FP32 1
 
@@ -825,4 +837,135 @@ void orc_qstats_mx(const void* x, int dt, int64_t rows, int64_t cols, const int6
             }
         base += (r1 - r0 + 31) / 32;
     }
+}
+
+/* ------------------------------------------------------------------ */
+/* MXFP4 and MXFP6 ("混合精度与 FP8 训练" 13.1: an MX block is k = 32    */
+/* elements and an E8M0 scale, e_max of E2M1 is 2; 13.2: E2M1 holds 0,  */
+/* 0.5, 1, 1.5, 2, 3, 4, 6 and negatives; "Blackwell GPU MXFP8 预训练最  */
+/* 佳实践" 3.2: Blackwell's block-scaled types MXFP8, MXFP6, MXFP4).     */
+/* The pages name MXFP6 but not its elements; they are read here as the */
+/* OCP microscaling pair E2M3 (bias 1, largest 7.5) and E3M2 (bias 3,   */
+/* largest 28).  All three formats have subnormals and no Inf or NaN; a */
+/* code is a sign bit above the magnitude bits (bit 3 for E2M1, bit 5   */
+/* for the FP6 formats).                                                */
+/* ------------------------------------------------------------------ */
+static int lp_ebits(int fmt) { return fmt == ORC_E3M2 ? 3 : 2; }
+static int lp_mbits(int fmt) { return fmt == ORC_E2M1 ? 1 : fmt == ORC_E2M3 ? 3 : 2; }
+static unsigned lp_top(int fmt) { return (1u << (lp_ebits(fmt) + lp_mbits(fmt))) - 1u; }
+
+/* Value of a code from its fields: exponent field 0 is subnormal. */
+double orc_lp_value(int fmt, unsigned code)
+{
+    int eb = lp_ebits(fmt), mb = lp_mbits(fmt), bias = (1 << (eb - 1)) - 1;
+    unsigned sign = (code >> (eb + mb)) & 1u;
+    unsigned e = (code >> mb) & ((1u << eb) - 1u), m = code & ((1u << mb) - 1u);
+    double f = ldexp((double)m, -mb);
+    double mag = e == 0 ? ldexp(f, 1 - bias) : ldexp(1.0 + f, (int)e - bias);
+    return sign ? -mag : mag;
+}
+
+/* Nearest code of a real value, ties to the even code, saturating at the
+ * largest magnitude; the sign of zero is kept.  (NaN is never encoded: an
+ * MX block holding one is marked by its scale.) */
+unsigned orc_lp_encode(int fmt, double a)
+{
+    unsigned top = lp_top(fmt), sign = signbit(a) ? top + 1u : 0u;
+    double m = fabs(a);
+    if (isnan(a)) return 0u;
+    if (m >= orc_lp_value(fmt, top)) return sign | top;
+    unsigned lo = 0;
+    while (orc_lp_value(fmt, lo + 1) <= m) lo++;
+    if (orc_lp_value(fmt, lo) == m) return sign | lo;
+    double dl = m - orc_lp_value(fmt, lo), dh = orc_lp_value(fmt, lo + 1) - m;
+    unsigned c = dl < dh ? lo : dh < dl ? lo + 1 : ((lo & 1u) ? lo + 1 : lo);
+    return sign | c;
+}
+
+/*
+ * One MX block of k <= 32 values with E2M1, E2M3 or E3M2 elements, under
+ * scale rule 0 (round-up: the smallest X with amax <= destmax * 2^X) or 1
+ * (OCP: X = floor(log2 amax) - e_max), X saturated to [-127, 127]; destmax
+ * is the format's largest value (6, 7.5, 28) and e_max its exponent (2, 2,
+ * 4).  Elements are the nearest codes of v / 2^X (exact), saturating;
+ * *sat counts |v / 2^X| > destmax.  amax 0: byte 0 and all codes +0;
+ * amax Inf or NaN: byte 0xFF and all codes +0 (the scale marks the block).
+ */
+uint8_t orc_mxlp_block(const float* v, int k, int fmt, int rule, uint8_t* q, int64_t* sat)
+{
+    uint32_t amax = 0;
+    double destmax = orc_lp_value(fmt, lp_top(fmt));
+    int emax = (int)floor(log2(destmax));
+    int X, i;
+    *sat = 0;
+    for (i = 0; i < k; i++) {
+        uint32_t mag = float_to_bits(v[i]) & 0x7FFFFFFFu;
+        if (mag > amax) amax = mag;
+    }
+    if (amax >= 0x7F800000u || amax == 0) {
+        for (i = 0; i < k; i++) q[i] = 0;
+        return amax ? 0xFF : 0x00;
+    }
+    double a = (double)bits_to_float(amax);
+    if (rule == 0) {
+        for (X = -127; X < 127; X++)
+            if (a <= ldexp(destmax, X)) break;
+    } else {
+        for (X = 127; X > -127; X--)
+            if (ldexp(1.0, X + emax) <= a) break;
+    }
+    for (i = 0; i < k; i++) {
+        double sv = ldexp((double)v[i], -X);
+        if (fabs(sv) > destmax) (*sat)++;
+        q[i] = (uint8_t)orc_lp_encode(fmt, sv);
+    }
+    return (uint8_t)(X + 127);
+}
+
+/* Code i of a copy's row, stored two per byte (E2M1: element 2j in the low
+ * nibble of byte j) or one per byte (FP6: bits 0-5). */
+static void lp_put(uint8_t* row, int fmt, int64_t i, uint8_t code)
+{
+    if (fmt != ORC_E2M1) {
+        row[i] = code;
+        return;
+    }
+    uint8_t* b = row + i / 2;
+    *b = (i & 1) ? (uint8_t)((*b & 0x0F) | (code << 4)) : (uint8_t)((*b & 0xF0) | code);
+}
+
+/*
+ * MXFP4 / MXFP6 quantization of a rows x cols tensor (cols % 32 == 0):
+ * dir 1 rowwise blocks x[r][32j .. 32j+31]; dir 2 columnwise blocks of 32
+ * rows (the last one shorter), stored transposed; 3 both.
+ *   E2M1: q_row [rows][cols / 2], q_col [cols][rows / 2] (rows even)
+ *   FP6:  q_row [rows][cols],     q_col [cols][rows]
+ *   s_row [rows][cols / 32], s_col [cols][ceil(rows / 32)]
+ * sat[0], sat[1]: the rowwise and columnwise saturation counts.
+ */
+void orc_mxlp_quantize(const void* x, int dt, int64_t rows, int64_t cols, int fmt, int dir, int rule,
+                       uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int64_t* sat)
+{
+    float v[32];
+    uint8_t qb[32];
+    int64_t s1, nb = (rows + 31) / 32;
+    int64_t rlen = fmt == ORC_E2M1 ? cols / 2 : cols, clen = fmt == ORC_E2M1 ? rows / 2 : rows;
+    sat[0] = sat[1] = 0;
+    if (dir & 1)
+        for (int64_t r = 0; r < rows; r++)
+            for (int64_t j = 0; j < cols / 32; j++) {
+                for (int i = 0; i < 32; i++) v[i] = orc_input_value(x, dt, r * cols + 32 * j + i);
+                s_row[r * (cols / 32) + j] = orc_mxlp_block(v, 32, fmt, rule, qb, &s1);
+                sat[0] += s1;
+                for (int i = 0; i < 32; i++) lp_put(q_row + r * rlen, fmt, 32 * j + i, qb[i]);
+            }
+    if (dir & 2)
+        for (int64_t c = 0; c < cols; c++)
+            for (int64_t b = 0; b < nb; b++) {
+                int k = rows - 32 * b < 32 ? (int)(rows - 32 * b) : 32;
+                for (int i = 0; i < k; i++) v[i] = orc_input_value(x, dt, (32 * b + i) * cols + c);
+                s_col[c * nb + b] = orc_mxlp_block(v, k, fmt, rule, qb, &s1);
+                sat[1] += s1;
+                for (int i = 0; i < k; i++) lp_put(q_col + c * clen, fmt, 32 * b + i, qb[i]);
+            }
 }

@@ -929,3 +929,176 @@ def test_qstats_nonfinite_elements_leave_the_sums():
     assert st["n_nonfinite"] == 32 and st["n"] == base["n"]
     assert st["signal"] == pytest.approx(part["signal"], rel=1e-15)
     assert st["noise"] == pytest.approx(part["noise"], rel=1e-15)
+
+
+# --------------------------------------------------------------------------
+# MXFP4 / MXFP6 ("混合精度与 FP8 训练" 13.1-13.2; E2M3 / E3M2 are the OCP
+# reading of the MXFP6 that "Blackwell GPU MXFP8 预训练最佳实践" 3.2 names)
+# --------------------------------------------------------------------------
+LP = {"e2m1": oracle.E2M1, "e2m3": oracle.E2M3, "e3m2": oracle.E3M2}
+LP_CODES = {oracle.E2M1: 8, oracle.E2M3: 32, oracle.E3M2: 32}
+
+
+def _lp_magnitudes(fmt):
+    """The non-negative values built binade by binade (a uniform grid of
+    2^m steps per binade, the subnormal range continuing the first
+    binade's step down to 0), not from the bit fields."""
+    m, lo_exp, hi_exp = {oracle.E2M1: (1, 0, 2), oracle.E2M3: (3, 0, 2), oracle.E3M2: (2, -2, 4)}[fmt]
+    step0 = Fraction(2) ** lo_exp / 2 ** m
+    vals = [k * step0 for k in range(2 ** m)]                      # [0, 2^lo_exp)
+    for e in range(lo_exp, hi_exp + 1):
+        vals += [Fraction(2) ** e * (1 + Fraction(k, 2 ** m)) for k in range(2 ** m)]
+    return vals
+
+
+@pytest.mark.parametrize("name", ["e2m1", "e2m3", "e3m2"])
+def test_lp_values_binade_construction(name):
+    """Codes 0 .. top decode to the binade-by-binade value list in order;
+    the sign bit negates; E2M1 is the page's list 0, 0.5, 1, 1.5, 2, 3, 4,
+    6; the largest values are 6, 7.5 and 28."""
+    fmt = LP[name]
+    n = LP_CODES[fmt]
+    want = _lp_magnitudes(fmt)
+    assert len(want) == n
+    got = [Fraction(oracle.lp_value(fmt, c)) for c in range(n)]
+    assert got == want
+    assert [oracle.lp_value(fmt, c + n) for c in range(n)] == [-float(v) for v in want]
+    assert float(want[-1]) == {"e2m1": 6.0, "e2m3": 7.5, "e3m2": 28.0}[name]
+    if name == "e2m1":
+        assert [float(v) for v in want] == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+
+
+@pytest.mark.parametrize("name", ["e2m1", "e2m3", "e3m2"])
+def test_lp_encoding_brute_force(name):
+    """Nearest value, ties to the even code, saturating at the largest
+    magnitude, sign (of zero too) kept -- over a fine grid and every
+    midpoint."""
+    fmt = LP[name]
+    n = LP_CODES[fmt]
+    mags = [float(v) for v in _lp_magnitudes(fmt)]
+    top = mags[-1]
+    grid = np.concatenate([np.linspace(-1.2 * top, 1.2 * top, 6001), [(a + b) / 2 for a, b in zip(mags, mags[1:])],
+                           [-(a + b) / 2 for a, b in zip(mags, mags[1:])], [0.0, -0.0]])
+    for a in grid:
+        m = abs(a)
+        best = n - 1 if m >= top else min(range(n), key=lambda c: (abs(mags[c] - m), c & 1))
+        want = best | (n if math.copysign(1.0, a) < 0 else 0)
+        assert oracle.lp_encode(fmt, a) == want, (name, a)
+
+
+def test_page_mxfp4_example():
+    """The amax-5.3 block with E2M1 elements: e_max 2, shared exponent 0,
+    scale 1; 5.3 rounds to 6, a 13% error (OCP rule; the round-up rule
+    gives the same exponent since 5.3 <= 6)."""
+    case = next(c for c in PAGES["mx"] if c["id"] == "T6-e2m1")
+    v = np.zeros(32, np.float32)
+    v[5] = case["amax"]
+    for rule in (1, 0):
+        byte, q, sat = oracle.mxlp_block(v, oracle.E2M1, rule)
+        assert byte == case["scale_byte"] and byte - 127 == case["X"] and sat == 0
+        assert oracle.lp_value(oracle.E2M1, int(q[5])) == case["element_value"]
+        assert round(100 * (case["element_value"] - case["amax"]) / case["amax"]) == case["rel_err_pct"]
+        assert not np.delete(q, 5).any()
+
+
+@pytest.mark.parametrize("name", ["e2m1", "e2m3", "e3m2"])
+def test_mxlp_rules(name):
+    """Round-up X is the smallest with amax <= destmax * 2^X (never
+    saturates); OCP X = floor(log2 amax) - e_max, never above round-up X and
+    at most one below, saturating exactly the elements above destmax."""
+    fmt = LP[name]
+    destmax = float(_lp_magnitudes(fmt)[-1])
+    emax = math.floor(math.log2(destmax))
+    rng = np.random.default_rng(71)
+    for _ in range(300):
+        v = (rng.standard_normal(32) * 2.0 ** rng.integers(-30, 30)).astype(np.float32)
+        amax = float(np.max(np.abs(v)))
+        bu, qu, su = oracle.mxlp_block(v, fmt, 0)
+        bo, qo, so = oracle.mxlp_block(v, fmt, 1)
+        xu, xo = bu - 127, bo - 127
+        assert amax <= destmax * 2.0 ** xu and not amax <= destmax * 2.0 ** (xu - 1)
+        assert xo == math.floor(math.log2(amax)) - emax
+        assert xu - xo in (0, 1) and su == 0
+        assert so == int(np.sum(np.abs(v.astype(np.float64)) * 2.0 ** -xo > destmax))
+        for c, q in ((xu, qu), (xo, qo)):
+            for i in range(32):
+                assert q[i] == oracle.lp_encode(fmt, math.ldexp(float(v[i]), -c))
+
+
+@pytest.mark.parametrize("name", ["e2m1", "e2m3", "e3m2"])
+def test_mxlp_exact_blocks_and_special_blocks(name):
+    """A block of representable values times 2^X that holds the largest
+    code quantizes back to its codes with scale byte X + 127; an all-zero
+    block gets byte 0 and +0 codes; Inf or NaN gets 0xFF and +0 codes; a -0
+    in a nonzero block keeps its sign."""
+    fmt = LP[name]
+    n = LP_CODES[fmt]
+    rng = np.random.default_rng(72)
+    for X in (-100, -3, 0, 5, 90):
+        codes = rng.integers(0, 2 * n, size=32)
+        codes[7] = n - 1
+        v = np.array([oracle.lp_value(fmt, int(c)) * 2.0 ** X for c in codes], np.float32)
+        byte, q, _ = oracle.mxlp_block(v, fmt, 0)
+        assert byte == X + 127
+        np.testing.assert_array_equal([oracle.lp_value(fmt, int(c)) for c in q],
+                                      [oracle.lp_value(fmt, int(c)) for c in codes])
+    zero = np.zeros(32, np.float32)
+    zero[3] = -0.0
+    assert oracle.mxlp_block(zero, fmt, 0)[0] == 0 and not oracle.mxlp_block(zero, fmt, 0)[1].any()
+    for bad in (np.inf, np.nan):
+        v = np.ones(32, np.float32)
+        v[9] = bad
+        byte, q, _ = oracle.mxlp_block(v, fmt, 1)
+        assert byte == 0xFF and not q.any()
+    v = np.ones(32, np.float32)
+    v[2] = -0.0
+    assert oracle.mxlp_block(v, fmt, 0)[1][2] == n
+
+
+@pytest.mark.parametrize("name", ["e2m1", "e2m3", "e3m2"])
+def test_mxlp_quantize_layout(name):
+    """Rowwise copy = the blocks of each row (E2M1 two codes per byte, even
+    element low); columnwise copy = the rowwise copy of the transpose,
+    with a shorter last block when rows % 32 != 0."""
+    fmt = LP[name]
+    rng = np.random.default_rng(73)
+    x = (rng.standard_normal((40, 64)) * np.exp(rng.standard_normal((40, 1)) * 3)).astype(np.float32)
+    r = oracle.mxlp_quantize(x, fmt, 3, rule=1)
+    for i in range(40):
+        for j in range(2):
+            byte, q, _ = oracle.mxlp_block(x[i, 32 * j:32 * j + 32], fmt, 1)
+            assert r["s_row"][i, j] == byte
+            row = r["q_row"][i]
+            got = np.stack([row & 0xF, row >> 4], 1).reshape(-1) if fmt == oracle.E2M1 else row
+            np.testing.assert_array_equal(got[32 * j:32 * j + 32], q)
+    xt = np.ascontiguousarray(np.concatenate([x, np.zeros((24, 64), np.float32)]).T)  # 64 x 64
+    rt = oracle.mxlp_quantize(xt, fmt, 1, rule=1)
+    np.testing.assert_array_equal(r["s_col"][:, 0], rt["s_row"][:, 0])
+    half = 16 if fmt == oracle.E2M1 else 32
+    np.testing.assert_array_equal(r["q_col"][:, :half], rt["q_row"][:, :half])
+    for c in range(64):  # the last block holds rows 32 .. 39 only
+        byte, q, _ = oracle.mxlp_block(x[32:, c], fmt, 1)
+        assert r["s_col"][c, 1] == byte
+
+
+@pytest.mark.parametrize("name", ["e2m1", "e2m3", "e3m2"])
+def test_mxlp_rule_boundaries(name):
+    """Exact boundaries: an amax that is a power of two 2^k gets OCP X =
+    k - e_max; an amax exactly on destmax * 2^X sits on the maximum code
+    under both rules and is not counted as saturated."""
+    fmt = LP[name]
+    destmax = float(_lp_magnitudes(fmt)[-1])
+    emax = math.floor(math.log2(destmax))
+    for k in (-20, 0, 3, 17):
+        v = np.full(32, 2.0 ** (k - 3), np.float32)
+        v[11] = -(2.0 ** k)
+        byte, q, sat = oracle.mxlp_block(v, fmt, 1)
+        assert byte - 127 == k - emax and sat == 0
+        assert oracle.lp_value(fmt, int(q[11])) == -(2.0 ** emax)
+    for X in (-5, 0, 9):
+        v = np.full(32, destmax * 2.0 ** (X - 2), np.float32)
+        v[4] = destmax * 2.0 ** X
+        for rule in (0, 1):
+            byte, q, sat = oracle.mxlp_block(v, fmt, rule)
+            assert byte - 127 == X and sat == 0
+            assert oracle.lp_value(fmt, int(q[4])) == destmax
