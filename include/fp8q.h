@@ -62,8 +62,13 @@ typedef enum {
 typedef enum { FP8Q_IN_BF16 = 0, FP8Q_IN_FP32 = 1 } fp8q_in_dtype;
 
 /* E4M3: bias 7, no Inf, max 448.  E5M2: IEEE style, bias 15, max 57344.
- * ("混合精度与 FP8 训练", 2.2; "Blackwell GPU MXFP8 预训练最佳实践", 3.1) */
-typedef enum { FP8Q_E4M3 = 0, FP8Q_E5M2 = 1 } fp8q_format;
+ * ("混合精度与 FP8 训练", 2.2; "Blackwell GPU MXFP8 预训练最佳实践", 3.1)
+ * MX element formats below 8 bits, for mx_quantize_fp4_fp6 only: E2M1
+ * (MXFP4: 0, 0.5, 1, 1.5, 2, 3, 4, 6; "混合精度与 FP8 训练" 13.2) and the
+ * MXFP6 pair E2M3 (bias 1, max 7.5) and E3M2 (bias 3, max 28), read as the
+ * OCP microscaling formats that "Blackwell GPU MXFP8 预训练最佳实践" 3.2
+ * names without defining.  None has Inf or NaN. */
+typedef enum { FP8Q_E4M3 = 0, FP8Q_E5M2 = 1, FP8Q_E2M1 = 2, FP8Q_E2M3 = 3, FP8Q_E3M2 = 4 } fp8q_format;
 
 typedef enum { MXFP8_ROW = 1, MXFP8_COL = 2, MXFP8_BOTH = 3 } mxfp8_dir;
 
@@ -304,6 +309,35 @@ FP8Q_API fp8q_status mxfp8_quantize_rule(const void* x, int32_t dt, int64_t rows
                                          int32_t dir, int32_t scale_rule, uint8_t* q_row, uint8_t* s_row,
                                          uint8_t* q_col, uint8_t* s_col, int64_t s_col_ld,
                                          unsigned long long* sat_count, void* stream);
+
+/*
+ * MXFP4 / MXFP6 quantization ("混合精度与 FP8 训练" 13.1-13.2; "Blackwell
+ * GPU MXFP8 预训练最佳实践" 3.2 and 4.1): blocks of 32 elements with one E8M0
+ * scale, as mxfp8_quantize_rule but with element format elem (FP8Q_E2M1,
+ * FP8Q_E2M3 or FP8Q_E3M2): destmax 6, 7.5 or 28 under FP8Q_MX_RULE_UP, e_max
+ * 2, 2 or 4 under FP8Q_MX_RULE_OCP.  Elements are the nearest codes of
+ * v / 2^X, saturating.  A block whose amax is 0 gets scale byte 0 and +0
+ * codes; one holding Inf or NaN gets 0xFF and +0 codes.  One pass over x
+ * writes both copies.  No groups.
+ *   rowwise (dir & MXFP8_ROW):
+ *     q_row  E2M1: device uint8 [rows][cols / 2], two codes per byte, the
+ *                  even element in the low nibble; FP6: [rows][cols], one
+ *                  code per byte in bits 0-5
+ *     s_row  device uint8 [rows][cols / 32]
+ *   columnwise (dir & MXFP8_COL): blocks of 32 rows (the last one shorter),
+ *   stored transposed:
+ *     q_col  E2M1: [cols][rows / 2] (rows must be even); FP6: [cols][rows]
+ *     s_col  device uint8 [cols][ceil(rows / 32)]
+ *   sat_count  device uint64[2] or NULL: elements whose |v / 2^X| exceeds
+ *              destmax (clamped), [0] rowwise, [1] columnwise; zeroed by
+ *              the call.  Never nonzero under FP8Q_MX_RULE_UP.
+ * cols % 32 == 0 (FP8Q_ERR_UNSUPPORTED otherwise); q_row and q_col 16-byte
+ * aligned; pointers of an unused copy may be NULL.
+ */
+FP8Q_API fp8q_status mx_quantize_fp4_fp6(const void* x, int32_t dt, int64_t rows, int64_t cols, int32_t elem,
+                                         int32_t dir, int32_t scale_rule, uint8_t* q_row, uint8_t* s_row,
+                                         uint8_t* q_col, uint8_t* s_col, unsigned long long* sat_count,
+                                         void* stream);
 
 /*
  * Blockwise FP8 with one FP32 scale per group ("混合精度与 FP8 训练" 10.2:

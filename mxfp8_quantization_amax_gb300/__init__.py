@@ -29,10 +29,14 @@ __all__ = [
     "fp8q_scale_from_amax", "debug_stall_mx_producer", "fp8q_dequantize_per_tensor", "mxfp8_dequantize",
     "RULE_UP", "RULE_OCP", "BLOCK_1X128", "BLOCK_128X128", "fp8q_quantize_blockwise", "fp8q_quantize_nvfp4",
     "fp8q_qstats_workspace_bytes", "fp8q_qstats_per_tensor", "mxfp8_qstats", "qstats_dict",
+    "E2M1", "E2M3", "E3M2", "mx_quantize_fp4_fp6",
 ]
 
 E4M3 = 0
 E5M2 = 1
+E2M1 = 2  # MXFP4 elements
+E2M3 = 3  # MXFP6 elements
+E3M2 = 4  # MXFP6 elements
 ROW = 1
 COL = 2
 BOTH = 3
@@ -59,6 +63,8 @@ _SIGS = {
                                               _c.c_int32, _P, _P]),
     "mxfp8_dequantize": (_c.c_int, [_P, _P, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32, _c.c_int32,
                                     _c.c_int64, _c.c_int32, _P, _P]),
+    "mx_quantize_fp4_fp6": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32,
+                                       _P, _P, _P, _P, _P, _P]),
     "fp8q_qstats_workspace_bytes": (_c.c_size_t, []),
     "fp8q_qstats_per_tensor": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32,
                                           _P, _P, _P, _P, _c.c_size_t, _P]),
@@ -454,6 +460,41 @@ def mxfp8_dequantize(q: torch.Tensor, s: torch.Tensor, rows: int, cols: int, fmt
     _check(lib().mxfp8_dequantize(_ptr(q), _ptr(s), rows, cols, _ptr(off), G, fmt, direction, s_ld,
                                   _out_dtype(out_dtype), _ptr(y), _stream()), "mxfp8_dequantize")
     return y
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 / MXFP6
+# ---------------------------------------------------------------------------
+def mx_quantize_fp4_fp6(x: torch.Tensor, elem: int = E2M1, direction: int = BOTH, rule: int = RULE_UP,
+                        count_saturation: bool = False, out: dict | None = None) -> dict:
+    """MXFP4 (elem E2M1: two codes per byte, even element low) or MXFP6
+    (E2M3 / E3M2: one code per byte) with E8M0 scales per 32 elements.
+
+    Returns q_row [rows, cols/2 or cols], s_row [rows, cols/32], q_col
+    [cols, rows/2 or rows], s_col [cols, ceil(rows/32)] for the requested
+    directions, and sat (uint64[2] saturated counts) when counted."""
+    _check_input(x)
+    rows, cols = _as_2d(x)
+    out = {} if out is None else out
+    fp4 = elem == E2M1
+    shapes = {"q_row": (rows, cols // 2 if fp4 else cols), "s_row": (rows, cols // 32),
+              "q_col": (cols, rows // 2 if fp4 else rows), "s_col": (cols, (rows + 31) // 32)}
+
+    def buf(name, wanted):
+        if not wanted:
+            return None
+        if name not in out:
+            out[name] = torch.empty(shapes[name], dtype=torch.uint8, device=x.device)
+        return out[name]
+
+    q_row, s_row = buf("q_row", direction & ROW), buf("s_row", direction & ROW)
+    q_col, s_col = buf("q_col", direction & COL), buf("s_col", direction & COL)
+    sat = None
+    if count_saturation:
+        sat = out.setdefault("sat", torch.zeros(2, dtype=torch.int64, device=x.device))
+    _check(lib().mx_quantize_fp4_fp6(_ptr(x), _dt(x), rows, cols, elem, direction, rule, _ptr(q_row), _ptr(s_row),
+                                     _ptr(q_col), _ptr(s_col), _ptr(sat), _stream()), "mx_quantize_fp4_fp6")
+    return out
 
 
 # ---------------------------------------------------------------------------

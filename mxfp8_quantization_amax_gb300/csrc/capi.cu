@@ -89,6 +89,11 @@ static fp8q_status check_common(const void* x, int32_t dt, int64_t rows, int64_t
 
 static bool fmt_ok(int32_t fmt) { return fmt == FP8Q_E4M3 || fmt == FP8Q_E5M2; }
 
+// MXFP4 / MXFP6 (mxlow.cu).
+fp8q_status launch_mxlow(const void* x, int dt, int64_t rows, int64_t cols, int elem, int dir, int round_up,
+                         uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, unsigned long long* sat,
+                         cudaStream_t stream);
+
 // Quantization statistics (qstats.cu).
 size_t qstats_workspace_bytes();
 fp8q_status launch_qstats(int kind, const void* x, int dt, const uint8_t* q, const uint8_t* s, const float* scale_inv,
@@ -455,6 +460,35 @@ fp8q_status mxfp8_dequantize(const uint8_t* q, const uint8_t* s, int64_t rows, i
   if (rows * cols == 0) return FP8Q_OK;
   return launch_dequant(dir == MXFP8_ROW ? 1 : 2, q, s, nullptr, group_offsets, num_groups, rows, cols, s_ld, fmt,
                         out_dt, y, (cudaStream_t)stream);
+}
+
+fp8q_status mx_quantize_fp4_fp6(const void* x, int32_t dt, int64_t rows, int64_t cols, int32_t elem, int32_t dir,
+                                int32_t scale_rule, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                unsigned long long* sat_count, void* stream) {
+  g_err[0] = 0;
+  fp8q_status r = check_common(x, dt, rows, cols, nullptr, 1);
+  if (r != FP8Q_OK) return r;
+  if (elem != FP8Q_E2M1 && elem != FP8Q_E2M3 && elem != FP8Q_E3M2)
+    return fail(FP8Q_ERR_INVALID_ARG, "elem must be FP8Q_E2M1, FP8Q_E2M3 or FP8Q_E3M2");
+  if (dir < MXFP8_ROW || dir > MXFP8_BOTH) return fail(FP8Q_ERR_INVALID_ARG, "dir must be MXFP8_ROW, _COL or _BOTH");
+  if (scale_rule != FP8Q_MX_RULE_UP && scale_rule != FP8Q_MX_RULE_OCP)
+    return fail(FP8Q_ERR_INVALID_ARG, "scale_rule must be FP8Q_MX_RULE_UP or FP8Q_MX_RULE_OCP");
+  if (cols % 32 != 0) return fail(FP8Q_ERR_UNSUPPORTED, "MX needs cols %% 32 == 0 (cols = %lld)", (long long)cols);
+  if (elem == FP8Q_E2M1 && (dir & MXFP8_COL) && rows % 2 != 0)
+    return fail(FP8Q_ERR_UNSUPPORTED, "the packed E2M1 columnwise copy needs an even row count");
+  const bool n = rows * cols > 0;
+  if ((dir & MXFP8_ROW) && n && (!q_row || !s_row)) return fail(FP8Q_ERR_INVALID_ARG, "q_row and s_row are required");
+  if ((dir & MXFP8_COL) && n && (!q_col || !s_col)) return fail(FP8Q_ERR_INVALID_ARG, "q_col and s_col are required");
+  if (!aligned(q_row, 16) || !aligned(q_col, 16)) return fail(FP8Q_ERR_INVALID_ARG, "q_row and q_col must be 16-byte aligned");
+  if (!aligned(sat_count, 8)) return fail(FP8Q_ERR_INVALID_ARG, "sat_count must be 8-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  if (sat_count) {
+    cudaError_t e = cudaMemsetAsync(sat_count, 0, 2 * sizeof(unsigned long long), st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing sat_count");
+  }
+  if (!n) return FP8Q_OK;
+  return launch_mxlow(x, dt, rows, cols, elem, dir, scale_rule == FP8Q_MX_RULE_UP ? 1 : 0, q_row, s_row, q_col, s_col,
+                      sat_count, st);
 }
 
 fp8q_status fp8q_qstats_per_tensor(const void* x, int32_t dt, int64_t rows, int64_t cols,

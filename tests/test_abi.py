@@ -42,7 +42,7 @@ def test_only_declared_symbols_are_exported(lib):
     """Internal helpers stay hidden (the build uses -fvisibility=hidden)."""
     out = os.popen(f"nm -D --defined-only {fq.library_path()}").read()
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
-    ours = {s for s in exported if s.startswith(("fp8q", "mxfp8"))}
+    ours = {s for s in exported if s.startswith(("fp8q", "mxfp8", "mx_"))}
     assert ours == set(declared_symbols())
 
 
@@ -186,3 +186,17 @@ def test_qstats_arguments_rejected_on_host(lib):
     assert lib.mxfp8_qstats(a, 0, 4, 64, None, 1, 0, 1, a, a, 0, a, None, wsb, None) == 1
     # a grouped call needs num_groups + 1 offsets; NULL offsets mean one group
     assert lib.mxfp8_qstats(a, 0, 4, 64, None, 2, 0, 2, a, a, 1, a, a, wsb, None) == 1
+
+
+def test_fp4_fp6_arguments_rejected_on_host(lib):
+    buf = ctypes.create_string_buffer(256)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    # an FP8 format, an unknown rule, cols % 32, odd rows for the packed E2M1 columnwise copy
+    assert lib.mx_quantize_fp4_fp6(a, 0, 4, 64, 0, 3, 0, a, a, a, a, None, None) == 1
+    assert lib.mx_quantize_fp4_fp6(a, 0, 4, 64, 2, 3, 2, a, a, a, a, None, None) == 1
+    assert lib.mx_quantize_fp4_fp6(a, 0, 4, 48, 3, 1, 0, a, a, None, None, None, None) == 2
+    assert lib.mx_quantize_fp4_fp6(a, 0, 5, 64, 2, 2, 0, None, None, a, a, None, None) == 2
+    # missing outputs of a requested copy, misaligned codes or counter
+    assert lib.mx_quantize_fp4_fp6(a, 0, 4, 64, 4, 2, 0, a, a, None, a, None, None) == 1
+    assert lib.mx_quantize_fp4_fp6(a, 0, 4, 64, 4, 1, 0, a + 2, a, None, None, None, None) == 1
+    assert lib.mx_quantize_fp4_fp6(a, 0, 4, 64, 4, 1, 0, a, a, None, None, a + 4, None) == 1
