@@ -61,7 +61,7 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="activation",
                    choices=["activation", "mx_8192", "per_tensor_1024", "delayed_8192", "linear_layer", "moe",
                             "dequant_8192", "mx_rules_4096", "blockwise_8192", "nvfp4_8192",
-                            "qstats_8192"])
+                            "qstats_8192", "mxfp4_fp6_8192"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
@@ -132,6 +132,14 @@ def workload_spec(name):
                 "gen": ("c2", 0)}]
         return {"workload": "nvfp4_8192x8192_bf16", "rows": r, "cols": c,
                 "ops": ["nvfp4: tensor amax, then E2M1 codes and E4M3 scales per 16"]}, ops
+    if name == "mxfp4_fp6_8192":
+        r = c = 8192
+        ops = [{"kind": "mxlow", "elem": 2, "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + r * c // 16,
+                "gen": ("c2", 0)},
+               {"kind": "mxlow", "elem": 3, "shape": (r, c), "fmt": E4M3, "bytes": 4 * r * c + r * c // 16,
+                "gen": ("c2", 0)}]
+        return {"workload": "mxfp4_mxfp6_8192x8192_bf16", "rows": r, "cols": c,
+                "ops": ["mxfp4 (e2m1) row+col, round-up rule", "mxfp6 (e2m3) row+col, round-up rule"]}, ops
     if name == "qstats_8192":
         r = c = 8192
         ops = [{"kind": "qs_mx_row", "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + r * c // 32 + 48, "gen": ("c2", 0)},
@@ -153,7 +161,8 @@ def workload_spec(name):
 
 DQ_KINDS = ("dq_mx_row", "dq_mx_col", "dq_tensor")
 QS_KINDS = ("qs_mx_row", "qs_mx_col", "qs_tensor")
-ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule", "bw", "nvfp4", "qs_mx_row")
+ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule", "bw", "nvfp4", "qs_mx_row", "mxlow")
+LOW_NAMES = {2: "e2m1", 3: "e2m3", 4: "e3m2"}
 
 
 def host_input(gen, shape):
@@ -340,6 +349,12 @@ def run_ours(args):
                 b["ld"] = ld
                 if op["kind"] == "mx_rule":
                     b["sat"] = torch.zeros(2, dtype=torch.int64, device=dev)
+            elif op["kind"] == "mxlow":
+                fp4 = op["elem"] == 2
+                b["lo"] = {"q_row": torch.empty((r, c // 2 if fp4 else c), dtype=torch.uint8, device=dev),
+                           "s_row": torch.empty((r, c // 32), dtype=torch.uint8, device=dev),
+                           "q_col": torch.empty((c, r // 2 if fp4 else r), dtype=torch.uint8, device=dev),
+                           "s_col": torch.empty((c, (r + 31) // 32), dtype=torch.uint8, device=dev)}
             elif op["kind"] == "nvfp4":
                 b["nv"] = {"q": torch.empty((r, c // 2), dtype=torch.uint8, device=dev),
                            "s": torch.empty((r, c // 16), dtype=torch.uint8, device=dev),
@@ -421,6 +436,12 @@ def run_ours(args):
                     o["s_row"].data_ptr(), o["q_col"].data_ptr(), o["s_col"].data_ptr(), b["ld"],
                     b["sat"].data_ptr(), stream))
                 b["launches"] = 1  # (plus the driver's memset of the two counters)
+            elif k == "mxlow":
+                o = b["lo"]
+                b["call"] = (lib.mx_quantize_fp4_fp6, (
+                    b["x"].data_ptr(), 0, r, c, op["elem"], 3, 0, o["q_row"].data_ptr(), o["s_row"].data_ptr(),
+                    o["q_col"].data_ptr(), o["s_col"].data_ptr(), None, stream))
+                b["launches"] = 1
             elif k == "nvfp4":
                 o = b["nv"]
                 b["call"] = (lib.fp8q_quantize_nvfp4, (
@@ -525,6 +546,8 @@ def run_ours(args):
                 return [b["bw"][k] for k in ("q", "s", "q_t", "s_t")]
             if op["kind"] == "nvfp4":
                 return [b["nv"][k] for k in ("q", "s", "scale")]
+            if op["kind"] == "mxlow":
+                return [b["lo"][k] for k in ("q_row", "s_row", "q_col", "s_col")]
             if op["kind"] in QS_KINDS:
                 return [b["st"]]
             return [b["y"]] if op["kind"] in DQ_KINDS else [b["q"]]
@@ -576,15 +599,16 @@ def run_ours(args):
         # average over the sampled launches of the step's first MXFP8 op
         avg_ms = sum(mx_ms) / len(mx_ms)
         achieved = mx_op["bytes"] / (avg_ms * 1e-3) / 1e9
+        fmt_name = "e4m3" if mx_op["fmt"] == E4M3 else "e5m2"
+        label = {"dq_mx_row": f"dequant_kernel<mx_row,{fmt_name},bf16>",
+                 "mx_rule": f"mx_kernel<bf16,{fmt_name},both,rule+counts>",
+                 "bw": f"blockwise_kernel<{fmt_name},1x128,both>",
+                 "nvfp4": "amax_kernel+nvfp4_kernel<bf16>",
+                 "qs_mx_row": f"qstats_lin_kernel<bf16,{fmt_name},mx_row>",
+                 "mxlow": f"mxlow_kernel<bf16,{LOW_NAMES.get(mx_op.get('elem'), '')},both>"}.get(
+                     mx_op["kind"], f"mx_kernel<bf16,{fmt_name},both>")
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                    "kernel": ({"dq_mx_row": "dequant_kernel<mx_row,%s,bf16>",
-                                "mx_rule": "mx_kernel<bf16,%s,both,rule+counts>",
-                                "bw": "blockwise_kernel<%s,1x128,both>",
-                                "nvfp4": "amax_kernel+nvfp4_kernel<bf16> (%s block scales)",
-                                "qs_mx_row": "qstats_lin_kernel<bf16,%s,mx_row>"}.get(mx_op["kind"],
-                                                                                     "mx_kernel<bf16,%s,both>")
-                               % ("e4m3" if mx_op["fmt"] == E4M3 else "e5m2")),
+                    "frac": round(achieved / peak, 4), "peak_source": peak_src, "kernel": label,
                     "algorithmic_bytes_per_launch": mx_op["bytes"], "avg_launch_us": round(avg_ms * 1e3, 3),
                     "launches_timed": len(mx_ms),
                     "traffic": kernel_traffic(args.workload)}
@@ -634,6 +658,9 @@ def oracle_sample_step(workload, sample_rows, inputs, states):
         elif k == "mx_rule":
             oracle.mx_quantize_rule(x, op["fmt"], 3, op["rule"])
             total += mx_bytes(r, c)
+        elif k == "mxlow":
+            oracle.mxlp_quantize(x, op["elem"], 3, 0)
+            total += (3 if op["elem"] == 2 else 4) * r * c + r * c // 16
         elif k == "nvfp4":
             oracle.nvfp4(x)
             total += 4 * r * c + r * c // 2 + r * c // 16
@@ -694,7 +721,7 @@ def oracle_inputs(workload, sample_rows):
 def sample_rows_for(workload):
     return {"activation": 256, "mx_8192": 128, "per_tensor_1024": 1024, "delayed_8192": 128, "linear_layer": 64,
             "moe": 32, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128, "nvfp4_8192": 128,
-            "qstats_8192": 128}[workload]
+            "qstats_8192": 128, "mxfp4_fp6_8192": 128}[workload]
 
 
 def cpu_baseline(workload, budget_s=10.0):

@@ -449,8 +449,10 @@ __global__ void __launch_bounds__(kQsThreads) qstats_col_kernel(QsParams p) {
   const int64_t ntr = (p.rows + 31) / 32, ntc = (p.cols + kQsTileCols - 1) / kQsTileCols;
   const int64_t ntiles = ntr * ntc;
   const bool qvec = (p.rows % 16) == 0 && ((uintptr_t)p.q & 15) == 0;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const int64_t tr = t / ntc, tc = t - tr * ntc;
+  // tile t = tr * ntc + tc, stepped by the grid size without a division per step
+  const int64_t G = gridDim.x, dr = G / ntc, dc = G - dr * ntc;
+  int64_t tr = (int64_t)blockIdx.x / ntc, tc = (int64_t)blockIdx.x - tr * ntc;
+  for (int64_t t = blockIdx.x; t < ntiles; t += G, tr += dr, tc += dc, (tc >= ntc ? (tc -= ntc, tr++) : 0)) {
     const int64_t c = tc * kQsTileCols + 2 * threadIdx.x;  // cols % 32 == 0: c + 1 < cols too
     if (c >= p.cols) continue;
     const int64_t r0 = tr * 32;
