@@ -242,8 +242,10 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the files whose text compiles into the MXFP8 kernel (internal.h holds only
+# host-side declarations of all launchers and is left out)
 MX_SOURCES = ("mxfp8_quantization_amax_gb300/csrc/mxfp8.cu", "mxfp8_quantization_amax_gb300/csrc/fp8q_device.cuh",
-              "mxfp8_quantization_amax_gb300/csrc/tma.cuh", "mxfp8_quantization_amax_gb300/csrc/internal.h")
+              "mxfp8_quantization_amax_gb300/csrc/tma.cuh")
 
 
 def sources_sha(paths=MX_SOURCES):
@@ -256,20 +258,24 @@ def sources_sha(paths=MX_SOURCES):
 
 
 def kernel_traffic(workload):
-    """DRAM bytes per launch of the MXFP8 kernel from the committed ncu
-    summary (profiles/traffic.txt: one `key=value ...` line per workload),
-    or None if there is none or the kernel's sources changed since."""
+    """DRAM bytes per launch of the workload's first kernel from the
+    committed ncu summary (profiles/traffic.txt: one `key=value ...` line per
+    workload; `sources=a,b,...` names the files whose hash keys it, the
+    MXFP8 kernel's by default), or None if there is none or those sources
+    changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
             lines = [ln.split() for ln in f if ln.startswith("workload=")]
-        sha = sources_sha()
+        for toks in lines:
+            d = dict(t.split("=", 1) for t in toks if "=" in t)
+            if d.get("workload") != workload:
+                continue
+            paths = tuple(d["sources"].split(",")) if "sources" in d else MX_SOURCES
+            if d.get("sha") == sources_sha(paths):
+                return int(d["bytes_per_launch"])
     except OSError:
         return None
-    for toks in lines:
-        d = dict(t.split("=", 1) for t in toks if "=" in t)
-        if d.get("workload") == workload and d.get("sha") == sha:
-            return int(d["bytes_per_launch"])
     return None
 
 
