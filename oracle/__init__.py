@@ -103,6 +103,7 @@ def _load():
         "orc_lp_encode": (c.c_uint, [c.c_int, c.c_double]),
         "orc_mxlp_block": (c.c_uint8, [P, c.c_int, c.c_int, c.c_int, P, c.POINTER(c.c_int64)]),
         "orc_mxlp_quantize": (None, [P, c.c_int, c.c_int64, c.c_int64, c.c_int, c.c_int, c.c_int, P, P, P, P, P]),
+        "orc_mma_scale_layout": (None, [P, c.c_int64, c.c_int64, c.c_int64, P]),
         "orc_qstats_per_tensor": (None, [P, c.c_int, c.c_int64, c.c_int64, P, c.c_int, c.c_int, P, P, P, P]),
         "orc_qstats_mx": (None, [P, c.c_int, c.c_int64, c.c_int64, P, c.c_int, c.c_int, c.c_int, P, P,
                                  c.c_int64, P, P]),
@@ -478,6 +479,21 @@ def mxlp_quantize(x: np.ndarray, fmt: int, direction: int = 3, rule: int = 0) ->
     _load().orc_mxlp_quantize(_ptr(x), _dtype_code(x), rows, cols, fmt, direction, rule, _ptr(out["q_row"]),
                               _ptr(out["s_row"]), _ptr(out["q_col"]), _ptr(out["s_col"]), _ptr(sat))
     out["sat"] = sat.tolist()
+    return out
+
+
+# --------------------------------------------------------------------------
+# Block-scale layout for block-scaled tensor-core MMA
+# --------------------------------------------------------------------------
+def mma_scale_layout(s: np.ndarray, scale_cols: int | None = None) -> np.ndarray:
+    """A [rows, s_ld] scale array (the first scale_cols columns used) in
+    the 128 x 4 block layout: a flat uint8 array of ceil(rows/128)*128 *
+    ceil(scale_cols/4)*4 bytes."""
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    rows, s_ld = s.shape
+    sc = s_ld if scale_cols is None else scale_cols
+    out = np.zeros(((rows + 127) // 128 * 128) * ((sc + 3) // 4 * 4), dtype=np.uint8)
+    _load().orc_mma_scale_layout(_ptr(s), rows, sc, s_ld, _ptr(out))
     return out
 
 

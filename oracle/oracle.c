@@ -62,7 +62,9 @@
  *     the round-up rule and its exponent as e_max under the OCP rule; a
  *     non-finite block gets scale 0xFF and +0 codes (the formats have no
  *     NaN); E2M1 codes are stored two per byte (even element low), FP6
- *     codes one per byte (bits 0-5).
+ *     codes one per byte (bits 0-5);
+ *   - the block-scale layout for tensor-core MMA is NVIDIA's public
+ *     128 x 4 block layout (the pages give none): parity unpinned.
  * Those readings are pinned only by their own definition ("parity unpinned"
  * by the pages); everything else is pinned by page values, closed forms and
  * library routines in tests/test_oracle_pins.py.
@@ -968,4 +970,28 @@ void orc_mxlp_quantize(const void* x, int dt, int64_t rows, int64_t cols, int fm
                 sat[1] += s1;
                 for (int i = 0; i < k; i++) lp_put(q_col + c * clen, fmt, 32 * b + i, qb[i]);
             }
+}
+
+/* ------------------------------------------------------------------ */
+/* Block-scale layout for block-scaled tensor-core MMA.  The pages give */
+/* none ("Blackwell GPU MXFP8 预训练最佳实践" 3.2 only says Blackwell's  */
+/* tensor cores take the MX types natively); this follows NVIDIA's      */
+/* public description of the scale-factor layout for block-scaled GEMM  */
+/* operands: the scale array (rows x scale_cols, e.g. the rowwise MX    */
+/* scales [rows][cols / 32]) is padded to multiples of 128 rows and 4   */
+/* columns and cut into 128 x 4 blocks of 512 bytes, stored block row   */
+/* by block row; inside a block, element (r, c) sits at byte            */
+/* (r % 32) * 16 + (r / 32) * 4 + c.  Padding bytes are 0.  Parity      */
+/* unpinned by the pages.                                                */
+/* ------------------------------------------------------------------ */
+void orc_mma_scale_layout(const uint8_t* s, int64_t rows, int64_t scale_cols, int64_t s_ld, uint8_t* out)
+{
+    int64_t R = (rows + 127) / 128 * 128, C = (scale_cols + 3) / 4 * 4;
+    for (int64_t r = 0; r < R; r++)
+        for (int64_t c = 0; c < C; c++) {
+            int64_t block = (r / 128) * (C / 4) + c / 4;
+            int64_t rr = r % 128, cc = c % 4;
+            int64_t off = block * 512 + (rr % 32) * 16 + (rr / 32) * 4 + cc;
+            out[off] = (r < rows && c < scale_cols) ? s[r * s_ld + c] : 0;
+        }
 }

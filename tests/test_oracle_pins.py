@@ -1102,3 +1102,31 @@ def test_mxlp_rule_boundaries(name):
             byte, q, sat = oracle.mxlp_block(v, fmt, rule)
             assert byte - 127 == X and sat == 0
             assert oracle.lp_value(fmt, int(q[4])) == destmax
+
+
+# --------------------------------------------------------------------------
+# Block-scale layout for tensor-core MMA (not on the pages: NVIDIA's public
+# 128 x 4 block layout; parity unpinned by the pages)
+# --------------------------------------------------------------------------
+def _mma_layout_by_reshape(s, scale_cols):
+    """The same layout described another way: pad to 128 x 4 blocks; in a
+    block, 16-byte row j holds the four scales of rows j, j + 32, j + 64,
+    j + 96 in that order; blocks follow each other along a block row."""
+    rows = s.shape[0]
+    R, C = -(-rows // 128) * 128, -(-scale_cols // 4) * 4
+    pad = np.zeros((R, C), np.uint8)
+    pad[:rows, :scale_cols] = s[:, :scale_cols]
+    blocks = pad.reshape(R // 128, 128, C // 4, 4).transpose(0, 2, 1, 3)     # [br][bc][128][4]
+    inner = blocks.reshape(R // 128, C // 4, 4, 32, 4).transpose(0, 1, 3, 2, 4)  # [br][bc][j][r//32][c]
+    return inner.reshape(-1)
+
+
+@pytest.mark.parametrize("rows,scale_cols,s_ld", [(128, 4, 4), (300, 7, 7), (1, 1, 3), (257, 256, 260)])
+def test_mma_scale_layout(rows, scale_cols, s_ld):
+    rng = np.random.default_rng(81)
+    s = rng.integers(1, 256, size=(rows, s_ld), dtype=np.uint64).astype(np.uint8)
+    got = oracle.mma_scale_layout(s, scale_cols)
+    np.testing.assert_array_equal(got, _mma_layout_by_reshape(s, scale_cols))
+    # every real scale appears once, padding is zero
+    assert np.count_nonzero(got) == rows * scale_cols
+    assert sorted(got[got != 0].tolist()) == sorted(s[:, :scale_cols].reshape(-1).tolist())
