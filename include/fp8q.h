@@ -386,6 +386,23 @@ FP8Q_API fp8q_status fp8q_quantize_nvfp4(const void* x, int32_t dt, int64_t rows
                                          uint8_t* s, float* amax_out, float* scale_out, void* stream);
 
 /*
+ * Block scales rearranged for block-scaled tensor-core MMA.  The pages give
+ * no layout ("Blackwell GPU MXFP8 预训练最佳实践" 3.2 says only that the
+ * tensor cores take the MX types natively); this is NVIDIA's public one.
+ * The rows x scale_cols scale array is padded to multiples of 128 rows and
+ * 4 columns and cut into 128 x 4 blocks of 512 bytes, stored block row by
+ * block row; inside a block, scale (r, c) is byte (r % 32) * 16 + (r / 32)
+ * * 4 + c.  Padding bytes are 0.
+ *   s     device uint8 [rows][s_ld], the first scale_cols bytes of each row
+ *         used (e.g. s_row [rows][cols / 32], s_col [cols][s_col_ld] with
+ *         scale_cols = its block count, NVFP4 s [rows][cols / 16])
+ *   out   device uint8 [ceil(rows / 128) * 128 * ceil(scale_cols / 4) * 4],
+ *         4-byte aligned, fully written
+ */
+FP8Q_API fp8q_status mx_scales_to_mma_layout(const uint8_t* s, int64_t rows, int64_t scale_cols, int64_t s_ld,
+                                             uint8_t* out, void* stream);
+
+/*
  * Dequantization.  ("HiFloat8：高性能训练之路" 1.1-1.2: a quantized tensor is
  * de-scaled by scale_inv = 1 / Scale; "Blackwell GPU MXFP8 预训练最佳实践"
  * 4.1 and 4.3: an MX element stands for value * 2^X, X = byte - 127, and

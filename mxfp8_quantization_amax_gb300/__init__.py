@@ -29,7 +29,7 @@ __all__ = [
     "fp8q_scale_from_amax", "debug_stall_mx_producer", "fp8q_dequantize_per_tensor", "mxfp8_dequantize",
     "RULE_UP", "RULE_OCP", "BLOCK_1X128", "BLOCK_128X128", "fp8q_quantize_blockwise", "fp8q_quantize_nvfp4",
     "fp8q_qstats_workspace_bytes", "fp8q_qstats_per_tensor", "mxfp8_qstats", "qstats_dict",
-    "E2M1", "E2M3", "E3M2", "mx_quantize_fp4_fp6",
+    "E2M1", "E2M3", "E3M2", "mx_quantize_fp4_fp6", "mx_scales_to_mma_layout",
 ]
 
 E4M3 = 0
@@ -65,6 +65,7 @@ _SIGS = {
                                     _c.c_int64, _c.c_int32, _P, _P]),
     "mx_quantize_fp4_fp6": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32,
                                        _P, _P, _P, _P, _P, _P]),
+    "mx_scales_to_mma_layout": (_c.c_int, [_P, _c.c_int64, _c.c_int64, _c.c_int64, _P, _P]),
     "fp8q_qstats_workspace_bytes": (_c.c_size_t, []),
     "fp8q_qstats_per_tensor": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32,
                                           _P, _P, _P, _P, _c.c_size_t, _P]),
@@ -495,6 +496,24 @@ def mx_quantize_fp4_fp6(x: torch.Tensor, elem: int = E2M1, direction: int = BOTH
     _check(lib().mx_quantize_fp4_fp6(_ptr(x), _dt(x), rows, cols, elem, direction, rule, _ptr(q_row), _ptr(s_row),
                                      _ptr(q_col), _ptr(s_col), _ptr(sat), _stream()), "mx_quantize_fp4_fp6")
     return out
+
+
+# ---------------------------------------------------------------------------
+# block scales for tensor-core MMA
+# ---------------------------------------------------------------------------
+def mx_scales_to_mma_layout(s: torch.Tensor, scale_cols: int | None = None,
+                            out: torch.Tensor | None = None) -> torch.Tensor:
+    """A [rows, s_ld] uint8 scale array (first scale_cols columns) in the
+    128 x 4 block layout of block-scaled MMA: a flat uint8 tensor of
+    ceil(rows/128)*128 * ceil(scale_cols/4)*4 bytes, padding 0."""
+    if not s.is_cuda or s.dtype != torch.uint8 or s.dim() != 2 or not s.is_contiguous():
+        raise ValueError("s must be a contiguous 2-D uint8 CUDA tensor")
+    rows, s_ld = s.shape
+    sc = s_ld if scale_cols is None else scale_cols
+    n = ((rows + 127) // 128 * 128) * ((sc + 3) // 4 * 4)
+    y = torch.empty(n, dtype=torch.uint8, device=s.device) if out is None else out
+    _check(lib().mx_scales_to_mma_layout(_ptr(s), rows, sc, s_ld, _ptr(y), _stream()), "mx_scales_to_mma_layout")
+    return y
 
 
 # ---------------------------------------------------------------------------

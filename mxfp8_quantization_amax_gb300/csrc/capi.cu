@@ -94,6 +94,10 @@ fp8q_status launch_mxlow(const void* x, int dt, int64_t rows, int64_t cols, int 
                          uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, unsigned long long* sat,
                          cudaStream_t stream);
 
+// Block scales for tensor-core MMA (mmascale.cu).
+fp8q_status launch_mma_scale(const uint8_t* s, int64_t rows, int64_t scale_cols, int64_t s_ld, uint8_t* out,
+                             cudaStream_t stream);
+
 // Quantization statistics (qstats.cu).
 size_t qstats_workspace_bytes();
 fp8q_status launch_qstats(int kind, const void* x, int dt, const uint8_t* q, const uint8_t* s, const float* scale_inv,
@@ -489,6 +493,19 @@ fp8q_status mx_quantize_fp4_fp6(const void* x, int32_t dt, int64_t rows, int64_t
   if (!n) return FP8Q_OK;
   return launch_mxlow(x, dt, rows, cols, elem, dir, scale_rule == FP8Q_MX_RULE_UP ? 1 : 0, q_row, s_row, q_col, s_col,
                       sat_count, st);
+}
+
+fp8q_status mx_scales_to_mma_layout(const uint8_t* s, int64_t rows, int64_t scale_cols, int64_t s_ld, uint8_t* out,
+                                    void* stream) {
+  g_err[0] = 0;
+  if (rows < 0 || scale_cols < 0) return fail(FP8Q_ERR_INVALID_ARG, "rows and scale_cols must be >= 0");
+  if (s_ld < scale_cols) return fail(FP8Q_ERR_INVALID_ARG, "s_ld must be >= scale_cols");
+  if (scale_cols > 0 && rows > (INT64_C(1) << 40) / (scale_cols + 3))
+    return fail(FP8Q_ERR_INVALID_ARG, "rows * scale_cols too large");
+  if (rows * scale_cols == 0) return FP8Q_OK;
+  if (!s || !out) return fail(FP8Q_ERR_INVALID_ARG, "s and out must not be NULL");
+  if (!aligned(out, 4)) return fail(FP8Q_ERR_INVALID_ARG, "out must be 4-byte aligned");
+  return launch_mma_scale(s, rows, scale_cols, s_ld, out, (cudaStream_t)stream);
 }
 
 fp8q_status fp8q_qstats_per_tensor(const void* x, int32_t dt, int64_t rows, int64_t cols,

@@ -200,3 +200,12 @@ def test_fp4_fp6_arguments_rejected_on_host(lib):
     assert lib.mx_quantize_fp4_fp6(a, 0, 4, 64, 4, 2, 0, a, a, None, a, None, None) == 1
     assert lib.mx_quantize_fp4_fp6(a, 0, 4, 64, 4, 1, 0, a + 2, a, None, None, None, None) == 1
     assert lib.mx_quantize_fp4_fp6(a, 0, 4, 64, 4, 1, 0, a, a, None, None, a + 4, None) == 1
+
+
+def test_mma_scale_layout_arguments_rejected_on_host(lib):
+    buf = ctypes.create_string_buffer(64)
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert lib.mx_scales_to_mma_layout(a, 4, 8, 4, a, None) == 1       # s_ld < scale_cols
+    assert lib.mx_scales_to_mma_layout(None, 4, 8, 8, a, None) == 1    # no input
+    assert lib.mx_scales_to_mma_layout(a, 4, 8, 8, a + 1, None) == 1   # misaligned output
+    assert lib.mx_scales_to_mma_layout(None, 0, 8, 8, None, None) == 0  # empty: nothing to do
