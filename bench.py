@@ -61,7 +61,7 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="activation",
                    choices=["activation", "mx_8192", "per_tensor_1024", "delayed_8192", "linear_layer", "moe",
                             "dequant_8192", "mx_rules_4096", "blockwise_8192", "nvfp4_8192",
-                            "qstats_8192", "mxfp4_fp6_8192"])
+                            "qstats_8192", "mxfp4_fp6_8192", "mma_scales_8192"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
@@ -132,6 +132,13 @@ def workload_spec(name):
                 "gen": ("c2", 0)}]
         return {"workload": "nvfp4_8192x8192_bf16", "rows": r, "cols": c,
                 "ops": ["nvfp4: tensor amax, then E2M1 codes and E4M3 scales per 16"]}, ops
+    if name == "mma_scales_8192":
+        r = c = 8192
+        nb = r * (c // 32)  # scale bytes of one MX copy; 8192 is a multiple of 128 rows and 4 columns
+        ops = [{"kind": "mmascale", "copy": "s_row", "shape": (r, c), "fmt": E4M3, "bytes": 2 * nb, "gen": ("c2", 0)},
+               {"kind": "mmascale", "copy": "s_col", "shape": (r, c), "fmt": E4M3, "bytes": 2 * nb, "gen": ("c2", 0)}]
+        return {"workload": "mma_scale_layout_8192x8192", "rows": r, "cols": c,
+                "ops": ["rowwise mx scales [8192][256] -> 128x4 blocks", "columnwise mx scales [8192][256] -> 128x4 blocks"]}, ops
     if name == "mxfp4_fp6_8192":
         r = c = 8192
         ops = [{"kind": "mxlow", "elem": 2, "shape": (r, c), "fmt": E4M3, "bytes": 3 * r * c + r * c // 16,
@@ -161,7 +168,7 @@ def workload_spec(name):
 
 DQ_KINDS = ("dq_mx_row", "dq_mx_col", "dq_tensor")
 QS_KINDS = ("qs_mx_row", "qs_mx_col", "qs_tensor")
-ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule", "bw", "nvfp4", "qs_mx_row", "mxlow")
+ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule", "bw", "nvfp4", "qs_mx_row", "mxlow", "mmascale")
 LOW_NAMES = {2: "e2m1", 3: "e2m3", 4: "e3m2"}
 
 
@@ -334,7 +341,7 @@ def run_ours(args):
     # enough buffer sets that a set is out of L2 when it comes round again
     l2 = 129 * 2 ** 20
     per_set = in_bytes + sum(op["bytes"] - 2 * int(np.prod(op["shape"])) for op in ops)
-    nsets = max(1, min(8, -(-4 * l2 // per_set)))
+    nsets = max(1, min(64, -(-4 * l2 // per_set)))
     off_dev = None if offsets_host is None else torch.from_numpy(offsets_host).to(dev)
 
     sets = []
@@ -373,6 +380,15 @@ def run_ours(args):
                            "q_t": torch.empty((c, r), dtype=torch.uint8, device=dev),
                            "s_t": torch.empty((c, tr) if op["block"] == 1 else (tc, tr), dtype=torch.float32,
                                               device=dev)}
+            elif op["kind"] == "mmascale":
+                # the scales to rearrange, made by the library's MX quantizer before timing
+                qr = fq.mxfp8_quantize(x, op["fmt"], 3)
+                b["in"] = [qr[op["copy"]]]
+                del qr
+                sr, sc = b["in"][0].shape
+                b["y"] = torch.empty(((sr + 127) // 128 * 128) * ((sc + 3) // 4 * 4), dtype=torch.uint8, device=dev)
+                b["x"] = None
+                del x
             elif op["kind"] in QS_KINDS:
                 # the copy to measure, made by the library's own quantizers
                 # before timing; x stays as the reference
@@ -465,6 +481,10 @@ def run_ours(args):
                     b["in"][0].data_ptr(), r, c, None, 1, op["fmt"], b["in"][1].data_ptr(), 0, b["y"].data_ptr(),
                     stream))
                 b["launches"] = 1
+            elif k == "mmascale":
+                sr, sc = b["in"][0].shape
+                b["call"] = (lib.mx_scales_to_mma_layout, (b["in"][0].data_ptr(), sr, sc, sc, b["y"].data_ptr(), stream))
+                b["launches"] = 1
             elif k == "qs_tensor":
                 b["call"] = (lib.fp8q_qstats_per_tensor, (
                     b["x"].data_ptr(), 0, r, c, None, 1, op["fmt"], b["in"][1].data_ptr(), b["in"][2].data_ptr(),
@@ -556,7 +576,7 @@ def run_ours(args):
                 return [b["lo"][k] for k in ("q_row", "s_row", "q_col", "s_col")]
             if op["kind"] in QS_KINDS:
                 return [b["st"]]
-            return [b["y"]] if op["kind"] in DQ_KINDS else [b["q"]]
+            return [b["y"]] if op["kind"] in DQ_KINDS or op["kind"] == "mmascale" else [b["q"]]
 
         ins_host = [[t.cpu().pin_memory() for t in sets[0][j]["in"]] for j in range(len(ops))]
         outs_host = [[torch.empty(t.numel() * t.element_size(), dtype=torch.uint8).pin_memory()
@@ -611,7 +631,8 @@ def run_ours(args):
                  "bw": f"blockwise_kernel<{fmt_name},1x128,both>",
                  "nvfp4": "amax_kernel+nvfp4_kernel<bf16>",
                  "qs_mx_row": f"qstats_lin_kernel<bf16,{fmt_name},mx_row>",
-                 "mxlow": f"mxlow_kernel<bf16,{LOW_NAMES.get(mx_op.get('elem'), '')},both>"}.get(
+                 "mxlow": f"mxlow_kernel<bf16,{LOW_NAMES.get(mx_op.get('elem'), '')},both>",
+                 "mmascale": "mma_scale_kernel (rowwise mx scales)"}.get(
                      mx_op["kind"], f"mx_kernel<bf16,{fmt_name},both>")
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "kernel": label,
@@ -657,13 +678,16 @@ def oracle_sample_step(workload, sample_rows, inputs, states):
     total = 0
     for op, x, st in zip(ops, inputs, states):
         k = op["kind"]
-        r, c = x["shape"] if k in DQ_KINDS or k in QS_KINDS else x.shape
+        r, c = x["shape"] if k in DQ_KINDS or k in QS_KINDS or k == "mmascale" else x.shape
         if k in ("mx", "mx_grouped"):
             oracle.mx_quantize(x, op["fmt"], 3)
             total += mx_bytes(r, c)
         elif k == "mx_rule":
             oracle.mx_quantize_rule(x, op["fmt"], 3, op["rule"])
             total += mx_bytes(r, c)
+        elif k == "mmascale":
+            oracle.mma_scale_layout(x["s"])
+            total += 2 * x["s"].size
         elif k == "mxlow":
             oracle.mxlp_quantize(x, op["elem"], 3, 0)
             total += (3 if op["elem"] == 2 else 4) * r * c + r * c // 16
@@ -712,6 +736,9 @@ def oracle_inputs(workload, sample_rows):
             m = oracle.mx_quantize(x, op["fmt"], 3)
             x = ({"q": m["q_row"], "s": m["s_row"], "shape": (rr, c)} if op["kind"] == "dq_mx_row"
                  else {"q": m["q_col"], "s": m["s_col"], "shape": (rr, c)})
+        elif op["kind"] == "mmascale":  # the scales to rearrange, made by the oracle before timing
+            m = oracle.mx_quantize(x, op["fmt"], 3)
+            x = {"s": m[op["copy"]], "shape": (rr, c)}
         elif op["kind"] == "qs_tensor":  # the copy to measure, made by the oracle before timing
             cs = oracle.current_scaling(x, op["fmt"])
             x = {"x": x, "q": cs["q"].reshape(rr, c), "scale_inv": cs["scale_inv"], "shape": (rr, c)}
@@ -727,7 +754,7 @@ def oracle_inputs(workload, sample_rows):
 def sample_rows_for(workload):
     return {"activation": 256, "mx_8192": 128, "per_tensor_1024": 1024, "delayed_8192": 128, "linear_layer": 64,
             "moe": 32, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128, "nvfp4_8192": 128,
-            "qstats_8192": 128, "mxfp4_fp6_8192": 128}[workload]
+            "qstats_8192": 128, "mxfp4_fp6_8192": 128, "mma_scales_8192": 1024}[workload]
 
 
 def cpu_baseline(workload, budget_s=10.0):
