@@ -167,8 +167,9 @@ struct Unit {
 };
 
 struct Tile {
-  int64_t r0;  // first row
-  int nr;      // rows of the block (1..32)
+  int64_t r0;  // first row of the window
+  int lo;      // window rows [lo, nr) are this CTA's rows
+  int nr;      // end of those rows (1..32)
   int64_t c0;
   int nc;
 };
@@ -195,6 +196,7 @@ __device__ __forceinline__ Unit unit_of(const MxParams& p, const int* blk, const
 __device__ __forceinline__ Tile block_of(const Unit& U, int j) {
   Tile t;
   t.r0 = U.r_first + 32LL * j;
+  t.lo = 0;
   t.nr = (int)min((int64_t)kTileRows, U.rg1 - t.r0);
   t.c0 = U.c0;
   t.nc = U.nc;
@@ -384,6 +386,7 @@ __device__ __forceinline__ void store_scales(const MxParams& p, int64_t c, int64
 __device__ __forceinline__ void flush_scales8(const MxParams& p, uint8_t* win, int from, int to, int64_t gbw,
                                               uint64_t v, const StorePolicy& sp) {
   if (gbw + to > p.s_col_ld) to = (int)(p.s_col_ld - gbw);
+  if (gbw + from < 0) from = (int)-gbw;  // window bytes before the column's first scale
   if (from >= to) return;
   const uint32_t o[8] = {(uint32_t)v, (uint32_t)(v >> 32), 0, 0, 0, 0, 0, 0};
   store_range8(win, o, from, to, sp.scale);
@@ -455,7 +458,7 @@ __device__ __forceinline__ uint32_t mx_fix(uint32_t w, uint32_t byte, uint32_t a
 template <int FMT, bool EXT>
 __device__ __forceinline__ uint32_t row_block_bf16(const MxParams& p, const Tile& t, const unsigned char* stage,
                                                    int r, int b, const StorePolicy& sp, uint32_t& nsat) {
-  if (r >= t.nr || 32 * b >= t.nc) return 0u;
+  if (r < t.lo || r >= t.nr || 32 * b >= t.nc) return 0u;
   const unsigned char* line = stage + (b >> 1) * kSubBytes + r * 128;
   const int c0 = (b & 1) * 4;
   uint32_t w[16];
@@ -507,7 +510,7 @@ __device__ __forceinline__ void store_row_scales(const MxParams& p, const Tile& 
   const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 8);
   const uint32_t v2 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 16);
   const uint32_t v3 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 24);
-  if (r >= t.nr) return;
+  if (r < t.lo || r >= t.nr) return;
   if (t.nc == kTileCols && ((uintptr_t)dst & 7u) == 0) {
     if (lane < 8) {
       const uint64_t lo = (v & 0xFFu) | ((v1 & 0xFFu) << 8) | ((v2 & 0xFFu) << 16) | ((v3 & 0xFFu) << 24);
@@ -517,7 +520,7 @@ __device__ __forceinline__ void store_row_scales(const MxParams& p, const Tile& 
     return;
   }
 #endif
-  if (r < t.nr) {  // one byte per block
+  if (r >= t.lo && r < t.nr) {  // one byte per block
     const int b = lane >> 3;
     if (32 * b < t.nc) st_scale8(dst + b, byte0, sp);
     if (32 * (b + 4) < t.nc) st_scale8(dst + b + 4, byte1, sp);
@@ -535,10 +538,10 @@ __device__ __forceinline__ void window32(const uint32_t (&a)[8], const uint32_t 
     c[8 + i] = b[i];
   }
   switch (off >> 2) {  // whole words; each case indexes registers statically
-#define FP8Q_WINDOW_CASE(Q)                                                           \
-  case Q:                                                                             \
-    _Pragma("unroll") for (int i = 0; i < 8; i++) o[i] =                              \
-        sh ? __funnelshift_r(c[Q + i], (Q + i + 1 < 16 ? c[Q + i + 1] : 0u), sh) : c[Q + i]; \
+#define FP8Q_WINDOW_CASE(Q)                                                              \
+  case Q:                                                                                \
+    _Pragma("unroll") for (int i = 0; i < 8; i++) o[i] =                                 \
+        __funnelshift_r(c[Q + i], (Q + i + 1 < 16 ? c[Q + i + 1] : 0u), sh); /* sh 0: c[Q+i] */ \
     break;
     FP8Q_WINDOW_CASE(0)
     FP8Q_WINDOW_CASE(1)
@@ -589,12 +592,14 @@ __device__ __forceinline__ void emit_col_block(uint8_t* run, int len, int j, int
   for (int i = 0; i < 8; i++) prev[i] = d[i];
 }
 
-// Columnwise: thread t owns columns 2t, 2t+1 (one 32-bit word per row).
-// Returns the two scale bytes (column 2t in bits 0-7).
+// Columnwise: thread t owns columns 2t, 2t+1 (one 32-bit word per row) of
+// the block in window rows [0, t.nr).  Writes the two columns' 32 codes to
+// d0 / d1 and returns the two scale bytes (column 2t in bits 0-7).
+// Saturated elements are counted over window rows [sat_lo, sat_hi).
 template <int FMT, bool EXT>
-__device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit& U, const Tile& t,
-                                                  const unsigned char* stage, int tid, const StorePolicy& sp, int j,
-                                                  uint32_t (&prev0)[8], uint32_t (&prev1)[8], uint32_t& nsat) {
+__device__ __forceinline__ uint32_t col_codes_bf16(const MxParams& p, const Tile& t, const unsigned char* stage,
+                                                   int tid, uint32_t (&d0)[8], uint32_t (&d1)[8], uint32_t& nsat,
+                                                   int sat_lo, int sat_hi) {
   const unsigned char* seg = stage + (tid >> 5) * kSubBytes + 4 * (tid & 3);
   const int c = (tid & 31) >> 2;  // 16-byte chunk of the word within the 128-byte line
   uint32_t off[8];
@@ -623,11 +628,11 @@ __device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit&
       const bool s0 = block_saturates<FMT>(a0, b0, m0), s1 = block_saturates<FMT>(a1, b1, m1);
       if (s0 || s1) {
 #pragma unroll
-        for (int r = 0; r < kTileRows; r++) nsat += sat_pair<FMT>(w[r], s0 ? m0 : 0.0f, s1 ? m1 : 0.0f);
+        for (int r = 0; r < kTileRows; r++)
+          if (r >= sat_lo && r < sat_hi) nsat += sat_pair<FMT>(w[r], s0 ? m0 : 0.0f, s1 ? m1 : 0.0f);
       }
     }
   }
-  uint32_t d0[8], d1[8];
   if (b0 == 0xFFu || a0 == 0u || b1 == 0xFFu || a1 == 0u) {
 #pragma unroll
     for (int k = 0; k < 8; k++) {
@@ -647,11 +652,22 @@ __device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit&
       d1[k] = cvt4<FMT>(h[0], h[1], h[2], h[3]);
     }
   }
+  return b0 | (b1 << 8);
+}
+
+// The unit-based kernel's column pass: codes of block j of unit U, written
+// into the unit's run of the transposed output.
+template <int FMT, bool EXT>
+__device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit& U, const Tile& t,
+                                                  const unsigned char* stage, int tid, const StorePolicy& sp, int j,
+                                                  uint32_t (&prev0)[8], uint32_t (&prev1)[8], uint32_t& nsat) {
+  uint32_t d0[8], d1[8];
+  const uint32_t b = col_codes_bf16<FMT, EXT>(p, t, stage, tid, d0, d1, nsat, 0, kTileRows);
   const int64_t col = t.c0 + 2 * tid;
   const int len = (int)min((int64_t)(32 * U.nblk), U.rg1 - U.r_first);
   emit_col_block(p.q_col + col * p.rows + U.r_first, len, j, U.nblk, d0, prev0, sp);
   emit_col_block(p.q_col + (col + 1) * p.rows + U.r_first, len, j, U.nblk, d1, prev1, sp);
-  return b0 | (b1 << 8);
+  return b;
 }
 
 // EXT: the scale rule and saturation counting of mxfp8_quantize_rule; the
@@ -765,6 +781,266 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(c
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (gave_up || abort_flag) return;
+  }
+  if constexpr (EXT) {
+    if (p.sat != nullptr) {  // one atomic per warp and direction
+      const uint32_t a = __reduce_add_sync(0xFFFFFFFFu, nsat_r), c = __reduce_add_sync(0xFFFFFFFFu, nsat_c);
+      if (lane == 0 && a) atomicAdd(p.sat, (unsigned long long)a);
+      if (lane == 0 && c) atomicAdd(p.sat + 1, (unsigned long long)c);
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// BF16, grouped, rows % 32 == 0: bands of aligned rows
+// ---------------------------------------------------------------------------
+// Units are bands of kBandRows aligned rows in one 256-column strip, dealt
+// out band-major.  A unit walks, in row order, the column blocks that
+// overlap its rows; each block is loaded as one 32-row window from its own
+// first row (the window of a group's short last block also holds rows of
+// the next group, which it leaves alone).  A block that straddles the
+// band's first row is loaded by both bands: the earlier band owns its scale
+// and its rows above the boundary, the later one takes only its rows below.
+//
+// The transposed codes of one column form a byte stream over the band's
+// rows.  With rows % 32 == 0 and a 32-byte aligned q_col, each column's
+// stream starts on a 32-byte boundary and every column is at the same phase
+// `pos` (the structure of the blocks does not depend on the column), so
+// every q_col store is one whole aligned sector and no sector is written by
+// two CTAs.  Blocks are 32 rows except at a group's end, so inside a group
+// the phase stays put and a sector is the previous block's last pos codes
+// followed by this block's first 32 - pos.
+
+#ifndef FP8Q_MX_BAND_SECTORS  // 32-row sectors per band
+#define FP8Q_MX_BAND_SECTORS 32
+#endif
+constexpr int64_t kBandRows = 32 * FP8Q_MX_BAND_SECTORS;
+
+struct BandBlk {
+  int64_t s;   // first row of the block, and of its window
+  int64_t e;   // end of the block's rows (e - s in 1..32)
+  int64_t gb;  // s_col index of the block; -1: rows in no group
+};
+
+// The group whose rows a unit's walk is in: index and clamped bounds.  The
+// walk moves forward, so the bounds are looked up again (binary search)
+// only when it leaves them.
+struct GroupCursor {
+  int g = 0;
+  int64_t o = 0, o1 = -1;  // empty until the first lookup
+};
+
+// The column block holding row `cur`.  Rows outside every group (offsets
+// that do not cover [0, rows)) form gap blocks that end at the next 32-row
+// boundary: their rowwise copy is produced, their transposed codes are 0 and
+// they have no scale.  The walk advances by at least one row per block and
+// stays in [0, rows) for any offsets.
+__device__ __forceinline__ BandBlk band_block(const MxParams& p, const int* blk, GroupCursor& gc, int64_t cur) {
+  if (!(gc.o <= cur && cur < gc.o1)) {
+    gc.g = group_of_row(p.off, p.G, cur);
+    gc.o = grp_row(p, gc.g);
+    gc.o1 = grp_row(p, gc.g + 1);
+  }
+  BandBlk b;
+  if (gc.o <= cur && cur < gc.o1) {
+    const int64_t k = (cur - gc.o) >> 5;
+    b.s = gc.o + 32 * k;
+    b.e = min(b.s + 32, gc.o1);
+    b.gb = (int64_t)blk[gc.g] + k;
+  } else {
+    b.s = cur;
+    b.e = min((cur & ~(int64_t)31) + 32, p.rows);
+    b.gb = -1;
+  }
+  return b;
+}
+
+// Appends `len` codes, bytes [skip, skip + len) of d, to a column's stream
+// whose pending codes are the last `pos` bytes of prev; a completed sector
+// is stored at dst.  pos, skip and len are the same for every thread of the
+// CTA, so each branch is uniform.
+__device__ __forceinline__ void stream_append(uint8_t* dst, uint32_t (&prev)[8], const uint32_t (&din)[8], int pos,
+                                              int skip, int len, const StorePolicy& sp) {
+  const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  uint32_t d[8];
+  if (skip) {
+    window32(din, z, skip, d);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; i++) d[i] = din[i];
+  }
+  if (pos + len >= 32) {
+    if (pos) {
+      uint32_t o[8];
+      window32(prev, d, 32 - pos, o);
+      st_data32(dst, o, sp);
+    } else {
+      st_data32(dst, d, sp);
+    }
+  }
+  if (len == 32) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) prev[i] = d[i];
+  } else {
+    uint32_t o[8];
+    window32(prev, d, len, o);  // ends with the pending codes
+#pragma unroll
+    for (int i = 0; i < 8; i++) prev[i] = o[i];
+  }
+}
+
+template <int FMT, int DIR, bool EXT>
+__global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_band_kernel(const __grid_constant__ CUtensorMap tmap, MxParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t full[kStages], empty[kStages];
+  __shared__ volatile int abort_flag;
+  unsigned char* stages = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  int* blk = (int*)(stages + kStages * kStageBytes);
+  int* sup = blk + (p.G + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers / 32);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (tid == kConsumers) prefetch_tensormap(&tmap);
+  pdl_wait();
+  build_prefix<kTmaThreads>(p, blk, sup);
+  const int64_t bands = (p.rows + kBandRows - 1) / kBandRows;
+  const int64_t units = bands * p.strips;
+  const uint64_t budget = g_wait_budget_ns;
+
+  if (warp == kConsumers / 32) {
+    // ---------------- producer ----------------
+    if (lane != 0) return;
+    int64_t k = 0;
+    const bool stall = *(volatile unsigned*)&g_mx_stall_producer != 0;
+    bool stop = false;
+    for (int64_t u = blockIdx.x; u < units && !abort_flag && !stall && !stop; u += gridDim.x) {
+      const int64_t band = u / p.strips;
+      const int c0 = (int)((u - band * p.strips) * kTileCols);
+      const int64_t A = band * kBandRows, B = min(A + kBandRows, p.rows);
+      GroupCursor gc;
+      for (int64_t cur = A; cur < B; ++k) {
+        const BandBlk bb = band_block(p, blk, gc, cur);
+        const int s = (int)(k % kStages);
+        const uint32_t round = (uint32_t)(k / kStages);
+        if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, budget)) {
+          atomicOr(&g_mx_error, 1u);
+          abort_flag = 1;
+          stop = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        unsigned char* dst = stages + s * kStageBytes;
+#pragma unroll
+        for (int q = 0; q < kTileCols / kSubCols; q++)
+          tma_load_2d(dst + q * kSubBytes, &tmap, c0 + q * kSubCols, (int)bb.s, &full[s]);
+        cur = bb.e;
+      }
+    }
+    pdl_launch_dependents();  // all loads issued: the next kernel may launch
+    // every issued copy lands before the CTA can exit (fixed 2 s bound)
+    const int64_t first = k > kStages ? k - kStages : 0;
+    for (int64_t j = first; j < k; j++)
+      mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1), 2000000000ull);
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const StorePolicy sp = make_policy();
+  uint32_t nsat_r = 0, nsat_c = 0;  // saturated elements (counted when p.sat is set)
+  int64_t k = 0;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int64_t band = u / p.strips;
+    const int64_t c0 = (u - band * p.strips) * kTileCols;
+    const int nc = (int)min((int64_t)kTileCols, p.cols - c0);
+    const int64_t A = band * kBandRows, B = min(A + kBandRows, p.rows);
+    const int64_t col = c0 + 2 * tid;
+    uint8_t* qc0 = p.q_col + col * p.rows;
+    uint8_t* qc1 = qc0 + p.rows;
+    uint64_t sc0 = 0, sc1 = 0;   // scale bytes of this thread's two columns, gathered per 8-byte window
+    uint32_t prev0[8], prev1[8];  // the columns' pending codes (the last `pos` bytes)
+    int pos = 0;                  // stream phase: pending codes
+    int64_t sec = A;              // first row of the next sector to store
+    int nown = 0;                 // blocks whose scale this unit has produced
+    bool gave_up = false;
+    GroupCursor gc;
+    for (int64_t cur = A; cur < B; ++k) {
+      const BandBlk bb = band_block(p, blk, gc, cur);
+      const int s = (int)(k % kStages);
+      const uint32_t round = (uint32_t)(k / kStages);
+      // every lane waits; the warp acts on one voted answer so it never splits
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], round & 1u, budget))) {
+        atomicOr(&g_mx_error, 1u);
+        abort_flag = 1;
+        gave_up = true;
+        break;
+      }
+      const int64_t end = min(bb.e, B);
+      Tile t;  // this unit's rows of the window
+      t.r0 = bb.s;
+      t.lo = (int)(cur - bb.s);
+      t.nr = (int)(end - bb.s);
+      t.c0 = c0;
+      t.nc = nc;
+      const unsigned char* stage = stages + s * kStageBytes;
+      if constexpr (DIR & MXFP8_ROW) {
+        const int r = 8 * warp + (lane & 7);
+        const uint32_t y0 = row_block_bf16<FMT, EXT>(p, t, stage, r, lane >> 3, sp, nsat_r);
+        const uint32_t y1 = row_block_bf16<FMT, EXT>(p, t, stage, r, 4 + (lane >> 3), sp, nsat_r);
+        store_row_scales(p, t, warp, lane, y0, y1, sp);
+      }
+      if constexpr (DIR & MXFP8_COL) {
+        if (2 * tid < nc) {
+          Tile tb = t;  // the whole block: its amax takes every one of its rows
+          tb.lo = 0;
+          tb.nr = (int)(bb.e - bb.s);
+          uint32_t d0[8], d1[8];
+          const uint32_t b = col_codes_bf16<FMT, EXT>(p, tb, stage, tid, d0, d1, nsat_c, t.lo, bb.gb < 0 ? t.lo : t.nr);
+          if (bb.gb < 0) {
+#pragma unroll
+            for (int i = 0; i < 8; i++) d0[i] = d1[i] = 0u;
+          }
+          const int len = t.nr - t.lo;
+          stream_append(qc0 + sec, prev0, d0, pos, t.lo, len, sp);
+          stream_append(qc1 + sec, prev1, d1, pos, t.lo, len, sp);
+          if (pos + len >= 32) sec += 32;
+          pos = (pos + len) & 31;
+          const bool last = bb.e >= B;
+          if (bb.gb >= 0 && bb.s >= A) {
+            // scale bytes go to s_col[c][gb]; gathered in the 8-byte aligned
+            // window of the destination, stored when the window is complete
+            // or the unit ends
+            uint8_t* d0p = p.s_col + col * p.s_col_ld + bb.gb;
+            uint8_t* d1p = d0p + p.s_col_ld;
+            const int q0 = (int)((uintptr_t)d0p & 7u), q1 = (int)((uintptr_t)d1p & 7u);
+            sc0 |= (uint64_t)(b & 0xFFu) << (8 * q0);
+            sc1 |= (uint64_t)(b >> 8) << (8 * q1);
+            if (q0 == 7 || last) {
+              const int from = nown < q0 ? q0 - nown : 0;  // window bytes before the unit's first scale
+              flush_scales8(p, d0p - q0, from, q0 + 1, bb.gb - q0, sc0, sp);
+              sc0 = 0;
+            }
+            if (q1 == 7 || last) {
+              const int from = nown < q1 ? q1 - nown : 0;
+              flush_scales8(p, d1p - q1, from, q1 + 1, bb.gb - q1, sc1, sp);
+              sc1 = 0;
+            }
+            ++nown;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      cur = bb.e;
     }
     if (gave_up || abort_flag) return;
   }
@@ -931,7 +1207,7 @@ static fp8q_status ctas_per_sm(K kernel, int threads, size_t smem, size_t* attr,
   return FP8Q_OK;
 }
 
-template <int FMT, int DIR, bool EXT>
+template <int FMT, int DIR, bool EXT, bool BAND>
 static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
   auto enc = encode_fn();
   if (!enc) return fail(FP8Q_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -945,20 +1221,23 @@ static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FP8Q_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   MxParams q = p;
-  q.super = p.off != nullptr ? FP8Q_MX_SUPER_GROUPED : FP8Q_MX_SUPER;
+  q.super = BAND ? 1 : (p.off != nullptr ? FP8Q_MX_SUPER_GROUPED : FP8Q_MX_SUPER);
   const size_t smem = 1024 + (size_t)kStages * kStageBytes + 2 * sizeof(int) * (p.G + 1);
+  auto kernel = BAND ? mx_band_kernel<FMT, DIR, EXT> : mx_tma_kernel<FMT, DIR, EXT>;
   static size_t attr = 0;
   static int per_sm_cache = 0;
   static std::mutex mu;
   int per_sm = 0;
-  fp8q_status st = ctas_per_sm(mx_tma_kernel<FMT, DIR, EXT>, kTmaThreads, smem, &attr, &per_sm_cache, &mu, &per_sm);
+  fp8q_status st = ctas_per_sm(kernel, kTmaThreads, smem, &attr, &per_sm_cache, &mu, &per_sm);
   if (st != FP8Q_OK) return st;
-  // units over any valid offsets: blocks per group rounded up to `super`
-  const int64_t max_units = ((p.rows + 31) / 32 / q.super + 1 + p.G) * p.strips;
+  // units: bands x strips, or (over any valid offsets) blocks per group
+  // rounded up to `super`, x strips
+  const int64_t max_units = BAND ? (p.rows + kBandRows - 1) / kBandRows * p.strips
+                                 : ((p.rows + 31) / 32 / q.super + 1 + p.G) * p.strips;
   int64_t grid = (int64_t)per_sm * sm_count();
   if (max_units < grid) grid = max_units;
   if (grid < 1) grid = 1;
-  const cudaError_t e = launch_kernel(mx_tma_kernel<FMT, DIR, EXT>, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, map, q);
+  const cudaError_t e = launch_kernel(kernel, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, map, q);
   if (e != cudaSuccess) return cuda_fail(e, "mxfp8 tma kernel launch");
   return check_launch("mxfp8 tma kernel");
 }
@@ -983,17 +1262,33 @@ static fp8q_status launch_f32(const MxParams& p, cudaStream_t s) {
   return check_launch("mxfp8 fp32 kernel");
 }
 
+#ifndef FP8Q_MX_BAND_UNGROUPED  // route ungrouped BF16 calls to the band kernel as well
+#define FP8Q_MX_BAND_UNGROUPED 0
+#endif
+
+template <int FMT, bool EXT, bool BAND>
+static fp8q_status launch_tma_dir(const MxParams& p, int dir, cudaStream_t s) {
+  if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW, EXT, BAND>(p, s);
+  if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL, EXT, BAND>(p, s);
+  return launch_tma<FMT, MXFP8_BOTH, EXT, BAND>(p, s);
+}
+
 template <int FMT>
 static fp8q_status launch_fmt(const MxParams& p, int dt, int dir, cudaStream_t s) {
   if (dt == kBF16) {
-    if (p.round_up == 0 || p.sat != nullptr) {
-      if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW, true>(p, s);
-      if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL, true>(p, s);
-      return launch_tma<FMT, MXFP8_BOTH, true>(p, s);
+    const bool ext = p.round_up == 0 || p.sat != nullptr;
+    if (dir == MXFP8_ROW && p.off != nullptr) {
+      // the rowwise copy does not depend on the groups
+      MxParams q = p;
+      q.off = nullptr;
+      q.G = 1;
+      return ext ? launch_tma_dir<FMT, true, false>(q, dir, s) : launch_tma_dir<FMT, false, false>(q, dir, s);
     }
-    if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW, false>(p, s);
-    if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL, false>(p, s);
-    return launch_tma<FMT, MXFP8_BOTH, false>(p, s);
+    // bands of aligned rows: every transposed store is a whole aligned sector
+    const bool band = (dir & MXFP8_COL) && p.rows % 32 == 0 && ((uintptr_t)p.q_col & 31u) == 0 &&
+                      (p.off != nullptr || FP8Q_MX_BAND_UNGROUPED);
+    if (band) return ext ? launch_tma_dir<FMT, true, true>(p, dir, s) : launch_tma_dir<FMT, false, true>(p, dir, s);
+    return ext ? launch_tma_dir<FMT, true, false>(p, dir, s) : launch_tma_dir<FMT, false, false>(p, dir, s);
   }
   if (dir == MXFP8_ROW) return launch_f32<FMT, MXFP8_ROW>(p, s);
   if (dir == MXFP8_COL) return launch_f32<FMT, MXFP8_COL>(p, s);

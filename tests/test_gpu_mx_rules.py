@@ -49,6 +49,16 @@ def test_grouped_ragged_rules(rule):
 
 @pytest.mark.parametrize("fmt", [0, 1])
 @pytest.mark.parametrize("rule", ["up", "ocp"])
+def test_grouped_band_rules(fmt, rule):
+    """rows % 32 == 0 (512-row bands): groups straddling and ending on band
+    edges; saturated elements of a block loaded by two bands count once."""
+    fq = require_cuda()
+    x = synth.config2(1600, 256, seed=16)
+    _check(fq, x, fmt, rule, offsets=[0, 0, 45, 46, 130, 500, 511, 512, 530, 1024, 1025, 1599, 1600])
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("rule", ["up", "ocp"])
 def test_fp32_input_rules(fmt, rule):
     fq = require_cuda()
     rng = np.random.default_rng(14)

@@ -158,6 +158,77 @@ def test_ragged_groups(fq, fmt):
     check_mx(fq, x, fmt, 2, offsets=offsets, s_col_ld=oracle.mx_col_blocks(rows, np.array(offsets)) + 5)
 
 
+BAND_OFFSETS = [0, 0, 1, 32, 65, 65, 98, 131, 163, 200, 201, 511, 512, 513, 600, 1023, 1024, 1025, 1056, 1100,
+                1536, 1537, 1599, 1600]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_ragged_groups_aligned_rows(fq, fmt):
+    """rows % 32 == 0 (the kernel that walks 512-row bands): empty, 1-row and
+    31/33-row groups, groups that straddle a band edge and groups that end
+    exactly on one, both directions and the columnwise copy alone with an
+    odd scale stride."""
+    rows, cols = 1600, 320
+    x = synth.student_t(rows, cols, 4.0, seed=23)
+    check_mx(fq, x, fmt, 3, offsets=BAND_OFFSETS)
+    T = oracle.mx_col_blocks(rows, np.array(BAND_OFFSETS))
+    check_mx(fq, x, fmt, 2, offsets=BAND_OFFSETS, s_col_ld=T + 5)
+
+
+def test_grouped_rowwise_only_ignores_groups(fq):
+    """The rowwise copy does not depend on the groups."""
+    x = synth.config2(1600, 256, seed=24)
+    got = check_mx(fq, x, oracle.E4M3, 1, offsets=BAND_OFFSETS)
+    ref = oracle.mx_quantize(x, oracle.E4M3, 1)
+    np.testing.assert_array_equal(got["q_row"], ref["q_row"])
+
+
+def test_one_group_covering_all_rows(fq):
+    """Explicit offsets [0, rows] give the ungrouped result."""
+    x = synth.config2(2048, 512, seed=25)
+    got = check_mx(fq, x, oracle.E5M2, 3, offsets=[0, 2048])
+    ref = oracle.mx_quantize(x, oracle.E5M2, 3)
+    np.testing.assert_array_equal(got["q_col"], ref["q_col"])
+
+
+def test_grouped_special_blocks(fq):
+    """Zero, -0, NaN, Inf and subnormal column blocks inside ragged groups,
+    including blocks that straddle a band edge and a group's short last block."""
+    rows, cols = 1056, 256
+    x = synth.student_t(rows, cols, 4.0, seed=26).copy()
+    offsets = [0, 500, 530, 1000, 1056]
+    x[500:530, 0] = 0                    # a whole 30-row group, zero in column 0
+    x[500:530, 1] = 0x8000               # ... and -0 in column 1
+    x[510, 2] = 0x7FC0                   # NaN in a short group
+    x[520, 3] = 0xFF80                   # -Inf
+    x[0:32, 4] = 0x0001                  # subnormal amax
+    x[490:522, 5] = 0                    # crosses a group boundary
+    x[507:515, 6] = 0x7F81               # NaN rows straddling the 512 band edge
+    x[1040, 7] = 0x7F80                  # +Inf in the last group's short block
+    x[996:1000, 8] = 0x43E8              # 464 > 448 at a group's end
+    for fmt in FMTS:
+        check_mx(fq, x, fmt, 3, offsets=offsets)
+
+
+def test_grouped_unaligned_transposed_output(fq):
+    """A q_col that is 16 but not 32-byte aligned takes the unit kernel."""
+    rows, cols = 1600, 256
+    x = synth.student_t(rows, cols, 4.0, seed=27)
+    T = oracle.mx_col_blocks(rows, np.array(BAND_OFFSETS))
+    raw = torch.full((cols * rows + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+    base = (32 - raw.data_ptr() % 32) % 32 + 16
+    q_col = raw[base:base + cols * rows].view(cols, rows)
+    assert q_col.data_ptr() % 32 == 16
+    out = {"q_col": q_col, "s_col": torch.empty((cols, T), dtype=torch.uint8, device="cuda")}
+    off = torch.tensor(BAND_OFFSETS, dtype=torch.int64, device="cuda")
+    r = fq.mxfp8_quantize(dev(x), oracle.E4M3, 2, group_offsets=off, s_col_ld=T, out=out)
+    ref = oracle.mx_quantize(x, oracle.E4M3, 2, offsets=np.array(BAND_OFFSETS))
+    np.testing.assert_array_equal(host(r["q_col"]), ref["q_col"])
+    np.testing.assert_array_equal(host(r["s_col"]), ref["s_col"][:, :T])
+    rawh = host(raw)
+    assert (rawh[:base] == 0xA5).all() and (rawh[base + cols * rows:] == 0xA5).all()
+
+
 def test_moe_groups_fp32(fq):
     x = synth.f32_tensor(517, 96, seed=17)
     check_mx(fq, x, oracle.E5M2, 3, offsets=[0, 17, 17, 300, 517])
@@ -176,41 +247,3 @@ def test_moe_routing_64_experts(fq):
 def test_activation_4096x4096_full(fq):
     """The MXFP8 workload: 4096x4096 BF16 activation, both directions, E4M3."""
     check_mx(fq, synth.config2(), oracle.E4M3, 3)
-
-
-def _sampled_check(fq, x, fmt, offsets=None, nsamp=3000, seed=0):
-    """Full-size run; the oracle recomputes randomly chosen blocks one by one."""
-    rows, cols = x.shape
-    got = run_mx(fq, x, fmt, 3, offsets)
-    rng = np.random.default_rng(seed)
-    xf = bf16_to_f32(x) if x.dtype == np.uint16 else x
-    for r, j in zip(rng.integers(0, rows, nsamp), rng.integers(0, cols // 32, nsamp)):
-        b, q = oracle.mx_block(xf[r, 32 * j:32 * j + 32], fmt)
-        assert got["s_row"][r, j] == b
-        np.testing.assert_array_equal(got["q_row"][r, 32 * j:32 * j + 32], q)
-    bounds = [(0, rows)] if offsets is None else [(offsets[g], offsets[g + 1]) for g in range(len(offsets) - 1)]
-    base = np.cumsum([0] + [(b1 - b0 + 31) // 32 for b0, b1 in bounds])
-    for c, g in zip(rng.integers(0, cols, nsamp), rng.integers(0, len(bounds), nsamp)):
-        b0, b1 = bounds[g]
-        if b1 == b0:
-            continue
-        blk = rng.integers(0, (b1 - b0 + 31) // 32)
-        r0 = b0 + 32 * blk
-        r1 = min(r0 + 32, b1)
-        b, q = oracle.mx_block(np.ascontiguousarray(xf[r0:r1, c]), fmt)
-        assert got["s_col"][c, base[g] + blk] == b
-        np.testing.assert_array_equal(got["q_col"][c, r0:r1], q)
-
-
-def test_linear_layer_tensors_full_size(fq):
-    """A 16384x4096, W 14336x4096 (E4M3) and E 16384x14336 (E5M2), both directions."""
-    t = synth.config4()
-    _sampled_check(fq, t["A"], oracle.E4M3, seed=1)
-    _sampled_check(fq, t["W"], oracle.E4M3, seed=2)
-    _sampled_check(fq, t["E"], oracle.E5M2, seed=3)
-
-
-def test_moe_full_size(fq):
-    """65536x7168 Student-t(4) over 64 experts with multinomial counts."""
-    x, offs = synth.config5()
-    _sampled_check(fq, x, oracle.E4M3, offsets=[int(v) for v in offs], seed=4)
