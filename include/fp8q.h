@@ -202,11 +202,14 @@ FP8Q_API fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t row
  *   - Arguments and results are those of fp8q_cast_per_tensor, minus the
  *     workspace; num_groups must be at most 256 (FP8Q_ERR_INVALID_ARG
  *     otherwise).
- *   - The first call on each device looks up the array's device address;
- *     make that first call before any stream capture.
- *   - All calls on a device share the array; each clears the part it uses
- *     at its start (one cudaMemsetAsync on `stream`).  Calls whose work
- *     may overlap on the GPU race on it: order them on one stream.
+ *   - The first call on each device looks up the array's device address
+ *     and keeps it; make that first call before any stream capture.  A
+ *     context reset (cudaDeviceReset) is not supported afterwards: the
+ *     array may be reloaded at another address.
+ *   - All calls on a device share the array.  A call checks its arguments
+ *     first (a rejected call touches nothing), then clears the part it
+ *     uses (one cudaMemsetAsync on `stream`).  Calls whose work may
+ *     overlap on the GPU race on it: order them on one stream.
  */
 FP8Q_API fp8q_status fp8q_cast_per_tensor_static_ws(const void* x, int32_t dt, int64_t rows, int64_t cols,
                                                     const int64_t* group_offsets, int32_t num_groups,
@@ -231,7 +234,9 @@ FP8Q_API fp8q_status fp8q_cast_per_tensor_static_ws(const void* x, int32_t dt, i
 typedef struct fp8q_delayed_state fp8q_delayed_state;
 
 /* Allocates the state on the current device (history_len 1..1024,
- * interval >= 1, margin 0..63). */
+ * interval >= 1, margin 0..63).  That device owns the state: reset and step
+ * must be called with it current (FP8Q_ERR_INVALID_ARG otherwise); get, set
+ * and destroy switch to it themselves and restore the caller's device. */
 FP8Q_API fp8q_status fp8q_delayed_create(int32_t history_len, int32_t interval, int32_t margin,
                                 int32_t fmt, fp8q_delayed_state** out);
 FP8Q_API fp8q_status fp8q_delayed_destroy(fp8q_delayed_state* st);
@@ -249,7 +254,7 @@ FP8Q_API fp8q_status fp8q_delayed_step(fp8q_delayed_state* st, const void* x, in
                               uint8_t* q, float* scale_used_out, float* scale_inv_out,
                               float* amax_out, unsigned long long* sat_count_out,
                               void* stream);
-/* Copies the state to the host (synchronizes the device): history_host
+/* Copies the state to the host (synchronizes the state's device): history_host
  * float[history_len] (ring order), head (next slot), count (filled entries),
  * step, nonfinite flag.  Any output pointer may be NULL. */
 FP8Q_API fp8q_status fp8q_delayed_get(const fp8q_delayed_state* st, float* history_host, int32_t* head,

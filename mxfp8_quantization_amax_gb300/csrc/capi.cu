@@ -179,12 +179,13 @@ size_t fp8q_cast_workspace_bytes(int32_t num_groups) {
   return cast_workspace_bytes(num_groups);
 }
 
-fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t rows, int64_t cols,
-                                 const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
-                                 int32_t margin, const float* scale_in, uint8_t* q, float* amax_out,
-                                 float* scale_out, float* scale_inv_out, unsigned long long* sat_count_out,
-                                 void* workspace, size_t workspace_bytes, void* stream) {
-  g_err[0] = 0;
+}  // extern "C"
+
+namespace fp8q {
+fp8q_status check_cast_args(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
+                            int32_t num_groups, int32_t fmt, int32_t margin, const float* scale_in, const uint8_t* q,
+                            const float* amax_out, const float* scale_out, const float* scale_inv_out,
+                            const unsigned long long* sat_count_out) {
   fp8q_status r = check_common(x, dt, rows, cols, group_offsets, num_groups);
   if (r != FP8Q_OK) return r;
   if (!fmt_ok(fmt)) return fail(FP8Q_ERR_INVALID_ARG, "fmt must be FP8Q_E4M3 or FP8Q_E5M2");
@@ -194,6 +195,21 @@ fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t rows, int64_
   if (scale_in && !aligned(scale_in, 4)) return fail(FP8Q_ERR_INVALID_ARG, "scale_in must be 4-byte aligned");
   if (!aligned(amax_out, 4) || !aligned(scale_out, 4) || !aligned(scale_inv_out, 4) || !aligned(sat_count_out, 8))
     return fail(FP8Q_ERR_INVALID_ARG, "misaligned output pointer");
+  return FP8Q_OK;
+}
+}  // namespace fp8q
+
+extern "C" {
+
+fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                 const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
+                                 int32_t margin, const float* scale_in, uint8_t* q, float* amax_out,
+                                 float* scale_out, float* scale_inv_out, unsigned long long* sat_count_out,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  fp8q_status r = check_cast_args(x, dt, rows, cols, group_offsets, num_groups, fmt, margin, scale_in, q, amax_out,
+                                  scale_out, scale_inv_out, sat_count_out);
+  if (r != FP8Q_OK) return r;
   if (!workspace || !aligned(workspace, 8)) return fail(FP8Q_ERR_INVALID_ARG, "workspace must be an 8-byte aligned device pointer");
   if (workspace_bytes < cast_workspace_bytes(num_groups))
     return fail(FP8Q_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,

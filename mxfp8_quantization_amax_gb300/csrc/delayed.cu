@@ -47,6 +47,34 @@ static void carve(fp8q_delayed_state* st) {
   st->sat = (unsigned long long*)(b + hb + 16);
 }
 
+// Makes the state's device current for the life of the guard and restores
+// the caller's device afterwards, so get / set / destroy synchronize and
+// copy on the device that runs the state's steps.
+struct DeviceGuard {
+  int prev = -1;
+  cudaError_t err = cudaSuccess;
+  explicit DeviceGuard(int dev) {
+    err = cudaGetDevice(&prev);
+    if (err == cudaSuccess && prev != dev) err = cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+// Steps and resets are enqueued on the caller's stream, which belongs to
+// the current device: it must be the state's.
+static fp8q_status delayed_check_device(const fp8q_delayed_state* st) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != st->device)
+    return fail(FP8Q_ERR_INVALID_ARG, "the delayed-scaling state lives on device %d but device %d is current",
+                st->device, dev);
+  return FP8Q_OK;
+}
+
 fp8q_status delayed_create(int H, int interval, int margin, int fmt, fp8q_delayed_state** out) {
   fp8q_delayed_state* st = new (std::nothrow) fp8q_delayed_state();
   if (!st) return fail(FP8Q_ERR_CUDA, "out of host memory");
@@ -76,12 +104,15 @@ fp8q_status delayed_create(int H, int interval, int margin, int fmt, fp8q_delaye
 }
 
 fp8q_status delayed_destroy(fp8q_delayed_state* st) {
-  cudaError_t e = cudaFree(st->dmem);
+  DeviceGuard guard(st->device);
+  cudaError_t e = guard.err != cudaSuccess ? guard.err : cudaFree(st->dmem);
   delete st;
   return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, "cudaFree(delayed state)");
 }
 
 fp8q_status delayed_reset(fp8q_delayed_state* st, cudaStream_t s) {
+  fp8q_status r0 = delayed_check_device(st);
+  if (r0 != FP8Q_OK) return r0;
   cudaError_t e = cudaMemsetAsync(st->dmem, 0, delayed_bytes(st->H), s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(delayed reset)");
   st->head = 0;
@@ -93,6 +124,8 @@ fp8q_status delayed_reset(fp8q_delayed_state* st, cudaStream_t s) {
 fp8q_status delayed_step(fp8q_delayed_state* st, const void* x, int dt, int64_t n, uint8_t* q,
                          float* scale_used_out, float* scale_inv_out, float* amax_out,
                          unsigned long long* sat_out, cudaStream_t s) {
+  fp8q_status r0 = delayed_check_device(st);
+  if (r0 != FP8Q_OK) return r0;
   const bool record = (st->step % st->interval) == 0;
   PtLaunch L{};
   L.x = x;
@@ -153,6 +186,8 @@ int delayed_history_len(const fp8q_delayed_state* st) { return st->H; }
 
 fp8q_status delayed_get(const fp8q_delayed_state* st, float* hist, int32_t* head, int32_t* count,
                         int64_t* step, int32_t* nonfinite) {
+  DeviceGuard guard(st->device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice(delayed state)");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   if (hist) {
@@ -172,6 +207,8 @@ fp8q_status delayed_get(const fp8q_delayed_state* st, float* hist, int32_t* head
 }
 
 fp8q_status delayed_set(fp8q_delayed_state* st, const float* hist, int32_t head, int32_t count, int64_t step) {
+  DeviceGuard guard(st->device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice(delayed state)");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   e = cudaMemset(st->dmem, 0, delayed_bytes(st->H));

@@ -18,6 +18,11 @@ fp8q_status fail(fp8q_status st, const char* fmt, ...);
 fp8q_status cuda_fail(cudaError_t e, const char* what);
 // Checks cudaGetLastError() after launches.
 fp8q_status check_launch(const char* what);
+// Every argument check of fp8q_cast_per_tensor except the workspace's.
+fp8q_status check_cast_args(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
+                            int32_t num_groups, int32_t fmt, int32_t margin, const float* scale_in, const uint8_t* q,
+                            const float* amax_out, const float* scale_out, const float* scale_inv_out,
+                            const unsigned long long* sat_count_out);
 
 int sm_count();
 

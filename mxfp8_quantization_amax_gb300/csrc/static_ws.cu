@@ -11,8 +11,10 @@
 // The array is loaded with the library on every GPU that uses it and stays
 // there until the process exits.  Its device address is looked up once per
 // device, on that device's first call (so make that first call before any
-// stream capture).  Every call on a device shares the one array: the part a
-// call uses is cleared at its start, and calls whose work overlaps on the
+// stream capture), and kept: a context reset (cudaDeviceReset) is not
+// supported, since the array may come back at another address.  Every call
+// on a device shares the one array: a call checks its arguments, then
+// clears the part it uses, then launches; calls whose work overlaps on the
 // GPU (different streams, no ordering between them) race on it.
 #include <mutex>
 
@@ -65,8 +67,13 @@ extern "C" fp8q_status fp8q_cast_per_tensor_static_ws(const void* x, int32_t dt,
   const size_t need = fp8q_cast_workspace_bytes(num_groups);
   if (need > kStaticWsBytes)
     return fail(FP8Q_ERR_INVALID_ARG, "static workspace too small: %zu > %zu bytes", need, kStaticWsBytes);
+  // a call that would be rejected must not touch the shared array, which
+  // another stream's call may be using
+  fp8q_status r = check_cast_args(x, dt, rows, cols, group_offsets, num_groups, fmt, margin, scale_in, q, amax_out,
+                                  scale_out, scale_inv_out, sat_count_out);
+  if (r != FP8Q_OK) return r;
   void* ws = nullptr;
-  fp8q_status r = static_ws_address(&ws);
+  r = static_ws_address(&ws);
   if (r != FP8Q_OK) return r;
   // the counters and accumulators must start at zero whatever an earlier call left
   cudaError_t e = cudaMemsetAsync(ws, 0, need, (cudaStream_t)stream);
