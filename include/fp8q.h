@@ -452,9 +452,12 @@ FP8Q_API fp8q_status mxfp8_dequantize(const uint8_t* q, const uint8_t* s, int64_
  * fl32(value(q) * scale_inv[g]); MX value(q) * 2^X rounded to FP32 (exact
  * unless it reaches 2^128, which gives Inf; scale byte 0xFF gives NaN).
  * Over the elements where x and xh are both finite:
- *   SQNR = 10 log10(signal / noise) dB,  zero-rate = n_flushed / n.
- * Sums are exact to about 2e-6 relative (FP32 sums of 32 elements added in
- * FP64) and repeat exactly from run to run on one GPU.
+ *   SQNR = 10 log10(signal / noise) dB,  zero-rate = n_flushed / n,
+ * both computed on the device from the sums and counts (SQNR +inf for an
+ * exact copy of a nonzero signal, NaN when signal and noise are both 0;
+ * zero-rate 0 for an empty tensor).  Sums are exact to about 2e-6 relative
+ * (FP32 sums of 32 elements added in FP64) and repeat exactly from run to
+ * run on one GPU.
  */
 typedef struct fp8q_qstats {
     double signal;                   /* sum of x^2 over the finite pairs */
@@ -463,6 +466,8 @@ typedef struct fp8q_qstats {
     unsigned long long n_zero;       /* elements with xh == 0 */
     unsigned long long n_flushed;    /* xh == 0 while x != 0 (a NaN x is not 0) */
     unsigned long long n_nonfinite;  /* x or xh Inf or NaN: left out of the sums */
+    double sqnr_db;                  /* 10 log10(signal / noise) */
+    double zero_rate;                /* n_flushed / n */
 } fp8q_qstats;
 
 /* Bytes of workspace the statistics calls need (a constant, under 100 KB). */

@@ -519,7 +519,7 @@ def mx_scales_to_mma_layout(s: torch.Tensor, scale_cols: int | None = None,
 # ---------------------------------------------------------------------------
 # quantization-error statistics (SQNR, zero-rate)
 # ---------------------------------------------------------------------------
-QSTATS_BYTES = 48  # fp8q_qstats: 2 doubles, 4 uint64
+QSTATS_BYTES = 64  # fp8q_qstats: 2 doubles, 4 uint64, 2 doubles
 
 
 def fp8q_qstats_workspace_bytes() -> int:
@@ -542,7 +542,7 @@ def _qstats_out(x: torch.Tensor, out):
     if out is None:
         return torch.empty(QSTATS_BYTES // 8, dtype=torch.float64, device=x.device)
     if not out.is_cuda or out.numel() * out.element_size() < QSTATS_BYTES or out.data_ptr() % 8:
-        raise ValueError("out must be an 8-byte aligned CUDA tensor of at least 48 bytes")
+        raise ValueError(f"out must be an 8-byte aligned CUDA tensor of at least {QSTATS_BYTES} bytes")
     return out
 
 
@@ -585,18 +585,14 @@ def mxfp8_qstats(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, fmt: int = E
 
 
 def qstats_dict(t: torch.Tensor) -> dict:
-    """The fp8q_qstats in a device tensor as a dict, with the SQNR in dB
-    (10 log10(signal / noise)) and the zero-rate (n_flushed / n)."""
+    """The fp8q_qstats in a device tensor as a dict (the library computes
+    the SQNR in dB and the zero-rate on the device)."""
     raw = t.reshape(-1).view(torch.uint8)[:QSTATS_BYTES].cpu()
     f = raw[:16].view(torch.float64).tolist()
-    c = raw[16:].view(torch.int64).tolist()
-    d = {"signal": f[0], "noise": f[1], "n": c[0], "n_zero": c[1], "n_flushed": c[2], "n_nonfinite": c[3]}
-    if d["noise"] > 0:
-        d["sqnr_db"] = 10.0 * math.log10(d["signal"] / d["noise"]) if d["signal"] > 0 else float("-inf")
-    else:
-        d["sqnr_db"] = float("inf") if d["signal"] > 0 else float("nan")
-    d["zero_rate"] = d["n_flushed"] / d["n"] if d["n"] else 0.0
-    return d
+    c = raw[16:48].view(torch.int64).tolist()
+    g = raw[48:64].view(torch.float64).tolist()
+    return {"signal": f[0], "noise": f[1], "n": c[0], "n_zero": c[1], "n_flushed": c[2], "n_nonfinite": c[3],
+            "sqnr_db": g[0], "zero_rate": g[1]}
 
 
 # ---------------------------------------------------------------------------

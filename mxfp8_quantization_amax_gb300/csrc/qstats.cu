@@ -338,6 +338,8 @@ __device__ void qs_finish(const QsParams& p, const QsAcc& a) {
     p.out->n_zero = c[1];
     p.out->n_flushed = c[2];
     p.out->n_nonfinite = c[3];
+    p.out->sqnr_db = n == 0.0 ? (s > 0.0 ? (double)INFINITY : (double)NAN) : 10.0 * log10(s / n);
+    p.out->zero_rate = c[0] ? (double)c[2] / (double)c[0] : 0.0;
     *p.counter = 0;
   }
 }

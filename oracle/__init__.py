@@ -550,6 +550,14 @@ def sqnr_db(stats: dict) -> float:
     return 10.0 * np.log10(stats["signal"] / stats["noise"])
 
 
+def zero_rate(stats: dict) -> float:
+    """The share of the compared elements whose quantized value is 0 while
+    the input is not ("昇腾 Ascend 950 低精度格式", appendix 3.4, compares
+    formats by it without defining it): n_flushed / n, 0 for an empty
+    tensor."""
+    return stats["n_flushed"] / stats["n"] if stats["n"] else 0.0
+
+
 # --------------------------------------------------------------------------
 # Blockwise FP8 (1x128, 128x1, 128x128 groups with FP32 scales)
 # --------------------------------------------------------------------------

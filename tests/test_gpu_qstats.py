@@ -27,11 +27,23 @@ def _gpu(fq, t):
     return fq.qstats_dict(t)
 
 
+# SQNR: relative errors of RTOL in the two sums move 10 log10(signal/noise)
+# by at most 10 / ln(10) * 2 * RTOL dB.
+SQNR_TOL_DB = 10.0 / np.log(10.0) * 2 * RTOL
+
+
 def _same(got, want):
     for k in ("n", "n_zero", "n_flushed", "n_nonfinite"):
         assert got[k] == want[k], (k, got, want)
     for k in ("signal", "noise"):
         assert got[k] == pytest.approx(want[k], rel=RTOL, abs=0.0), (k, got, want)
+    # the SQNR and zero-rate the library computes on the device
+    w_db = oracle.sqnr_db(want)
+    if np.isfinite(w_db):
+        assert abs(got["sqnr_db"] - w_db) <= SQNR_TOL_DB, (got["sqnr_db"], w_db)
+    else:
+        assert got["sqnr_db"] == w_db or (np.isnan(w_db) and np.isnan(got["sqnr_db"])), (got["sqnr_db"], w_db)
+    assert got["zero_rate"] == oracle.zero_rate(want), (got["zero_rate"], oracle.zero_rate(want))
 
 
 def _mx_case(fq, x, fmt, offsets=None):

@@ -863,6 +863,9 @@ def test_qstats_worked_elements():
     assert F(st["signal"]) == (1 + F(1, 32)) ** 2 + F(1, 2 ** 22) + 500 ** 2
     assert F(st["noise"]) == F(1, 2 ** 10) + F(1, 2 ** 22) + 52 ** 2
     assert (st["n"], st["n_zero"], st["n_flushed"], st["n_nonfinite"]) == (6, 2, 1, 2)
+    # one flushed element (2^-11) of the six compared
+    assert oracle.zero_rate(st) == 1 / 6
+    assert oracle.zero_rate({"n": 0, "n_flushed": 0}) == 0.0
 
 
 @pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
