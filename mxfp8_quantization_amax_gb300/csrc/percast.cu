@@ -92,6 +92,39 @@ __device__ __forceinline__ int group_of_elem(const KParams& p, int64_t e) {
   return group_of_row(p.off, p.G, e / p.cols);
 }
 
+// Elements [e0, e1) of group g, from offsets clamped to [0, rows].
+struct GroupSpan {
+  int g;
+  int64_t e0, e1;
+};
+
+__device__ __forceinline__ int64_t clamped_row(const KParams& p, int g) {
+  if (p.off == nullptr) return g == 0 ? 0 : p.rows;
+  const int64_t v = __ldg(p.off + g);
+  return v < 0 ? 0 : (v > p.rows ? p.rows : v);
+}
+
+// The group of element e (the last g with offsets[g] <= its row, as
+// group_of_elem) and that group's span.  e may lie outside the span when
+// the offsets leave rows uncovered; such elements belong to group g all the
+// same, as they always have.
+__device__ __forceinline__ GroupSpan span_of(const KParams& p, int64_t e) {
+  GroupSpan s;
+  s.g = group_of_elem(p, e);
+  s.e0 = clamped_row(p, s.g) * p.cols;
+  s.e1 = clamped_row(p, s.g + 1) * p.cols;
+  return s;
+}
+
+// A forward cursor over the groups: elements are visited in increasing
+// order, so the span is looked up again (binary search) only when an
+// element leaves it.  Returns the group of e.
+__device__ __forceinline__ int cursor_group(const KParams& p, GroupSpan& s, int64_t e) {
+  if (p.off == nullptr || p.G <= 1) return 0;
+  if (!(s.e0 <= e && e < s.e1)) s = span_of(p, e);
+  return s.g;
+}
+
 // Block-wide max / sum; every thread must call (block-uniform control flow).
 __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* sh) {
   v = warp_max_u32(v);
@@ -137,64 +170,85 @@ __device__ __forceinline__ void amax_pass(const KParams& p, int64_t c_begin, int
                                           uint32_t* sh_max) {
   int cur_g = -1;
   uint32_t cur = 0;
-
   auto flush = [&]() {  // block-uniform
     const uint32_t m = block_max(cur, sh_max);
     if (threadIdx.x == 0 && cur_g >= 0 && m != 0) atomicMax(p.acc + cur_g, m);
     cur = 0;
   };
+  constexpr int PV = InT<DT>::kPerVec;
+  constexpr int V = kVecs;
+  GroupSpan span{0, 0, -1};  // the chunk's group (block-uniform)
 
   for (int64_t c = c_begin; c < c_end; ++c) {
     const int64_t e0 = c * InT<DT>::kChunk;
     const int64_t e1 = min(e0 + (int64_t)InT<DT>::kChunk, p.n);
-    const int g0 = group_of_elem(p, e0), g1 = group_of_elem(p, e1 - 1);
-    if (g0 == g1) {
+    const int g0 = cursor_group(p, span, e0);
+    const bool one_group = p.off == nullptr || p.G <= 1 || (span.e0 <= e0 && e1 <= span.e1);
+    if (one_group) {
       if (g0 != cur_g) {
         if (cur_g >= 0) flush();
         cur_g = g0;
       }
-      if (e1 - e0 == InT<DT>::kChunk) {
-        constexpr int V = kVecs;
-        uint4 v[V];
+    } else if (cur_g >= 0) {
+      flush();  // per-thread group runs below, merged with atomics
+      cur_g = -1;
+    }
+    if (one_group && e1 - e0 == InT<DT>::kChunk) {
+      // whole vectors: all loads first, then the maxima
+      uint4 v[V];
+#pragma unroll
+      for (int k = 0; k < V; k++)
+        v[k] = ld_hint((const char*)p.x + (e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV) * (DT == kBF16 ? 2 : 4), pol);
+#pragma unroll
+      for (int k = 0; k < V; k++) reg_fence(v[k]);
+      if constexpr (DT == kBF16) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < V; k++) {
+          m = absmax_bf16x2(m, v[k].x);
+          m = absmax_bf16x2(m, v[k].y);
+          m = absmax_bf16x2(m, v[k].z);
+          m = absmax_bf16x2(m, v[k].w);
+        }
+        cur = max(cur, max(m << 16, m & 0xFFFF0000u));
+      } else {
 #pragma unroll
         for (int k = 0; k < V; k++)
-          v[k] = ld_hint((const char*)p.x + (e0 + (int64_t)(k * kPtThreads + threadIdx.x) * InT<DT>::kPerVec) * (DT == kBF16 ? 2 : 4), pol);
-#pragma unroll
-        for (int k = 0; k < V; k++) reg_fence(v[k]);
-        if constexpr (DT == kBF16) {
-          uint32_t m = 0;
-#pragma unroll
-          for (int k = 0; k < V; k++) {
-            m = absmax_bf16x2(m, v[k].x);
-            m = absmax_bf16x2(m, v[k].y);
-            m = absmax_bf16x2(m, v[k].z);
-            m = absmax_bf16x2(m, v[k].w);
-          }
-          cur = max(cur, max(m << 16, m & 0xFFFF0000u));
-        } else {
-#pragma unroll
-          for (int k = 0; k < V; k++)
-            cur = max(max(cur, max(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu)),
-                      max(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu));
-        }
-      } else {
-        for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads)
-          cur = max(cur, InT<DT>::bits(p.x, e) & 0x7FFFFFFFu);
+          cur = max(max(cur, max(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu)),
+                    max(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu));
       }
+    } else if (one_group) {
+      for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) cur = max(cur, InT<DT>::bits(p.x, e) & 0x7FFFFFFFu);
     } else {
-      // chunk crosses group boundaries: per-thread runs, atomics on change
-      if (cur_g >= 0) flush();
-      cur_g = -1;
+      // a chunk that crosses groups (rare): per-thread group runs, merged
+      // with atomics; whole vectors when no vector can straddle a group
+      GroupSpan tspan{0, 0, -1};
       int tg = -1;
       uint32_t tm = 0;
-      for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) {
-        const int g = group_of_elem(p, e);
+      auto take = [&](int64_t e, uint32_t m) {
+        const int g = cursor_group(p, tspan, e);
         if (g != tg) {
           if (tg >= 0 && tm) atomicMax(p.acc + tg, tm);
           tg = g;
           tm = 0;
         }
-        tm = max(tm, InT<DT>::bits(p.x, e) & 0x7FFFFFFFu);
+        tm = max(tm, m);
+      };
+      if (e1 - e0 == InT<DT>::kChunk && p.cols % PV == 0) {
+        for (int k = 0; k < V; k++) {
+          const int64_t e = e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV;
+          const uint4 v = ld_hint((const char*)p.x + e * (DT == kBF16 ? 2 : 4), pol);
+          uint32_t m;
+          if constexpr (DT == kBF16) {
+            const uint32_t h = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(0u, v.x), v.y), v.z), v.w);
+            m = max(h << 16, h & 0xFFFF0000u);
+          } else {
+            m = max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu));
+          }
+          take(e, m);
+        }
+      } else {
+        for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) take(e, InT<DT>::bits(p.x, e) & 0x7FFFFFFFu);
       }
       if (tg >= 0 && tm) atomicMax(p.acc + tg, tm);
     }
@@ -249,10 +303,52 @@ __device__ __forceinline__ float group_scale(const KParams& p, int g, float hist
 // Cast of the CTA's chunks [c_begin, c_end) with the per-group scale of
 // `p.src`; optional fused amax (p.acc) and saturation count (p.sat_acc).
 // Block-uniform: every thread calls it.
+// One 16-byte vector: codes of its PV elements scaled by s, stored at q[e];
+// its amax and saturated elements are added to m / nsat.
+template <int DT, int FMT>
+__device__ __forceinline__ void cast_vec(const KParams& p, const uint4& v, int64_t e, float s, bool do_amax,
+                                         bool do_sat, uint32_t& m, unsigned long long& nsat) {
+  constexpr float kMax = Fmt<FMT>::kMax;
+  if constexpr (DT == kBF16) {
+    float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+    for (int i = 0; i < 8; i++) f[i] = __fmul_rn(f[i], s);
+    if (do_sat) {
+#pragma unroll
+      for (int i = 0; i < 8; i++) nsat += fabsf(f[i]) > kMax;
+    }
+    if (do_amax) {
+      const uint32_t h = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(0u, v.x), v.y), v.z), v.w);
+      m = max(m, max(h << 16, h & 0xFFFF0000u));
+    }
+    uint2 o;
+    o.x = canon_nan4<FMT>(cvt4<FMT>(f[0], f[1], f[2], f[3]));
+    o.y = canon_nan4<FMT>(cvt4<FMT>(f[4], f[5], f[6], f[7]));
+    st_stream(p.q + e, o);
+  } else {
+    float f[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w)};
+    if (do_amax)
+      m = max(max(m, max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu)), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu));
+#pragma unroll
+    for (int i = 0; i < 4; i++) f[i] = __fmul_rn(f[i], s);
+    if (do_sat) {
+#pragma unroll
+      for (int i = 0; i < 4; i++) nsat += fabsf(f[i]) > kMax;
+    }
+    *(uint32_t*)(p.q + e) = canon_nan4<FMT>(cvt4<FMT>(f[0], f[1], f[2], f[3]));
+  }
+}
+
+// Cast of the CTA's chunks [c_begin, c_end) with the per-group scale of
+// `p.src`; optional fused amax (p.acc) and saturation count (p.sat_acc).
+// Block-uniform: every thread calls it.
 template <int DT, int FMT>
 __device__ __forceinline__ void cast_pass(const KParams& p, int64_t c_begin, int64_t c_end, uint64_t pol,
                                           float hist_scale, uint32_t* sh_max, unsigned long long* sh_sum) {
   constexpr float kMax = Fmt<FMT>::kMax;
+  constexpr int PV = InT<DT>::kPerVec;
+  constexpr int V = kVecs;
   const bool do_amax = p.acc != nullptr;
   const bool do_sat = p.sat_acc != nullptr;
   int cur_g = -1;
@@ -271,20 +367,25 @@ __device__ __forceinline__ void cast_pass(const KParams& p, int64_t c_begin, int
     cur = 0;
     nsat = 0;
   };
+  GroupSpan span{0, 0, -1};
 
   for (int64_t c = c_begin; c < c_end; ++c) {
     const int64_t e0 = c * InT<DT>::kChunk;
     const int64_t e1 = min(e0 + (int64_t)InT<DT>::kChunk, p.n);
-    const int g0 = group_of_elem(p, e0), g1 = group_of_elem(p, e1 - 1);
-    if (g0 == g1) {
+    const int g0 = cursor_group(p, span, e0);
+    const bool one_group = p.off == nullptr || p.G <= 1 || (span.e0 <= e0 && e1 <= span.e1);
+    if (one_group) {
       if (g0 != cur_g) {
         if (cur_g >= 0) flush();
         cur_g = g0;
       }
+    } else if (cur_g >= 0) {
+      flush();
+      cur_g = -1;
+    }
+    if (one_group) {
       const float s = group_scale(p, g0, hist_scale);
       if (e1 - e0 == InT<DT>::kChunk) {
-        constexpr int PV = InT<DT>::kPerVec;
-        constexpr int V = kVecs;
         uint4 v[V];
 #pragma unroll
         for (int k = 0; k < V; k++)
@@ -292,40 +393,8 @@ __device__ __forceinline__ void cast_pass(const KParams& p, int64_t c_begin, int
 #pragma unroll
         for (int k = 0; k < V; k++) reg_fence(v[k]);
 #pragma unroll
-        for (int k = 0; k < V; k++) {
-          const int64_t e = e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV;
-          if constexpr (DT == kBF16) {
-            float f[8] = {bf16_lo(v[k].x), bf16_hi(v[k].x), bf16_lo(v[k].y), bf16_hi(v[k].y),
-                          bf16_lo(v[k].z), bf16_hi(v[k].z), bf16_lo(v[k].w), bf16_hi(v[k].w)};
-#pragma unroll
-            for (int i = 0; i < 8; i++) f[i] = __fmul_rn(f[i], s);
-            if (do_sat) {
-#pragma unroll
-              for (int i = 0; i < 8; i++) nsat += fabsf(f[i]) > kMax;
-            }
-            if (do_amax) {
-              uint32_t m = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(0u, v[k].x), v[k].y), v[k].z), v[k].w);
-              cur = max(cur, max(m << 16, m & 0xFFFF0000u));
-            }
-            uint2 o;
-            o.x = canon_nan4<FMT>(cvt4<FMT>(f[0], f[1], f[2], f[3]));
-            o.y = canon_nan4<FMT>(cvt4<FMT>(f[4], f[5], f[6], f[7]));
-            st_stream(p.q + e, o);
-          } else {
-            float f[4] = {__uint_as_float(v[k].x), __uint_as_float(v[k].y), __uint_as_float(v[k].z),
-                          __uint_as_float(v[k].w)};
-            if (do_amax)
-              cur = max(max(cur, max(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu)),
-                        max(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu));
-#pragma unroll
-            for (int i = 0; i < 4; i++) f[i] = __fmul_rn(f[i], s);
-            if (do_sat) {
-#pragma unroll
-              for (int i = 0; i < 4; i++) nsat += fabsf(f[i]) > kMax;
-            }
-            *(uint32_t*)(p.q + e) = canon_nan4<FMT>(cvt4<FMT>(f[0], f[1], f[2], f[3]));
-          }
-        }
+        for (int k = 0; k < V; k++)
+          cast_vec<DT, FMT>(p, v[k], e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV, s, do_amax, do_sat, cur, nsat);
       } else {
         for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) {
           const uint32_t b = InT<DT>::bits(p.x, e);
@@ -336,34 +405,42 @@ __device__ __forceinline__ void cast_pass(const KParams& p, int64_t c_begin, int
         }
       }
     } else {
-      if (cur_g >= 0) flush();
-      cur_g = -1;
+      // a chunk that crosses groups (rare): per-thread group runs, merged
+      // with atomics; whole vectors when no vector can straddle a group
+      GroupSpan tspan{0, 0, -1};
       int tg = -1;
       uint32_t tm = 0;
       unsigned long long ts = 0;
-      float s = 1.0f;
-      for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) {
-        const int g = group_of_elem(p, e);
-        if (g != tg) {
-          if (tg >= 0) {
-            if (do_amax && tm) atomicMax(p.acc + tg, tm);
-            if (do_sat && ts) atomicAdd(p.sat_acc + tg, ts);
-          }
-          tg = g;
-          tm = 0;
-          ts = 0;
-          s = group_scale(p, g, hist_scale);
+      float tscale = 1.0f;
+      auto thread_group = [&](int g) {
+        if (g == tg) return;
+        if (tg >= 0) {
+          if (do_amax && tm) atomicMax(p.acc + tg, tm);
+          if (do_sat && ts) atomicAdd(p.sat_acc + tg, ts);
         }
-        const uint32_t b = InT<DT>::bits(p.x, e);
-        const float f = __fmul_rn(__uint_as_float(b), s);
-        if (do_sat) ts += fabsf(f) > kMax;
-        if (do_amax) tm = max(tm, b & 0x7FFFFFFFu);
-        p.q[e] = (uint8_t)canon_nan4<FMT>(cvt2<FMT>(f, 0.0f));
+        tg = g;
+        tm = 0;
+        ts = 0;
+        if (g >= 0) tscale = group_scale(p, g, hist_scale);
+      };
+      if (e1 - e0 == InT<DT>::kChunk && p.cols % PV == 0) {
+        for (int k = 0; k < V; k++) {
+          const int64_t e = e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV;
+          const uint4 v = ld_hint((const char*)p.x + e * (DT == kBF16 ? 2 : 4), pol);
+          thread_group(cursor_group(p, tspan, e));
+          cast_vec<DT, FMT>(p, v, e, tscale, do_amax, do_sat, tm, ts);
+        }
+      } else {
+        for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) {
+          thread_group(cursor_group(p, tspan, e));
+          const uint32_t b = InT<DT>::bits(p.x, e);
+          const float f = __fmul_rn(__uint_as_float(b), tscale);
+          if (do_sat) ts += fabsf(f) > kMax;
+          if (do_amax) tm = max(tm, b & 0x7FFFFFFFu);
+          p.q[e] = (uint8_t)canon_nan4<FMT>(cvt2<FMT>(f, 0.0f));
+        }
       }
-      if (tg >= 0) {
-        if (do_amax && tm) atomicMax(p.acc + tg, tm);
-        if (do_sat && ts) atomicAdd(p.sat_acc + tg, ts);
-      }
+      thread_group(-1);  // merge this thread's last run
     }
   }
   if (cur_g >= 0) flush();
