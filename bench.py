@@ -228,7 +228,7 @@ def kernel_label(op):
             "dq_mx_col": f"dequant_kernel<mx_col,{fmt_name},bf16>",
             "dq_tensor": f"dequant_kernel<tensor,{fmt_name},bf16>",
             "mx_rule": f"mx_tma_kernel<bf16,{fmt_name},both,rule+counts>",
-            "mx_grouped": f"mx_tma_kernel<bf16,{fmt_name},both> (64 groups)",
+            "mx_grouped": f"mx_band_kernel<bf16,{fmt_name},both> (64 groups)",
             "bw": f"blockwise_kernel<{fmt_name},{'1x128' if op.get('block') == 1 else '128x128'},both>",
             "nvfp4": "amax_kernel + nvfp4_kernel<bf16>",
             "qs_mx_row": f"qstats_lin_kernel<bf16,{fmt_name},mx_row>",

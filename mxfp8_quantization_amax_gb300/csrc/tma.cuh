@@ -50,12 +50,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
-// false if budget_ns elapses first.
+// false if budget_ns elapses first.  The clock is read on every 16th failed
+// try only (each try may suspend the thread for a while in hardware), so the
+// wait gives up between budget_ns and budget_ns plus 16 tries.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > budget_ns) return false;
+  for (uint32_t n = 1; !mbar_try_wait(bar, parity); ++n) {
+    if ((n & 15u) == 0 && globaltimer_ns() - t0 > budget_ns) return false;
   }
   return true;
 }
