@@ -52,7 +52,7 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 ROOFLINE_MIN_LAUNCHES = 100
 E4M3, E5M2 = 0, 1
-WORKLOADS = ["moe", "per_tensor_1024", "mx_4096", "delayed_8192", "linear_layer", "activation", "mx_8192",
+WORKLOADS = ["moe", "moe_16384", "per_tensor_1024", "mx_4096", "delayed_8192", "linear_layer", "activation", "mx_8192",
              "dequant_8192", "mx_rules_4096", "blockwise_8192", "nvfp4_8192", "qstats_8192", "mxfp4_fp6_8192",
              "mma_scales_8192"]
 # the configurations measured beside the headline, by name
@@ -92,6 +92,12 @@ def workload_spec(name):
         ops = [{"kind": "mx_grouped", "shape": (r, c), "fmt": E4M3, "bytes": None, "gen": ("c5", 0)},
                {"kind": "current_grouped", "shape": (r, c), "fmt": E4M3, "bytes": 5 * r * c, "gen": ("c5", 0)}]
         return {"workload": "moe_64_experts_65536x7168_bf16", "rows": r, "cols": c, "experts": 64,
+                "ops": ["grouped mxfp8 e4m3 row+col", "grouped current scaling e4m3"]}, ops
+    if name == "moe_16384":
+        r, c = 16384, 7168
+        ops = [{"kind": "mx_grouped", "shape": (r, c), "fmt": E4M3, "bytes": None, "gen": ("c5", 0)},
+               {"kind": "current_grouped", "shape": (r, c), "fmt": E4M3, "bytes": 5 * r * c, "gen": ("c5", 0)}]
+        return {"workload": "moe_16_experts_16384x7168_bf16", "rows": r, "cols": c, "experts": 16,
                 "ops": ["grouped mxfp8 e4m3 row+col", "grouped current scaling e4m3"]}, ops
     if name == "per_tensor_1024":
         ops = [{"kind": "current", "shape": (1024, 1024), "fmt": E4M3, "bytes": 5 * 1024 * 1024, "gen": ("c1", 0)}]
@@ -228,7 +234,7 @@ def kernel_label(op):
             "dq_mx_col": f"dequant_kernel<mx_col,{fmt_name},bf16>",
             "dq_tensor": f"dequant_kernel<tensor,{fmt_name},bf16>",
             "mx_rule": f"mx_tma_kernel<bf16,{fmt_name},both,rule+counts>",
-            "mx_grouped": f"mx_band_kernel<bf16,{fmt_name},both> (64 groups)",
+            "mx_grouped": f"mx_band_kernel<bf16,{fmt_name},both> ({op.get('G')} groups)",
             "bw": f"blockwise_kernel<{fmt_name},{'1x128' if op.get('block') == 1 else '128x128'},both>",
             "nvfp4": "amax_kernel + nvfp4_kernel<bf16>",
             "qs_mx_row": f"qstats_lin_kernel<bf16,{fmt_name},mx_row>",
@@ -237,7 +243,7 @@ def kernel_label(op):
             "mxlow": f"mxlow_kernel<bf16,{LOW_NAMES.get(op.get('elem'), '')},both>",
             "mmascale": "mma_scale_kernel",
             "current": f"amax_kernel + cast_kernel<bf16,{fmt_name}>",
-            "current_grouped": f"amax_kernel + cast_kernel<bf16,{fmt_name}> (64 groups)",
+            "current_grouped": f"amax_kernel + cast_kernel<bf16,{fmt_name}> ({op.get('G')} groups)",
             "delayed": f"cast_kernel<bf16,{fmt_name},history> (interval {op.get('interval')})",
             }.get(op["kind"], f"mx_tma_kernel<bf16,{fmt_name},both>")
 
@@ -373,11 +379,13 @@ class Prepared:
         self.cfg, self.ops = workload_spec(name)
         ops = self.ops
         self.offsets_host = None
-        if name == "moe":
-            self.offsets_host = synth.moe_offsets(65536, 64, seed=5)
+        if name in ("moe", "moe_16384"):
+            rows, self.G = self.ops[0]["shape"][0], self.cfg["experts"]
+            self.offsets_host = synth.moe_offsets(rows, self.G, seed=5)
             o = self.offsets_host
-            self.ncb = int(sum((int(o[g + 1] - o[g]) + 31) // 32 for g in range(64)))
+            self.ncb = int(sum((int(o[g + 1] - o[g]) + 31) // 32 for g in range(self.G)))
             for op in ops:
+                op["G"] = self.G
                 if op["kind"] == "mx_grouped":
                     op["bytes"] = mx_bytes(*op["shape"], ncolblocks=self.ncb)
         self.bytes_per_step = sum(op["bytes"] for op in ops)
@@ -508,7 +516,7 @@ class Prepared:
             b["dl"] = {n: torch.empty(1, dtype=torch.float32, device=dev) for n in ("scale", "scale_inv", "amax")}
         else:  # current, current_grouped
             b["q"] = torch.empty((r, c), dtype=torch.uint8, device=dev)
-            G = 64 if k == "current_grouped" else 1
+            G = op.get("G", 1)
             b["pt"] = {n: torch.empty(G, dtype=torch.float32, device=dev) for n in ("amax", "scale", "scale_inv")}
             b["ws"] = torch.zeros(fq.fp8q_cast_workspace_bytes(G), dtype=torch.uint8, device=dev)
         return b
@@ -522,14 +530,14 @@ class Prepared:
             o = b["out"]
             g = k == "mx_grouped"
             return (lib.mxfp8_quantize, (
-                b["x"].data_ptr(), 0, r, c, off_ptr if g else None, 64 if g else 1, op["fmt"], 3,
+                b["x"].data_ptr(), 0, r, c, off_ptr if g else None, op.get("G", 1), op["fmt"], 3,
                 o["q_row"].data_ptr(), o["s_row"].data_ptr(), o["q_col"].data_ptr(), o["s_col"].data_ptr(), b["ld"],
                 stream)), 1
         if k in ("current", "current_grouped"):
             pt = b["pt"]
             g = k == "current_grouped"
             return (lib.fp8q_cast_per_tensor, (
-                b["x"].data_ptr(), 0, r, c, off_ptr if g else None, 64 if g else 1, op["fmt"], 0, None,
+                b["x"].data_ptr(), 0, r, c, off_ptr if g else None, op.get("G", 1), op["fmt"], 0, None,
                 b["q"].data_ptr(), pt["amax"].data_ptr(), pt["scale"].data_ptr(), pt["scale_inv"].data_ptr(), None,
                 b["ws"].data_ptr(), b["ws"].numel(), stream)), 2
         if k == "mx_rule":
@@ -1011,7 +1019,7 @@ def oracle_inputs(workload, sample_rows):
 
 def sample_rows_for(workload):
     return {"activation": 256, "mx_4096": 256, "mx_8192": 128, "per_tensor_1024": 1024, "delayed_8192": 64,
-            "linear_layer": 64, "moe": 1024, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128,
+            "linear_layer": 64, "moe": 1024, "moe_16384": 1024, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128,
             "nvfp4_8192": 128, "qstats_8192": 128, "mxfp4_fp6_8192": 128, "mma_scales_8192": 1024}[workload]
 
 
