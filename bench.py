@@ -53,6 +53,7 @@ L2_BYTES = 129 * 2 ** 20
 ROOFLINE_MIN_LAUNCHES = 100
 E4M3, E5M2 = 0, 1
 WORKLOADS = ["moe", "moe_16384", "per_tensor_1024", "mx_4096", "delayed_8192", "linear_layer", "activation", "mx_8192",
+             "mx_mma_8192",
              "dequant_8192", "mx_rules_4096", "blockwise_8192", "nvfp4_8192", "qstats_8192", "mxfp4_fp6_8192",
              "mma_scales_8192"]
 # the configurations measured beside the headline, by name
@@ -142,6 +143,11 @@ def workload_spec(name):
         r = c = 8192
         ops = [{"kind": "mx", "shape": (r, c), "fmt": E4M3, "bytes": mx_bytes(r, c), "gen": ("c2", 0)}]
         return {"workload": "mxfp8_8192x8192_bf16", "rows": r, "cols": c, "ops": ["mxfp8 e4m3 row+col"]}, ops
+    if name == "mx_mma_8192":
+        r = c = 8192
+        ops = [{"kind": "mx_mma", "shape": (r, c), "fmt": E4M3, "bytes": mx_bytes(r, c), "gen": ("c2", 0)}]
+        return {"workload": "mxfp8_mma_scales_8192x8192_bf16", "rows": r, "cols": c,
+                "ops": ["mxfp8 e4m3 row+col, scales written in the 128x4 MMA block layout"]}, ops
     if name == "mx_rules_4096":
         r = c = 4096
         ops = [{"kind": "mx_rule", "rule": 0, "shape": (r, c), "fmt": E4M3, "bytes": mx_bytes(r, c), "gen": ("c2", 0)},
@@ -202,7 +208,7 @@ def workload_spec(name):
 
 DQ_KINDS = ("dq_mx_row", "dq_mx_col", "dq_tensor")
 QS_KINDS = ("qs_mx_row", "qs_mx_col", "qs_tensor")
-ROOFLINE_KINDS = ("mx", "mx_grouped", "dq_mx_row", "mx_rule", "bw", "nvfp4", "qs_mx_row", "mxlow", "mmascale",
+ROOFLINE_KINDS = ("mx", "mx_grouped", "mx_mma", "dq_mx_row", "mx_rule", "bw", "nvfp4", "qs_mx_row", "mxlow", "mmascale",
                   "delayed")
 LOW_NAMES = {2: "e2m1", 3: "e2m3", 4: "e3m2"}
 
@@ -234,6 +240,7 @@ def kernel_label(op):
             "dq_mx_col": f"dequant_kernel<mx_col,{fmt_name},bf16>",
             "dq_tensor": f"dequant_kernel<tensor,{fmt_name},bf16>",
             "mx_rule": f"mx_tma_kernel<bf16,{fmt_name},both,rule+counts>",
+            "mx_mma": f"mx_tma_kernel<bf16,{fmt_name},both> (MMA scale layout)",
             "mx_grouped": f"mx_band_kernel<bf16,{fmt_name},both> ({op.get('G')} groups)",
             "bw": f"blockwise_kernel<{fmt_name},{'1x128' if op.get('block') == 1 else '128x128'},both>",
             "nvfp4": "amax_kernel + nvfp4_kernel<bf16>",
@@ -472,7 +479,14 @@ class Prepared:
         r, c = op["shape"]
         k = op["kind"]
         b = {}
-        if k in ("mx", "mx_grouped", "mx_rule"):
+        if k == "mx_mma":
+            ld = fq.mxfp8_col_blocks(r, None)
+            b["out"] = {"q_row": torch.empty((r, c), dtype=torch.uint8, device=dev),
+                        "s_row": torch.empty(fq.mxfp8_mma_scale_bytes(r, c // 32), dtype=torch.uint8, device=dev),
+                        "q_col": torch.empty((c, r), dtype=torch.uint8, device=dev),
+                        "s_col": torch.empty(fq.mxfp8_mma_scale_bytes(c, ld), dtype=torch.uint8, device=dev)}
+            b["ld"] = ld
+        elif k in ("mx", "mx_grouped", "mx_rule"):
             ld = fq.mxfp8_col_blocks(r, None if k != "mx_grouped" else list(self.offsets_host))
             if k == "mx_grouped":
                 ld = (ld + 15) // 16 * 16  # the library's default layout for grouped scales
@@ -540,6 +554,11 @@ class Prepared:
                 b["x"].data_ptr(), 0, r, c, off_ptr if g else None, op.get("G", 1), op["fmt"], 0, None,
                 b["q"].data_ptr(), pt["amax"].data_ptr(), pt["scale"].data_ptr(), pt["scale_inv"].data_ptr(), None,
                 b["ws"].data_ptr(), b["ws"].numel(), stream)), 2
+        if k == "mx_mma":
+            o = b["out"]
+            return (lib.mxfp8_quantize_ex, (
+                b["x"].data_ptr(), 0, r, c, None, 1, op["fmt"], 3, 0, 1, o["q_row"].data_ptr(), o["s_row"].data_ptr(),
+                o["q_col"].data_ptr(), o["s_col"].data_ptr(), b["ld"], None, stream)), 1
         if k == "mx_rule":
             o = b["out"]
             return (lib.mxfp8_quantize_rule, (
@@ -601,7 +620,7 @@ class Prepared:
     def outputs(self, j, i=0):
         op, b = self.ops[j], self.sets[i % self.nsets][j]
         k = op["kind"]
-        if k in ("mx", "mx_grouped", "mx_rule"):
+        if k in ("mx", "mx_grouped", "mx_rule", "mx_mma"):
             o = b["out"]
             return [o["q_row"], o["s_row"], o["q_col"], o["s_col"]]
         if k == "bw":
@@ -944,6 +963,11 @@ def oracle_sample_step(workload, sample_rows, inputs, states):
         if k in ("mx", "mx_grouped"):
             oracle.mx_quantize(x, op["fmt"], 3)
             total += mx_bytes(r, c)
+        elif k == "mx_mma":
+            m = oracle.mx_quantize(x, op["fmt"], 3)
+            oracle.mma_scale_layout(m["s_row"])
+            oracle.mma_scale_layout(m["s_col"])
+            total += mx_bytes(r, c)
         elif k == "mx_rule":
             oracle.mx_quantize_rule(x, op["fmt"], 3, op["rule"])
             total += mx_bytes(r, c)
@@ -1019,7 +1043,7 @@ def oracle_inputs(workload, sample_rows):
 
 def sample_rows_for(workload):
     return {"activation": 256, "mx_4096": 256, "mx_8192": 128, "per_tensor_1024": 1024, "delayed_8192": 64,
-            "linear_layer": 64, "moe": 1024, "moe_16384": 1024, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128,
+            "linear_layer": 64, "moe": 1024, "moe_16384": 1024, "mx_mma_8192": 128, "dequant_8192": 128, "mx_rules_4096": 256, "blockwise_8192": 128,
             "nvfp4_8192": 128, "qstats_8192": 128, "mxfp4_fp6_8192": 128, "mma_scales_8192": 1024}[workload]
 
 

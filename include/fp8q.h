@@ -316,6 +316,42 @@ FP8Q_API fp8q_status mxfp8_quantize_rule(const void* x, int32_t dt, int64_t rows
                                          unsigned long long* sat_count, void* stream);
 
 /*
+ * Scale layouts of mxfp8_quantize_ex.  FP8Q_SCALES_ROW_MAJOR is the layout of
+ * mxfp8_quantize.  FP8Q_SCALES_MMA_128X4 writes the same scales straight into
+ * the 128 x 4 block layout that block-scaled tensor-core MMA reads, the
+ * layout mx_scales_to_mma_layout produces from row-major scales (the pages
+ * give none; "Blackwell GPU MXFP8 预训练最佳实践" 3.2 only says the tensor
+ * cores take the MX types natively): the scale matrix is padded to 128-row
+ * and 4-column multiples and cut into 512-byte blocks, stored block row by
+ * block row; scale (r, c) sits at byte (r % 32) * 16 + (r / 32 % 4) * 4 +
+ * c % 4 of its block.  Padding bytes are 0.
+ */
+typedef enum { FP8Q_SCALES_ROW_MAJOR = 0, FP8Q_SCALES_MMA_128X4 = 1 } fp8q_scale_layout;
+
+/* Bytes of a scale matrix of rows x scale_cols in the 128 x 4 block layout:
+ * ceil(rows / 128) * 128 * ceil(scale_cols / 4) * 4 (-1 for negative sizes). */
+FP8Q_API int64_t mxfp8_mma_scale_bytes(int64_t rows, int64_t scale_cols);
+
+/*
+ * mxfp8_quantize_rule with a choice of scale layout (fp8q_scale_layout).
+ * Under FP8Q_SCALES_MMA_128X4:
+ *   s_row  device uint8[mxfp8_mma_scale_bytes(rows, cols / 32)]
+ *   s_col  device uint8[mxfp8_mma_scale_bytes(cols, s_col_ld)], the columnwise
+ *          scales as a cols x s_col_ld matrix; s_col_ld must be the column
+ *          block count itself (mxfp8_col_blocks; checked without groups, a
+ *          precondition with groups), so that no block index is padding
+ * Both are written in full: the kernels store every scale and, for shapes
+ * with padding (rows or cols not a multiple of 128, cols / 32 or s_col_ld
+ * not a multiple of 4) and for FP32 input, the call clears the buffer with
+ * one cudaMemsetAsync first.  Other arguments as mxfp8_quantize_rule.
+ */
+FP8Q_API fp8q_status mxfp8_quantize_ex(const void* x, int32_t dt, int64_t rows, int64_t cols,
+                                       const int64_t* group_offsets, int32_t num_groups, int32_t fmt,
+                                       int32_t dir, int32_t scale_rule, int32_t scale_layout, uint8_t* q_row,
+                                       uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int64_t s_col_ld,
+                                       unsigned long long* sat_count, void* stream);
+
+/*
  * MXFP4 / MXFP6 quantization ("混合精度与 FP8 训练" 13.1-13.2; "Blackwell
  * GPU MXFP8 预训练最佳实践" 3.2 and 4.1): blocks of 32 elements with one E8M0
  * scale, as mxfp8_quantize_rule but with element format elem (FP8Q_E2M1,

@@ -30,6 +30,7 @@ __all__ = [
     "RULE_UP", "RULE_OCP", "BLOCK_1X128", "BLOCK_128X128", "fp8q_quantize_blockwise", "fp8q_quantize_nvfp4",
     "fp8q_qstats_workspace_bytes", "fp8q_qstats_per_tensor", "mxfp8_qstats", "qstats_dict",
     "E2M1", "E2M3", "E3M2", "mx_quantize_fp4_fp6", "mx_scales_to_mma_layout",
+    "SCALES_ROW_MAJOR", "SCALES_MMA", "mxfp8_mma_scale_bytes",
 ]
 
 E4M3 = 0
@@ -41,6 +42,8 @@ ROW = 1
 COL = 2
 BOTH = 3
 MAX_GROUPS = 4096
+SCALES_ROW_MAJOR = 0  # MX scale layouts (mxfp8_quantize scale_layout)
+SCALES_MMA = 1        # the 128 x 4 blocks of block-scaled tensor-core MMA
 RULE_UP = 0   # MX scale rule: X = ceil(log2(amax / destmax))
 RULE_OCP = 1  # MX scale rule: X = floor(log2(amax)) - e_max (can saturate)
 BLOCK_1X128 = 1      # blockwise groups: 1x128 (rowwise copy) / 128x1 (transposed copy)
@@ -56,6 +59,9 @@ _SIGS = {
     "fp8q_scale_from_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int32, _c.c_int32, _P, _P, _P]),
     "mxfp8_quantize_rule": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32,
                                        _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_int64, _P, _P]),
+    "mxfp8_quantize_ex": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32,
+                                     _c.c_int32, _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_int64, _P, _P]),
+    "mxfp8_mma_scale_bytes": (_c.c_int64, [_c.c_int64, _c.c_int64]),
     "fp8q_quantize_blockwise": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.c_int32,
                                            _c.c_int32, _c.c_int32, _P, _P, _P, _P, _P]),
     "fp8q_quantize_nvfp4": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _P, _P, _P, _P]),
@@ -366,28 +372,39 @@ def mxfp8_col_blocks(rows: int, group_offsets=None) -> int:
     return n
 
 
+def mxfp8_mma_scale_bytes(rows: int, scale_cols: int) -> int:
+    """Bytes of a rows x scale_cols scale matrix in the 128 x 4 block layout."""
+    return int(lib().mxfp8_mma_scale_bytes(rows, scale_cols))
+
+
 def mxfp8_quantize(x: torch.Tensor, fmt: int = E4M3, direction: int = BOTH, group_offsets=None,
                    s_col_ld: int | None = None, out: dict | None = None, rule: int = RULE_UP,
-                   count_saturation: bool = False) -> dict:
+                   count_saturation: bool = False, scale_layout: int = SCALES_ROW_MAJOR) -> dict:
     """MXFP8 rowwise and/or columnwise quantization of a 2-D tensor.
 
     Returns dict(q_row [rows, cols], s_row [rows, cols/32], q_col [cols, rows],
     s_col [cols, s_col_ld]) (uint8; unused direction -> None).  The default
     s_col_ld is ceil(rows / 32) without groups, and the column-block count
     rounded up to a multiple of 16 with groups (the padding is not written).
+    scale_layout SCALES_MMA writes both scale arrays in the 128 x 4 block
+    layout of block-scaled MMA instead (flat uint8 tensors of
+    mxfp8_mma_scale_bytes bytes; s_col_ld is then the column-block count).
     """
     _check_input(x)
     rows, cols = _as_2d(x)
     off, G = _offsets(group_offsets, x.device)
     dev = x.device
+    mma = scale_layout == SCALES_MMA
     if s_col_ld is None:
         if group_offsets is None:
             s_col_ld = (rows + 31) // 32
         else:
             host = group_offsets.cpu() if isinstance(group_offsets, torch.Tensor) else group_offsets
-            # padded to 16 bytes: scale rows then start aligned, which lets
-            # the kernel store a column's scales in whole 8-byte words
-            s_col_ld = (mxfp8_col_blocks(rows, host) + 15) // 16 * 16
+            s_col_ld = mxfp8_col_blocks(rows, host)
+            if not mma:
+                # padded to 16 bytes: scale rows then start aligned, which
+                # lets the kernel store a column's scales in whole 8-byte words
+                s_col_ld = (s_col_ld + 15) // 16 * 16
     o = out or {}
 
     def buf(name, shape):
@@ -397,29 +414,27 @@ def mxfp8_quantize(x: torch.Tensor, fmt: int = E4M3, direction: int = BOTH, grou
     q_row = s_row = q_col = s_col = None
     if direction & ROW:
         q_row = buf("q_row", (rows, cols))
-        s_row = buf("s_row", (rows, cols // 32 if cols % 32 == 0 else 0))
+        nsc = cols // 32 if cols % 32 == 0 else 0
+        s_row = buf("s_row", (mxfp8_mma_scale_bytes(rows, nsc),) if mma else (rows, nsc))
     if direction & COL:
         q_col = buf("q_col", (cols, rows))
-        s_col = buf("s_col", (cols, max(s_col_ld, 1)))
+        s_col = buf("s_col", (mxfp8_mma_scale_bytes(cols, s_col_ld),) if mma else (cols, max(s_col_ld, 1)))
     sat = o.get("sat")
     if count_saturation and sat is None:
         sat = torch.empty(2, dtype=torch.int64, device=dev)
-    if rule == RULE_UP and not count_saturation:
+    if rule == RULE_UP and not count_saturation and not mma:
         _check(lib().mxfp8_quantize(_ptr(x), _dt(x), rows, cols, _ptr(off), G, fmt, direction,
                                     _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), s_col_ld, _stream()),
                "mxfp8_quantize")
     else:
-        _check(lib().mxfp8_quantize_rule(_ptr(x), _dt(x), rows, cols, _ptr(off), G, fmt, direction, rule,
-                                         _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), s_col_ld,
-                                         _ptr(sat) if count_saturation else None, _stream()),
-               "mxfp8_quantize_rule")
+        _check(lib().mxfp8_quantize_ex(_ptr(x), _dt(x), rows, cols, _ptr(off), G, fmt, direction, rule, scale_layout,
+                                       _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), s_col_ld,
+                                       _ptr(sat) if count_saturation else None, _stream()),
+               "mxfp8_quantize_ex")
     return {"q_row": q_row, "s_row": s_row, "q_col": q_col, "s_col": s_col, "s_col_ld": s_col_ld,
             "sat": sat if count_saturation else None}
 
 
-# ---------------------------------------------------------------------------
-# dequantization
-# ---------------------------------------------------------------------------
 def _out_dtype(out_dtype) -> int:
     if out_dtype == torch.bfloat16:
         return 0

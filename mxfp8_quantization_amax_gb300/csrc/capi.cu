@@ -335,7 +335,22 @@ fp8q_status mxfp8_quantize_rule(const void* x, int32_t dt, int64_t rows, int64_t
                                 const int64_t* group_offsets, int32_t num_groups, int32_t fmt, int32_t dir,
                                 int32_t scale_rule, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                                 uint8_t* s_col, int64_t s_col_ld, unsigned long long* sat_count, void* stream) {
+  return mxfp8_quantize_ex(x, dt, rows, cols, group_offsets, num_groups, fmt, dir, scale_rule,
+                           FP8Q_SCALES_ROW_MAJOR, q_row, s_row, q_col, s_col, s_col_ld, sat_count, stream);
+}
+
+int64_t mxfp8_mma_scale_bytes(int64_t rows, int64_t scale_cols) {
+  if (rows < 0 || scale_cols < 0) return -1;
+  return (rows + 127) / 128 * 128 * ((scale_cols + 3) / 4 * 4);
+}
+
+fp8q_status mxfp8_quantize_ex(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
+                              int32_t num_groups, int32_t fmt, int32_t dir, int32_t scale_rule,
+                              int32_t scale_layout, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                              int64_t s_col_ld, unsigned long long* sat_count, void* stream) {
   g_err[0] = 0;
+  if (scale_layout != FP8Q_SCALES_ROW_MAJOR && scale_layout != FP8Q_SCALES_MMA_128X4)
+    return fail(FP8Q_ERR_INVALID_ARG, "scale_layout must be FP8Q_SCALES_ROW_MAJOR or FP8Q_SCALES_MMA_128X4");
   if (scale_rule != FP8Q_MX_RULE_UP && scale_rule != FP8Q_MX_RULE_OCP)
     return fail(FP8Q_ERR_INVALID_ARG, "scale_rule must be FP8Q_MX_RULE_UP or FP8Q_MX_RULE_OCP");
   if (!aligned(sat_count, 8)) return fail(FP8Q_ERR_INVALID_ARG, "sat_count must be 8-byte aligned");
@@ -360,9 +375,26 @@ fp8q_status mxfp8_quantize_rule(const void* x, int32_t dt, int64_t rows, int64_t
     if (s_col_ld < (rows + 31) / 32)
       return fail(FP8Q_ERR_INVALID_ARG, "s_col_ld (%lld) is below ceil(rows / 32) = %lld", (long long)s_col_ld,
                   (long long)((rows + 31) / 32));
+    if (scale_layout == FP8Q_SCALES_MMA_128X4 && group_offsets == nullptr && s_col_ld != (rows + 31) / 32)
+      return fail(FP8Q_ERR_INVALID_ARG, "in the MMA layout s_col_ld is the column block count, ceil(rows / 32)");
+  }
+  if (scale_layout == FP8Q_SCALES_MMA_128X4) {
+    // The kernels write every scale; the layout's padding (rows past a
+    // multiple of 128, scale columns past a multiple of 4) is cleared here,
+    // only for shapes that have some, and for the FP32 path.
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((dir & MXFP8_ROW) && (rows % 128 != 0 || (cols / 32) % 4 != 0 || dt == FP8Q_IN_FP32)) {
+      cudaError_t e = cudaMemsetAsync(s_row, 0, (size_t)mxfp8_mma_scale_bytes(rows, cols / 32), st);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(s_row padding)");
+    }
+    if ((dir & MXFP8_COL) && (cols % 128 != 0 || s_col_ld % 4 != 0 || dt == FP8Q_IN_FP32)) {
+      cudaError_t e = cudaMemsetAsync(s_col, 0, (size_t)mxfp8_mma_scale_bytes(cols, s_col_ld), st);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(s_col padding)");
+    }
   }
   return launch_mx(x, dt, rows, cols, group_offsets, num_groups, fmt, dir, q_row, s_row, q_col, s_col, s_col_ld,
-                   scale_rule == FP8Q_MX_RULE_UP ? 1 : 0, sat_count, (cudaStream_t)stream);
+                   scale_rule == FP8Q_MX_RULE_UP ? 1 : 0, sat_count, scale_layout == FP8Q_SCALES_MMA_128X4,
+                   (cudaStream_t)stream);
 }
 
 fp8q_status fp8q_quantize_blockwise(const void* x, int32_t dt, int64_t rows, int64_t cols, int32_t fmt,

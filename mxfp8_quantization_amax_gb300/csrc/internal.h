@@ -126,7 +126,7 @@ fp8q_status launch_nvfp4(const void* x, int dt, int64_t rows, int64_t cols, cons
 fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* off, int G,
                       int fmt, int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                       uint8_t* s_col, int64_t s_col_ld, int round_up, unsigned long long* sat,
-                      cudaStream_t stream);
+                      int mma_layout, cudaStream_t stream);
 
 // Device failure words of the MXFP8 pipeline (synchronizes `stream`) and
 // of the per-tensor pipeline, and their wait budgets.

@@ -90,7 +90,46 @@ struct MxParams {
   int64_t s_col_ld;
   int round_up;              // scale rule: 1 round-up (default), 0 OCP round-down
   unsigned long long* sat;   // saturated-element counts [row, col], or nullptr
+  // scale layout: 0 row-major ([rows][cols/32], [cols][s_col_ld]); 1 the
+  // 128 x 4 blocks of block-scaled MMA, with row_bcols / col_bcols blocks
+  // per block row (ceil(cols/32 / 4), ceil(s_col_ld / 4))
+  int mma;
+  int64_t row_bcols, col_bcols;
 };
+
+// Byte of scale (r, c) in the 128 x 4 block layout: blocks of 128 scale
+// rows x 4 scale columns (512 bytes) stored block row by block row, and in
+// a block (r, c) at (r % 32) * 16 + (r / 32 % 4) * 4 + c % 4.
+__device__ __forceinline__ int64_t mma_off(int64_t r, int64_t c, int64_t bcols) {
+  return ((r >> 7) * bcols + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+
+// Where column c's scale of block gb goes: the aligned window holding it
+// (8 bytes of a row-major s_col row, or one 4-byte row of an MMA block), the
+// byte's place `q` in that window and the block index of the window's first
+// byte.  Consecutive blocks of a column fill a window from q = 0 to W - 1.
+struct ScaleSlot {
+  uint8_t* win;
+  int q;
+  int64_t gbw;
+};
+template <bool MMA>
+__device__ __forceinline__ ScaleSlot col_scale_slot(const MxParams& p, int64_t c, int64_t gb) {
+  ScaleSlot sl;
+  if constexpr (MMA) {
+    sl.q = (int)(gb & 3);
+    sl.gbw = gb - sl.q;
+    sl.win = p.s_col + mma_off(c, sl.gbw, p.col_bcols);
+  } else {
+    uint8_t* d = p.s_col + c * p.s_col_ld + gb;
+    sl.q = (int)((uintptr_t)d & 7u);
+    sl.gbw = gb - sl.q;
+    sl.win = d - sl.q;
+  }
+  return sl;
+}
+template <bool MMA>
+__device__ __forceinline__ constexpr int col_scale_window() { return MMA ? 4 : 8; }
 
 // Clamped group boundary: offsets outside [0, rows] are pulled back in, so
 // blocks never leave the tensor whatever the caller passes.
@@ -521,6 +560,7 @@ __device__ __forceinline__ uint32_t row_block_bf16(const MxParams& p, const Tile
 
 // s_row bytes of one warp's 8 rows: lane l holds row 8w + l % 8, blocks
 // l / 8 (byte0) and 4 + l / 8 (byte1).  All 32 lanes must call.
+template <bool MMA>
 __device__ __forceinline__ void store_row_scales(const MxParams& p, const Tile& t, int warp, int lane,
                                                  uint32_t byte0, uint32_t byte1, const StorePolicy& sp) {
   const int r = 8 * warp + (lane & 7);
@@ -533,6 +573,27 @@ __device__ __forceinline__ void store_row_scales(const MxParams& p, const Tile& 
   const uint32_t v2 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 16);
   const uint32_t v3 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 24);
   if (r < t.lo || r >= t.nr) return;
+  if constexpr (MMA) {  // two 4-byte rows of MMA blocks: scale columns sc .. sc + 3 and sc + 4 .. sc + 7
+    if (lane < 8) {
+      const uint32_t lo = (v & 0xFFu) | ((v1 & 0xFFu) << 8) | ((v2 & 0xFFu) << 16) | ((v3 & 0xFFu) << 24);
+      const uint32_t hi = (v >> 8) | ((v1 >> 8) << 8) | ((v2 >> 8) << 16) | ((v3 >> 8) << 24);
+      const int64_t row = t.r0 + r, sc = t.c0 / 32;
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        const int64_t c = sc + 4 * h;
+        const int64_t nvalid = min((int64_t)4, sld - c);
+        if (nvalid <= 0) break;
+        uint8_t* d = p.s_row + mma_off(row, c, p.row_bcols);
+        const uint32_t w = h ? hi : lo;
+        if (nvalid == 4) {
+          st_scale32(d, w, sp);
+        } else {
+          for (int i = 0; i < nvalid; i++) st_scale8(d + i, w >> (8 * i), sp);
+        }
+      }
+    }
+    return;
+  }
   if (t.nc == kTileCols && ((uintptr_t)dst & 7u) == 0) {
     if (lane < 8) {
       const uint64_t lo = (v & 0xFFu) | ((v1 & 0xFFu) << 8) | ((v2 & 0xFFu) << 16) | ((v3 & 0xFFu) << 24);
@@ -702,7 +763,9 @@ __device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit&
 
 // EXT: the scale rule and saturation counting of mxfp8_quantize_rule; the
 // plain instantiation (round-up rule, no counting) carries none of that code.
-template <int FMT, int DIR, bool EXT>
+// MMA: scales in the 128 x 4 block layout of block-scaled MMA (a template
+// parameter, so the row-major instantiations carry none of its code).
+template <int FMT, int DIR, bool EXT, bool MMA>
 __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(const __grid_constant__ CUtensorMap tmap, MxParams p) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t full[kStages], empty[kStages];
@@ -783,7 +846,7 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(c
         const int r = 8 * warp + (lane & 7);
         const uint32_t y0 = row_block_bf16<FMT, EXT, false>(p, t, stage, r, lane >> 3, sp, nsat_r);
         const uint32_t y1 = row_block_bf16<FMT, EXT, false>(p, t, stage, r, 4 + (lane >> 3), sp, nsat_r);
-        store_row_scales(p, t, warp, lane, y0, y1, sp);
+        store_row_scales<MMA>(p, t, warp, lane, y0, y1, sp);
       }
       if constexpr (DIR & MXFP8_COL) {
         if (2 * tid < t.nc) {
@@ -791,20 +854,20 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(c
           // scale bytes go to s_col[c][gb0 + j]; they are gathered in the
           // 8-byte aligned window of the destination and leave when the
           // window is complete or the unit ends
-          uint8_t* d0 = p.s_col + (U.c0 + 2 * tid) * p.s_col_ld + U.gb0 + j;
-          uint8_t* d1 = d0 + p.s_col_ld;
-          const int q0 = (int)((uintptr_t)d0 & 7u), q1 = (int)((uintptr_t)d1 & 7u);
-          sc0 |= (uint64_t)(b & 0xFFu) << (8 * q0);
-          sc1 |= (uint64_t)(b >> 8) << (8 * q1);
+          const ScaleSlot e0 = col_scale_slot<MMA>(p, U.c0 + 2 * tid, U.gb0 + j);
+          const ScaleSlot e1 = col_scale_slot<MMA>(p, U.c0 + 2 * tid + 1, U.gb0 + j);
+          constexpr int W = col_scale_window<MMA>();
+          sc0 |= (uint64_t)(b & 0xFFu) << (8 * e0.q);
+          sc1 |= (uint64_t)(b >> 8) << (8 * e1.q);
           const bool last = j == U.nblk - 1;
-          if (q0 == 7 || last) {
-            const int from = j < q0 ? q0 - j : 0;  // window bytes before the unit's first block
-            flush_scales8(p, d0 - q0, from, q0 + 1, U.gb0 + j - q0, sc0, sp);
+          if (e0.q == W - 1 || last) {
+            const int from = j < e0.q ? e0.q - j : 0;  // window bytes before the unit's first block
+            flush_scales8(p, e0.win, from, e0.q + 1, e0.gbw, sc0, sp);
             sc0 = 0;
           }
-          if (q1 == 7 || last) {
-            const int from = j < q1 ? q1 - j : 0;
-            flush_scales8(p, d1 - q1, from, q1 + 1, U.gb0 + j - q1, sc1, sp);
+          if (e1.q == W - 1 || last) {
+            const int from = j < e1.q ? e1.q - j : 0;
+            flush_scales8(p, e1.win, from, e1.q + 1, e1.gbw, sc1, sp);
             sc1 = 0;
           }
         }
@@ -922,7 +985,7 @@ __device__ __forceinline__ void stream_append(uint8_t* dst, uint32_t (&prev)[8],
   }
 }
 
-template <int FMT, int DIR, bool EXT>
+template <int FMT, int DIR, bool EXT, bool MMA>
 __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_band_kernel(const __grid_constant__ CUtensorMap tmap, MxParams p) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t full[kStages], empty[kStages];
@@ -1026,7 +1089,7 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_band_kernel(
         const int r = 8 * warp + (lane & 7);
         const uint32_t y0 = row_block_bf16<FMT, EXT, true>(p, t, stage, r, lane >> 3, sp, nsat_r);
         const uint32_t y1 = row_block_bf16<FMT, EXT, true>(p, t, stage, r, 4 + (lane >> 3), sp, nsat_r);
-        store_row_scales(p, t, warp, lane, y0, y1, sp);
+        store_row_scales<MMA>(p, t, warp, lane, y0, y1, sp);
       }
       if constexpr (DIR & MXFP8_COL) {
         if (2 * tid < nc) {
@@ -1050,19 +1113,18 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_band_kernel(
             // scale bytes go to s_col[c][gb]; gathered in the 8-byte aligned
             // window of the destination, stored when the window is complete
             // or the unit ends
-            uint8_t* d0p = p.s_col + col * p.s_col_ld + bb.gb;
-            uint8_t* d1p = d0p + p.s_col_ld;
-            const int q0 = (int)((uintptr_t)d0p & 7u), q1 = (int)((uintptr_t)d1p & 7u);
-            sc0 |= (uint64_t)(b & 0xFFu) << (8 * q0);
-            sc1 |= (uint64_t)(b >> 8) << (8 * q1);
-            if (q0 == 7 || last) {
-              const int from = nown < q0 ? q0 - nown : 0;  // window bytes before the unit's first scale
-              flush_scales8(p, d0p - q0, from, q0 + 1, bb.gb - q0, sc0, sp);
+            const ScaleSlot e0 = col_scale_slot<MMA>(p, col, bb.gb), e1 = col_scale_slot<MMA>(p, col + 1, bb.gb);
+            constexpr int W = col_scale_window<MMA>();
+            sc0 |= (uint64_t)(b & 0xFFu) << (8 * e0.q);
+            sc1 |= (uint64_t)(b >> 8) << (8 * e1.q);
+            if (e0.q == W - 1 || last) {
+              const int from = nown < e0.q ? e0.q - nown : 0;  // window bytes before the unit's first scale
+              flush_scales8(p, e0.win, from, e0.q + 1, e0.gbw, sc0, sp);
               sc0 = 0;
             }
-            if (q1 == 7 || last) {
-              const int from = nown < q1 ? q1 - nown : 0;
-              flush_scales8(p, d1p - q1, from, q1 + 1, bb.gb - q1, sc1, sp);
+            if (e1.q == W - 1 || last) {
+              const int from = nown < e1.q ? e1.q - nown : 0;
+              flush_scales8(p, e1.win, from, e1.q + 1, e1.gbw, sc1, sp);
               sc1 = 0;
             }
             ++nown;
@@ -1142,7 +1204,10 @@ __global__ void __launch_bounds__(kConsumers) mx_f32_kernel(MxParams p) {
                                       __uint_as_float(v[i][1].z), __uint_as_float(v[i][1].w), mult), byte, am);
           const int64_t row = t.r0 + r;
           st_stream(p.q_row + row * p.cols + t.c0 + lane * 8, o);
-          if ((lane & 3) == 0) p.s_row[row * (p.cols / 32) + (t.c0 + lane * 8) / 32] = (uint8_t)byte;
+          if ((lane & 3) == 0) {
+            const int64_t sc = (t.c0 + lane * 8) / 32;
+            p.s_row[p.mma ? mma_off(row, sc, p.row_bcols) : row * (p.cols / 32) + sc] = (uint8_t)byte;
+          }
         }
       }
       if constexpr (DIR & MXFP8_COL) {
@@ -1189,8 +1254,8 @@ __global__ void __launch_bounds__(kConsumers) mx_f32_kernel(MxParams p) {
         store_col32(p.q_col + c * p.rows + t.r0, d0, t.nr, sp);
         store_col32(p.q_col + (c + 1) * p.rows + t.r0, d1, t.nr, sp);
         if (U.gb0 < p.s_col_ld) {
-          p.s_col[c * p.s_col_ld + U.gb0] = (uint8_t)b0;
-          p.s_col[(c + 1) * p.s_col_ld + U.gb0] = (uint8_t)b1;
+          p.s_col[p.mma ? mma_off(c, U.gb0, p.col_bcols) : c * p.s_col_ld + U.gb0] = (uint8_t)b0;
+          p.s_col[p.mma ? mma_off(c + 1, U.gb0, p.col_bcols) : (c + 1) * p.s_col_ld + U.gb0] = (uint8_t)b1;
         }
       }
       __syncthreads();  // the tile is rewritten by the next unit
@@ -1238,7 +1303,7 @@ static fp8q_status ctas_per_sm(K kernel, int threads, size_t smem, size_t* attr,
   return FP8Q_OK;
 }
 
-template <int FMT, int DIR, bool EXT, bool BAND>
+template <int FMT, int DIR, bool EXT, bool BAND, bool MMA>
 static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
   auto enc = encode_fn();
   if (!enc) return fail(FP8Q_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -1254,7 +1319,7 @@ static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
   MxParams q = p;
   q.super = BAND ? 1 : (p.off != nullptr ? FP8Q_MX_SUPER_GROUPED : FP8Q_MX_SUPER);
   const size_t smem = 1024 + (size_t)kStages * kStageBytes + 2 * sizeof(int) * (p.G + 1);
-  auto kernel = BAND ? mx_band_kernel<FMT, DIR, EXT> : mx_tma_kernel<FMT, DIR, EXT>;
+  auto kernel = BAND ? mx_band_kernel<FMT, DIR, EXT, MMA> : mx_tma_kernel<FMT, DIR, EXT, MMA>;
   static size_t attr = 0;
   static int per_sm_cache = 0;
   static std::mutex mu;
@@ -1297,11 +1362,21 @@ static fp8q_status launch_f32(const MxParams& p, cudaStream_t s) {
 #define FP8Q_MX_BAND_UNGROUPED 0
 #endif
 
-template <int FMT, bool EXT, bool BAND>
+template <int FMT, bool EXT, bool BAND, bool MMA>
 static fp8q_status launch_tma_dir(const MxParams& p, int dir, cudaStream_t s) {
-  if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW, EXT, BAND>(p, s);
-  if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL, EXT, BAND>(p, s);
-  return launch_tma<FMT, MXFP8_BOTH, EXT, BAND>(p, s);
+  if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW, EXT, BAND, MMA>(p, s);
+  if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL, EXT, BAND, MMA>(p, s);
+  return launch_tma<FMT, MXFP8_BOTH, EXT, BAND, MMA>(p, s);
+}
+
+template <int FMT, bool BAND, bool MMA>
+static fp8q_status launch_tma_ext(const MxParams& p, int dir, bool ext, cudaStream_t s) {
+  return ext ? launch_tma_dir<FMT, true, BAND, MMA>(p, dir, s) : launch_tma_dir<FMT, false, BAND, MMA>(p, dir, s);
+}
+
+template <int FMT, bool BAND>
+static fp8q_status launch_tma_layout(const MxParams& p, int dir, bool ext, cudaStream_t s) {
+  return p.mma ? launch_tma_ext<FMT, BAND, true>(p, dir, ext, s) : launch_tma_ext<FMT, BAND, false>(p, dir, ext, s);
 }
 
 template <int FMT>
@@ -1313,13 +1388,12 @@ static fp8q_status launch_fmt(const MxParams& p, int dt, int dir, cudaStream_t s
       MxParams q = p;
       q.off = nullptr;
       q.G = 1;
-      return ext ? launch_tma_dir<FMT, true, false>(q, dir, s) : launch_tma_dir<FMT, false, false>(q, dir, s);
+      return launch_tma_layout<FMT, false>(q, dir, ext, s);
     }
     // bands of aligned rows: every transposed store is a whole aligned sector
     const bool band = (dir & MXFP8_COL) && p.rows % 32 == 0 && ((uintptr_t)p.q_col & 31u) == 0 &&
                       (p.off != nullptr || FP8Q_MX_BAND_UNGROUPED);
-    if (band) return ext ? launch_tma_dir<FMT, true, true>(p, dir, s) : launch_tma_dir<FMT, false, true>(p, dir, s);
-    return ext ? launch_tma_dir<FMT, true, false>(p, dir, s) : launch_tma_dir<FMT, false, false>(p, dir, s);
+    return band ? launch_tma_layout<FMT, true>(p, dir, ext, s) : launch_tma_layout<FMT, false>(p, dir, ext, s);
   }
   if (dir == MXFP8_ROW) return launch_f32<FMT, MXFP8_ROW>(p, s);
   if (dir == MXFP8_COL) return launch_f32<FMT, MXFP8_COL>(p, s);
@@ -1328,7 +1402,7 @@ static fp8q_status launch_fmt(const MxParams& p, int dt, int dir, cudaStream_t s
 
 fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const int64_t* off, int G, int fmt,
                       int dir, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, int64_t s_col_ld,
-                      int round_up, unsigned long long* sat, cudaStream_t stream) {
+                      int round_up, unsigned long long* sat, int mma_layout, cudaStream_t stream) {
   MxParams p{};
   p.x = x;
   p.rows = rows;
@@ -1344,6 +1418,9 @@ fp8q_status launch_mx(const void* x, int dt, int64_t rows, int64_t cols, const i
   p.s_col_ld = s_col_ld;
   p.round_up = round_up;
   p.sat = sat;
+  p.mma = mma_layout;
+  p.row_bcols = (cols / 32 + 3) / 4;
+  p.col_bcols = (s_col_ld + 3) / 4;
   return fmt == kE4M3 ? launch_fmt<kE4M3>(p, dt, dir, stream) : launch_fmt<kE5M2>(p, dt, dir, stream);
 }
 
