@@ -247,7 +247,7 @@ def kernel_label(op):
             "qs_mx_row": f"qstats_lin_kernel<bf16,{fmt_name},mx_row>",
             "qs_mx_col": f"qstats_col_kernel<bf16,{fmt_name}>",
             "qs_tensor": f"qstats_lin_kernel<bf16,{fmt_name},tensor>",
-            "mxlow": f"mxlow_kernel<bf16,{LOW_NAMES.get(op.get('elem'), '')},both>",
+            "mxlow": f"mxlow_tma_kernel<{LOW_NAMES.get(op.get('elem'), '')},both>",
             "mmascale": "mma_scale_kernel",
             "current": f"amax_kernel + cast_kernel<bf16,{fmt_name}>",
             "current_grouped": f"amax_kernel + cast_kernel<bf16,{fmt_name}> ({op.get('G')} groups)",

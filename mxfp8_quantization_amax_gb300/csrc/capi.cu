@@ -90,6 +90,8 @@ static fp8q_status check_common(const void* x, int32_t dt, int64_t rows, int64_t
 static bool fmt_ok(int32_t fmt) { return fmt == FP8Q_E4M3 || fmt == FP8Q_E5M2; }
 
 // MXFP4 / MXFP6 (mxlow.cu).
+fp8q_status low_device_status(bool clear, unsigned* word);
+fp8q_status low_set_wait_budget(unsigned long long ns);
 fp8q_status launch_mxlow(const void* x, int dt, int64_t rows, int64_t cols, int elem, int dir, int round_up,
                          uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, unsigned long long* sat,
                          cudaStream_t stream);
@@ -116,12 +118,13 @@ const char* fp8q_last_error_string(void) { return g_err; }
 
 fp8q_status fp8q_check_device(void* stream) {
   g_err[0] = 0;
-  unsigned mx = 0, pt = 0, bw = 0;
+  unsigned mx = 0, pt = 0, bw = 0, lo = 0;
   fp8q_status r = mx_device_status((cudaStream_t)stream, true, &mx);
   if (r != FP8Q_OK) return r;
   if ((r = pt_device_status(true, &pt)) != FP8Q_OK) return r;
   if ((r = bw_device_status(true, &bw)) != FP8Q_OK) return r;
-  if ((mx | pt | bw) & 1u)
+  if ((r = low_device_status(true, &lo)) != FP8Q_OK) return r;
+  if ((mx | pt | bw | lo) & 1u)
     return fail(FP8Q_ERR_TIMEOUT, "a bounded device-side wait gave up; the outputs of that call are incomplete");
   return FP8Q_OK;
 }
@@ -130,6 +133,7 @@ fp8q_status fp8q_set_wait_budget_ns(uint64_t ns) {
   g_err[0] = 0;
   fp8q_status r = mx_set_wait_budget((unsigned long long)ns);
   if (r == FP8Q_OK) r = pt_set_wait_budget((unsigned long long)ns);
+  if (r == FP8Q_OK) r = low_set_wait_budget((unsigned long long)ns);
   return r != FP8Q_OK ? r : bw_set_wait_budget((unsigned long long)ns);
 }
 

@@ -28,8 +28,19 @@
 // are XOR-swizzled within each 128-byte line so that both read patterns are
 // free of bank conflicts.  Conversions are the hardware
 // cvt.rn.satfinite.{e2m1,e2m3,e3m2}x2 (nearest even, saturating).
+//
+// BF16 input takes a second kernel built like the MXFP8 one: a producer warp
+// streams 32-row x 256-column blocks into a two-stage shared-memory ring with
+// 2-D TMA loads (128-byte swizzle), four consumer warps convert them (a lane
+// per rowwise block, a thread per column pair), four CTAs per SM, units of
+// four blocks down one strip dealt out row band by row band.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "fp8q_device.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace fp8q {
 
@@ -366,6 +377,336 @@ __global__ void __launch_bounds__(kLowThreads, FP8Q_LOW_MIN_CTAS) mxlow_kernel(L
   }
 }
 
+// ---------------------------------------------------------------------------
+// BF16: TMA-fed, warp-specialised kernel
+// ---------------------------------------------------------------------------
+constexpr int kLtCons = 128;                    // four consumer warps
+constexpr int kLtThreads = kLtCons + 32;        // + one producer warp
+constexpr int kLtCols = 256;                    // columns per block (a strip)
+constexpr int kLtSubCols = 64;                  // columns per TMA box (128 bytes)
+constexpr int kLtSubBytes = 32 * 128;           // one box in shared memory
+constexpr int kLtStageBytes = 32 * kLtCols * 2; // one BF16 block: 16 KB
+constexpr int kLtStages = 2;
+constexpr int kLtUnit = 4;                      // blocks per unit
+
+// Failure word (bit 0: a bounded wait gave up) and wait budget of this
+// kernel; read and cleared by fp8q_check_device().
+__device__ unsigned int g_low_error;
+__device__ unsigned long long g_low_budget_ns = 1000000000ull;
+
+// Rowwise: one lane per 1x32 block (row r of the block's 32, column block b
+// of the strip's 8).  Writes the codes, returns the scale byte (0 if the
+// block is not ours).  Stage layout as in the MXFP8 kernel: 16-byte chunk c
+// of row r of a 64-column box sits at chunk c ^ (r % 8).
+template <int EF, bool SAT>
+__device__ __forceinline__ uint32_t lt_row_block(const LowParams& p, const unsigned char* stage, int r, int b,
+                                                 int64_t r0, int nr, int64_t c0, int nc, unsigned long long& nsat) {
+  constexpr bool kFp4 = EF == kE2M1;
+  if (r >= nr || 32 * b >= nc) return 0u;
+  const unsigned char* line = stage + (b >> 1) * kLtSubBytes + r * 128;
+  const int cb = (b & 1) * 4;
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+    const uint4 v = *(const uint4*)(line + (((cb + j) ^ (r & 7)) << 4));
+    w[4 * j] = v.x;
+    w[4 * j + 1] = v.y;
+    w[4 * j + 2] = v.z;
+    w[4 * j + 3] = v.w;
+  }
+  uint32_t m = 0;
+#pragma unroll
+  for (int q = 0; q < 16; q++) m = absmax_nan_bf16x2(m, w[q]);
+  const uint32_t amax = max((m & 0x7FFFu) << 16, m & 0x7FFF0000u);
+  const uint32_t byte = low_scale_byte<EF>(amax, p.round_up);
+  const bool zero = amax == 0u || byte == 0xFFu;
+  const float mul = low_multiplier(byte);
+  const low_f2 M = low_f2_make(mul, mul);
+  uint32_t pr[16];
+#pragma unroll
+  for (int k = 0; k < 16; k++) pr[k] = low_pair<EF, SAT>(low_f2_make(bf16_lo(w[k]), bf16_hi(w[k])), M, !zero, nsat);
+  uint32_t o[8] = {};
+  if (!zero) low_pack<EF>(pr, o);
+  uint8_t* dst = p.q_row + (r0 + r) * (kFp4 ? p.cols / 2 : p.cols) + (c0 / 32 + b) * (kFp4 ? 16 : 32);
+  *(uint4*)dst = make_uint4(o[0], o[1], o[2], o[3]);
+  if constexpr (!kFp4) *(uint4*)(dst + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+  return byte;
+}
+
+// s_row bytes of one warp's 8 rows: lane l holds row 8w + l % 8, blocks
+// l / 8 (y0) and 4 + l / 8 (y1).  All 32 lanes must call.
+__device__ __forceinline__ void lt_row_scales(const LowParams& p, int warp, int lane, int64_t r0, int nr,
+                                              int64_t c0, int nc, uint32_t y0, uint32_t y1) {
+  const int r = 8 * warp + (lane & 7);
+  const uint32_t v = y0 | (y1 << 8);
+  const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 8);
+  const uint32_t v2 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 16);
+  const uint32_t v3 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 24);
+  if (r >= nr) return;
+  uint8_t* dst = p.s_row + (r0 + r) * (p.cols / 32) + c0 / 32;
+  if (nc == kLtCols && ((uintptr_t)dst & 7u) == 0) {
+    if (lane < 8) {
+      const uint64_t lo = (v & 0xFFu) | ((v1 & 0xFFu) << 8) | ((v2 & 0xFFu) << 16) | ((v3 & 0xFFu) << 24);
+      const uint64_t hi = (v >> 8) | ((v1 >> 8) << 8) | ((v2 >> 8) << 16) | ((v3 >> 8) << 24);
+      *(uint64_t*)dst = lo | (hi << 32);
+    }
+    return;
+  }
+  const int b = lane >> 3;
+  if (32 * b < nc) dst[b] = (uint8_t)y0;
+  if (32 * (b + 4) < nc) dst[b + 4] = (uint8_t)y1;
+}
+
+// Columnwise: thread t owns columns 2t and 2t + 1 (one 32-bit word per row).
+// Writes both columns' codes; returns their scale bytes (column 2t in bits
+// 0-7).  Rows past the tensor's end are zeros (TMA fill).
+template <int EF, bool SAT>
+__device__ __forceinline__ uint32_t lt_col_pair(const LowParams& p, const unsigned char* stage, int tid, int64_t r0,
+                                                int nr, int64_t c0, int64_t col_len, bool col_vec,
+                                                unsigned long long& nsat) {
+  constexpr bool kFp4 = EF == kE2M1;
+  const unsigned char* seg = stage + (tid >> 5) * kLtSubBytes + 4 * (tid & 3);
+  const int c = (tid & 31) >> 2;
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; i++) w[i] = *(const uint32_t*)(seg + i * 128 + ((c ^ (i & 7)) << 4));
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 32; i++) m = absmax_nan_bf16x2(m, w[i]);
+  const uint32_t ma = (m & 0x7FFFu) << 16, mb = m & 0x7FFF0000u;
+  const uint32_t ba = low_scale_byte<EF>(ma, p.round_up), bb = low_scale_byte<EF>(mb, p.round_up);
+  const bool za = ma == 0u || ba == 0xFFu, zb = mb == 0u || bb == 0xFFu;
+  const low_f2 Ma = low_f2_make(low_multiplier(ba), low_multiplier(ba));
+  const low_f2 Mb = low_f2_make(low_multiplier(bb), low_multiplier(bb));
+  uint32_t pa[16], pb[16];
+#pragma unroll
+  for (int k = 0; k < 16; k++) {
+    // rows 2k and 2k + 1 of column 2t (low halves) and of column 2t + 1
+    pa[k] = low_pair<EF, SAT>(low_f2_make(bf16_lo(w[2 * k]), bf16_lo(w[2 * k + 1])), Ma, !za, nsat);
+    pb[k] = low_pair<EF, SAT>(low_f2_make(bf16_hi(w[2 * k]), bf16_hi(w[2 * k + 1])), Mb, !zb, nsat);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    uint32_t o[8] = {};
+    if (!(h ? zb : za)) low_pack<EF>(h ? pb : pa, o);
+    uint8_t* dst = p.q_col + (c0 + 2 * tid + h) * col_len + (kFp4 ? r0 / 2 : r0);
+    if (col_vec && nr == 32) {
+      *(uint4*)dst = make_uint4(o[0], o[1], o[2], o[3]);
+      if constexpr (!kFp4) *(uint4*)(dst + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+    } else {
+      const int nbytes = kFp4 ? nr / 2 : nr;
+#pragma unroll
+      for (int k = 0; k < (kFp4 ? 16 : 32); k++)
+        if (k < nbytes) dst[k] = (uint8_t)(o[k >> 2] >> (8 * (k & 3)));
+    }
+  }
+  return ba | (bb << 8);
+}
+
+template <int EF, int DIR, bool SAT>
+__global__ void __launch_bounds__(kLtThreads, 4) mxlow_tma_kernel(const __grid_constant__ CUtensorMap tmap, LowParams p) {
+  constexpr bool kFp4 = EF == kE2M1;
+  extern __shared__ unsigned char lt_smem[];
+  __shared__ uint64_t full[kLtStages], empty[kLtStages];
+  __shared__ volatile int abort_flag;
+  unsigned char* stages = lt_smem + ((1024 - (smem_u32(lt_smem) & 1023)) & 1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kLtStages; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kLtCons / 32);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (tid == kLtCons) prefetch_tensormap(&tmap);
+  pdl_wait();
+  __syncthreads();
+  const int64_t nbr = (p.rows + 31) / 32, strips = (p.cols + kLtCols - 1) / kLtCols;
+  const int64_t units = (nbr + kLtUnit - 1) / kLtUnit * strips;
+  const uint64_t budget = g_low_budget_ns;
+
+  if (warp == kLtCons / 32) {
+    // ---------------- producer ----------------
+    if (lane != 0) return;
+    int64_t k = 0;
+    bool stop = false;
+    for (int64_t u = blockIdx.x; u < units && !abort_flag && !stop; u += gridDim.x) {
+      const int64_t ur = u / strips;
+      const int c0 = (int)((u - ur * strips) * kLtCols);
+      for (int j = 0; j < kLtUnit && ur * kLtUnit + j < nbr; j++, ++k) {
+        const int s = (int)(k % kLtStages);
+        const uint32_t round = (uint32_t)(k / kLtStages);
+        if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, budget)) {
+          atomicOr(&g_low_error, 1u);
+          abort_flag = 1;
+          stop = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kLtStageBytes);
+        unsigned char* dst = stages + s * kLtStageBytes;
+        const int row = (int)((ur * kLtUnit + j) * 32);
+#pragma unroll
+        for (int q = 0; q < kLtCols / kLtSubCols; q++)
+          tma_load_2d(dst + q * kLtSubBytes, &tmap, c0 + q * kLtSubCols, row, &full[s]);
+      }
+    }
+    pdl_launch_dependents();
+    const int64_t first = k > kLtStages ? k - kLtStages : 0;  // every issued copy lands before exit
+    for (int64_t j = first; j < k; j++)
+      mbar_wait(&full[j % kLtStages], (uint32_t)((j / kLtStages) & 1), 2000000000ull);
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  unsigned long long sat_r = 0, sat_c = 0;
+  const int64_t col_len = kFp4 ? p.rows / 2 : p.rows;
+  const bool col_vec = (col_len % 16) == 0 && ((uintptr_t)p.q_col & 15) == 0;
+  int64_t k = 0;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int64_t ur = u / strips;
+    const int64_t c0 = (u - ur * strips) * kLtCols;
+    const int nc = (int)min((int64_t)kLtCols, p.cols - c0);
+    const int64_t rb0 = ur * kLtUnit;
+    const int nblk = (int)min((int64_t)kLtUnit, nbr - rb0);
+    uint32_t sc = 0, sd = 0;  // this thread's two columns' scale bytes over the unit
+    bool gave_up = false;
+    for (int j = 0; j < nblk; j++, ++k) {
+      const int s = (int)(k % kLtStages);
+      const uint32_t round = (uint32_t)(k / kLtStages);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], round & 1u, budget))) {
+        atomicOr(&g_low_error, 1u);
+        abort_flag = 1;
+        gave_up = true;
+        break;
+      }
+      const unsigned char* stage = stages + s * kLtStageBytes;
+      const int64_t r0 = (rb0 + j) * 32;
+      const int nr = (int)min((int64_t)32, p.rows - r0);
+      if constexpr (DIR & MXFP8_ROW) {
+        const int r = 8 * warp + (lane & 7);
+        const uint32_t y0 = lt_row_block<EF, SAT>(p, stage, r, lane >> 3, r0, nr, c0, nc, sat_r);
+        const uint32_t y1 = lt_row_block<EF, SAT>(p, stage, r, 4 + (lane >> 3), r0, nr, c0, nc, sat_r);
+        lt_row_scales(p, warp, lane, r0, nr, c0, nc, y0, y1);
+      }
+      if constexpr (DIR & MXFP8_COL) {
+        if (2 * tid < nc) {
+          const uint32_t b = lt_col_pair<EF, SAT>(p, stage, tid, r0, nr, c0, col_len, col_vec, sat_c);
+          sc |= (b & 0xFFu) << (8 * j);
+          sd |= (b >> 8) << (8 * j);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (gave_up || abort_flag) return;
+    if constexpr (DIR & MXFP8_COL) {
+      if (2 * tid < nc) {  // s_col[c][rb0 .. rb0 + nblk): one word when aligned and whole
+        uint8_t* d0 = p.s_col + (c0 + 2 * tid) * nbr + rb0;
+        uint8_t* d1 = d0 + nbr;
+        if (nblk == kLtUnit && ((uintptr_t)d0 & 3u) == 0 && ((uintptr_t)d1 & 3u) == 0) {
+          *(uint32_t*)d0 = sc;
+          *(uint32_t*)d1 = sd;
+        } else {
+          for (int j = 0; j < nblk; j++) {
+            d0[j] = (uint8_t)(sc >> (8 * j));
+            d1[j] = (uint8_t)(sd >> (8 * j));
+          }
+        }
+      }
+    }
+  }
+  if constexpr (SAT) {
+    const unsigned long long a = warp_sum_u64(sat_r), c = warp_sum_u64(sat_c);
+    if (lane == 0 && a) atomicAdd(p.sat, a);
+    if (lane == 0 && c) atomicAdd(p.sat + 1, c);
+  }
+  pdl_launch_dependents();
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 lt_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  });
+  return fn;
+}
+
+template <int EF, int DIR, bool SAT>
+static cudaError_t lt_launch(const CUtensorMap& map, const LowParams& p, cudaStream_t stream) {
+  auto kernel = mxlow_tma_kernel<EF, DIR, SAT>;
+  constexpr size_t smem = 1024 + (size_t)kLtStages * kLtStageBytes;
+  static bool attr = false;
+  static int per_sm = 1;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kLtThreads, smem) != cudaSuccess ||
+          per_sm < 1)
+        per_sm = 1;
+      attr = true;
+    }
+  }
+  const int64_t units = ((p.rows + 31) / 32 + kLtUnit - 1) / kLtUnit * ((p.cols + kLtCols - 1) / kLtCols);
+  int64_t grid = (int64_t)per_sm * sm_count();
+  if (grid > units) grid = units;
+  if (grid < 1) grid = 1;
+  return launch_kernel(kernel, dim3((unsigned)grid), dim3(kLtThreads), smem, stream, map, p);
+}
+
+template <int EF, bool SAT>
+static cudaError_t lt_launch_dir(const CUtensorMap& map, const LowParams& p, cudaStream_t stream) {
+  if (p.dir == MXFP8_ROW) return lt_launch<EF, MXFP8_ROW, SAT>(map, p, stream);
+  if (p.dir == MXFP8_COL) return lt_launch<EF, MXFP8_COL, SAT>(map, p, stream);
+  return lt_launch<EF, MXFP8_BOTH, SAT>(map, p, stream);
+}
+
+template <int EF>
+static cudaError_t lt_launch_typed(const LowParams& p, cudaStream_t stream, bool* encoded) {
+  auto enc = lt_encode_fn();
+  *encoded = enc != nullptr;
+  if (!enc) return cudaSuccess;
+  CUtensorMap map;
+  cuuint64_t dims[2] = {(cuuint64_t)p.cols, (cuuint64_t)p.rows};
+  cuuint64_t strides[1] = {(cuuint64_t)p.cols * 2};
+  cuuint32_t box[2] = {kLtSubCols, 32};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *encoded = false;
+    return cudaSuccess;
+  }
+  return p.sat ? lt_launch_dir<EF, true>(map, p, stream) : lt_launch_dir<EF, false>(map, p, stream);
+}
+
+fp8q_status low_device_status(bool clear, unsigned* word) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_low_error, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+  if (clear && v) {
+    const unsigned z = 0;
+    e = cudaMemcpyToSymbol(g_low_error, &z, sizeof(z));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+  }
+  *word = v;
+  return FP8Q_OK;
+}
+
+fp8q_status low_set_wait_budget(unsigned long long ns) {
+  cudaError_t e = cudaMemcpyToSymbol(g_low_budget_ns, &ns, sizeof(ns));
+  return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, "cudaMemcpyToSymbol(wait budget)");
+}
+
 template <int DT, int EF>
 static cudaError_t low_launch_typed(const LowParams& p, cudaStream_t stream) {
   constexpr int kTileCols = kLowRowBytes / (DT == kBF16 ? 2 : 4);
@@ -398,6 +739,20 @@ fp8q_status launch_mxlow(const void* x, int dt, int64_t rows, int64_t cols, int 
   p.s_col = s_col;
   p.sat = sat;
   cudaError_t e;
+#ifndef FP8Q_LOW_TMA  // BF16 input through the TMA-fed kernel
+#define FP8Q_LOW_TMA 1
+#endif
+  if (dt == kBF16 && FP8Q_LOW_TMA) {
+    // the TMA kernel needs a tensor map (16-byte aligned x, row pitch a
+    // multiple of 16 bytes: cols % 32 == 0 gives it); it falls back to the
+    // cp.async kernel when the driver cannot encode one
+    bool encoded = false;
+    e = elem == kE2M1 ? lt_launch_typed<kE2M1>(p, stream, &encoded)
+        : elem == kE2M3 ? lt_launch_typed<kE2M3>(p, stream, &encoded)
+                        : lt_launch_typed<kE3M2>(p, stream, &encoded);
+    if (e != cudaSuccess) return cuda_fail(e, "MXFP4/MXFP6 TMA kernel launch");
+    if (encoded) return check_launch("MXFP4/MXFP6 TMA kernel");
+  }
   if (dt == kBF16)
     e = elem == kE2M1 ? low_launch_typed<kBF16, kE2M1>(p, stream)
         : elem == kE2M3 ? low_launch_typed<kBF16, kE2M3>(p, stream)

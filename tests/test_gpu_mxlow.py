@@ -96,3 +96,31 @@ def test_activation_8192_both_copies():
     x = synth.config2(8192, 8192, seed=0)
     for elem in (oracle.E2M1, oracle.E2M3):
         _check(fq, x, elem, 0)
+
+
+@pytest.mark.parametrize("elem", ["e2m1", "e2m3", "e3m2"])
+def test_bf16_specials_each_direction(elem):
+    """BF16 input (the TMA kernel): rows over 2^-133 .. 2^120 (subnormal
+    BF16 inputs, clamped scales), zero, -0, Inf and NaN blocks, values near
+    every rounding midpoint; each direction alone and both, both rules."""
+    fq = require_cuda()
+    rng = np.random.default_rng(45)
+    fmt = ELEMS[elem]
+    x = (rng.standard_normal((96, 320)) * 2.0 ** rng.integers(-133, 120, size=(96, 1))).astype(np.float32)
+    x[3, :] = 0.0
+    x[4, 32:64] = -0.0
+    x[5, 7] = np.inf
+    x[6, 40] = -np.inf
+    x[7, 100] = np.nan
+    x[40:48, 9] = np.nan
+    n = 8 if fmt == oracle.E2M1 else 32
+    mags = [oracle.lp_value(fmt, c) for c in range(n)]
+    mids = np.array([(a + b) / 2 for a, b in zip(mags, mags[1:])], np.float32)
+    x[10, :mids.size] = mids
+    x[10, 31] = mags[-1]
+    x[11, :mids.size] = -mids
+    x[11, 31] = -mags[-1]
+    xb = synth.to_bf16_bits(x)
+    for d in (1, 2, 3):
+        _check(fq, xb, fmt, 0, d)
+        _check(fq, xb, fmt, 1, d)
