@@ -56,6 +56,9 @@
 #ifndef FP8Q_MX_SROW8  // one 8-byte s_row store per row and strip
 #define FP8Q_MX_SROW8 1
 #endif
+#ifndef FP8Q_MX_UNIT_BMUL  // packed BF16 scaling in the unit kernel too
+#define FP8Q_MX_UNIT_BMUL 0
+#endif
 
 namespace fp8q {
 
@@ -753,7 +756,7 @@ __device__ __forceinline__ uint32_t col_pair_bf16(const MxParams& p, const Unit&
                                                   const unsigned char* stage, int tid, const StorePolicy& sp, int j,
                                                   uint32_t (&prev0)[8], uint32_t (&prev1)[8], uint32_t& nsat) {
   uint32_t d0[8], d1[8];
-  const uint32_t b = col_codes_bf16<FMT, EXT, false>(p, t, stage, tid, d0, d1, nsat, 0, kTileRows);
+  const uint32_t b = col_codes_bf16<FMT, EXT, FP8Q_MX_UNIT_BMUL>(p, t, stage, tid, d0, d1, nsat, 0, kTileRows);
   const int64_t col = t.c0 + 2 * tid;
   const int len = (int)min((int64_t)(32 * U.nblk), U.rg1 - U.r_first);
   emit_col_block(p.q_col + col * p.rows + U.r_first, len, j, U.nblk, d0, prev0, sp);
@@ -844,8 +847,8 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(c
       const unsigned char* stage = stages + s * kStageBytes;
       if constexpr (DIR & MXFP8_ROW) {
         const int r = 8 * warp + (lane & 7);
-        const uint32_t y0 = row_block_bf16<FMT, EXT, false>(p, t, stage, r, lane >> 3, sp, nsat_r);
-        const uint32_t y1 = row_block_bf16<FMT, EXT, false>(p, t, stage, r, 4 + (lane >> 3), sp, nsat_r);
+        const uint32_t y0 = row_block_bf16<FMT, EXT, FP8Q_MX_UNIT_BMUL>(p, t, stage, r, lane >> 3, sp, nsat_r);
+        const uint32_t y1 = row_block_bf16<FMT, EXT, FP8Q_MX_UNIT_BMUL>(p, t, stage, r, 4 + (lane >> 3), sp, nsat_r);
         store_row_scales<MMA>(p, t, warp, lane, y0, y1, sp);
       }
       if constexpr (DIR & MXFP8_COL) {
@@ -876,6 +879,222 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(c
       if (lane == 0) mbar_arrive(&empty[s]);
     }
     if (gave_up || abort_flag) return;
+  }
+  if constexpr (EXT) {
+    if (p.sat != nullptr) {  // one atomic per warp and direction
+      const uint32_t a = __reduce_add_sync(0xFFFFFFFFu, nsat_r), c = __reduce_add_sync(0xFFFFFFFFu, nsat_c);
+      if (lane == 0 && a) atomicAdd(p.sat, (unsigned long long)a);
+      if (lane == 0 && c) atomicAdd(p.sat + 1, (unsigned long long)c);
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// BF16, ungrouped, row-major scales: the lean unit kernel
+// ---------------------------------------------------------------------------
+// Same pipeline and units as mx_tma_kernel, for the common case the general
+// kernel carries state for but never uses here: no groups, so every unit is
+// `super` whole blocks from a row multiple of 32 * super, and (when the
+// columnwise copy is written) rows % 32 == 0 with a 32-byte aligned q_col, so
+// every column's 32 codes of a block are one aligned sector.  Output
+// pointers are set up once per unit and advanced per block; a column's scale
+// bytes of the unit leave in one store at its end.  Rowwise only, rows may
+// be ragged (the last block's rows past the end are skipped).
+
+// Rowwise, one lane per 1x32 block: codes of block b of row r of the stage
+// to dst; returns the scale byte.
+template <int FMT, bool EXT>
+__device__ __forceinline__ uint32_t lean_row_block(const MxParams& p, const unsigned char* stage, int r, int b,
+                                                   uint8_t* dst, const StorePolicy& sp, uint32_t& nsat) {
+  const unsigned char* line = stage + (b >> 1) * kSubBytes + r * 128;
+  const int c0 = (b & 1) * 4;
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+    const uint4 v = *(const uint4*)(line + (((c0 + j) ^ (r & 7)) << 4));
+    w[4 * j] = v.x;
+    w[4 * j + 1] = v.y;
+    w[4 * j + 2] = v.z;
+    w[4 * j + 3] = v.w;
+  }
+  uint32_t m4[4];
+#pragma unroll
+  for (int j = 0; j < 4; j++)
+    m4[j] = absmax_nan_bf16x2(absmax_nan_bf16x2(w[4 * j], w[4 * j + 1]), absmax_nan_bf16x2(w[4 * j + 2], w[4 * j + 3]));
+  const uint32_t m = absmax_nan_bf16x2(absmax_nan_bf16x2(m4[0], m4[1]), absmax_nan_bf16x2(m4[2], m4[3]));
+  const uint32_t am = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu) << 16;
+  const uint32_t byte = e8m0_from_amax<FMT>(am, EXT ? p.round_up : 1);
+  const float mult = e8m0_multiplier(byte);
+  uint32_t d[8];
+#pragma unroll
+  for (int k = 0; k < 8; k++) d[k] = row_codes4<FMT, false>(w[2 * k], w[2 * k + 1], mult);
+  if (byte == 0xFFu || am == 0u) {  // Inf/NaN block: 0x7F codes; zero block: +0 codes
+    const uint32_t fill = am == 0u ? 0u : 0x7F7F7F7Fu;
+#pragma unroll
+    for (int k = 0; k < 8; k++) d[k] = fill;
+  } else if constexpr (EXT) {
+    if (p.sat != nullptr && block_saturates<FMT>(am, byte, mult)) {
+#pragma unroll
+      for (int k = 0; k < 16; k++) nsat += sat_pair<FMT>(w[k], mult, mult);
+    }
+  }
+  st_data32(dst, d, sp);
+  return byte;
+}
+
+template <int FMT, int DIR, bool EXT>
+__global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_lean_kernel(const __grid_constant__ CUtensorMap tmap, MxParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t full[kStages], empty[kStages];
+  __shared__ volatile int abort_flag;
+  unsigned char* stages = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers / 32);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (tid == kConsumers) prefetch_tensormap(&tmap);
+  pdl_wait();
+  __syncthreads();
+  const int64_t nbr = (p.rows + 31) / 32;
+  const int S = p.super;
+  const int64_t units = (nbr + S - 1) / S * p.strips;
+  const uint64_t budget = g_wait_budget_ns;
+
+  if (warp == kConsumers / 32) {
+    // ---------------- producer ----------------
+    if (lane != 0) return;
+    int64_t k = 0;
+    const bool stall = *(volatile unsigned*)&g_mx_stall_producer != 0;
+    bool stop = false;
+    for (int64_t u = blockIdx.x; u < units && !abort_flag && !stall && !stop; u += gridDim.x) {
+      const int64_t ti = u / p.strips;
+      const int c0 = (int)((u - ti * p.strips) * kTileCols);
+      const int64_t rb0 = ti * S;
+      const int nblk = (int)min((int64_t)S, nbr - rb0);
+      for (int j = 0; j < nblk; j++, ++k) {
+        const int s = (int)(k % kStages);
+        const uint32_t round = (uint32_t)(k / kStages);
+        if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, budget)) {
+          atomicOr(&g_mx_error, 1u);
+          abort_flag = 1;
+          stop = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        unsigned char* dst = stages + s * kStageBytes;
+        const int row = (int)((rb0 + j) * kTileRows);
+#pragma unroll
+        for (int q = 0; q < kTileCols / kSubCols; q++)
+          tma_load_2d(dst + q * kSubBytes, &tmap, c0 + q * kSubCols, row, &full[s]);
+      }
+    }
+    pdl_launch_dependents();
+    const int64_t first = k > kStages ? k - kStages : 0;  // every issued copy lands before exit
+    for (int64_t j = first; j < k; j++)
+      mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1), 2000000000ull);
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const StorePolicy sp = make_policy();
+  uint32_t nsat_r = 0, nsat_c = 0;
+  const int64_t sld = p.cols / 32;
+  const int r = 8 * warp + (lane & 7);  // rowwise: this lane's row of a block and its two blocks
+  const int b0 = lane >> 3, b1 = 4 + (lane >> 3);
+  int64_t k = 0;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int64_t ti = u / p.strips;
+    const int64_t c0 = (u - ti * p.strips) * kTileCols;
+    const int nc = (int)min((int64_t)kTileCols, p.cols - c0);
+    const int64_t rb0 = ti * S;
+    const int nblk = (int)min((int64_t)S, nbr - rb0);
+    const int64_t row0 = rb0 * kTileRows;
+    // rowwise destinations of block 0; + 32 rows per block
+    uint8_t* qr = p.q_row + (row0 + r) * p.cols + c0;
+    uint8_t* sr = p.s_row + (row0 + r) * sld + c0 / 32;
+    const bool rb0_ok = 32 * b0 < nc, rb1_ok = 32 * b1 < nc;
+    const bool srow8 = nc == kTileCols && (((uintptr_t)sr | (uintptr_t)(32 * sld)) & 7u) == 0;
+    // columnwise: columns c0 + 2 tid and + 1, block 0 at row0
+    const bool col_ok = 2 * tid < nc;
+    uint8_t* qc = p.q_col + (c0 + 2 * tid) * p.rows + row0;
+    uint32_t sc0 = 0, sc1 = 0;
+    bool gave_up = false;
+    for (int j = 0; j < nblk; j++, ++k) {
+      const int s = (int)(k % kStages);
+      const uint32_t round = (uint32_t)(k / kStages);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], round & 1u, budget))) {
+        atomicOr(&g_mx_error, 1u);
+        abort_flag = 1;
+        gave_up = true;
+        break;
+      }
+      const unsigned char* stage = stages + s * kStageBytes;
+      if constexpr (DIR & MXFP8_ROW) {
+        const bool row_ok = row0 + 32 * j + r < p.rows;
+        uint32_t y0 = 0, y1 = 0;
+        if (row_ok && rb0_ok) y0 = lean_row_block<FMT, EXT>(p, stage, r, b0, qr + 32 * b0, sp, nsat_r);
+        if (row_ok && rb1_ok) y1 = lean_row_block<FMT, EXT>(p, stage, r, b1, qr + 32 * b1, sp, nsat_r);
+        // the row's 8 scale bytes gathered into lane r % 8
+        const uint32_t v = y0 | (y1 << 8);
+        const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 8);
+        const uint32_t v2 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 16);
+        const uint32_t v3 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 24);
+        if (row_ok) {
+          if (srow8) {
+            if (lane < 8) {
+              const uint32_t lo = (v & 0xFFu) | ((v1 & 0xFFu) << 8) | ((v2 & 0xFFu) << 16) | ((v3 & 0xFFu) << 24);
+              const uint32_t hi = (v >> 8) | ((v1 >> 8) << 8) | ((v2 >> 8) << 16) | ((v3 >> 8) << 24);
+              st_scale64(sr, (uint64_t)lo | ((uint64_t)hi << 32), sp);
+            }
+          } else {
+            if (rb0_ok) st_scale8(sr + b0, y0, sp);
+            if (rb1_ok) st_scale8(sr + b1, y1, sp);
+          }
+        }
+        qr += 32 * p.cols;
+        sr += 32 * sld;
+      }
+      if constexpr (DIR & MXFP8_COL) {
+        if (col_ok) {
+          Tile t;
+          t.r0 = row0 + 32 * j;
+          t.lo = 0;
+          t.nr = kTileRows;
+          t.c0 = c0;
+          t.nc = nc;
+          uint32_t d0[8], d1[8];
+          const uint32_t b = col_codes_bf16<FMT, EXT, false>(p, t, stage, tid, d0, d1, nsat_c, 0, kTileRows);
+          st_data32(qc + 32 * j, d0, sp);
+          st_data32(qc + p.rows + 32 * j, d1, sp);
+          sc0 |= (b & 0xFFu) << (8 * j);
+          sc1 |= (b >> 8) << (8 * j);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (gave_up || abort_flag) return;
+    if constexpr (DIR & MXFP8_COL) {
+      if (col_ok) {  // s_col[c][rb0 .. rb0 + nblk): one word when whole and aligned
+        uint8_t* e0 = p.s_col + (c0 + 2 * tid) * p.s_col_ld + rb0;
+        uint8_t* e1 = e0 + p.s_col_ld;
+        if (nblk == 4 && (((uintptr_t)e0 | (uintptr_t)e1) & 3u) == 0) {
+          st_scale32(e0, sc0, sp);
+          st_scale32(e1, sc1, sp);
+        } else {
+          for (int j = 0; j < nblk; j++) {
+            st_scale8(e0 + j, sc0 >> (8 * j), sp);
+            st_scale8(e1 + j, sc1 >> (8 * j), sp);
+          }
+        }
+      }
+    }
   }
   if constexpr (EXT) {
     if (p.sat != nullptr) {  // one atomic per warp and direction
@@ -1303,8 +1522,14 @@ static fp8q_status ctas_per_sm(K kernel, int threads, size_t smem, size_t* attr,
   return FP8Q_OK;
 }
 
-template <int FMT, int DIR, bool EXT, bool BAND, bool MMA>
+// Kernel kinds of the BF16 path.
+enum : int { kUnitKernel = 0, kBandKernel = 1, kLeanKernel = 2 };
+
+template <int FMT, int DIR, bool EXT, int KIND, bool MMA>
 static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
+  constexpr bool BAND = KIND == kBandKernel, LEAN = KIND == kLeanKernel;
+  static_assert(!(LEAN && MMA), "the lean kernel writes row-major scales");
+  static_assert(FP8Q_MX_SUPER >= 1 && FP8Q_MX_SUPER <= 4, "a unit's scale bytes of a column fill one word");
   auto enc = encode_fn();
   if (!enc) return fail(FP8Q_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   CUtensorMap map;
@@ -1318,8 +1543,8 @@ static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
   if (r != CUDA_SUCCESS) return fail(FP8Q_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   MxParams q = p;
   q.super = BAND ? 1 : (p.off != nullptr ? FP8Q_MX_SUPER_GROUPED : FP8Q_MX_SUPER);
-  const size_t smem = 1024 + (size_t)kStages * kStageBytes + 2 * sizeof(int) * (p.G + 1);
-  auto kernel = BAND ? mx_band_kernel<FMT, DIR, EXT, MMA> : mx_tma_kernel<FMT, DIR, EXT, MMA>;
+  const size_t smem = 1024 + (size_t)kStages * kStageBytes + (LEAN ? 0 : 2 * sizeof(int) * (p.G + 1));
+  auto kernel = LEAN ? mx_lean_kernel<FMT, DIR, EXT> : BAND ? mx_band_kernel<FMT, DIR, EXT, MMA> : mx_tma_kernel<FMT, DIR, EXT, MMA>;
   static size_t attr = 0;
   static int per_sm_cache = 0;
   static std::mutex mu;
@@ -1328,8 +1553,9 @@ static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
   if (st != FP8Q_OK) return st;
   // units: bands x strips, or (over any valid offsets) blocks per group
   // rounded up to `super`, x strips
-  const int64_t max_units = BAND ? (p.rows + kBandRows - 1) / kBandRows * p.strips
-                                 : ((p.rows + 31) / 32 / q.super + 1 + p.G) * p.strips;
+  const int64_t max_units = BAND   ? (p.rows + kBandRows - 1) / kBandRows * p.strips
+                           : LEAN ? ((p.rows + 31) / 32 + q.super - 1) / q.super * p.strips
+                                  : ((p.rows + 31) / 32 / q.super + 1 + p.G) * p.strips;
   int64_t grid = (int64_t)per_sm * sm_count();
   if (max_units < grid) grid = max_units;
   if (grid < 1) grid = 1;
@@ -1362,38 +1588,47 @@ static fp8q_status launch_f32(const MxParams& p, cudaStream_t s) {
 #define FP8Q_MX_BAND_UNGROUPED 0
 #endif
 
-template <int FMT, bool EXT, bool BAND, bool MMA>
+#ifndef FP8Q_MX_LEAN  // ungrouped BF16 calls with row-major scales take the lean kernel
+#define FP8Q_MX_LEAN 1
+#endif
+
+template <int FMT, bool EXT, int KIND, bool MMA>
 static fp8q_status launch_tma_dir(const MxParams& p, int dir, cudaStream_t s) {
-  if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW, EXT, BAND, MMA>(p, s);
-  if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL, EXT, BAND, MMA>(p, s);
-  return launch_tma<FMT, MXFP8_BOTH, EXT, BAND, MMA>(p, s);
+  if (dir == MXFP8_ROW) return launch_tma<FMT, MXFP8_ROW, EXT, KIND, MMA>(p, s);
+  if (dir == MXFP8_COL) return launch_tma<FMT, MXFP8_COL, EXT, KIND, MMA>(p, s);
+  return launch_tma<FMT, MXFP8_BOTH, EXT, KIND, MMA>(p, s);
 }
 
-template <int FMT, bool BAND, bool MMA>
+template <int FMT, int KIND, bool MMA>
 static fp8q_status launch_tma_ext(const MxParams& p, int dir, bool ext, cudaStream_t s) {
-  return ext ? launch_tma_dir<FMT, true, BAND, MMA>(p, dir, s) : launch_tma_dir<FMT, false, BAND, MMA>(p, dir, s);
+  return ext ? launch_tma_dir<FMT, true, KIND, MMA>(p, dir, s) : launch_tma_dir<FMT, false, KIND, MMA>(p, dir, s);
 }
 
-template <int FMT, bool BAND>
+template <int FMT, int KIND>
 static fp8q_status launch_tma_layout(const MxParams& p, int dir, bool ext, cudaStream_t s) {
-  return p.mma ? launch_tma_ext<FMT, BAND, true>(p, dir, ext, s) : launch_tma_ext<FMT, BAND, false>(p, dir, ext, s);
+  if constexpr (KIND == kLeanKernel) return launch_tma_ext<FMT, KIND, false>(p, dir, ext, s);
+  else
+    return p.mma ? launch_tma_ext<FMT, KIND, true>(p, dir, ext, s) : launch_tma_ext<FMT, KIND, false>(p, dir, ext, s);
 }
 
 template <int FMT>
 static fp8q_status launch_fmt(const MxParams& p, int dt, int dir, cudaStream_t s) {
   if (dt == kBF16) {
     const bool ext = p.round_up == 0 || p.sat != nullptr;
-    if (dir == MXFP8_ROW && p.off != nullptr) {
-      // the rowwise copy does not depend on the groups
-      MxParams q = p;
+    MxParams q = p;
+    if (dir == MXFP8_ROW && p.off != nullptr) {  // the rowwise copy does not depend on the groups
       q.off = nullptr;
       q.G = 1;
-      return launch_tma_layout<FMT, false>(q, dir, ext, s);
     }
+    const bool col_aligned = p.rows % 32 == 0 && ((uintptr_t)p.q_col & 31u) == 0;
+    // no groups and row-major scales: the lean kernel (the columnwise copy
+    // needs every column's blocks on whole aligned sectors)
+    if (FP8Q_MX_LEAN && q.off == nullptr && !q.mma && (!(dir & MXFP8_COL) || col_aligned))
+      return launch_tma_layout<FMT, kLeanKernel>(q, dir, ext, s);
     // bands of aligned rows: every transposed store is a whole aligned sector
-    const bool band = (dir & MXFP8_COL) && p.rows % 32 == 0 && ((uintptr_t)p.q_col & 31u) == 0 &&
-                      (p.off != nullptr || FP8Q_MX_BAND_UNGROUPED);
-    return band ? launch_tma_layout<FMT, true>(p, dir, ext, s) : launch_tma_layout<FMT, false>(p, dir, ext, s);
+    const bool band = (dir & MXFP8_COL) && col_aligned && (q.off != nullptr || FP8Q_MX_BAND_UNGROUPED);
+    return band ? launch_tma_layout<FMT, kBandKernel>(q, dir, ext, s)
+                : launch_tma_layout<FMT, kUnitKernel>(q, dir, ext, s);
   }
   if (dir == MXFP8_ROW) return launch_f32<FMT, MXFP8_ROW>(p, s);
   if (dir == MXFP8_COL) return launch_f32<FMT, MXFP8_COL>(p, s);
