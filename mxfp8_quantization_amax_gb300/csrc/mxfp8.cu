@@ -56,6 +56,12 @@
 #ifndef FP8Q_MX_SROW8  // one 8-byte s_row store per row and strip
 #define FP8Q_MX_SROW8 1
 #endif
+#ifndef FP8Q_MX_LEAN_GRID_ALL  // lean kernel: one CTA per unit instead of a persistent grid
+#define FP8Q_MX_LEAN_GRID_ALL 1
+#endif
+#ifndef FP8Q_MX_BAND_GRID_ALL  // band kernel: one CTA per unit instead of a persistent grid
+#define FP8Q_MX_BAND_GRID_ALL 1
+#endif
 #ifndef FP8Q_MX_UNIT_BMUL  // packed BF16 scaling in the unit kernel too
 #define FP8Q_MX_UNIT_BMUL 0
 #endif
@@ -133,6 +139,14 @@ __device__ __forceinline__ ScaleSlot col_scale_slot(const MxParams& p, int64_t c
 }
 template <bool MMA>
 __device__ __forceinline__ constexpr int col_scale_window() { return MMA ? 4 : 8; }
+// The row-major slot of the scale at d (block gb of its column).
+__device__ __forceinline__ ScaleSlot scale_slot_at(uint8_t* d, int64_t gb) {
+  ScaleSlot sl;
+  sl.q = (int)((uintptr_t)d & 7u);
+  sl.gbw = gb - sl.q;
+  sl.win = d - sl.q;
+  return sl;
+}
 
 // Clamped group boundary: offsets outside [0, rows] are pulled back in, so
 // blocks never leave the tensor whatever the caller passes.
@@ -902,6 +916,26 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_tma_kernel(c
 // bytes of the unit leave in one store at its end.  Rowwise only, rows may
 // be ragged (the last block's rows past the end are skipped).
 
+// Unit u = ti * strips + strip of a CTA's walk u = blockIdx.x, + gridDim.x,
+// ...: (ti, strip) advanced without a 64-bit division per unit.
+struct UnitWalk {
+  int64_t strips, ti, strip, dq, dr;
+  __device__ __forceinline__ explicit UnitWalk(int64_t n) : strips(n) {
+    ti = blockIdx.x / n;
+    strip = blockIdx.x - ti * n;
+    dq = gridDim.x / n;
+    dr = gridDim.x - dq * n;
+  }
+  __device__ __forceinline__ void next() {
+    ti += dq;
+    strip += dr;
+    if (strip >= strips) {
+      strip -= strips;
+      ++ti;
+    }
+  }
+};
+
 // Rowwise, one lane per 1x32 block: codes of block b of row r of the stage
 // to dst; returns the scale byte.
 template <int FMT, bool EXT>
@@ -943,6 +977,30 @@ __device__ __forceinline__ uint32_t lean_row_block(const MxParams& p, const unsi
   return byte;
 }
 
+// Row-major s_row bytes of one warp's 8 rows: lane l holds row 8w + l % 8,
+// blocks l / 8 (y0) and 4 + l / 8 (y1); sr is the lane's row's first scale of
+// the strip.  With a whole, 8-byte aligned strip the row's 8 bytes leave from
+// lane l % 8 in one store.  All 32 lanes must call.
+__device__ __forceinline__ void lean_row_scales(uint8_t* sr, int lane, bool row_ok, bool srow8, bool ok0, bool ok1,
+                                                uint32_t y0, uint32_t y1, const StorePolicy& sp) {
+  const uint32_t v = y0 | (y1 << 8);
+  const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 8);
+  const uint32_t v2 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 16);
+  const uint32_t v3 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 24);
+  if (!row_ok) return;
+  if (srow8) {
+    if (lane < 8) {
+      const uint32_t lo = (v & 0xFFu) | ((v1 & 0xFFu) << 8) | ((v2 & 0xFFu) << 16) | ((v3 & 0xFFu) << 24);
+      const uint32_t hi = (v >> 8) | ((v1 >> 8) << 8) | ((v2 >> 8) << 16) | ((v3 >> 8) << 24);
+      st_scale64(sr, (uint64_t)lo | ((uint64_t)hi << 32), sp);
+    }
+  } else {
+    const int b = lane >> 3;
+    if (ok0) st_scale8(sr + b, y0, sp);
+    if (ok1) st_scale8(sr + b + 4, y1, sp);
+  }
+}
+
 template <int FMT, int DIR, bool EXT>
 __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_lean_kernel(const __grid_constant__ CUtensorMap tmap, MxParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -972,10 +1030,10 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_lean_kernel(
     int64_t k = 0;
     const bool stall = *(volatile unsigned*)&g_mx_stall_producer != 0;
     bool stop = false;
-    for (int64_t u = blockIdx.x; u < units && !abort_flag && !stall && !stop; u += gridDim.x) {
-      const int64_t ti = u / p.strips;
-      const int c0 = (int)((u - ti * p.strips) * kTileCols);
-      const int64_t rb0 = ti * S;
+    UnitWalk w(p.strips);
+    for (int64_t u = blockIdx.x; u < units && !abort_flag && !stall && !stop; u += gridDim.x, w.next()) {
+      const int c0 = (int)(w.strip * kTileCols);
+      const int64_t rb0 = w.ti * S;
       const int nblk = (int)min((int64_t)S, nbr - rb0);
       for (int j = 0; j < nblk; j++, ++k) {
         const int s = (int)(k % kStages);
@@ -1008,11 +1066,11 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_lean_kernel(
   const int r = 8 * warp + (lane & 7);  // rowwise: this lane's row of a block and its two blocks
   const int b0 = lane >> 3, b1 = 4 + (lane >> 3);
   int64_t k = 0;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    const int64_t ti = u / p.strips;
-    const int64_t c0 = (u - ti * p.strips) * kTileCols;
+  UnitWalk w(p.strips);
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x, w.next()) {
+    const int64_t c0 = w.strip * kTileCols;
     const int nc = (int)min((int64_t)kTileCols, p.cols - c0);
-    const int64_t rb0 = ti * S;
+    const int64_t rb0 = w.ti * S;
     const int nblk = (int)min((int64_t)S, nbr - rb0);
     const int64_t row0 = rb0 * kTileRows;
     // rowwise destinations of block 0; + 32 rows per block
@@ -1040,23 +1098,7 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_lean_kernel(
         uint32_t y0 = 0, y1 = 0;
         if (row_ok && rb0_ok) y0 = lean_row_block<FMT, EXT>(p, stage, r, b0, qr + 32 * b0, sp, nsat_r);
         if (row_ok && rb1_ok) y1 = lean_row_block<FMT, EXT>(p, stage, r, b1, qr + 32 * b1, sp, nsat_r);
-        // the row's 8 scale bytes gathered into lane r % 8
-        const uint32_t v = y0 | (y1 << 8);
-        const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 8);
-        const uint32_t v2 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 16);
-        const uint32_t v3 = __shfl_sync(0xFFFFFFFFu, v, (lane & 7) + 24);
-        if (row_ok) {
-          if (srow8) {
-            if (lane < 8) {
-              const uint32_t lo = (v & 0xFFu) | ((v1 & 0xFFu) << 8) | ((v2 & 0xFFu) << 16) | ((v3 & 0xFFu) << 24);
-              const uint32_t hi = (v >> 8) | ((v1 >> 8) << 8) | ((v2 >> 8) << 16) | ((v3 >> 8) << 24);
-              st_scale64(sr, (uint64_t)lo | ((uint64_t)hi << 32), sp);
-            }
-          } else {
-            if (rb0_ok) st_scale8(sr + b0, y0, sp);
-            if (rb1_ok) st_scale8(sr + b1, y1, sp);
-          }
-        }
+        lean_row_scales(sr, lane, row_ok, srow8, rb0_ok, rb1_ok, y0, y1, sp);
         qr += 32 * p.cols;
         sr += 32 * sld;
       }
@@ -1278,6 +1320,11 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_band_kernel(
     const int64_t col = c0 + 2 * tid;
     uint8_t* qc0 = p.q_col + col * p.rows;
     uint8_t* qc1 = qc0 + p.rows;
+    uint8_t* sb0 = p.s_col + col * p.s_col_ld;  // row-major: the columns' scale rows
+    uint8_t* sb1 = sb0 + p.s_col_ld;
+    const int r = 8 * warp + (lane & 7);  // rowwise: this lane's window row and its two blocks
+    const int rb0 = lane >> 3, rb1 = 4 + (lane >> 3);
+    const bool rb0_ok = 32 * rb0 < nc, rb1_ok = 32 * rb1 < nc;
     uint64_t sc0 = 0, sc1 = 0;   // scale bytes of this thread's two columns, gathered per 8-byte window
     uint32_t prev0[8], prev1[8];  // the columns' pending codes (the last `pos` bytes)
     int pos = 0;                  // stream phase: pending codes
@@ -1305,10 +1352,19 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_band_kernel(
       t.nc = nc;
       const unsigned char* stage = stages + s * kStageBytes;
       if constexpr (DIR & MXFP8_ROW) {
-        const int r = 8 * warp + (lane & 7);
-        const uint32_t y0 = row_block_bf16<FMT, EXT, true>(p, t, stage, r, lane >> 3, sp, nsat_r);
-        const uint32_t y1 = row_block_bf16<FMT, EXT, true>(p, t, stage, r, 4 + (lane >> 3), sp, nsat_r);
-        store_row_scales<MMA>(p, t, warp, lane, y0, y1, sp);
+        if constexpr (MMA) {
+          const uint32_t y0 = row_block_bf16<FMT, EXT, true>(p, t, stage, r, rb0, sp, nsat_r);
+          const uint32_t y1 = row_block_bf16<FMT, EXT, true>(p, t, stage, r, rb1, sp, nsat_r);
+          store_row_scales<MMA>(p, t, warp, lane, y0, y1, sp);
+        } else {
+          const bool row_ok = r >= t.lo && r < t.nr;
+          uint8_t* qr = p.q_row + (bb.s + r) * p.cols + c0;
+          uint8_t* sr = p.s_row + (bb.s + r) * (p.cols / 32) + c0 / 32;
+          uint32_t y0 = 0, y1 = 0;
+          if (row_ok && rb0_ok) y0 = lean_row_block<FMT, EXT>(p, stage, r, rb0, qr + 32 * rb0, sp, nsat_r);
+          if (row_ok && rb1_ok) y1 = lean_row_block<FMT, EXT>(p, stage, r, rb1, qr + 32 * rb1, sp, nsat_r);
+          lean_row_scales(sr, lane, row_ok, nc == kTileCols && ((uintptr_t)sr & 7u) == 0, rb0_ok, rb1_ok, y0, y1, sp);
+        }
       }
       if constexpr (DIR & MXFP8_COL) {
         if (2 * tid < nc) {
@@ -1332,7 +1388,8 @@ __global__ void __launch_bounds__(kTmaThreads, FP8Q_MX_MIN_CTAS) mx_band_kernel(
             // scale bytes go to s_col[c][gb]; gathered in the 8-byte aligned
             // window of the destination, stored when the window is complete
             // or the unit ends
-            const ScaleSlot e0 = col_scale_slot<MMA>(p, col, bb.gb), e1 = col_scale_slot<MMA>(p, col + 1, bb.gb);
+            const ScaleSlot e0 = MMA ? col_scale_slot<MMA>(p, col, bb.gb) : scale_slot_at(sb0 + bb.gb, bb.gb);
+            const ScaleSlot e1 = MMA ? col_scale_slot<MMA>(p, col + 1, bb.gb) : scale_slot_at(sb1 + bb.gb, bb.gb);
             constexpr int W = col_scale_window<MMA>();
             sc0 |= (uint64_t)(b & 0xFFu) << (8 * e0.q);
             sc1 |= (uint64_t)(b >> 8) << (8 * e1.q);
@@ -1557,7 +1614,11 @@ static fp8q_status launch_tma(const MxParams& p, cudaStream_t s) {
                            : LEAN ? ((p.rows + 31) / 32 + q.super - 1) / q.super * p.strips
                                   : ((p.rows + 31) / 32 / q.super + 1 + p.G) * p.strips;
   int64_t grid = (int64_t)per_sm * sm_count();
-  if (max_units < grid) grid = max_units;
+  // One CTA per unit (the lean kernel; measured: 16384 x 14336 161 -> 144 us,
+  // the hardware's block scheduler balancing what a strided persistent walk
+  // left uneven), else a persistent grid of every resident slot.
+  if (max_units < grid || (LEAN && FP8Q_MX_LEAN_GRID_ALL) || (BAND && FP8Q_MX_BAND_GRID_ALL)) grid = max_units;
+  if (grid > 0x7FFFFFFF) grid = 0x7FFFFFFF;  // the kernels walk any remaining units
   if (grid < 1) grid = 1;
   const cudaError_t e = launch_kernel(kernel, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, map, q);
   if (e != cudaSuccess) return cuda_fail(e, "mxfp8 tma kernel launch");
