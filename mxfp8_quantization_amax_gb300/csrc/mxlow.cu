@@ -388,6 +388,9 @@ constexpr int kLtSubBytes = 32 * 128;           // one box in shared memory
 constexpr int kLtStageBytes = 32 * kLtCols * 2; // one BF16 block: 16 KB
 constexpr int kLtStages = 2;
 constexpr int kLtUnit = 4;                      // blocks per unit
+#ifndef FP8Q_LOW_GRID_ALL  // one CTA per unit instead of a persistent grid
+#define FP8Q_LOW_GRID_ALL 1
+#endif
 
 // Failure word (bit 0: a bounded wait gave up) and wait budget of this
 // kernel; read and cleared by fp8q_check_device().
@@ -656,8 +659,11 @@ static cudaError_t lt_launch(const CUtensorMap& map, const LowParams& p, cudaStr
     }
   }
   const int64_t units = ((p.rows + 31) / 32 + kLtUnit - 1) / kLtUnit * ((p.cols + kLtCols - 1) / kLtCols);
-  int64_t grid = (int64_t)per_sm * sm_count();
+  // one CTA per unit (the hardware's block scheduler balances the tail), or
+  // a persistent grid of every resident slot
+  int64_t grid = FP8Q_LOW_GRID_ALL ? units : (int64_t)per_sm * sm_count();
   if (grid > units) grid = units;
+  if (grid > 0x7FFFFFFF) grid = 0x7FFFFFFF;  // the kernel walks any remaining units
   if (grid < 1) grid = 1;
   return launch_kernel(kernel, dim3((unsigned)grid), dim3(kLtThreads), smem, stream, map, p);
 }

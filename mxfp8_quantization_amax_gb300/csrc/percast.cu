@@ -567,8 +567,26 @@ static int ctas_per_sm(K kernel) {
 #ifndef FP8Q_PT_BALANCED_GRID  // 1: as few CTAs as give every CTA the same chunk count
 #define FP8Q_PT_BALANCED_GRID 1
 #endif
+// Large tensors: CTAs of FP8Q_PT_CHUNKS_PER_CTA chunks, many waves of them,
+// which the hardware's block scheduler hands out in order as slots free (the
+// CTAs in flight then cover one moving window of the tensor, and the last
+// wave is a small share of the launch).  Measured for amax + cast:
+// 65536 x 7168 with 64 groups 386 -> 358 us, 16384 x 14336 192 -> 179 us.
+// Smaller tensors (fewer than FP8Q_PT_MANY_WAVES waves of such CTAs) keep
+// one wave of resident CTAs with equal contiguous ranges: at 8192 x 8192,
+// 1.7 waves of small CTAs cost 55.8 -> 61.9 us.
+#ifndef FP8Q_PT_CHUNKS_PER_CTA
+#define FP8Q_PT_CHUNKS_PER_CTA 4
+#endif
+#ifndef FP8Q_PT_MANY_WAVES
+#define FP8Q_PT_MANY_WAVES 2
+#endif
 static int grid_for(int64_t n_chunks, int per_sm) {
   const int64_t resident = (int64_t)per_sm * sm_count();
+  if (FP8Q_PT_CHUNKS_PER_CTA > 0 && n_chunks >= (int64_t)FP8Q_PT_MANY_WAVES * FP8Q_PT_CHUNKS_PER_CTA * resident) {
+    const int64_t g = (n_chunks + FP8Q_PT_CHUNKS_PER_CTA - 1) / FP8Q_PT_CHUNKS_PER_CTA;
+    return (int)(g > 0x7FFFFFFF ? 0x7FFFFFFF : g);
+  }
   int64_t g = n_chunks < resident ? n_chunks : resident;
   if (FP8Q_PT_BALANCED_GRID && n_chunks > resident) {
     const int64_t per_cta = (n_chunks + resident - 1) / resident;
