@@ -397,6 +397,78 @@ constexpr int kLtUnit = 4;                      // blocks per unit
 __device__ unsigned int g_low_error;
 __device__ unsigned long long g_low_budget_ns = 1000000000ull;
 
+// Codes of scaled pairs written straight into their output word: E2M1, the
+// four bytes of pairs a..d (each pair's first element in the low nibble);
+// FP6, the two 16-bit halves of pairs a and b.  The conversions write parts
+// of one register, with no masking or byte permutes to join them.
+__device__ __forceinline__ uint32_t lt_fp4_word(low_f2 a, low_f2 b, low_f2 c, low_f2 d) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t.reg .f32 a0, a1, b0, b1, c0, c1, d0, d1;\n\t"
+      "mov.b64 {a0, a1}, %1;\n\tmov.b64 {b0, b1}, %2;\n\tmov.b64 {c0, c1}, %3;\n\tmov.b64 {d0, d1}, %4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, a1, a0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, b1, b0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, c1, c0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, d1, d0;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+      : "=r"(r)
+      : "l"(a), "l"(b), "l"(c), "l"(d));
+  return r;
+}
+template <int EF>
+__device__ __forceinline__ uint32_t lt_fp6_word(low_f2 a, low_f2 b) {
+  uint32_t r;
+  if constexpr (EF == kE2M3)
+    asm("{\n\t.reg .b16 t0, t1;\n\t.reg .f32 a0, a1, b0, b1;\n\t"
+        "mov.b64 {a0, a1}, %1;\n\tmov.b64 {b0, b1}, %2;\n\t"
+        "cvt.rn.satfinite.e2m3x2.f32 t0, a1, a0;\n\t"
+        "cvt.rn.satfinite.e2m3x2.f32 t1, b1, b0;\n\t"
+        "mov.b32 %0, {t0, t1};\n\t}"
+        : "=r"(r)
+        : "l"(a), "l"(b));
+  else
+    asm("{\n\t.reg .b16 t0, t1;\n\t.reg .f32 a0, a1, b0, b1;\n\t"
+        "mov.b64 {a0, a1}, %1;\n\tmov.b64 {b0, b1}, %2;\n\t"
+        "cvt.rn.satfinite.e3m2x2.f32 t0, a1, a0;\n\t"
+        "cvt.rn.satfinite.e3m2x2.f32 t1, b1, b0;\n\t"
+        "mov.b32 %0, {t0, t1};\n\t}"
+        : "=r"(r)
+        : "l"(a), "l"(b));
+  return r;
+}
+// Saturated elements of a scaled pair (counted for finite, nonzero blocks).
+template <int EF>
+__device__ __forceinline__ uint32_t lt_sat2(low_f2 v) {
+  return (uint32_t)(fabsf(low_f2_lo(v)) > LowFmt<EF>::kMax) + (uint32_t)(fabsf(low_f2_hi(v)) > LowFmt<EF>::kMax);
+}
+// The output words of 16 pairs x[k] scaled by m (FP4: words 0-3; FP6: 0-7),
+// all zero when `zero`; saturated elements added to nsat when SAT.
+template <int EF, bool SAT>
+__device__ __forceinline__ void lt_codes16(const low_f2 (&x)[16], low_f2 m, bool zero, uint32_t (&o)[8],
+                                           unsigned long long& nsat) {
+  const uint32_t keep = zero ? 0u : 0xFFFFFFFFu;
+  uint32_t ns = 0;
+  if constexpr (EF == kE2M1) {
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const low_f2 a = low_f2_mul(x[4 * j], m), b = low_f2_mul(x[4 * j + 1], m);
+      const low_f2 c = low_f2_mul(x[4 * j + 2], m), d = low_f2_mul(x[4 * j + 3], m);
+      if constexpr (SAT) ns += lt_sat2<EF>(a) + lt_sat2<EF>(b) + lt_sat2<EF>(c) + lt_sat2<EF>(d);
+      o[j] = lt_fp4_word(a, b, c, d) & keep;
+    }
+#pragma unroll
+    for (int j = 4; j < 8; j++) o[j] = 0u;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const low_f2 a = low_f2_mul(x[2 * j], m), b = low_f2_mul(x[2 * j + 1], m);
+      if constexpr (SAT) ns += lt_sat2<EF>(a) + lt_sat2<EF>(b);
+      o[j] = lt_fp6_word<EF>(a, b) & keep;
+    }
+  }
+  if constexpr (SAT)
+    if (!zero) nsat += ns;
+}
+
 // Rowwise: one lane per 1x32 block (row r of the block's 32, column block b
 // of the strip's 8).  Writes the codes, returns the scale byte (0 if the
 // block is not ours).  Stage layout as in the MXFP8 kernel: 16-byte chunk c
@@ -424,12 +496,11 @@ __device__ __forceinline__ uint32_t lt_row_block(const LowParams& p, const unsig
   const uint32_t byte = low_scale_byte<EF>(amax, p.round_up);
   const bool zero = amax == 0u || byte == 0xFFu;
   const float mul = low_multiplier(byte);
-  const low_f2 M = low_f2_make(mul, mul);
-  uint32_t pr[16];
+  low_f2 x[16];
 #pragma unroll
-  for (int k = 0; k < 16; k++) pr[k] = low_pair<EF, SAT>(low_f2_make(bf16_lo(w[k]), bf16_hi(w[k])), M, !zero, nsat);
-  uint32_t o[8] = {};
-  if (!zero) low_pack<EF>(pr, o);
+  for (int k = 0; k < 16; k++) x[k] = low_f2_make(bf16_lo(w[k]), bf16_hi(w[k]));
+  uint32_t o[8];
+  lt_codes16<EF, SAT>(x, low_f2_make(mul, mul), zero, o, nsat);
   uint8_t* dst = p.q_row + (r0 + r) * (kFp4 ? p.cols / 2 : p.cols) + (c0 / 32 + b) * (kFp4 ? 16 : 32);
   *(uint4*)dst = make_uint4(o[0], o[1], o[2], o[3]);
   if constexpr (!kFp4) *(uint4*)(dst + 16) = make_uint4(o[4], o[5], o[6], o[7]);
@@ -479,19 +550,17 @@ __device__ __forceinline__ uint32_t lt_col_pair(const LowParams& p, const unsign
   const uint32_t ma = (m & 0x7FFFu) << 16, mb = m & 0x7FFF0000u;
   const uint32_t ba = low_scale_byte<EF>(ma, p.round_up), bb = low_scale_byte<EF>(mb, p.round_up);
   const bool za = ma == 0u || ba == 0xFFu, zb = mb == 0u || bb == 0xFFu;
-  const low_f2 Ma = low_f2_make(low_multiplier(ba), low_multiplier(ba));
-  const low_f2 Mb = low_f2_make(low_multiplier(bb), low_multiplier(bb));
-  uint32_t pa[16], pb[16];
-#pragma unroll
-  for (int k = 0; k < 16; k++) {
-    // rows 2k and 2k + 1 of column 2t (low halves) and of column 2t + 1
-    pa[k] = low_pair<EF, SAT>(low_f2_make(bf16_lo(w[2 * k]), bf16_lo(w[2 * k + 1])), Ma, !za, nsat);
-    pb[k] = low_pair<EF, SAT>(low_f2_make(bf16_hi(w[2 * k]), bf16_hi(w[2 * k + 1])), Mb, !zb, nsat);
-  }
 #pragma unroll
   for (int h = 0; h < 2; h++) {
-    uint32_t o[8] = {};
-    if (!(h ? zb : za)) low_pack<EF>(h ? pb : pa, o);
+    // rows 2k and 2k + 1 of column 2t (low halves, h = 0) or 2t + 1 (h = 1)
+    low_f2 x[16];
+#pragma unroll
+    for (int k = 0; k < 16; k++)
+      x[k] = h ? low_f2_make(bf16_hi(w[2 * k]), bf16_hi(w[2 * k + 1]))
+               : low_f2_make(bf16_lo(w[2 * k]), bf16_lo(w[2 * k + 1]));
+    const float mul = low_multiplier(h ? bb : ba);
+    uint32_t o[8];
+    lt_codes16<EF, SAT>(x, low_f2_make(mul, mul), h ? zb : za, o, nsat);
     uint8_t* dst = p.q_col + (c0 + 2 * tid + h) * col_len + (kFp4 ? r0 / 2 : r0);
     if (col_vec && nr == 32) {
       *(uint4*)dst = make_uint4(o[0], o[1], o[2], o[3]);
