@@ -102,6 +102,8 @@ fp8q_status launch_mma_scale(const uint8_t* s, int64_t rows, int64_t scale_cols,
 
 // Quantization statistics (qstats.cu).
 size_t qstats_workspace_bytes();
+fp8q_status qs_device_status(bool clear, unsigned* word);
+fp8q_status qs_set_wait_budget(unsigned long long ns);
 fp8q_status launch_qstats(int kind, const void* x, int dt, const uint8_t* q, const uint8_t* s, const float* scale_inv,
                           const int64_t* off, int G, int64_t rows, int64_t cols, int64_t s_ld, int fmt,
                           fp8q_qstats* out, void* workspace, cudaStream_t stream);
@@ -118,13 +120,14 @@ const char* fp8q_last_error_string(void) { return g_err; }
 
 fp8q_status fp8q_check_device(void* stream) {
   g_err[0] = 0;
-  unsigned mx = 0, pt = 0, bw = 0, lo = 0;
+  unsigned mx = 0, pt = 0, bw = 0, lo = 0, qs = 0;
   fp8q_status r = mx_device_status((cudaStream_t)stream, true, &mx);
   if (r != FP8Q_OK) return r;
   if ((r = pt_device_status(true, &pt)) != FP8Q_OK) return r;
   if ((r = bw_device_status(true, &bw)) != FP8Q_OK) return r;
   if ((r = low_device_status(true, &lo)) != FP8Q_OK) return r;
-  if ((mx | pt | bw | lo) & 1u)
+  if ((r = qs_device_status(true, &qs)) != FP8Q_OK) return r;
+  if ((mx | pt | bw | lo | qs) & 1u)
     return fail(FP8Q_ERR_TIMEOUT, "a bounded device-side wait gave up; the outputs of that call are incomplete");
   return FP8Q_OK;
 }
@@ -134,6 +137,7 @@ fp8q_status fp8q_set_wait_budget_ns(uint64_t ns) {
   fp8q_status r = mx_set_wait_budget((unsigned long long)ns);
   if (r == FP8Q_OK) r = pt_set_wait_budget((unsigned long long)ns);
   if (r == FP8Q_OK) r = low_set_wait_budget((unsigned long long)ns);
+  if (r == FP8Q_OK) r = qs_set_wait_budget((unsigned long long)ns);
   return r != FP8Q_OK ? r : bw_set_wait_budget((unsigned long long)ns);
 }
 

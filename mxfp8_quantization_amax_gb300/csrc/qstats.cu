@@ -31,14 +31,25 @@
 // Totals.  Each CTA writes its partial sums to the workspace; the last CTA
 // to finish (atomic ticket) adds them in a fixed order, so results repeat
 // exactly from run to run on one GPU.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "fp8q_device.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace fp8q {
 
 constexpr int kQsThreads = 256;
-constexpr int kQsMaxGrid = 2048;
+constexpr int kQsMaxGrid = 2048;  // partials in the workspace (one per CTA)
 constexpr int kQsTileCols = 2 * kQsThreads;  // columnwise: a column pair per thread
+#ifndef FP8Q_QS_COL_TMA  // BF16 columnwise copies without groups through the TMA-fed kernel
+#define FP8Q_QS_COL_TMA 1
+#endif
+#ifndef FP8Q_QS_TMA_CTAS_PER_SM  // grid of the TMA-fed kernel: CTAs per SM (its residency is 4)
+#define FP8Q_QS_TMA_CTAS_PER_SM 4
+#endif
 
 struct QsPartial {
   double signal, noise;
@@ -266,10 +277,11 @@ __device__ void qs_build_blk(const QsParams& p, int* blk) {
   __syncthreads();
 }
 
-// Block sum of the six totals; thread 0 gets the result.
+// Block sum of the six totals over NT threads; thread 0 gets the result.
+template <int NT = kQsThreads>
 __device__ __forceinline__ void qs_block_sum(double& s, double& n, unsigned long long (&c)[4]) {
-  __shared__ double sd[2][kQsThreads / 32];
-  __shared__ unsigned long long sc[4][kQsThreads / 32];
+  __shared__ double sd[2][NT / 32];
+  __shared__ unsigned long long sc[4][NT / 32];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
@@ -289,7 +301,7 @@ __device__ __forceinline__ void qs_block_sum(double& s, double& n, unsigned long
   if (threadIdx.x == 0) {
     s = n = 0.0;
     for (int j = 0; j < 4; j++) c[j] = 0;
-    for (int i = 0; i < kQsThreads / 32; i++) {
+    for (int i = 0; i < NT / 32; i++) {
       s += sd[0][i];
       n += sd[1][i];
       for (int j = 0; j < 4; j++) c[j] += sc[j][i];
@@ -298,11 +310,13 @@ __device__ __forceinline__ void qs_block_sum(double& s, double& n, unsigned long
 }
 
 // The CTA's partial into the workspace; the last CTA adds all partials in
-// index order, writes the result and re-arms the ticket.
+// index order, writes the result and re-arms the ticket.  Every one of the
+// CTA's NT threads calls it.
+template <int NT = kQsThreads>
 __device__ void qs_finish(const QsParams& p, const QsAcc& a) {
   double s = a.signal, n = a.noise;
   unsigned long long c[4] = {a.n, a.nz, a.nf, a.nn};
-  qs_block_sum(s, n, c);
+  qs_block_sum<NT>(s, n, c);
   if (threadIdx.x == 0) {
     QsPartial& d = p.part[blockIdx.x];
     d.signal = s;
@@ -321,7 +335,7 @@ __device__ void qs_finish(const QsParams& p, const QsAcc& a) {
   __threadfence();
   s = n = 0.0;
   for (int j = 0; j < 4; j++) c[j] = 0;
-  for (int i = threadIdx.x; i < (int)gridDim.x; i += kQsThreads) {
+  for (int i = threadIdx.x; i < (int)gridDim.x; i += NT) {
     const QsPartial* d = p.part + i;
     s += __ldcg(&d->signal);
     n += __ldcg(&d->noise);
@@ -330,7 +344,7 @@ __device__ void qs_finish(const QsParams& p, const QsAcc& a) {
     c[2] += __ldcg(&d->n_flushed);
     c[3] += __ldcg(&d->n_nonfinite);
   }
-  qs_block_sum(s, n, c);
+  qs_block_sum<NT>(s, n, c);
   if (threadIdx.x == 0) {
     p.out->signal = s;
     p.out->noise = n;
@@ -565,6 +579,302 @@ __global__ void __launch_bounds__(kQsThreads) qstats_col_kernel(QsParams p) {
   qs_finish(p, a);
 }
 
+// ---------------------------------------------------------------------------
+// Columnwise MX copy of a BF16 tensor without groups, rows % 32 == 0: TMA-fed
+// ---------------------------------------------------------------------------
+// A producer warp streams, per block of 32 rows x 256 columns, the x tile
+// (four 64-column boxes, 128-byte swizzle: 16 KB) and the block's codes from
+// the transposed copy (one box of 32 codes x 256 columns: 8 KB) into a
+// two-stage mbarrier ring; four consumer warps take a column pair per thread
+// as the kernel above does, reading both from shared memory.  A unit is up
+// to 4 blocks of one 256-column strip, so a column's scale bytes of the unit
+// are one 4-byte load; each CTA takes a contiguous range of units.  Waits
+// are bounded: on expiry the failure word is set, the rest is skipped, and
+// the CTA still adds its (then meaningless) partial so that the ticket
+// re-arms.
+constexpr int kQtCons = 128;
+constexpr int kQtThreads = kQtCons + 32;
+constexpr int kQtCols = 256;
+constexpr int kQtSubCols = 64;
+constexpr int kQtSubBytes = 32 * 128;
+constexpr int kQtXBytes = 32 * kQtCols * 2;
+constexpr int kQtCodeBytes = 32 * kQtCols;
+constexpr int kQtStageBytes = kQtXBytes + kQtCodeBytes;
+constexpr int kQtStages = 2;
+#ifndef FP8Q_QS_TMA_UNIT  // blocks per unit (1..4)
+#define FP8Q_QS_TMA_UNIT 4
+#endif
+constexpr int kQtUnit = FP8Q_QS_TMA_UNIT;
+static_assert(kQtUnit >= 1 && kQtUnit <= 4, "a unit's scale bytes of a column fill one word");
+
+__device__ unsigned int g_qs_error;
+__device__ unsigned long long g_qs_budget_ns = 1000000000ull;
+
+template <int FMT>
+__global__ void __launch_bounds__(kQtThreads, 4)
+    qstats_col_tma_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap qmap,
+                          QsParams p) {
+  extern __shared__ unsigned char qt_smem[];
+  __shared__ uint64_t full[kQtStages], empty[kQtStages];
+  __shared__ volatile int abort_flag;
+  unsigned char* stages = qt_smem + ((1024 - (smem_u32(qt_smem) & 1023)) & 1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kQtStages; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kQtCons / 32);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (tid == kQtCons) {
+    prefetch_tensormap(&xmap);
+    prefetch_tensormap(&qmap);
+  }
+  pdl_wait();
+  __syncthreads();
+  const int64_t nbr = p.rows / 32;
+  const int64_t strips = (p.cols + kQtCols - 1) / kQtCols;
+  const int64_t units = (nbr + kQtUnit - 1) / kQtUnit * strips;
+  const int64_t u_begin = units * blockIdx.x / gridDim.x, u_end = units * (blockIdx.x + 1) / gridDim.x;
+  const uint64_t budget = g_qs_budget_ns;
+  QsAcc a;
+
+  if (warp == kQtCons / 32) {
+    // ---------------- producer (lane 0; the warp then joins the finish) ----------------
+    if (lane == 0) {
+      int64_t k = 0;
+      bool stop = false;
+      for (int64_t u = u_begin; u < u_end && !abort_flag && !stop; u++) {
+        const int64_t ti = u / strips;
+        const int c0 = (int)((u - ti * strips) * kQtCols);
+        const int64_t rb0 = ti * kQtUnit;
+        const int nblk = (int)min((int64_t)kQtUnit, nbr - rb0);
+        for (int j = 0; j < nblk; j++, ++k) {
+          const int s = (int)(k % kQtStages);
+          const uint32_t round = (uint32_t)(k / kQtStages);
+          if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, budget)) {
+            atomicOr(&g_qs_error, 1u);
+            abort_flag = 1;
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], kQtStageBytes);
+          unsigned char* dst = stages + s * kQtStageBytes;
+          const int row = (int)((rb0 + j) * 32);
+#pragma unroll
+          for (int q = 0; q < kQtCols / kQtSubCols; q++)
+            tma_load_2d(dst + q * kQtSubBytes, &xmap, c0 + q * kQtSubCols, row, &full[s]);
+          tma_load_2d(dst + kQtXBytes, &qmap, row, c0, &full[s]);
+        }
+      }
+      const int64_t first = k > kQtStages ? k - kQtStages : 0;  // every issued copy lands before the finish
+      for (int64_t j = first; j < k; j++)
+        mbar_wait(&full[j % kQtStages], (uint32_t)((j / kQtStages) & 1), 2000000000ull);
+    }
+  } else {
+    // ---------------- consumers ----------------
+    const float nan = __uint_as_float(0x7FC00000u);
+    int64_t k = 0;
+    for (int64_t u = u_begin; u < u_end && !abort_flag; u++) {
+      const int64_t ti = u / strips;
+      const int64_t c0 = (u - ti * strips) * kQtCols;
+      const int64_t rb0 = ti * kQtUnit;
+      const int nblk = (int)min((int64_t)kQtUnit, nbr - rb0);
+      const int64_t c = c0 + 2 * tid;  // this thread's columns c, c + 1
+      const bool col_ok = c < p.cols;
+      // the two columns' scale bytes of the unit's blocks
+      uint32_t sa = 0, sb = 0;
+      if (col_ok) {
+        const uint8_t* ea = p.s + c * p.s_ld + rb0;
+        const uint8_t* eb = ea + p.s_ld;
+        if (nblk == kQtUnit && rb0 + kQtUnit <= p.s_ld && (((uintptr_t)ea | (uintptr_t)eb) & 3u) == 0) {
+          sa = __ldg((const unsigned*)ea);
+          sb = __ldg((const unsigned*)eb);
+        } else {
+          for (int j = 0; j < nblk && rb0 + j < p.s_ld; j++) {
+            sa |= (uint32_t)__ldg(ea + j) << (8 * j);
+            sb |= (uint32_t)__ldg(eb + j) << (8 * j);
+          }
+        }
+      }
+      bool gave_up = false;
+      for (int j = 0; j < nblk; j++, ++k) {
+        const int s = (int)(k % kQtStages);
+        const uint32_t round = (uint32_t)(k / kQtStages);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], round & 1u, budget))) {
+          atomicOr(&g_qs_error, 1u);
+          abort_flag = 1;
+          gave_up = true;
+          break;
+        }
+        const unsigned char* stage = stages + s * kQtStageBytes;
+        if (col_ok) {
+          const int64_t r0 = (rb0 + j) * 32;
+          const bool in_ld = rb0 + j < p.s_ld;
+          const float ma = in_ld ? qs_e8m0((sa >> (8 * j)) & 0xFFu) : nan;
+          const float mb = in_ld ? qs_e8m0((sb >> (8 * j)) & 0xFFu) : nan;
+          // x: row i's word holds columns c (low half) and c + 1
+          const unsigned char* xs = stage + (tid >> 5) * kQtSubBytes + 4 * (tid & 3);
+          const int ch = (tid & 31) >> 2;
+          uint32_t xv[32];
+#pragma unroll
+          for (int i = 0; i < 32; i++) xv[i] = *(const uint32_t*)(xs + i * 128 + ((ch ^ (i & 7)) << 4));
+          // codes: column c's 32 bytes, then column c + 1's
+          const uint4* qs = (const uint4*)(stage + kQtXBytes + 64 * tid);
+          const uint4 a0 = qs[0], a1 = qs[1], b0 = qs[2], b1 = qs[3];
+          const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+          f32x2 S = f2_make(0.0f, 0.0f), N = S;
+          const f32x2 M = f2_make(ma, mb);
+#pragma unroll
+          for (int i = 0; i < 32; i++) {
+            const int jj = i & 3;
+            float va, vb;
+            qs_decode2<FMT>(__byte_perm(wa[i >> 2], wb[i >> 2], jj | ((4 + jj) << 4)), va, vb);
+            qs_pair(f2_make(bf16_lo(xv[i]), bf16_hi(xv[i])), f2_make(va, vb), M, S, N);
+          }
+          uint32_t za = 0xFFFFFFFFu, zb = 0xFFFFFFFFu;
+#pragma unroll
+          for (int w = 0; w < 8; w++) {
+            za &= qs_nonzero_codes(wa[w]);
+            zb &= qs_nonzero_codes(wb[w]);
+          }
+          // whether every x / every code of a column is +-0: settling needs
+          // it only for a chunk whose sums fall below 2^-100
+          const bool small = !(fminf(fminf(f2_lo(S), f2_hi(S)), fminf(f2_lo(N), f2_hi(N))) >= kQsSmall);
+          uint32_t ca = 1u, cb = 1u, xa = 1u, xb = 1u;
+          if (small) {
+            ca = cb = xa = xb = 0u;
+#pragma unroll
+            for (int w = 0; w < 8; w++) {
+              ca |= wa[w] & 0x7F7F7F7Fu;
+              cb |= wb[w] & 0x7F7F7F7Fu;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+              xa |= xv[i] & 0x7FFFu;
+              xb |= xv[i] & 0x7FFF0000u;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 2; h++) {
+            const int64_t cc = c + h;
+            const uint8_t* qc = p.q + cc * p.rows + r0;
+            auto xg = [&](int i) { return qs_x<kBF16>(p.x, (r0 + i) * p.cols + cc); };
+            auto cg = [&](int i) { return (uint32_t)__ldg(qc + i); };
+            auto count = [&](QsAcc& acc) {
+#pragma unroll
+              for (int w = 0; w < 8; w++) {
+                uint32_t t[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) t[q] = (xv[4 * w + q] & 0x7FFF7FFFu) + 0x7FFF7FFFu;
+                // bit 15 (column c) or bit 31 (column c + 1) of each row
+                const uint32_t sel = h == 0 ? 0x0051u : 0x0073u;
+                const uint32_t xnz = __byte_perm(__byte_perm(t[0], t[1], sel), __byte_perm(t[2], t[3], sel), 0x5410);
+                qs_count4(acc, qs_nonzero_codes(h ? wb[w] : wa[w]), xnz);
+              }
+            };
+            qs_settle<FMT>(a, h ? f2_hi(S) : f2_lo(S), h ? f2_hi(N) : f2_lo(N), h ? zb : za, (h ? xb : xa) == 0u,
+                           (h ? cb : ca) == 0u, true, h ? mb : ma, xg, cg, count);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      if (gave_up) break;
+    }
+  }
+  pdl_launch_dependents();
+  qs_finish<kQtThreads>(p, a);
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 qs_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  });
+  return fn;
+}
+
+// Launches the TMA-fed columnwise kernel; *used = false when the call does
+// not qualify (grouped, FP32, ragged rows, unaligned buffers) or no tensor
+// map could be encoded, and the caller takes the kernel above.
+template <int FMT>
+static cudaError_t qs_col_tma(const QsParams& p, cudaStream_t stream, bool* used) {
+  *used = false;
+  if (!(p.off == nullptr || p.G <= 1) || p.rows % 32 != 0 || p.rows <= 0 || p.cols <= 0 ||
+      ((uintptr_t)p.x & 15u) != 0 || ((uintptr_t)p.q & 15u) != 0)
+    return cudaSuccess;
+  auto enc = qs_encode_fn();
+  if (!enc) return cudaSuccess;
+  CUtensorMap xmap, qmap;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)p.cols, (cuuint64_t)p.rows};
+    cuuint64_t strides[1] = {(cuuint64_t)p.cols * 2};
+    cuuint32_t box[2] = {kQtSubCols, 32};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaSuccess;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)p.rows, (cuuint64_t)p.cols};
+    cuuint64_t strides[1] = {(cuuint64_t)p.rows};
+    cuuint32_t box[2] = {32, kQtCols};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaSuccess;
+  }
+  auto kernel = qstats_col_tma_kernel<FMT>;
+  constexpr size_t smem = 1024 + (size_t)kQtStages * kQtStageBytes;
+  static bool attr = false;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+  }
+  const int64_t units = (p.rows / 32 + kQtUnit - 1) / kQtUnit * ((p.cols + kQtCols - 1) / kQtCols);
+  // each CTA a contiguous range of units: one wave of resident CTAs (every
+  // CTA ends with a block reduction and a ticket, which many small CTAs
+  // would repeat), at most one CTA per unit
+  int64_t grid = (int64_t)FP8Q_QS_TMA_CTAS_PER_SM * sm_count();
+  if (grid > units) grid = units;
+  if (grid > kQsMaxGrid) grid = kQsMaxGrid;
+  *used = true;
+  return launch_kernel(kernel, dim3((unsigned)grid), dim3(kQtThreads), smem, stream, xmap, qmap, p);
+}
+
+fp8q_status qs_device_status(bool clear, unsigned* word) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_qs_error, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+  if (clear && v) {
+    const unsigned z = 0;
+    e = cudaMemcpyToSymbol(g_qs_error, &z, sizeof(z));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+  }
+  *word = v;
+  return FP8Q_OK;
+}
+
+fp8q_status qs_set_wait_budget(unsigned long long ns) {
+  cudaError_t e = cudaMemcpyToSymbol(g_qs_budget_ns, &ns, sizeof(ns));
+  return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, "cudaMemcpyToSymbol(wait budget)");
+}
+
 template <class K>
 static int qs_grid(K kernel, size_t smem, int64_t units) {
   int per_sm = 0;
@@ -580,6 +890,12 @@ template <int DT, int FMT>
 static fp8q_status qs_launch_typed(int kind, QsParams p, cudaStream_t stream) {
   cudaError_t e;
   if (kind == 2) {
+    if constexpr (DT == kBF16 && FP8Q_QS_COL_TMA) {
+      bool used = false;
+      e = qs_col_tma<FMT>(p, stream, &used);
+      if (e != cudaSuccess) return cuda_fail(e, "quantization statistics kernel launch");
+      if (used) return check_launch("quantization statistics kernel");
+    }
     const size_t smem = (p.off != nullptr && p.G > 1) ? sizeof(int) * (size_t)(p.G + 1) : 0;
     const int64_t tiles = ((p.rows + 31) / 32) * ((p.cols + kQsTileCols - 1) / kQsTileCols);
     const int grid = qs_grid(qstats_col_kernel<DT, FMT>, smem, tiles);
