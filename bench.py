@@ -239,20 +239,20 @@ def kernel_label(op):
     return {"dq_mx_row": f"dequant_kernel<mx_row,{fmt_name},bf16>",
             "dq_mx_col": f"dequant_kernel<mx_col,{fmt_name},bf16>",
             "dq_tensor": f"dequant_kernel<tensor,{fmt_name},bf16>",
-            "mx_rule": f"mx_tma_kernel<bf16,{fmt_name},both,rule+counts>",
+            "mx_rule": f"mx_lean_kernel<bf16,{fmt_name},both,rule+counts>",
             "mx_mma": f"mx_tma_kernel<bf16,{fmt_name},both> (MMA scale layout)",
             "mx_grouped": f"mx_band_kernel<bf16,{fmt_name},both> ({op.get('G')} groups)",
             "bw": f"blockwise_kernel<{fmt_name},{'1x128' if op.get('block') == 1 else '128x128'},both>",
             "nvfp4": "amax_kernel + nvfp4_kernel<bf16>",
             "qs_mx_row": f"qstats_lin_kernel<bf16,{fmt_name},mx_row>",
-            "qs_mx_col": f"qstats_col_kernel<bf16,{fmt_name}>",
+            "qs_mx_col": f"qstats_col_tma_kernel<bf16,{fmt_name}>",
             "qs_tensor": f"qstats_lin_kernel<bf16,{fmt_name},tensor>",
             "mxlow": f"mxlow_tma_kernel<{LOW_NAMES.get(op.get('elem'), '')},both>",
             "mmascale": "mma_scale_kernel",
             "current": f"amax_kernel + cast_kernel<bf16,{fmt_name}>",
             "current_grouped": f"amax_kernel + cast_kernel<bf16,{fmt_name}> ({op.get('G')} groups)",
             "delayed": f"cast_kernel<bf16,{fmt_name},history> (interval {op.get('interval')})",
-            }.get(op["kind"], f"mx_tma_kernel<bf16,{fmt_name},both>")
+            }.get(op["kind"], f"mx_lean_kernel<bf16,{fmt_name},both>")
 
 
 # ---------------------------------------------------------------------------
