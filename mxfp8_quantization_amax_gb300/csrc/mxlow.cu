@@ -386,7 +386,10 @@ constexpr int kLtCols = 256;                    // columns per block (a strip)
 constexpr int kLtSubCols = 64;                  // columns per TMA box (128 bytes)
 constexpr int kLtSubBytes = 32 * 128;           // one box in shared memory
 constexpr int kLtStageBytes = 32 * kLtCols * 2; // one BF16 block: 16 KB
-constexpr int kLtStages = 2;
+#ifndef FP8Q_LOW_TMA_STAGES  // TMA ring depth of the BF16 kernel (16 KB per stage)
+#define FP8Q_LOW_TMA_STAGES 2
+#endif
+constexpr int kLtStages = FP8Q_LOW_TMA_STAGES;
 constexpr int kLtUnit = 4;                      // blocks per unit
 #ifndef FP8Q_LOW_GRID_ALL  // one CTA per unit instead of a persistent grid
 #define FP8Q_LOW_GRID_ALL 1

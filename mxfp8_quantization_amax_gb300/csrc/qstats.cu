@@ -148,6 +148,11 @@ __device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
   f32x2 d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
@@ -402,7 +407,9 @@ __global__ void __launch_bounds__(kQsThreads) qstats_lin_kernel(QsParams p) {
     auto xg = [&](int i) { return qs_x<DT>(p.x, e0 + i); };
     auto cg = [&](int i) { return (uint32_t)__ldg(p.q + e0 + i); };
     if (uniform) {
-      f32x2 S = f2_make(0.0f, 0.0f), N = S;
+      // four independent accumulation chains (pairs k % 4), added at the end
+      const f32x2 zero2 = f2_make(0.0f, 0.0f);
+      f32x2 Sc[4] = {zero2, zero2, zero2, zero2}, Nc[4] = {zero2, zero2, zero2, zero2};
       const f32x2 M = f2_make(m, m);
 #pragma unroll
       for (int k = 0; k < 16; k++) {
@@ -411,8 +418,10 @@ __global__ void __launch_bounds__(kQsThreads) qstats_lin_kernel(QsParams p) {
         f32x2 X;
         if constexpr (DT == kBF16) X = f2_make(bf16_lo(xw[k]), bf16_hi(xw[k]));
         else X = f2_make(__uint_as_float(xw[2 * k]), __uint_as_float(xw[2 * k + 1]));
-        qs_pair(X, f2_make(v0, v1), M, S, N);
+        qs_pair(X, f2_make(v0, v1), M, Sc[k & 3], Nc[k & 3]);
       }
+      const f32x2 S = f2_add(f2_add(Sc[0], Sc[1]), f2_add(Sc[2], Sc[3]));
+      const f32x2 N = f2_add(f2_add(Nc[0], Nc[1]), f2_add(Nc[2], Nc[3]));
       uint32_t nzc = 0xFFFFFFFFu, cor = 0u, xor_ = 0u;
 #pragma unroll
       for (int j = 0; j < 8; j++) {
@@ -728,15 +737,19 @@ __global__ void __launch_bounds__(kQtThreads, 4)
           const uint4 a0 = qs[0], a1 = qs[1], b0 = qs[2], b1 = qs[3];
           const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
           const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-          f32x2 S = f2_make(0.0f, 0.0f), N = S;
+          // four independent accumulation chains (rows i % 4), added at the end
+          const f32x2 zero2 = f2_make(0.0f, 0.0f);
+          f32x2 Sc[4] = {zero2, zero2, zero2, zero2}, Nc[4] = {zero2, zero2, zero2, zero2};
           const f32x2 M = f2_make(ma, mb);
 #pragma unroll
           for (int i = 0; i < 32; i++) {
             const int jj = i & 3;
             float va, vb;
             qs_decode2<FMT>(__byte_perm(wa[i >> 2], wb[i >> 2], jj | ((4 + jj) << 4)), va, vb);
-            qs_pair(f2_make(bf16_lo(xv[i]), bf16_hi(xv[i])), f2_make(va, vb), M, S, N);
+            qs_pair(f2_make(bf16_lo(xv[i]), bf16_hi(xv[i])), f2_make(va, vb), M, Sc[jj], Nc[jj]);
           }
+          const f32x2 S = f2_add(f2_add(Sc[0], Sc[1]), f2_add(Sc[2], Sc[3]));
+          const f32x2 N = f2_add(f2_add(Nc[0], Nc[1]), f2_add(Nc[2], Nc[3]));
           uint32_t za = 0xFFFFFFFFu, zb = 0xFFFFFFFFu;
 #pragma unroll
           for (int w = 0; w < 8; w++) {
