@@ -67,6 +67,22 @@ def test_mx_bf16(fmt, shape):
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
+def test_mx_bf16_columnwise_edges(fmt):
+    """BF16 without groups and rows % 32 == 0 (the TMA-fed columnwise
+    kernel): a partial last 256-column strip (800 columns), a last unit of
+    two blocks (320 rows), rows over 2^-80 .. 2^40 (tiny chunks take the
+    FP64 path), and zero, -0, Inf and NaN chunks."""
+    fq = require_cuda()
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal((320, 800)) * 2.0 ** rng.integers(-80, 40, size=(320, 1))).astype(np.float32)
+    x[0:32, 5] = 0.0
+    x[32:64, 7] = -0.0
+    x[70, 9] = np.inf
+    x[100, 11] = np.nan
+    _mx_case(fq, synth.to_bf16_bits(x), fmt)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
 def test_mx_fp32_wide_range(fmt):
     """FP32 rows spread over 2^-40 .. 2^40 (tiny rows take the FP64 path)."""
     fq = require_cuda()
