@@ -377,7 +377,7 @@ class Prepared:
     Input sets rotate (so an input is out of L2 when it is read again), and
     so do output sets; a drifting sequence has one input set per step."""
 
-    def __init__(self, name, dev):
+    def __init__(self, name, dev, min_sets=1):
         import torch
 
         import mxfp8_quantization_amax_gb300 as fq
@@ -404,7 +404,7 @@ class Prepared:
         in_bytes = sum(2 * int(np.prod(s)) for _, s in gens)
         out_bytes = sum(op["bytes"] - 2 * int(np.prod(op["shape"])) for op in ops)
         per_set = in_bytes + max(out_bytes, 0)
-        n_rot = max(1, min(64, -(-4 * L2_BYTES // per_set)))
+        n_rot = max(min_sets, min(64, -(-4 * L2_BYTES // per_set)))
         self.n_in = C3_STEPS if seq else n_rot
         self.n_out = n_rot
         self.nsets = max(self.n_in, self.n_out)
@@ -883,7 +883,8 @@ def e2e_leg(P, steps, world, dev):
     ms = max_over_ranks(ms, world, dev)
     return {"value": round(job_gbs(P.bytes_per_step, world, ms), 2), "unit": "GB/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 4),
-            "copies": "upload of step i + 1 and download of step i on their own streams, overlapping the kernels"}
+            "copies": "upload of step i + 1 and download of step i on their own streams, overlapping the kernels",
+            "buffer_sets": P.nsets}
 
 
 def measure_config(name, dev, peak, peak_src, steps, warmup):
@@ -951,8 +952,16 @@ def run_ours(args):
                                                "n_flushed": d["n_flushed"], "n_zero": d["n_zero"]}
     if args.workload == "delayed_8192" and rank == 0:
         extra["delayed_vs_current"] = delayed_vs_current(P)
-    # last: the end-to-end leg overwrites the device inputs with host copies
-    e2e = None if args.no_e2e else e2e_leg(P, args.e2e_steps, world, dev)
+    # last: the end-to-end leg overwrites the device inputs with host copies.
+    # It double-buffers, as a pipelined caller does: with a single buffer set
+    # the next step's kernels would wait for this step's download.
+    e2e = None
+    if not args.no_e2e:
+        PE = P if min(P.n_in, P.n_out) >= 2 else Prepared(args.workload, dev, min_sets=2)
+        e2e = e2e_leg(PE, args.e2e_steps, world, dev)
+        if PE is not P:
+            PE.close()
+            del PE
     fq.check_device()
     roofline = roofline_entry(P, P.ops[jr], rl_ms, rl_n, peak, peak_src, args.workload)
     cfg = dict(P.cfg)
