@@ -293,7 +293,9 @@ FP8Q_API int64_t mxfp8_col_blocks(const int64_t* group_offsets_host, int32_t num
  *            multiple of 16 keeps every scale row 16-byte aligned, which
  *            the grouped path stores faster
  * cols % 32 == 0 is required (FP8Q_ERR_UNSUPPORTED otherwise); rows is any.
- * Pointers of the unused direction may be NULL.
+ * x is 16-byte aligned and q_row 32-byte aligned (a block's 32 codes leave
+ * in one 32-byte store; FP8Q_ERR_INVALID_ARG otherwise).  Pointers of the
+ * unused direction may be NULL.  A rejected call writes nothing.
  */
 FP8Q_API fp8q_status mxfp8_quantize(const void* x, int32_t dt, int64_t rows, int64_t cols,
                            const int64_t* group_offsets, int32_t num_groups, int32_t fmt,

@@ -368,24 +368,31 @@ fp8q_status mxfp8_quantize_ex(const void* x, int32_t dt, int64_t rows, int64_t c
   if (dir != MXFP8_ROW && dir != MXFP8_COL && dir != MXFP8_BOTH)
     return fail(FP8Q_ERR_INVALID_ARG, "dir must be MXFP8_ROW, MXFP8_COL or MXFP8_BOTH");
   if (cols % 32 != 0) return fail(FP8Q_ERR_UNSUPPORTED, "MXFP8 needs cols %% 32 == 0 (cols = %lld)", (long long)cols);
-  if (sat_count) {  // zero even for an empty tensor
+  const bool empty = rows * cols == 0;
+  // every check before the first write, so that a rejected call leaves the
+  // caller's buffers untouched
+  if (!empty) {
+    if (rows > INT32_MAX / 2) return fail(FP8Q_ERR_UNSUPPORTED, "rows too large");
+    if (dir & MXFP8_ROW) {
+      if (!q_row || !s_row) return fail(FP8Q_ERR_INVALID_ARG, "q_row and s_row are required for rowwise output");
+      // the rowwise codes of a block leave in one 32-byte store, and every
+      // row starts on that alignment since cols % 32 == 0
+      if (!aligned(q_row, 32)) return fail(FP8Q_ERR_INVALID_ARG, "q_row must be 32-byte aligned");
+    }
+    if (dir & MXFP8_COL) {
+      if (!q_col || !s_col) return fail(FP8Q_ERR_INVALID_ARG, "q_col and s_col are required for columnwise output");
+      if (s_col_ld < (rows + 31) / 32)
+        return fail(FP8Q_ERR_INVALID_ARG, "s_col_ld (%lld) is below ceil(rows / 32) = %lld", (long long)s_col_ld,
+                    (long long)((rows + 31) / 32));
+      if (scale_layout == FP8Q_SCALES_MMA_128X4 && group_offsets == nullptr && s_col_ld != (rows + 31) / 32)
+        return fail(FP8Q_ERR_INVALID_ARG, "in the MMA layout s_col_ld is the column block count, ceil(rows / 32)");
+    }
+  }
+  if (sat_count) {  // zeroed even for an empty tensor
     cudaError_t e = cudaMemsetAsync(sat_count, 0, 2 * sizeof(unsigned long long), (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(sat_count)");
   }
-  if (rows * cols == 0) return FP8Q_OK;
-  if (rows > INT32_MAX / 2) return fail(FP8Q_ERR_UNSUPPORTED, "rows too large");
-  if (dir & MXFP8_ROW) {
-    if (!q_row || !s_row) return fail(FP8Q_ERR_INVALID_ARG, "q_row and s_row are required for rowwise output");
-    if (!aligned(q_row, 16)) return fail(FP8Q_ERR_INVALID_ARG, "q_row must be 16-byte aligned");
-  }
-  if (dir & MXFP8_COL) {
-    if (!q_col || !s_col) return fail(FP8Q_ERR_INVALID_ARG, "q_col and s_col are required for columnwise output");
-    if (s_col_ld < (rows + 31) / 32)
-      return fail(FP8Q_ERR_INVALID_ARG, "s_col_ld (%lld) is below ceil(rows / 32) = %lld", (long long)s_col_ld,
-                  (long long)((rows + 31) / 32));
-    if (scale_layout == FP8Q_SCALES_MMA_128X4 && group_offsets == nullptr && s_col_ld != (rows + 31) / 32)
-      return fail(FP8Q_ERR_INVALID_ARG, "in the MMA layout s_col_ld is the column block count, ceil(rows / 32)");
-  }
+  if (empty) return FP8Q_OK;
   if (scale_layout == FP8Q_SCALES_MMA_128X4) {
     // The kernels write every scale; the layout's padding (rows past a
     // multiple of 128, scale columns past a multiple of 4) is cleared here,

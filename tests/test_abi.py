@@ -162,6 +162,16 @@ def test_nvfp4_arguments_rejected_on_host(lib):
     assert lib.fp8q_quantize_nvfp4(a, 0, 4, 32, a + 4, a, a, None, None) == 1  # q alignment
 
 
+def test_mx_q_row_alignment_checked_before_any_write(lib):
+    """A q_row that is 16- but not 32-byte aligned is refused (its codes leave
+    in 32-byte stores) before any CUDA call: the call needs no GPU."""
+    buf = ctypes.create_string_buffer(512)
+    a = (ctypes.addressof(buf) + 63) // 64 * 64
+    assert lib.mxfp8_quantize(a, 0, 32, 64, None, 1, 0, 1, a + 16, a, None, None, 0, None) == 1
+    assert b"32-byte" in lib.fp8q_last_error_string()
+    assert lib.mxfp8_quantize_rule(a, 0, 32, 64, None, 1, 0, 3, 0, a + 16, a, a, a, 2, a, None) == 1
+
+
 def test_empty_mx_is_a_no_op(lib):
     # rows * cols == 0 returns before any launch
     assert lib.mxfp8_quantize(None, 0, 0, 64, None, 1, 0, 3, None, None, None, None, 0, None) == 0
