@@ -11,6 +11,10 @@
 
 struct fp8q_delayed_state;
 
+#ifndef FP8Q_PT_KEEP_PREFIX  // current scaling of a tensor larger than L2 keeps a prefix of it there
+#define FP8Q_PT_KEEP_PREFIX 1
+#endif
+
 namespace fp8q {
 
 fp8q_status delayed_create(int H, int interval, int margin, int fmt, fp8q_delayed_state** out);
@@ -239,19 +243,26 @@ fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t rows, int64_
   L.sat_out = sat_count_out;
   L.stream = (cudaStream_t)stream;
   if (scale_in == nullptr) {
-    // current scaling: amax pass (publishes scales), then the cast; a tensor
-    // that fits comfortably in L2 is kept there for the second pass
-    const bool keep = rows * cols * (dt == FP8Q_IN_BF16 ? 2 : 4) <= kL2KeepBytes;
+    // current scaling: amax pass (publishes scales), then the cast.  The
+    // first kL2KeepBytes of x (all of a tensor that small) are kept in L2
+    // for the second pass: evict-last in the amax pass, which reads the rest
+    // evict-first so that it does not push the prefix out, and evict-first
+    // (last use) in the cast.
+    const int64_t esz = dt == FP8Q_IN_BF16 ? 2 : 4;
     PtLaunch A = L;
     A.acc = ws.acc;
     A.amax_out = amax_out;
     A.scale_out = scale_out;
     A.scale_inv_out = scale_inv_out;
     A.sat_acc = nullptr;
-    A.l2_hint = keep ? 1 : 0;
+    A.keep_n = FP8Q_PT_KEEP_PREFIX || rows * cols * esz <= kL2KeepBytes ? kL2KeepBytes / esz : 0;
+    A.l2_hint_pre = 1;
+    A.l2_hint = FP8Q_PT_KEEP_PREFIX ? 2 : 0;
     if ((r = launch_amax(A, true)) != FP8Q_OK) return r;
     L.src = kSrcWorkspace;
-    L.l2_hint = keep ? 2 : 0;
+    L.keep_n = A.keep_n;
+    L.l2_hint_pre = 2;
+    L.l2_hint = 0;
     return launch_cast(L);
   }
   L.src = kSrcGiven;

@@ -91,13 +91,15 @@ struct PtLaunch {
   float* hist_slot;
   unsigned* flag;
   // L2 policy for reading x: 0 default, 1 keep (a second pass follows),
-  // 2 last use
+  // 2 last use; elements [0, keep_n) take l2_hint_pre instead
   int l2_hint;
+  int64_t keep_n;
+  int l2_hint_pre;
   cudaStream_t stream;
 };
 
 // Tensors up to this size stay in L2 between the amax and the cast pass of
-// current scaling.
+// current scaling; of a larger tensor, a prefix of this size does.
 constexpr int64_t kL2KeepBytes = 48ll << 20;
 
 // Amax pass.  finalize_scales: the last CTA turns acc[] into ws_scale[] and

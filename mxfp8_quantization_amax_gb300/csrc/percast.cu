@@ -70,6 +70,10 @@ struct KParams {
   float* hist_slot;
   unsigned* flag;
   int l2_hint;  // 0: default, 1: keep the input in L2 (a second pass follows), 2: last use
+  // elements [0, keep_n) of x are loaded with the hint l2_hint_pre instead:
+  // the prefix of a tensor too large for L2 that the second pass re-reads
+  int64_t keep_n;
+  int l2_hint_pre;
 };
 
 // 16-byte read-only load with an L2 eviction policy (createpolicy value).
@@ -166,8 +170,8 @@ __device__ __forceinline__ bool arrive_last(unsigned* counter) {
 // Amax of the CTA's chunks [c_begin, c_end), merged into p.acc[group] with
 // one atomic per CTA and group.  Block-uniform: every thread calls it.
 template <int DT>
-__device__ __forceinline__ void amax_pass(const KParams& p, int64_t c_begin, int64_t c_end, uint64_t pol,
-                                          uint32_t* sh_max) {
+__device__ __forceinline__ void amax_pass(const KParams& p, int64_t c_begin, int64_t c_end, uint64_t pol_rest,
+                                          uint64_t pol_pre, uint32_t* sh_max) {
   int cur_g = -1;
   uint32_t cur = 0;
   auto flush = [&]() {  // block-uniform
@@ -181,6 +185,7 @@ __device__ __forceinline__ void amax_pass(const KParams& p, int64_t c_begin, int
 
   for (int64_t c = c_begin; c < c_end; ++c) {
     const int64_t e0 = c * InT<DT>::kChunk;
+    const uint64_t pol = e0 < p.keep_n ? pol_pre : pol_rest;
     const int64_t e1 = min(e0 + (int64_t)InT<DT>::kChunk, p.n);
     const int g0 = cursor_group(p, span, e0);
     const bool one_group = p.off == nullptr || p.G <= 1 || (span.e0 <= e0 && e1 <= span.e1);
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(kPtThreads) amax_kernel(KParams p) {
   pdl_wait();
   const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
   const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
-  amax_pass<DT>(p, c_begin, c_end, load_policy(p.l2_hint), sh_max);
+  amax_pass<DT>(p, c_begin, c_end, load_policy(p.l2_hint), load_policy(p.l2_hint_pre), sh_max);
   pdl_launch_dependents();  // main work done: the next kernel may launch
 
   if constexpr (FINALIZE) {
@@ -344,8 +349,9 @@ __device__ __forceinline__ void cast_vec(const KParams& p, const uint4& v, int64
 // `p.src`; optional fused amax (p.acc) and saturation count (p.sat_acc).
 // Block-uniform: every thread calls it.
 template <int DT, int FMT>
-__device__ __forceinline__ void cast_pass(const KParams& p, int64_t c_begin, int64_t c_end, uint64_t pol,
-                                          float hist_scale, uint32_t* sh_max, unsigned long long* sh_sum) {
+__device__ __forceinline__ void cast_pass(const KParams& p, int64_t c_begin, int64_t c_end, uint64_t pol_rest,
+                                          uint64_t pol_pre, float hist_scale, uint32_t* sh_max,
+                                          unsigned long long* sh_sum) {
   constexpr float kMax = Fmt<FMT>::kMax;
   constexpr int PV = InT<DT>::kPerVec;
   constexpr int V = kVecs;
@@ -371,6 +377,7 @@ __device__ __forceinline__ void cast_pass(const KParams& p, int64_t c_begin, int
 
   for (int64_t c = c_begin; c < c_end; ++c) {
     const int64_t e0 = c * InT<DT>::kChunk;
+    const uint64_t pol = e0 < p.keep_n ? pol_pre : pol_rest;
     const int64_t e1 = min(e0 + (int64_t)InT<DT>::kChunk, p.n);
     const int g0 = cursor_group(p, span, e0);
     const bool one_group = p.off == nullptr || p.G <= 1 || (span.e0 <= e0 && e1 <= span.e1);
@@ -471,7 +478,7 @@ __device__ __forceinline__ void publish_cast_results(const KParams& p) {
 }
 
 template <int DT, int FMT>
-__global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
+__global__ void __launch_bounds__(kPtThreads, 4) cast_kernel(KParams p) {
   __shared__ uint32_t sh_max[kPtThreads / 32];
   __shared__ unsigned long long sh_sum[kPtThreads / 32];
   constexpr float kMax = Fmt<FMT>::kMax;
@@ -494,7 +501,8 @@ __global__ void __launch_bounds__(kPtThreads) cast_kernel(KParams p) {
 
   const int64_t c_begin = p.n_chunks * blockIdx.x / gridDim.x;
   const int64_t c_end = p.n_chunks * (blockIdx.x + 1) / gridDim.x;
-  cast_pass<DT, FMT>(p, c_begin, c_end, load_policy(p.l2_hint), hist_scale, sh_max, sh_sum);
+  cast_pass<DT, FMT>(p, c_begin, c_end, load_policy(p.l2_hint), load_policy(p.l2_hint_pre), hist_scale, sh_max,
+                     sh_sum);
   pdl_launch_dependents();  // main work done: the next kernel may launch
 
   // The last CTA publishes per-group results and returns the scratch it used
@@ -553,6 +561,8 @@ static KParams make_params(const PtLaunch& L) {
   p.hist_slot = L.hist_slot;
   p.flag = L.flag;
   p.l2_hint = L.l2_hint;
+  p.keep_n = L.keep_n;
+  p.l2_hint_pre = L.l2_hint_pre;
   return p;
 }
 
