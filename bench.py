@@ -736,9 +736,18 @@ def op_table(P, peak):
     for j, op in enumerate(P.ops):
         ms, n = time_op(P, j)
         gbs = op["bytes"] / (ms * 1e-3) / 1e9
-        rows.append({"op": P.cfg["ops"][j] if "ops" in P.cfg else op["kind"], "kernels": kernel_label(op),
-                     "us_per_call": round(ms * 1e3, 3), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                     "calls_timed": n, "bytes_per_call": op["bytes"]})
+        row = {"op": P.cfg["ops"][j] if "ops" in P.cfg else op["kind"], "kernels": kernel_label(op),
+               "us_per_call": round(ms * 1e3, 3), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+               "calls_timed": n, "bytes_per_call": op["bytes"]}
+        if op["kind"] in ("current", "current_grouped"):
+            # the method reads x twice (amax before any cast, 5 B per BF16
+            # element); against the compulsory floor of one read and one
+            # write (3 B per element) the same time reads lower
+            r, c = op["shape"]
+            floor = 3 * r * c
+            row["floor_bytes_per_call"] = floor
+            row["floor_frac"] = round(floor / (ms * 1e-3) / 1e9 / peak, 4)
+        rows.append(row)
     return rows
 
 
