@@ -553,7 +553,7 @@ class Prepared:
             return (lib.fp8q_cast_per_tensor, (
                 b["x"].data_ptr(), 0, r, c, off_ptr if g else None, op.get("G", 1), op["fmt"], 0, None,
                 b["q"].data_ptr(), pt["amax"].data_ptr(), pt["scale"].data_ptr(), pt["scale_inv"].data_ptr(), None,
-                b["ws"].data_ptr(), b["ws"].numel(), stream)), 2
+                b["ws"].data_ptr(), b["ws"].numel(), stream)), 1 if not g and r * c <= current_one_launch_elems() else 2
         if k == "mx_mma":
             o = b["out"]
             return (lib.mxfp8_quantize_ex, (
@@ -647,6 +647,41 @@ class Prepared:
         for st in self.states:
             if st is not None:
                 st.close()
+
+
+def current_one_launch_elems():
+    """Largest BF16 tensor whose ungrouped current scaling is one launch:
+    one 16384-element slice per resident CTA, 4 CTAs per SM (larger tensors
+    take the amax and the cast kernel)."""
+    import torch
+    return 4 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count * 16384
+
+
+def time_graph(P, k):
+    """Milliseconds per step with the steps replayed from one CUDA graph, so
+    that no host launch cost is in the way: steps 0..m-1 (m = min(k, 256),
+    rotating over the buffer sets as the loop does) captured once on the
+    current stream, the graph replayed until at least k steps ran, CUDA
+    events around the replays."""
+    import torch
+    m = max(1, min(k, 256))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.current_stream()):
+        for i in range(m):
+            P.step(i)
+    reps = max(1, -(-k // m))
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    P.fq.check_device()
+    del g
+    return e0.elapsed_time(e1) / (reps * m)
 
 
 def time_loop(fn, n):
@@ -900,6 +935,13 @@ def measure_config(name, dev, peak, peak_src, steps, warmup):
     """One of the other configurations, measured as the headline is (device
     time of whole steps; each op timed alone in back-to-back loops)."""
     import torch
+    side = torch.cuda.Stream(dev)  # a graph cannot capture the legacy stream
+    with torch.cuda.stream(side):
+        return _measure_config(name, dev, peak, peak_src, steps, warmup)
+
+
+def _measure_config(name, dev, peak, peak_src, steps, warmup):
+    import torch
     P = Prepared(name, dev)
     try:
         est = time_loop(lambda i: P.step(i), 3)
@@ -917,6 +959,14 @@ def measure_config(name, dev, peak, peak_src, steps, warmup):
                "value": round(gbs, 2), "unit": "GB/s", "frac_of_hbm_peak": round(gbs / peak, 4),
                "bytes_per_step": P.bytes_per_step, "gpu_launches": launches, "ops": ops, "roofline": rf,
                "l2": P.l2_note}
+        try:
+            gms = time_graph(P, k)
+            ggbs = P.bytes_per_step / (gms * 1e-3) / 1e9
+            res["graph"] = {"ms_per_step": round(gms, 5), "value": round(ggbs, 2), "unit": "GB/s",
+                            "frac_of_hbm_peak": round(ggbs / peak, 4),
+                            "timing": "the same steps replayed from one CUDA graph (no host launch cost)"}
+        except Exception as e:  # a capture the runtime refuses: report the loop only
+            res["graph"] = {"unavailable": repr(e)[:200]}
         if name == "delayed_8192":
             res["delayed_vs_current"] = delayed_vs_current(P)
         return res

@@ -98,7 +98,8 @@ FP8Q_API const char* fp8q_last_error_string(void);
  * Synchronizes `stream`, then reports and clears device-side failures that
  * earlier calls on this device recorded: FP8Q_ERR_TIMEOUT when a bounded
  * wait inside a kernel (the shared-memory barriers of the MXFP8 and the
- * blockwise pipelines) gave up, in which case that call's outputs are
+ * blockwise pipelines, the grid-wide wait for the scale in the single-launch
+ * current scaling) gave up, in which case that call's outputs are
  * incomplete.  FP8Q_OK otherwise.
  */
 FP8Q_API fp8q_status fp8q_check_device(void* stream);
@@ -121,6 +122,18 @@ FP8Q_API fp8q_status fp8q_set_wait_budget_ns(uint64_t ns);
  * device; leave it off (the default) outside such tests.
  */
 FP8Q_API fp8q_status fp8q_debug_stall_mx_producer(int32_t on);
+
+/*
+ * Test hook for the same failure path in the single-launch current scaling
+ * of fp8q_cast_per_tensor (taken for an ungrouped tensor small enough that
+ * all of its CTAs are resident at once).  While `on` is nonzero, the CTA
+ * that should publish the scale does not, so every other CTA's wait for it
+ * gives up after the wait budget: no codes are written, fp8q_check_device
+ * reports FP8Q_ERR_TIMEOUT, and the workspace is zero-filled again by the
+ * last CTA to leave.  Applies to kernels launched afterwards on the current
+ * device; leave it off (the default) outside such tests.
+ */
+FP8Q_API fp8q_status fp8q_debug_stall_scale_publish(int32_t on);
 
 /*
  * amax_out[g] = max |x| over group g, bit-exact: the FP32 value whose bits
@@ -165,7 +178,11 @@ FP8Q_API size_t fp8q_cast_workspace_bytes(int32_t num_groups);
  *   1-2; "混合精度与 FP8 训练" 8.2): amax[g] is reduced first, then
  *   scale[g] = fl32(fl32(F8max / amax[g]) * 2^-margin), with amax = 0 giving
  *   scale 1, a non-finite amax giving scale 1, and an overflowing quotient
- *   giving FLT_MAX.  Two passes over x (read, read + write).
+ *   giving FLT_MAX.  Two passes over x (read, read + write), except for
+ *   an ungrouped tensor small enough that one CTA per 32 KB slice is
+ *   resident at once (up to about 10M BF16 elements on a GB300): one
+ *   launch then reads x once, keeps each slice in registers while the
+ *   scale is published, and casts from there.
  * scale_in != NULL: device float[num_groups] scales are used as given; if
  *   amax_out is non-NULL the amax of x is reduced in the same single pass.
  *
@@ -180,8 +197,10 @@ FP8Q_API size_t fp8q_cast_workspace_bytes(int32_t num_groups);
  *                  > F8max (NaN not counted), i.e. clamped by the cast
  *   workspace      device, >= fp8q_cast_workspace_bytes(num_groups) bytes,
  *                  8-byte aligned, zero-filled before its first use; every
- *                  successful call leaves it zero-filled again.  Calls that
- *                  may overlap on the GPU need separate workspaces.
+ *                  successful call leaves it zero-filled again (after a
+ *                  call that fp8q_check_device reports as timed out, fill
+ *                  it with zeros again).  Calls that may overlap on the GPU
+ *                  need separate workspaces.
  */
 FP8Q_API fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t rows, int64_t cols,
                                  const int64_t* group_offsets, int32_t num_groups,

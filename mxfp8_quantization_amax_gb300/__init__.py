@@ -26,7 +26,7 @@ __all__ = [
     "E4M3", "E5M2", "ROW", "COL", "BOTH", "build", "library_path", "lib",
     "fp8q_amax", "fp8q_cast_per_tensor", "fp8q_cast_workspace_bytes", "DelayedScaling",
     "mxfp8_quantize", "mxfp8_col_blocks", "Fp8qError", "check_device", "set_wait_budget_ns",
-    "fp8q_scale_from_amax", "debug_stall_mx_producer", "fp8q_dequantize_per_tensor", "mxfp8_dequantize",
+    "fp8q_scale_from_amax", "debug_stall_mx_producer", "debug_stall_scale_publish", "fp8q_dequantize_per_tensor", "mxfp8_dequantize",
     "RULE_UP", "RULE_OCP", "BLOCK_1X128", "BLOCK_128X128", "fp8q_quantize_blockwise", "fp8q_quantize_nvfp4",
     "fp8q_qstats_workspace_bytes", "fp8q_qstats_per_tensor", "mxfp8_qstats", "qstats_dict",
     "E2M1", "E2M3", "E3M2", "mx_quantize_fp4_fp6", "mx_scales_to_mma_layout",
@@ -56,6 +56,7 @@ _SIGS = {
     "fp8q_last_error_string": (_c.c_char_p, []),
     "fp8q_check_device": (_c.c_int, [_P]),
     "fp8q_debug_stall_mx_producer": (_c.c_int, [_c.c_int32]),
+    "fp8q_debug_stall_scale_publish": (_c.c_int, [_c.c_int32]),
     "fp8q_scale_from_amax": (_c.c_int, [_P, _c.c_int32, _c.c_int32, _c.c_int32, _P, _P, _P]),
     "mxfp8_quantize_rule": (_c.c_int, [_P, _c.c_int32, _c.c_int64, _c.c_int64, _P, _c.c_int32, _c.c_int32,
                                        _c.c_int32, _c.c_int32, _P, _P, _P, _P, _c.c_int64, _P, _P]),
@@ -197,6 +198,12 @@ def debug_stall_mx_producer(on: bool):
     """Test hook: the BF16 MXFP8 kernel's producer issues no loads while on,
     so its consumers' bounded waits expire (reported by check_device)."""
     _check(lib().fp8q_debug_stall_mx_producer(1 if on else 0), "fp8q_debug_stall_mx_producer")
+
+
+def debug_stall_scale_publish(on: bool):
+    """Test hook: while on, the single-launch current scaling never publishes
+    its scale, so the waits for it expire (reported by check_device)."""
+    _check(lib().fp8q_debug_stall_scale_publish(1 if on else 0), "fp8q_debug_stall_scale_publish")
 
 
 # ---------------------------------------------------------------------------

@@ -150,6 +150,11 @@ fp8q_status fp8q_debug_stall_mx_producer(int32_t on) {
   return mx_set_stall_producer(on != 0);
 }
 
+fp8q_status fp8q_debug_stall_scale_publish(int32_t on) {
+  g_err[0] = 0;
+  return pt_set_stall_publish(on != 0);
+}
+
 fp8q_status fp8q_amax(const void* x, int32_t dt, int64_t rows, int64_t cols, const int64_t* group_offsets,
                       int32_t num_groups, float* amax_out, void* stream) {
   g_err[0] = 0;
@@ -243,8 +248,9 @@ fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t rows, int64_
   L.sat_out = sat_count_out;
   L.stream = (cudaStream_t)stream;
   if (scale_in == nullptr) {
-    // current scaling: amax pass (publishes scales), then the cast.  The
-    // first kL2KeepBytes of x (all of a tensor that small) are kept in L2
+    // current scaling.  A small ungrouped tensor takes one launch that reads
+    // x once (launch_current_fused); any other takes the amax pass
+    // (publishes scales), then the cast.  The first kL2KeepBytes of x (all of a tensor that small) are kept in L2
     // for the second pass: evict-last in the amax pass, which reads the rest
     // evict-first so that it does not push the prefix out, and evict-first
     // (last use) in the cast.
@@ -254,6 +260,8 @@ fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t rows, int64_
     A.amax_out = amax_out;
     A.scale_out = scale_out;
     A.scale_inv_out = scale_inv_out;
+    bool taken = false;
+    if ((r = launch_current_fused(A, &taken)) != FP8Q_OK || taken) return r;
     A.sat_acc = nullptr;
     A.keep_n = FP8Q_PT_KEEP_PREFIX || rows * cols * esz <= kL2KeepBytes ? kL2KeepBytes / esz : 0;
     A.l2_hint_pre = 1;

@@ -108,6 +108,10 @@ constexpr int64_t kL2KeepBytes = 48ll << 20;
 fp8q_status launch_amax(const PtLaunch& p, bool finalize_scales);
 // Cast pass (optionally with fused amax into acc[] and saturation counts).
 fp8q_status launch_cast(const PtLaunch& p);
+// Current scaling in one launch (amax, scale and cast; the tensor read once)
+// for an ungrouped tensor small enough that every CTA is resident; *taken is
+// false, and nothing is launched, for any other.
+fp8q_status launch_current_fused(const PtLaunch& p, bool* taken);
 
 // Dequantization; kind 0 per-tensor, 1 MX rowwise copy, 2 MX columnwise copy.
 fp8q_status launch_dequant(int kind, const uint8_t* q, const uint8_t* s, const float* scale_inv,
@@ -139,5 +143,6 @@ fp8q_status launch_scale(const float* amax, int G, int fmt, int margin, float* s
                          cudaStream_t s);
 fp8q_status pt_device_status(bool clear, unsigned* word);
 fp8q_status pt_set_wait_budget(unsigned long long ns);
+fp8q_status pt_set_stall_publish(bool on);
 
 }  // namespace fp8q

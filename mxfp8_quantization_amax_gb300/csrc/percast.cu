@@ -18,6 +18,7 @@
 
 #include "fp8q_device.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace fp8q {
 
@@ -43,7 +44,9 @@ template <> struct InT<kFP32> {
   }
 };
 
-// The kernels in this file wait on nothing; their failure word stays zero.
+// Failure word of this file's kernels: bit 0 is set when the single-launch
+// current scaling gave up waiting for its scale.  Read and cleared by
+// fp8q_check_device().
 __device__ unsigned int g_pt_error;
 
 struct KParams {
@@ -516,6 +519,172 @@ __global__ void __launch_bounds__(kPtThreads, 4) cast_kernel(KParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Current scaling of a small ungrouped tensor in one launch
+// ---------------------------------------------------------------------------
+// One chunk per CTA, every CTA resident at once (a cooperative launch).  A
+// CTA loads its chunk into registers and merges its amax; the last CTA to
+// arrive turns the amax into the scale and publishes it (publish_scales);
+// the others wait for it and cast from their registers.  x is read once and
+// the two passes need no second launch.  The counter holds the arrivals and
+// departures in its low bits and kPublished once the scale is out; the last
+// CTA to depart publishes the saturation count and returns the workspace to
+// zero.  The wait is bounded: a CTA that gives up records it in g_pt_error
+// and writes no codes.
+constexpr unsigned kPublished = 0x80000000u;
+__device__ unsigned long long g_pt_wait_budget_ns = 1000000000ull;
+// Test hook: while nonzero the last CTA to arrive does not publish, so
+// every other CTA's wait runs out its budget.
+__device__ unsigned g_pt_stall_publish;
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Spins until `*word` has kPublished set; false once budget_ns has passed.
+__device__ __forceinline__ bool wait_published(const unsigned* word, uint64_t budget_ns) {
+  if (ld_acquire_u32(word) & kPublished) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1; !(ld_acquire_u32(word) & kPublished); ++n) {
+    if ((n & 15u) == 0 && globaltimer_ns() - t0 > budget_ns) return false;
+  }
+  return true;
+}
+
+#ifndef FP8Q_PT_FUSED_VECS  // 16-byte vectors per thread of the single-launch path
+#define FP8Q_PT_FUSED_VECS 8
+#endif
+template <int DT> struct FusedChunk {
+  static constexpr int kVecs = FP8Q_PT_FUSED_VECS;
+  static constexpr int kElems = kPtThreads * kVecs * InT<DT>::kPerVec;
+};
+
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kPtThreads, 4) current_fused_kernel(KParams p) {
+  __shared__ uint32_t sh_max[kPtThreads / 32];
+  __shared__ unsigned long long sh_sum[kPtThreads / 32];
+  __shared__ float sh_scale;
+  __shared__ int sh_state;  // 1: scale published, 0: wait gave up
+  constexpr int PV = InT<DT>::kPerVec;
+  constexpr int V = FusedChunk<DT>::kVecs;
+  constexpr float kMax = Fmt<FMT>::kMax;
+  constexpr int kEsz = DT == kBF16 ? 2 : 4;
+  pdl_wait();
+
+  const int64_t e0 = (int64_t)blockIdx.x * FusedChunk<DT>::kElems;
+  const int64_t e1 = min(e0 + (int64_t)FusedChunk<DT>::kElems, p.n);
+  const bool whole = e1 - e0 == FusedChunk<DT>::kElems;
+  const uint64_t pol = policy_evict_first();
+  uint4 v[V];
+  uint32_t m = 0;
+  if (whole) {
+#pragma unroll
+    for (int k = 0; k < V; k++)
+      v[k] = ld_hint((const char*)p.x + (e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV) * kEsz, pol);
+#pragma unroll
+    for (int k = 0; k < V; k++) reg_fence(v[k]);
+    if constexpr (DT == kBF16) {
+      uint32_t h = 0;
+#pragma unroll
+      for (int k = 0; k < V; k++) {
+        h = absmax_bf16x2(h, v[k].x);
+        h = absmax_bf16x2(h, v[k].y);
+        h = absmax_bf16x2(h, v[k].z);
+        h = absmax_bf16x2(h, v[k].w);
+      }
+      m = max(h << 16, h & 0xFFFF0000u);
+    } else {
+#pragma unroll
+      for (int k = 0; k < V; k++)
+        m = max(max(m, max(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu)),
+                max(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu));
+    }
+  } else {  // the ragged last chunk: element by element (read again below)
+    for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) m = max(m, InT<DT>::bits(p.x, e) & 0x7FFFFFFFu);
+  }
+  m = block_max(m, sh_max);
+
+  // Arrival, by thread 0 for the CTA: its amax, then a ticket.  The tickets
+  // form one chain of read-modify-writes with release semantics, so the last
+  // CTA's acquiring ticket sees every other CTA's amax; it publishes the
+  // scale with a releasing add, which the others' acquiring polls see.
+  if (threadIdx.x == 0) {
+    if (m != 0) atomicMax(p.acc, m);
+    if (atom_add_acq_rel(p.counter, 1u) == gridDim.x - 1u) {
+      if (!*(volatile unsigned*)&g_pt_stall_publish) {
+        publish_scales(p);  // one group: thread 0 alone does all of it
+        sh_scale = *(volatile float*)p.ws_scale;
+        sh_state = 1;
+        red_add_release(p.counter, kPublished);
+      } else {
+        sh_state = 0;
+      }
+    } else {
+      const bool ok = wait_published(p.counter, g_pt_wait_budget_ns);
+      sh_state = ok;
+      if (ok) {
+        sh_scale = *(volatile float*)p.ws_scale;
+      } else {
+        atomicOr(&g_pt_error, 1u);
+      }
+    }
+  }
+  __syncthreads();
+  const bool ok = sh_state != 0;
+  const float s = sh_scale;
+
+  // cast from the registers
+  unsigned long long nsat = 0;
+  if (ok) {
+    uint32_t unused = 0;
+    if (whole) {
+#pragma unroll
+      for (int k = 0; k < V; k++)
+        cast_vec<DT, FMT>(p, v[k], e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV, s, false,
+                          p.sat_acc != nullptr, unused, nsat);
+    } else {
+      for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) {
+        const float f = __fmul_rn(__uint_as_float(InT<DT>::bits(p.x, e)), s);
+        nsat += fabsf(f) > kMax;
+        p.q[e] = (uint8_t)canon_nan4<FMT>(cvt2<FMT>(f, 0.0f));
+      }
+    }
+  }
+  pdl_launch_dependents();
+  unsigned long long t = 0;
+  if (p.sat_acc != nullptr) t = block_sum(nsat, sh_sum);
+
+  // Departure, by thread 0: its saturation count, then a ticket on the same
+  // chain; the last CTA to depart publishes the count and clears the
+  // workspace.  The codes need no ordering with it.
+  if (threadIdx.x == 0) {
+    if (t != 0) atomicAdd(p.sat_acc, t);
+    const unsigned ticket = atom_add_acq_rel(p.counter, 1u) & ~kPublished;
+    if (ticket == 2u * gridDim.x - 1u) {
+      if (p.sat_acc != nullptr) {
+        const unsigned long long total = *(volatile unsigned long long*)p.sat_acc;
+        if (p.sat_out && ok) *p.sat_out = total;
+        *p.sat_acc = 0;
+      }
+      *p.acc = 0;
+      *p.ws_scale = 0.0f;
+      *p.counter = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Scales from given amaxes (the cast pass of a tensor split across devices,
 // after the per-device amaxes were combined)
 // ---------------------------------------------------------------------------
@@ -649,6 +818,61 @@ fp8q_status launch_cast(const PtLaunch& L) {
   return check_launch("cast kernel");
 }
 
+// Single-launch current scaling (current_fused_kernel): taken for an
+// ungrouped, non-empty tensor whose chunks fit one per resident CTA.
+#ifndef FP8Q_PT_FUSED  // 0: always the two-pass path
+#define FP8Q_PT_FUSED 1
+#endif
+#ifndef FP8Q_PT_FUSED_PDL  // 1: the launch also allows programmatic overlap with the kernel before it
+#define FP8Q_PT_FUSED_PDL 1
+#endif
+#ifndef FP8Q_PT_FUSED_COOP  // 1: a cooperative launch (all CTAs resident, or the launch fails)
+#define FP8Q_PT_FUSED_COOP 1
+#endif
+template <int DT, int FMT>
+static cudaError_t launch_fused_t(const KParams& p, int64_t chunks, cudaStream_t s, bool* taken) {
+  static const int per_sm = ctas_per_sm(current_fused_kernel<DT, FMT>);
+  *taken = false;
+  if (!FP8Q_PT_FUSED || chunks > (int64_t)per_sm * sm_count()) return cudaSuccess;
+  *taken = true;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)chunks);
+  cfg.blockDim = dim3(kPtThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (FP8Q_PT_FUSED_COOP) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na++].val.cooperative = 1;
+  }
+  if (FP8Q_PT_FUSED_PDL && FP8Q_PDL) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na++].val.programmaticStreamSerializationAllowed = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, current_fused_kernel<DT, FMT>, p);
+}
+
+fp8q_status launch_current_fused(const PtLaunch& L, bool* taken) {
+  *taken = false;
+  if (L.rows * L.cols == 0 || L.G != 1) return FP8Q_OK;
+  KParams p = make_params(L);
+  const int64_t n = p.n;
+  cudaError_t e;
+  if (L.dt == kBF16) {
+    const int64_t c = (n + FusedChunk<kBF16>::kElems - 1) / FusedChunk<kBF16>::kElems;
+    e = L.fmt == kE4M3 ? launch_fused_t<kBF16, kE4M3>(p, c, L.stream, taken)
+                       : launch_fused_t<kBF16, kE5M2>(p, c, L.stream, taken);
+  } else {
+    const int64_t c = (n + FusedChunk<kFP32>::kElems - 1) / FusedChunk<kFP32>::kElems;
+    e = L.fmt == kE4M3 ? launch_fused_t<kFP32, kE4M3>(p, c, L.stream, taken)
+                       : launch_fused_t<kFP32, kE5M2>(p, c, L.stream, taken);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "current scaling kernel launch");
+  return *taken ? check_launch("current scaling kernel") : FP8Q_OK;
+}
+
 fp8q_status launch_scale(const float* amax, int G, int fmt, int margin, float* scale_out, float* scale_inv_out,
                          cudaStream_t s) {
   const int blocks = (G + kPtThreads - 1) / kPtThreads;
@@ -671,6 +895,15 @@ fp8q_status pt_device_status(bool clear, unsigned* word) {
   return FP8Q_OK;
 }
 
-fp8q_status pt_set_wait_budget(unsigned long long) { return FP8Q_OK; }
+fp8q_status pt_set_wait_budget(unsigned long long ns) {
+  const cudaError_t e = cudaMemcpyToSymbol(g_pt_wait_budget_ns, &ns, sizeof(ns));
+  return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, "cudaMemcpyToSymbol(wait budget)");
+}
+
+fp8q_status pt_set_stall_publish(bool on) {
+  const unsigned v = on ? 1u : 0u;
+  const cudaError_t e = cudaMemcpyToSymbol(g_pt_stall_publish, &v, sizeof(v));
+  return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, "cudaMemcpyToSymbol(stall)");
+}
 
 }  // namespace fp8q

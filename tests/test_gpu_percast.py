@@ -115,6 +115,20 @@ def test_current_scaling_ragged_sizes(fq, shape):
     check_current(fq, synth.f32_tensor(shape[0], shape[1], seed=32), oracle.E5M2)
 
 
+def test_current_scaling_single_launch_boundary(fq):
+    """Ungrouped current scaling takes one launch while every 32 KB slice of
+    x has a resident CTA (4 per SM here), two passes beyond: the largest
+    single-launch tensors, one slice more, and a ragged last slice, in both
+    input types."""
+    cap = 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    for rows, seed in ((cap * 4, 71), (cap * 4 + 4, 72), (cap * 4 - 1, 73)):
+        check_current(fq, synth.normal_outliers(rows, 4096, seed=seed), oracle.E4M3)
+    for rows, seed in ((cap * 2, 74), (cap * 2 + 1, 75)):
+        check_current(fq, synth.f32_tensor(rows, 4096, seed=seed), oracle.E5M2, margin=1)
+    # one element short of the largest single-launch tensor: a ragged last slice
+    check_current(fq, synth.normal_outliers(1, cap * 16384 - 1, seed=76), oracle.E4M3)
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_current_scaling_grouped(fq, fmt):
     """Per-expert scaling on ragged groups (empty, 1-row, boundary-straddling chunks)."""

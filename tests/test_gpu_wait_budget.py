@@ -47,3 +47,39 @@ def test_expired_wait_is_reported_and_context_survives():
     fq.check_device()
     for k, v in ref.items():
         assert np.array_equal(again[k].cpu().numpy(), v.numpy()), k
+
+
+def test_expired_scale_wait_is_reported_and_workspace_cleared():
+    """Single-launch current scaling: the CTA that should publish the scale
+    holds it back (test hook), so every other CTA's wait for it expires.  No
+    code is written, the call is reported, the workspace is zero again, and
+    the next call is whole."""
+    fq = require_cuda()
+    g = torch.Generator().manual_seed(9)
+    x = (torch.randn(1024, 1024, generator=g) * 3).to(torch.bfloat16).cuda()
+    ws = torch.zeros(fq.fp8q_cast_workspace_bytes(1), dtype=torch.uint8, device="cuda")
+    ref = fq.fp8q_cast_per_tensor(x, fq.E4M3, want_sat=True, workspace=ws)
+    fq.check_device()
+    ref = {k: v.cpu() for k, v in ref.items() if isinstance(v, torch.Tensor)}
+
+    q = torch.full((1024, 1024), 0x5A, dtype=torch.uint8, device="cuda")
+    try:
+        fq.set_wait_budget_ns(10 ** 6)
+        fq.debug_stall_scale_publish(True)
+        fq.fp8q_cast_per_tensor(x, fq.E4M3, want_sat=True, q=q, workspace=ws)
+        status = fq.lib().fp8q_check_device(fq._stream())
+        msg = fq.lib().fp8q_last_error_string()
+    finally:
+        fq.debug_stall_scale_publish(False)
+        fq.set_wait_budget_ns(10 ** 9)
+    assert status == FP8Q_ERR_TIMEOUT
+    assert b"gave up" in msg
+    assert bool((q == 0x5A).all()), "codes written without a published scale"
+    assert int(ws.count_nonzero()) == 0, "workspace not left zero-filled"
+
+    fq.check_device()
+    again = fq.fp8q_cast_per_tensor(x, fq.E4M3, want_sat=True, workspace=ws)
+    fq.check_device()
+    for k, v in ref.items():
+        assert torch.equal(again[k].cpu(), v), k
+    assert int(ws.count_nonzero()) == 0
