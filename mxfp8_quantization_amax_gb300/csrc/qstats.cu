@@ -622,6 +622,32 @@ static_assert(kQtUnit >= 1 && kQtUnit <= 4, "a unit's scale bytes of a column fi
 __device__ unsigned int g_qs_error;
 __device__ unsigned long long g_qs_budget_ns = 1000000000ull;
 
+#ifndef FP8Q_QS_BLOCK_SPLIT  // 1: CTAs take equal ranges of blocks, 0: of whole units
+#define FP8Q_QS_BLOCK_SPLIT 1
+#endif
+
+// Blocks are numbered unit by unit: row group ti (kQtUnit row blocks, fewer
+// in a ragged last group), strip by strip, and within a unit by row block.
+// A run is the part of one unit that lies in a CTA's range of blocks.
+struct QtRun {
+  int64_t ti;    // row group
+  int64_t c0;    // first column of the strip
+  int j0, j1;    // row blocks [j0, j1) of the unit
+  int nblk;      // row blocks in the whole unit
+};
+
+__device__ __forceinline__ QtRun qt_run(int64_t b, int64_t b_end, int64_t nbr, int64_t strips) {
+  QtRun r;
+  r.ti = b / ((int64_t)kQtUnit * strips);
+  const int64_t rem = b - r.ti * kQtUnit * strips;
+  r.nblk = (int)min((int64_t)kQtUnit, nbr - r.ti * kQtUnit);
+  const int64_t strip = rem / r.nblk;
+  r.c0 = strip * kQtCols;
+  r.j0 = (int)(rem - strip * r.nblk);
+  r.j1 = (int)min((int64_t)r.nblk, r.j0 + (b_end - b));
+  return r;
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kQtThreads, 4)
     qstats_col_tma_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap qmap,
@@ -647,8 +673,20 @@ __global__ void __launch_bounds__(kQtThreads, 4)
   __syncthreads();
   const int64_t nbr = p.rows / 32;
   const int64_t strips = (p.cols + kQtCols - 1) / kQtCols;
-  const int64_t units = (nbr + kQtUnit - 1) / kQtUnit * strips;
-  const int64_t u_begin = units * blockIdx.x / gridDim.x, u_end = units * (blockIdx.x + 1) / gridDim.x;
+  // this CTA's blocks [b_begin, b_end): equal shares of blocks, or of units
+  int64_t b_begin, b_end;
+  if (FP8Q_QS_BLOCK_SPLIT) {
+    const int64_t blocks = nbr * strips;
+    b_begin = blocks * blockIdx.x / gridDim.x;
+    b_end = blocks * (blockIdx.x + 1) / gridDim.x;
+  } else {
+    const int64_t units = (nbr + kQtUnit - 1) / kQtUnit * strips;
+    const int64_t u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
+    // unit u starts at block u * kQtUnit, except in a ragged last row group
+    const int64_t full = nbr / kQtUnit * strips;
+    b_begin = u0 <= full ? u0 * kQtUnit : full * kQtUnit + (u0 - full) * (nbr % kQtUnit);
+    b_end = u1 <= full ? u1 * kQtUnit : full * kQtUnit + (u1 - full) * (nbr % kQtUnit);
+  }
   const uint64_t budget = g_qs_budget_ns;
   QsAcc a;
 
@@ -657,12 +695,12 @@ __global__ void __launch_bounds__(kQtThreads, 4)
     if (lane == 0) {
       int64_t k = 0;
       bool stop = false;
-      for (int64_t u = u_begin; u < u_end && !abort_flag && !stop; u++) {
-        const int64_t ti = u / strips;
-        const int c0 = (int)((u - ti * strips) * kQtCols);
-        const int64_t rb0 = ti * kQtUnit;
-        const int nblk = (int)min((int64_t)kQtUnit, nbr - rb0);
-        for (int j = 0; j < nblk; j++, ++k) {
+      for (int64_t b = b_begin; b < b_end && !abort_flag && !stop;) {
+        const QtRun run = qt_run(b, b_end, nbr, strips);
+        b += run.j1 - run.j0;
+        const int c0 = (int)run.c0;
+        const int64_t rb0 = run.ti * kQtUnit;
+        for (int j = run.j0; j < run.j1; j++, ++k) {
           const int s = (int)(k % kQtStages);
           const uint32_t round = (uint32_t)(k / kQtStages);
           if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u, budget)) {
@@ -688,30 +726,31 @@ __global__ void __launch_bounds__(kQtThreads, 4)
     // ---------------- consumers ----------------
     const float nan = __uint_as_float(0x7FC00000u);
     int64_t k = 0;
-    for (int64_t u = u_begin; u < u_end && !abort_flag; u++) {
-      const int64_t ti = u / strips;
-      const int64_t c0 = (u - ti * strips) * kQtCols;
-      const int64_t rb0 = ti * kQtUnit;
-      const int nblk = (int)min((int64_t)kQtUnit, nbr - rb0);
+    for (int64_t b = b_begin; b < b_end && !abort_flag;) {
+      const QtRun run = qt_run(b, b_end, nbr, strips);
+      b += run.j1 - run.j0;
+      const int64_t c0 = run.c0;
+      const int64_t rb0 = run.ti * kQtUnit;
       const int64_t c = c0 + 2 * tid;  // this thread's columns c, c + 1
       const bool col_ok = c < p.cols;
-      // the two columns' scale bytes of the unit's blocks
+      // the two columns' scale bytes of the run's blocks (byte j of the unit)
       uint32_t sa = 0, sb = 0;
       if (col_ok) {
         const uint8_t* ea = p.s + c * p.s_ld + rb0;
         const uint8_t* eb = ea + p.s_ld;
-        if (nblk == kQtUnit && rb0 + kQtUnit <= p.s_ld && (((uintptr_t)ea | (uintptr_t)eb) & 3u) == 0) {
+        if (run.j0 == 0 && run.j1 == kQtUnit && rb0 + kQtUnit <= p.s_ld &&
+            (((uintptr_t)ea | (uintptr_t)eb) & 3u) == 0) {
           sa = __ldg((const unsigned*)ea);
           sb = __ldg((const unsigned*)eb);
         } else {
-          for (int j = 0; j < nblk && rb0 + j < p.s_ld; j++) {
+          for (int j = run.j0; j < run.j1 && rb0 + j < p.s_ld; j++) {
             sa |= (uint32_t)__ldg(ea + j) << (8 * j);
             sb |= (uint32_t)__ldg(eb + j) << (8 * j);
           }
         }
       }
       bool gave_up = false;
-      for (int j = 0; j < nblk; j++, ++k) {
+      for (int j = run.j0; j < run.j1; j++, ++k) {
         const int s = (int)(k % kQtStages);
         const uint32_t round = (uint32_t)(k / kQtStages);
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], round & 1u, budget))) {
@@ -866,12 +905,12 @@ static cudaError_t qs_col_tma(const QsParams& p, cudaStream_t stream, bool* used
       attr = true;
     }
   }
-  const int64_t units = (p.rows / 32 + kQtUnit - 1) / kQtUnit * ((p.cols + kQtCols - 1) / kQtCols);
-  // each CTA a contiguous range of units: one wave of resident CTAs (every
+  const int64_t blocks = p.rows / 32 * ((p.cols + kQtCols - 1) / kQtCols);
+  // each CTA a contiguous range of blocks: one wave of resident CTAs (every
   // CTA ends with a block reduction and a ticket, which many small CTAs
-  // would repeat), at most one CTA per unit
+  // would repeat), at most one CTA per block
   int64_t grid = (int64_t)FP8Q_QS_TMA_CTAS_PER_SM * sm_count();
-  if (grid > units) grid = units;
+  if (grid > blocks) grid = blocks;
   if (grid > kQsMaxGrid) grid = kQsMaxGrid;
   *used = true;
   return launch_kernel(kernel, dim3((unsigned)grid), dim3(kQtThreads), smem, stream, xmap, qmap, p);
