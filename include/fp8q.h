@@ -179,10 +179,10 @@ FP8Q_API size_t fp8q_cast_workspace_bytes(int32_t num_groups);
  *   scale[g] = fl32(fl32(F8max / amax[g]) * 2^-margin), with amax = 0 giving
  *   scale 1, a non-finite amax giving scale 1, and an overflowing quotient
  *   giving FLT_MAX.  Two passes over x (read, read + write), except for
- *   an ungrouped tensor small enough that one CTA per 32 KB slice is
- *   resident at once (up to about 10M BF16 elements on a GB300): one
- *   launch then reads x once, keeps each slice in registers while the
- *   scale is published, and casts from there.
+ *   an ungrouped tensor small enough that its 32 KB slices fit one or two
+ *   per resident CTA (up to about 20M BF16 elements on a GB300): one
+ *   launch then reads x once, keeps the slices on chip (registers, shared
+ *   memory) while the scale is published, and casts from there.
  * scale_in != NULL: device float[num_groups] scales are used as given; if
  *   amax_out is non-NULL the amax of x is reduced in the same single pass.
  *

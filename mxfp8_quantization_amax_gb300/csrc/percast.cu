@@ -570,49 +570,92 @@ template <int DT> struct FusedChunk {
   static constexpr int kElems = kPtThreads * kVecs * InT<DT>::kPerVec;
 };
 
-template <int DT, int FMT>
+// Magnitude bits of a 16-byte vector folded into h (BF16: two lanes of
+// BF16 magnitudes, finished by absmax_bits; FP32: the bits themselves).
+template <int DT>
+__device__ __forceinline__ void absmax_fold(const uint4& v, uint32_t& h) {
+  if constexpr (DT == kBF16) {
+    h = absmax_bf16x2(h, v.x);
+    h = absmax_bf16x2(h, v.y);
+    h = absmax_bf16x2(h, v.z);
+    h = absmax_bf16x2(h, v.w);
+  } else {
+    h = max(max(h, max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu)), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu));
+  }
+}
+template <int DT>
+__device__ __forceinline__ uint32_t absmax_bits(uint32_t h) {
+  if constexpr (DT == kBF16) return max(h << 16, h & 0xFFFF0000u);
+  return h;
+}
+
+// SL slices per CTA: the first in registers, the second (SL == 2) staged in
+// shared memory by one bulk copy, which doubles the tensors that fit.
+template <int DT, int FMT, int SL>
 __global__ void __launch_bounds__(kPtThreads, 4) current_fused_kernel(KParams p) {
+  extern __shared__ uint4 fused_slice[];  // SL == 2: the CTA's second slice
+  __shared__ uint64_t slice_bar;
   __shared__ uint32_t sh_max[kPtThreads / 32];
   __shared__ unsigned long long sh_sum[kPtThreads / 32];
   __shared__ float sh_scale;
   __shared__ int sh_state;  // 1: scale published, 0: wait gave up
   constexpr int PV = InT<DT>::kPerVec;
   constexpr int V = FusedChunk<DT>::kVecs;
+  constexpr int kElems = FusedChunk<DT>::kElems;
   constexpr float kMax = Fmt<FMT>::kMax;
   constexpr int kEsz = DT == kBF16 ? 2 : 4;
   pdl_wait();
 
-  const int64_t e0 = (int64_t)blockIdx.x * FusedChunk<DT>::kElems;
-  const int64_t e1 = min(e0 + (int64_t)FusedChunk<DT>::kElems, p.n);
-  const bool whole = e1 - e0 == FusedChunk<DT>::kElems;
+  // slice held in registers: [e0, e1); second slice: [f0, f1), staged when whole
+  const int64_t e0 = (int64_t)blockIdx.x * SL * kElems;
+  const int64_t e1 = min(e0 + (int64_t)kElems, p.n);
+  const bool whole = e1 - e0 == kElems;
+  const int64_t f0 = e1, f1 = SL == 2 ? min(f0 + (int64_t)kElems, p.n) : f0;
+  const bool staged = SL == 2 && f1 - f0 == kElems;
   const uint64_t pol = policy_evict_first();
+  const uint64_t budget = g_pt_wait_budget_ns;
+  if constexpr (SL == 2) {
+    if (staged) {  // block-uniform
+      if (threadIdx.x == 0) {
+        mbar_init(&slice_bar, 1);
+        fence_barrier_init();
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&slice_bar, kElems * kEsz);
+        bulk_load(fused_slice, (const char*)p.x + f0 * kEsz, kElems * kEsz, &slice_bar, pol);
+      }
+    }
+  }
+
   uint4 v[V];
-  uint32_t m = 0;
+  uint32_t h = 0, m = 0;
   if (whole) {
 #pragma unroll
     for (int k = 0; k < V; k++)
       v[k] = ld_hint((const char*)p.x + (e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV) * kEsz, pol);
 #pragma unroll
     for (int k = 0; k < V; k++) reg_fence(v[k]);
-    if constexpr (DT == kBF16) {
-      uint32_t h = 0;
 #pragma unroll
-      for (int k = 0; k < V; k++) {
-        h = absmax_bf16x2(h, v[k].x);
-        h = absmax_bf16x2(h, v[k].y);
-        h = absmax_bf16x2(h, v[k].z);
-        h = absmax_bf16x2(h, v[k].w);
-      }
-      m = max(h << 16, h & 0xFFFF0000u);
-    } else {
-#pragma unroll
-      for (int k = 0; k < V; k++)
-        m = max(max(m, max(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu)),
-                max(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu));
-    }
-  } else {  // the ragged last chunk: element by element (read again below)
+    for (int k = 0; k < V; k++) absmax_fold<DT>(v[k], h);
+  } else {  // the ragged last slice: element by element (read again below)
     for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) m = max(m, InT<DT>::bits(p.x, e) & 0x7FFFFFFFu);
   }
+  bool landed = true;  // the staged slice arrived within the wait budget
+  if constexpr (SL == 2) {
+    if (staged) {
+      landed = __syncthreads_and(mbar_wait(&slice_bar, 0, budget)) != 0;
+      if (landed) {
+#pragma unroll
+        for (int k = 0; k < V; k++) absmax_fold<DT>(fused_slice[k * kPtThreads + threadIdx.x], h);
+      } else if (threadIdx.x == 0) {
+        atomicOr(&g_pt_error, 1u);
+      }
+    } else {
+      for (int64_t e = f0 + threadIdx.x; e < f1; e += kPtThreads) m = max(m, InT<DT>::bits(p.x, e) & 0x7FFFFFFFu);
+    }
+  }
+  m = max(m, absmax_bits<DT>(h));
   m = block_max(m, sh_max);
 
   // Arrival, by thread 0 for the CTA: its amax, then a ticket.  The tickets
@@ -644,8 +687,15 @@ __global__ void __launch_bounds__(kPtThreads, 4) current_fused_kernel(KParams p)
   const bool ok = sh_state != 0;
   const float s = sh_scale;
 
-  // cast from the registers
+  // cast from the registers (and the staged slice)
   unsigned long long nsat = 0;
+  auto cast_elems = [&](int64_t a, int64_t b) {
+    for (int64_t e = a + threadIdx.x; e < b; e += kPtThreads) {
+      const float f = __fmul_rn(__uint_as_float(InT<DT>::bits(p.x, e)), s);
+      nsat += fabsf(f) > kMax;
+      p.q[e] = (uint8_t)canon_nan4<FMT>(cvt2<FMT>(f, 0.0f));
+    }
+  };
   if (ok) {
     uint32_t unused = 0;
     if (whole) {
@@ -654,10 +704,19 @@ __global__ void __launch_bounds__(kPtThreads, 4) current_fused_kernel(KParams p)
         cast_vec<DT, FMT>(p, v[k], e0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV, s, false,
                           p.sat_acc != nullptr, unused, nsat);
     } else {
-      for (int64_t e = e0 + threadIdx.x; e < e1; e += kPtThreads) {
-        const float f = __fmul_rn(__uint_as_float(InT<DT>::bits(p.x, e)), s);
-        nsat += fabsf(f) > kMax;
-        p.q[e] = (uint8_t)canon_nan4<FMT>(cvt2<FMT>(f, 0.0f));
+      cast_elems(e0, e1);
+    }
+    if constexpr (SL == 2) {
+      if (staged) {
+        if (landed) {
+#pragma unroll
+          for (int k = 0; k < V; k++)
+            cast_vec<DT, FMT>(p, fused_slice[k * kPtThreads + threadIdx.x],
+                              f0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV, s, false, p.sat_acc != nullptr,
+                              unused, nsat);
+        }
+      } else {
+        cast_elems(f0, f1);
       }
     }
   }
@@ -681,6 +740,10 @@ __global__ void __launch_bounds__(kPtThreads, 4) current_fused_kernel(KParams p)
       *p.ws_scale = 0.0f;
       *p.counter = 0;
     }
+  }
+  if constexpr (SL == 2) {
+    // a copy that outlived the budget must land before the CTA exits
+    if (staged && !landed && threadIdx.x == 0) mbar_wait(&slice_bar, 0, 2000000000ull);
   }
 }
 
@@ -829,15 +892,15 @@ fp8q_status launch_cast(const PtLaunch& L) {
 #ifndef FP8Q_PT_FUSED_COOP  // 1: a cooperative launch (all CTAs resident, or the launch fails)
 #define FP8Q_PT_FUSED_COOP 1
 #endif
-template <int DT, int FMT>
-static cudaError_t launch_fused_t(const KParams& p, int64_t chunks, cudaStream_t s, bool* taken) {
-  static const int per_sm = ctas_per_sm(current_fused_kernel<DT, FMT>);
-  *taken = false;
-  if (!FP8Q_PT_FUSED || chunks > (int64_t)per_sm * sm_count()) return cudaSuccess;
-  *taken = true;
+#ifndef FP8Q_PT_FUSED_SLICES  // most slices per CTA of the single-launch path (1 or 2)
+#define FP8Q_PT_FUSED_SLICES 2
+#endif
+template <int DT, int FMT, int SL>
+static cudaError_t launch_fused_sl(const KParams& p, int64_t grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)chunks);
+  cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kPtThreads);
+  cfg.dynamicSmemBytes = SL == 2 ? (size_t)FusedChunk<DT>::kElems * (DT == kBF16 ? 2 : 4) : 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
@@ -851,7 +914,36 @@ static cudaError_t launch_fused_t(const KParams& p, int64_t chunks, cudaStream_t
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, current_fused_kernel<DT, FMT>, p);
+  return cudaLaunchKernelEx(&cfg, current_fused_kernel<DT, FMT, SL>, p);
+}
+
+// Resident CTAs per SM of current_fused_kernel<DT, FMT, SL> (SL == 2 with
+// its shared-memory slice).
+template <int DT, int FMT, int SL>
+static int fused_per_sm() {
+  int per_sm = 0;
+  const size_t smem = SL == 2 ? (size_t)FusedChunk<DT>::kElems * (DT == kBF16 ? 2 : 4) : 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, current_fused_kernel<DT, FMT, SL>, kPtThreads, smem) !=
+          cudaSuccess)
+    per_sm = 0;
+  return per_sm;
+}
+
+template <int DT, int FMT>
+static cudaError_t launch_fused_t(const KParams& p, int64_t slices, cudaStream_t s, bool* taken) {
+  static const int64_t cap1 = (int64_t)fused_per_sm<DT, FMT, 1>() * sm_count();
+  static const int64_t cap2 = FP8Q_PT_FUSED_SLICES >= 2 ? (int64_t)fused_per_sm<DT, FMT, 2>() * sm_count() : 0;
+  *taken = false;
+  if (!FP8Q_PT_FUSED) return cudaSuccess;
+  if (slices <= cap1) {
+    *taken = true;
+    return launch_fused_sl<DT, FMT, 1>(p, slices, s);
+  }
+  if ((slices + 1) / 2 <= cap2) {
+    *taken = true;
+    return launch_fused_sl<DT, FMT, 2>(p, (slices + 1) / 2, s);
+  }
+  return cudaSuccess;
 }
 
 fp8q_status launch_current_fused(const PtLaunch& L, bool* taken) {

@@ -116,17 +116,21 @@ def test_current_scaling_ragged_sizes(fq, shape):
 
 
 def test_current_scaling_single_launch_boundary(fq):
-    """Ungrouped current scaling takes one launch while every 32 KB slice of
-    x has a resident CTA (4 per SM here), two passes beyond: the largest
-    single-launch tensors, one slice more, and a ragged last slice, in both
-    input types."""
+    """Ungrouped current scaling takes one launch while the 32 KB slices of x
+    fit one per resident CTA (4 per SM here), then two slices per CTA (the
+    second staged in shared memory), and two passes beyond: the largest
+    tensors of each kind, one slice more, and ragged last slices in either
+    position, in both input types."""
     cap = 4 * torch.cuda.get_device_properties(0).multi_processor_count
-    for rows, seed in ((cap * 4, 71), (cap * 4 + 4, 72), (cap * 4 - 1, 73)):
-        check_current(fq, synth.normal_outliers(rows, 4096, seed=seed), oracle.E4M3)
-    for rows, seed in ((cap * 2, 74), (cap * 2 + 1, 75)):
-        check_current(fq, synth.f32_tensor(rows, 4096, seed=seed), oracle.E5M2, margin=1)
-    # one element short of the largest single-launch tensor: a ragged last slice
-    check_current(fq, synth.normal_outliers(1, cap * 16384 - 1, seed=76), oracle.E4M3)
+    bf16_rows = (cap * 4, cap * 4 + 4, cap * 4 - 1,     # one slice per CTA, then two
+                 cap * 4 + 2,                            # a ragged slice held in registers
+                 cap * 8, cap * 8 - 1, cap * 8 + 4)      # two per CTA (ragged second), then two passes
+    for i, rows in enumerate(bf16_rows):
+        check_current(fq, synth.normal_outliers(rows, 4096, seed=71 + i), oracle.E4M3)
+    for i, rows in enumerate((cap * 2, cap * 2 + 1, cap * 4, cap * 4 + 1)):
+        check_current(fq, synth.f32_tensor(rows, 4096, seed=81 + i), oracle.E5M2, margin=1)
+    # one element short of the largest single-slice tensor: a ragged last slice
+    check_current(fq, synth.normal_outliers(1, cap * 16384 - 1, seed=86), oracle.E4M3)
 
 
 @pytest.mark.parametrize("fmt", FMTS)
