@@ -636,15 +636,16 @@ struct QtRun {
   int nblk;      // row blocks in the whole unit
 };
 
-__device__ __forceinline__ QtRun qt_run(int64_t b, int64_t b_end, int64_t nbr, int64_t strips) {
+__device__ __forceinline__ QtRun qt_run(int b, int b_end, int nbr, int strips) {
   QtRun r;
-  r.ti = b / ((int64_t)kQtUnit * strips);
-  const int64_t rem = b - r.ti * kQtUnit * strips;
-  r.nblk = (int)min((int64_t)kQtUnit, nbr - r.ti * kQtUnit);
-  const int64_t strip = rem / r.nblk;
-  r.c0 = strip * kQtCols;
-  r.j0 = (int)(rem - strip * r.nblk);
-  r.j1 = (int)min((int64_t)r.nblk, r.j0 + (b_end - b));
+  const int ti = b / (kQtUnit * strips);
+  const int rem = b - ti * kQtUnit * strips;
+  r.ti = ti;
+  r.nblk = min(kQtUnit, nbr - ti * kQtUnit);
+  const int strip = rem / r.nblk;
+  r.c0 = (int64_t)strip * kQtCols;
+  r.j0 = rem - strip * r.nblk;
+  r.j1 = min(r.nblk, r.j0 + (b_end - b));
   return r;
 }
 
@@ -671,21 +672,22 @@ __global__ void __launch_bounds__(kQtThreads, 4)
   }
   pdl_wait();
   __syncthreads();
-  const int64_t nbr = p.rows / 32;
-  const int64_t strips = (p.cols + kQtCols - 1) / kQtCols;
+  const int nbr = (int)(p.rows / 32);
+  const int strips = (int)((p.cols + kQtCols - 1) / kQtCols);
   // this CTA's blocks [b_begin, b_end): equal shares of blocks, or of units
-  int64_t b_begin, b_end;
+  // (block indices fit 32 bits: the launcher checks)
+  int b_begin, b_end;
   if (FP8Q_QS_BLOCK_SPLIT) {
-    const int64_t blocks = nbr * strips;
-    b_begin = blocks * blockIdx.x / gridDim.x;
-    b_end = blocks * (blockIdx.x + 1) / gridDim.x;
+    const int64_t blocks = (int64_t)nbr * strips;
+    b_begin = (int)(blocks * blockIdx.x / gridDim.x);
+    b_end = (int)(blocks * (blockIdx.x + 1) / gridDim.x);
   } else {
     const int64_t units = (nbr + kQtUnit - 1) / kQtUnit * strips;
     const int64_t u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
     // unit u starts at block u * kQtUnit, except in a ragged last row group
     const int64_t full = nbr / kQtUnit * strips;
-    b_begin = u0 <= full ? u0 * kQtUnit : full * kQtUnit + (u0 - full) * (nbr % kQtUnit);
-    b_end = u1 <= full ? u1 * kQtUnit : full * kQtUnit + (u1 - full) * (nbr % kQtUnit);
+    b_begin = (int)(u0 <= full ? u0 * kQtUnit : full * kQtUnit + (u0 - full) * (nbr % kQtUnit));
+    b_end = (int)(u1 <= full ? u1 * kQtUnit : full * kQtUnit + (u1 - full) * (nbr % kQtUnit));
   }
   const uint64_t budget = g_qs_budget_ns;
   QsAcc a;
@@ -695,7 +697,7 @@ __global__ void __launch_bounds__(kQtThreads, 4)
     if (lane == 0) {
       int64_t k = 0;
       bool stop = false;
-      for (int64_t b = b_begin; b < b_end && !abort_flag && !stop;) {
+      for (int b = b_begin; b < b_end && !abort_flag && !stop;) {
         const QtRun run = qt_run(b, b_end, nbr, strips);
         b += run.j1 - run.j0;
         const int c0 = (int)run.c0;
@@ -726,7 +728,7 @@ __global__ void __launch_bounds__(kQtThreads, 4)
     // ---------------- consumers ----------------
     const float nan = __uint_as_float(0x7FC00000u);
     int64_t k = 0;
-    for (int64_t b = b_begin; b < b_end && !abort_flag;) {
+    for (int b = b_begin; b < b_end && !abort_flag;) {
       const QtRun run = qt_run(b, b_end, nbr, strips);
       b += run.j1 - run.j0;
       const int64_t c0 = run.c0;
@@ -906,6 +908,7 @@ static cudaError_t qs_col_tma(const QsParams& p, cudaStream_t stream, bool* used
     }
   }
   const int64_t blocks = p.rows / 32 * ((p.cols + kQtCols - 1) / kQtCols);
+  if (blocks >= INT32_MAX) return cudaSuccess;  // block indices are 32-bit in the kernel
   // each CTA a contiguous range of blocks: one wave of resident CTAs (every
   // CTA ends with a block reduction and a ticket, which many small CTAs
   // would repeat), at most one CTA per block
