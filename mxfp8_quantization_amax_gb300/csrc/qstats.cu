@@ -42,6 +42,13 @@
 namespace fp8q {
 
 constexpr int kQsThreads = 256;
+// The kernels in this file never trigger the next launch early
+// (griddepcontrol.launch_dependents): the next grid then starts once this
+// one has ended.  Their grids are one wave of resident CTAs with fixed
+// shares of the work, and a next grid launched into the slots this one
+// frees first was measured to slow both: the three qstats launches of an
+// 8192^2 step took 206.8 us with the trigger after the main loop and
+// 132.1 us without (38.8 + 57.1 + 39.0 us alone).
 constexpr int kQsMaxGrid = 2048;  // partials in the workspace (one per CTA)
 constexpr int kQsTileCols = 2 * kQsThreads;  // columnwise: a column pair per thread
 #ifndef FP8Q_QS_COL_TMA  // BF16 columnwise copies without groups through the TMA-fed kernel
@@ -451,7 +458,6 @@ __global__ void __launch_bounds__(kQsThreads) qstats_lin_kernel(QsParams p) {
       }
     }
   }
-  pdl_launch_dependents();
   if (tid == 0) {  // the ragged end (per-tensor only: MX rows are whole blocks)
     for (int64_t e = 32 * nchunk; e < n; e++) {
       float si;
@@ -587,7 +593,6 @@ __global__ void __launch_bounds__(kQsThreads) qstats_col_kernel(QsParams p) {
       }
     }
   }
-  pdl_launch_dependents();
   qs_finish(p, a);
 }
 
@@ -842,7 +847,6 @@ __global__ void __launch_bounds__(kQtThreads, 4)
       if (gave_up) break;
     }
   }
-  pdl_launch_dependents();
   qs_finish<kQtThreads>(p, a);
 }
 
