@@ -650,11 +650,11 @@ class Prepared:
 
 
 def current_one_launch_elems():
-    """Largest BF16 tensor whose ungrouped current scaling is one launch: two
-    16384-element slices per resident CTA, 4 CTAs per SM (larger tensors
-    take the amax and the cast kernel)."""
+    """Largest BF16 tensor whose ungrouped current scaling is one launch: 8
+    times the on-chip capacity of two 16384-element slices per resident CTA,
+    4 CTAs per SM (larger tensors take the amax and the cast kernel)."""
     import torch
-    return 2 * 4 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count * 16384
+    return 8 * 2 * 4 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count * 16384
 
 
 def time_graph(P, k):

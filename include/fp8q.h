@@ -178,11 +178,13 @@ FP8Q_API size_t fp8q_cast_workspace_bytes(int32_t num_groups);
  *   1-2; "混合精度与 FP8 训练" 8.2): amax[g] is reduced first, then
  *   scale[g] = fl32(fl32(F8max / amax[g]) * 2^-margin), with amax = 0 giving
  *   scale 1, a non-finite amax giving scale 1, and an overflowing quotient
- *   giving FLT_MAX.  Two passes over x (read, read + write), except for
- *   an ungrouped tensor small enough that its 32 KB slices fit one or two
- *   per resident CTA (up to about 20M BF16 elements on a GB300): one
- *   launch then reads x once, keeps the slices on chip (registers, shared
- *   memory) while the scale is published, and casts from there.
+ *   giving FLT_MAX.  Two passes over x (read, read + write) in two
+ *   launches, except for an ungrouped tensor of up to about 160M BF16
+ *   elements on a GB300, which takes one launch: the 32 KB slices that fit
+ *   one or two per resident CTA (about 20M elements) stay on chip
+ *   (registers, shared memory) while the scale is published and are read
+ *   once; the rest of the tensor is streamed by the same CTAs and read
+ *   twice, partly from L2.
  * scale_in != NULL: device float[num_groups] scales are used as given; if
  *   amax_out is non-NULL the amax of x is reduced in the same single pass.
  *

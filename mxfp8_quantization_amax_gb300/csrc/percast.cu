@@ -593,6 +593,21 @@ __device__ __forceinline__ uint32_t absmax_bits(uint32_t h) {
   return h;
 }
 
+// The streamed chunks [s0, s1) of this CTA when the tensor has more chunks
+// than the grid's on-chip slices (two per CTA), and the end of the share
+// kept in L2; false when there are none.
+template <int DT>
+__device__ __forceinline__ bool stream_range(const KParams& p, int64_t& s0, int64_t& s1, int64_t& keep) {
+  static_assert(FusedChunk<DT>::kElems == InT<DT>::kChunk, "streamed chunks are slices");
+  const int64_t on_chip = 2 * (int64_t)gridDim.x;
+  if (p.n_chunks <= on_chip) return false;
+  const int64_t rest = p.n_chunks - on_chip;
+  s0 = on_chip + rest * blockIdx.x / gridDim.x;
+  s1 = on_chip + rest * (blockIdx.x + 1) / gridDim.x;
+  keep = s0 + kL2KeepBytes / ((int64_t)InT<DT>::kChunk * (DT == kBF16 ? 2 : 4)) / gridDim.x;
+  return s1 > s0;
+}
+
 // SL slices per CTA: the first in registers, the second (SL == 2) staged in
 // shared memory by one bulk copy, which doubles the tensors that fit.
 template <int DT, int FMT, int SL>
@@ -632,8 +647,35 @@ __global__ void __launch_bounds__(kPtThreads, 4) current_fused_kernel(KParams p)
     }
   }
 
-  uint4 v[V];
+  // A tensor larger than the on-chip slices (two per CTA of a full grid):
+  // every CTA also streams an equal range of the remaining chunks (slices),
+  // reduced here and cast after the wait.  That range is read twice; its
+  // first chunks (an equal share of kL2KeepBytes per CTA) are loaded
+  // evict-last so that the second read finds them in L2.
   uint32_t h = 0, m = 0;
+  if constexpr (SL == 2) {
+    int64_t s0, s1, keep;
+    if (stream_range<DT>(p, s0, s1, keep)) {  // block-uniform
+      for (int64_t c = s0; c < s1; ++c) {
+        const int64_t c0 = c * kElems, c1 = min(c0 + (int64_t)kElems, p.n);
+        if (c1 - c0 == kElems) {
+          const uint64_t pc = c < keep ? policy_evict_last() : pol;
+          uint4 w[V];
+#pragma unroll
+          for (int k = 0; k < V; k++)
+            w[k] = ld_hint((const char*)p.x + (c0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV) * kEsz, pc);
+#pragma unroll
+          for (int k = 0; k < V; k++) reg_fence(w[k]);
+#pragma unroll
+          for (int k = 0; k < V; k++) absmax_fold<DT>(w[k], h);
+        } else {
+          for (int64_t e = c0 + threadIdx.x; e < c1; e += kPtThreads) m = max(m, InT<DT>::bits(p.x, e) & 0x7FFFFFFFu);
+        }
+      }
+    }
+  }
+
+  uint4 v[V];
   if (whole) {
 #pragma unroll
     for (int k = 0; k < V; k++)
@@ -721,6 +763,26 @@ __global__ void __launch_bounds__(kPtThreads, 4) current_fused_kernel(KParams p)
         }
       } else {
         cast_elems(f0, f1);
+      }
+      int64_t s0, s1, keep;
+      if (stream_range<DT>(p, s0, s1, keep)) {  // the streamed range, read again (last use)
+        for (int64_t c = s0; c < s1; ++c) {
+          const int64_t c0 = c * kElems, c1 = min(c0 + (int64_t)kElems, p.n);
+          if (c1 - c0 == kElems) {
+            uint4 w[V];
+#pragma unroll
+            for (int k = 0; k < V; k++)
+              w[k] = ld_hint((const char*)p.x + (c0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV) * kEsz, pol);
+#pragma unroll
+            for (int k = 0; k < V; k++) reg_fence(w[k]);
+#pragma unroll
+            for (int k = 0; k < V; k++)
+              cast_vec<DT, FMT>(p, w[k], c0 + (int64_t)(k * kPtThreads + threadIdx.x) * PV, s, false,
+                                p.sat_acc != nullptr, unused, nsat);
+          } else {
+            cast_elems(c0, c1);
+          }
+        }
       }
     }
   }
@@ -897,6 +959,13 @@ fp8q_status launch_cast(const PtLaunch& L) {
 #ifndef FP8Q_PT_FUSED_SLICES  // most slices per CTA of the single-launch path (1 or 2)
 #define FP8Q_PT_FUSED_SLICES 2
 #endif
+// Beyond the on-chip slices the single launch streams the rest of the tensor
+// (read twice, partly from L2), up to FP8Q_PT_STREAM_MAX times the on-chip
+// slices; larger tensors take the two kernels, which a single launch no
+// longer beats (16384 x 14336: 176.3 us two kernels, 178.4 us one launch).
+#ifndef FP8Q_PT_STREAM_MAX
+#define FP8Q_PT_STREAM_MAX 8
+#endif
 template <int DT, int FMT, int SL>
 static cudaError_t launch_fused_sl(const KParams& p, int64_t grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -944,6 +1013,10 @@ static cudaError_t launch_fused_t(const KParams& p, int64_t slices, cudaStream_t
   if ((slices + 1) / 2 <= cap2) {
     *taken = true;
     return launch_fused_sl<DT, FMT, 2>(p, (slices + 1) / 2, s);
+  }
+  if (cap2 > 0 && slices <= (int64_t)FP8Q_PT_STREAM_MAX * 2 * cap2) {  // on-chip slices plus streamed chunks
+    *taken = true;
+    return launch_fused_sl<DT, FMT, 2>(p, cap2, s);
   }
   return cudaSuccess;
 }

@@ -133,6 +133,19 @@ def test_current_scaling_single_launch_boundary(fq):
     check_current(fq, synth.normal_outliers(1, cap * 16384 - 1, seed=86), oracle.E4M3)
 
 
+def test_current_scaling_single_launch_streamed(fq):
+    """Past the on-chip slices the single launch also streams an equal range
+    of the remaining chunks per CTA (reduced, then cast after the wait), up
+    to 8 times the on-chip capacity; beyond it, two passes.  Ragged last
+    chunks, both input types, a margin, and the saturation count."""
+    cap = 4 * torch.cuda.get_device_properties(0).multi_processor_count  # CTAs; 2 slices each on chip
+    for i, rows in enumerate((cap * 8 * 3 + 5, cap * 8 * 8, cap * 8 * 8 + 4)):
+        check_current(fq, synth.normal_outliers(rows, 4096, seed=91 + i), oracle.E4M3, margin=i)
+    check_current(fq, synth.f32_tensor(cap * 4 * 3 + 3, 4096, seed=95), oracle.E5M2)
+    # an odd row count: the last chunk holds one row of four
+    check_current(fq, synth.normal_outliers(cap * 8 * 2 + 1, 4096, seed=96), oracle.E5M2)
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_current_scaling_grouped(fq, fmt):
     """Per-expert scaling on ragged groups (empty, 1-row, boundary-straddling chunks)."""
