@@ -146,6 +146,26 @@ def test_current_scaling_single_launch_streamed(fq):
     check_current(fq, synth.normal_outliers(cap * 8 * 2 + 1, 4096, seed=96), oracle.E5M2)
 
 
+def test_current_scaling_single_launch_specials(fq):
+    """Special values in each part of the single launch: a NaN or an Inf in
+    a streamed chunk, in the shared-memory slice and in the register slice
+    (each makes the scale 1 and the amax the largest magnitude bits), and an
+    all-zero tensor (amax 0, scale 1) at each size."""
+    cap = 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    rows = cap * 8 * 2  # on-chip slices plus a streamed range of the same size
+    base = synth.normal_outliers(rows, 4096, seed=97)
+    flat_of = lambda r, c: r * 4096 + c
+    cases = [(rows - 3, 17, 0x7FC1),        # NaN with a payload, in a streamed chunk
+             (1, 4000, 0xFF80),             # -Inf, in CTA 0's register slice (rows 0-3 are slice 0)
+             (6, 9, 0x7F80)]                # +Inf, in CTA 0's shared-memory slice (rows 4-7)
+    for r, c, bits in cases:
+        x = base.copy()
+        x.reshape(-1)[flat_of(r, c)] = bits
+        check_current(fq, x, oracle.E4M3)
+    for n_rows in (4, cap * 4 * 2, rows):
+        check_current(fq, np.zeros((n_rows, 4096), np.uint16), oracle.E5M2)
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_current_scaling_grouped(fq, fmt):
     """Per-expert scaling on ragged groups (empty, 1-row, boundary-straddling chunks)."""
