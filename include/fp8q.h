@@ -125,8 +125,9 @@ FP8Q_API fp8q_status fp8q_debug_stall_mx_producer(int32_t on);
 
 /*
  * Test hook for the same failure path in the single-launch current scaling
- * of fp8q_cast_per_tensor (taken for an ungrouped tensor small enough that
- * all of its CTAs are resident at once).  While `on` is nonzero, the CTA
+ * of fp8q_cast_per_tensor (taken for an ungrouped tensor of more than 2 MB
+ * and up to about 160M BF16 elements; smaller ones take a one-cluster
+ * kernel that has no grid-wide wait).  While `on` is nonzero, the CTA
  * that should publish the scale does not, so every other CTA's wait for it
  * gives up after the wait budget: no codes are written, fp8q_check_device
  * reports FP8Q_ERR_TIMEOUT, and the workspace is zero-filled again by the
@@ -180,10 +181,12 @@ FP8Q_API size_t fp8q_cast_workspace_bytes(int32_t num_groups);
  *   scale 1, a non-finite amax giving scale 1, and an overflowing quotient
  *   giving FLT_MAX.  Two passes over x (read, read + write) in two
  *   launches, except for an ungrouped tensor of up to about 160M BF16
- *   elements on a GB300, which takes one launch: the 32 KB slices that fit
- *   one or two per resident CTA (about 20M elements) stay on chip
+ *   elements on a GB300, which takes one launch: up to 2 MB of x, one
+ *   thread-block cluster of 16 CTAs holds it in shared memory and
+ *   exchanges the amax between them; beyond that, the 32 KB slices that
+ *   fit one or two per resident CTA (about 20M elements) stay on chip
  *   (registers, shared memory) while the scale is published and are read
- *   once; the rest of the tensor is streamed by the same CTAs and read
+ *   once, and the rest of the tensor is streamed by the same CTAs and read
  *   twice, partly from L2.
  * scale_in != NULL: device float[num_groups] scales are used as given; if
  *   amax_out is non-NULL the amax of x is reduced in the same single pass.

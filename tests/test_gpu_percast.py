@@ -115,6 +115,19 @@ def test_current_scaling_ragged_sizes(fq, shape):
     check_current(fq, synth.f32_tensor(shape[0], shape[1], seed=32), oracle.E5M2)
 
 
+def test_current_scaling_one_cluster_boundary(fq):
+    """Up to 2 MB, current scaling is one thread-block cluster of 16 CTAs
+    (the tensor in their shared memory, the amax exchanged between them):
+    the largest such tensors in both input types, one row more, a tensor
+    smaller than one 16-byte vector per CTA, and a ragged tail."""
+    for rows, seed in ((256, 101), (257, 102), (255, 103)):
+        check_current(fq, synth.normal_outliers(rows, 4096, seed=seed), oracle.E4M3)
+    for rows, seed in ((128, 104), (129, 105)):
+        check_current(fq, synth.f32_tensor(rows, 4096, seed=seed), oracle.E5M2, margin=2)
+    check_current(fq, synth.normal_outliers(1, 100, seed=106), oracle.E4M3)
+    check_current(fq, synth.normal_outliers(3, 1000 * 16 + 5, seed=107), oracle.E5M2)
+
+
 def test_current_scaling_single_launch_boundary(fq):
     """Ungrouped current scaling takes one launch while the 32 KB slices of x
     fit one per resident CTA (4 per SM here), then two slices per CTA (the

@@ -56,13 +56,14 @@ def test_expired_scale_wait_is_reported_and_workspace_cleared():
     the next call is whole."""
     fq = require_cuda()
     g = torch.Generator().manual_seed(9)
-    x = (torch.randn(1024, 1024, generator=g) * 3).to(torch.bfloat16).cuda()
+    # 8 MB: above the one-cluster kernel's 2 MB, so the grid-wide ticket runs
+    x = (torch.randn(2048, 2048, generator=g) * 3).to(torch.bfloat16).cuda()
     ws = torch.zeros(fq.fp8q_cast_workspace_bytes(1), dtype=torch.uint8, device="cuda")
     ref = fq.fp8q_cast_per_tensor(x, fq.E4M3, want_sat=True, workspace=ws)
     fq.check_device()
     ref = {k: v.cpu() for k, v in ref.items() if isinstance(v, torch.Tensor)}
 
-    q = torch.full((1024, 1024), 0x5A, dtype=torch.uint8, device="cuda")
+    q = torch.full((2048, 2048), 0x5A, dtype=torch.uint8, device="cuda")
     try:
         fq.set_wait_budget_ns(10 ** 6)
         fq.debug_stall_scale_publish(True)
