@@ -234,8 +234,22 @@ def host_input(gen, shape, t=0):
     raise ValueError(kind)
 
 
+def current_label(op, fmt_name):
+    """The kernel(s) of an ungrouped current-scaling call on a BF16 tensor of
+    op's shape: one cluster up to 2 MB, one launch up to the single-launch
+    limit, else the amax and the cast kernel."""
+    r, c = op["shape"]
+    if 2 * r * c <= 16 * 128 * 1024:
+        return f"current_cluster_kernel<bf16,{fmt_name}>"
+    if r * c <= current_one_launch_elems():
+        return f"current_fused_kernel<bf16,{fmt_name}>"
+    return f"amax_kernel + cast_kernel<bf16,{fmt_name}>"
+
+
 def kernel_label(op):
     fmt_name = "e4m3" if op["fmt"] == E4M3 else "e5m2"
+    if op["kind"] == "current":
+        return current_label(op, fmt_name)
     return {"dq_mx_row": f"dequant_kernel<mx_row,{fmt_name},bf16>",
             "dq_mx_col": f"dequant_kernel<mx_col,{fmt_name},bf16>",
             "dq_tensor": f"dequant_kernel<tensor,{fmt_name},bf16>",
