@@ -578,7 +578,7 @@ class Prepared:
             return (lib.mxfp8_quantize_rule, (
                 b["x"].data_ptr(), 0, r, c, None, 1, op["fmt"], 3, op["rule"], o["q_row"].data_ptr(),
                 o["s_row"].data_ptr(), o["q_col"].data_ptr(), o["s_col"].data_ptr(), b["ld"], b["sat"].data_ptr(),
-                stream)), 1  # (plus the driver's memset of the two counters)
+                stream)), 2  # the counters' zeroing kernel, then the quantizer
         if k == "mxlow":
             o = b["lo"]
             return (lib.mx_quantize_fp4_fp6, (
@@ -588,7 +588,7 @@ class Prepared:
             o = b["nv"]
             return (lib.fp8q_quantize_nvfp4, (
                 b["x"].data_ptr(), 0, r, c, o["q"].data_ptr(), o["s"].data_ptr(), o["amax"].data_ptr(),
-                o["scale"].data_ptr(), stream)), 2  # amax, then the quantization
+                o["scale"].data_ptr(), stream)), 3  # zeroing of the amax, amax, then the quantization
         if k == "bw":
             o = b["bw"]
             return (lib.fp8q_quantize_blockwise, (

@@ -162,8 +162,7 @@ fp8q_status fp8q_amax(const void* x, int32_t dt, int64_t rows, int64_t cols, con
   if (r != FP8Q_OK) return r;
   if (!amax_out || !aligned(amax_out, 4)) return fail(FP8Q_ERR_INVALID_ARG, "amax_out must be a 4-byte aligned device pointer");
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float) * num_groups, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(amax_out)");
+  if ((r = launch_zero_words(amax_out, sizeof(float) * num_groups, s)) != FP8Q_OK) return r;
   if (rows * cols == 0) return FP8Q_OK;
   PtLaunch L{};
   L.x = x;
@@ -408,8 +407,8 @@ fp8q_status mxfp8_quantize_ex(const void* x, int32_t dt, int64_t rows, int64_t c
     }
   }
   if (sat_count) {  // zeroed even for an empty tensor
-    cudaError_t e = cudaMemsetAsync(sat_count, 0, 2 * sizeof(unsigned long long), (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(sat_count)");
+    fp8q_status z = launch_zero_words(sat_count, 2 * sizeof(unsigned long long), (cudaStream_t)stream);
+    if (z != FP8Q_OK) return z;
   }
   if (empty) return FP8Q_OK;
   if (scale_layout == FP8Q_SCALES_MMA_128X4) {
@@ -472,8 +471,7 @@ fp8q_status fp8q_quantize_nvfp4(const void* x, int32_t dt, int64_t rows, int64_t
   if (rows * cols > 0 && (!q || !s)) return fail(FP8Q_ERR_INVALID_ARG, "q and s must not be NULL");
   if (!aligned(q, 8)) return fail(FP8Q_ERR_INVALID_ARG, "q must be 8-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), st);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(amax_out)");
+  if ((r = launch_zero_words(amax_out, sizeof(float), st)) != FP8Q_OK) return r;
   if (rows * cols > 0) {
     PtLaunch L{};
     L.x = x;
@@ -569,8 +567,8 @@ fp8q_status mx_quantize_fp4_fp6(const void* x, int32_t dt, int64_t rows, int64_t
   if (!aligned(sat_count, 8)) return fail(FP8Q_ERR_INVALID_ARG, "sat_count must be 8-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   if (sat_count) {
-    cudaError_t e = cudaMemsetAsync(sat_count, 0, 2 * sizeof(unsigned long long), st);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing sat_count");
+    fp8q_status z = launch_zero_words(sat_count, 2 * sizeof(unsigned long long), st);
+    if (z != FP8Q_OK) return z;
   }
   if (!n) return FP8Q_OK;
   return launch_mxlow(x, dt, rows, cols, elem, dir, scale_rule == FP8Q_MX_RULE_UP ? 1 : 0, q_row, s_row, q_col, s_col,

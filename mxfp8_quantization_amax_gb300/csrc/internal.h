@@ -144,5 +144,8 @@ fp8q_status launch_scale(const float* amax, int G, int fmt, int margin, float* s
 fp8q_status pt_device_status(bool clear, unsigned* word);
 fp8q_status pt_set_wait_budget(unsigned long long ns);
 fp8q_status pt_set_stall_publish(bool on);
+// Zeroes `bytes` (a multiple of 4) at p in stream order with a kernel that
+// keeps the chain of programmatic launches (a few counters or accumulators).
+fp8q_status launch_zero_words(void* p, size_t bytes, cudaStream_t s);
 
 }  // namespace fp8q

@@ -975,6 +975,20 @@ __global__ void __launch_bounds__(kPtThreads) scale_kernel(const float* amax, in
 }
 
 // ---------------------------------------------------------------------------
+// Zeroing of a few result words (counters, amax accumulators) in stream
+// order, as a kernel: a memset between two kernels breaks the chain of
+// programmatic launches, and the kernel after it could not start early (the
+// MXFP8 quantizer with saturation counts at 4096^2: 20.0 against 14.4 us per
+// call).  It lets the next kernel launch at once and only then waits for the
+// kernel before it; the next kernel's own wait covers this one.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPtThreads) zero_words_kernel(uint32_t* p, int n) {
+  pdl_launch_dependents();
+  pdl_wait();
+  for (int i = blockIdx.x * kPtThreads + threadIdx.x; i < n; i += gridDim.x * kPtThreads) p[i] = 0u;
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 static KParams make_params(const PtLaunch& L) {
@@ -1260,6 +1274,15 @@ fp8q_status launch_current_fused(const PtLaunch& L, bool* taken) {
   }
   if (e != cudaSuccess) return cuda_fail(e, "current scaling kernel launch");
   return *taken ? check_launch("current scaling kernel") : FP8Q_OK;
+}
+
+fp8q_status launch_zero_words(void* p, size_t bytes, cudaStream_t s) {
+  const int n = (int)(bytes / 4);
+  if (n == 0) return FP8Q_OK;
+  const int blocks = n < 64 * kPtThreads ? (n + kPtThreads - 1) / kPtThreads : 64;
+  const cudaError_t e = launch_kernel(zero_words_kernel, dim3(blocks), dim3(kPtThreads), 0, s, (uint32_t*)p, n);
+  if (e != cudaSuccess) return cuda_fail(e, "zeroing kernel launch");
+  return check_launch("zeroing kernel");
 }
 
 fp8q_status launch_scale(const float* amax, int G, int fmt, int margin, float* scale_out, float* scale_inv_out,
