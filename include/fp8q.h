@@ -232,7 +232,7 @@ FP8Q_API fp8q_status fp8q_cast_per_tensor(const void* x, int32_t dt, int64_t row
  *     array may be reloaded at another address.
  *   - All calls on a device share the array.  A call checks its arguments
  *     first (a rejected call touches nothing), then clears the part it
- *     uses (one cudaMemsetAsync on `stream`).  Calls whose work may
+ *     uses (one small zeroing kernel on `stream`).  Calls whose work may
  *     overlap on the GPU race on it: order them on one stream.
  */
 FP8Q_API fp8q_status fp8q_cast_per_tensor_static_ws(const void* x, int32_t dt, int64_t rows, int64_t cols,

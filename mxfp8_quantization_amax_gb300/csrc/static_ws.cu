@@ -75,9 +75,9 @@ extern "C" fp8q_status fp8q_cast_per_tensor_static_ws(const void* x, int32_t dt,
   void* ws = nullptr;
   r = static_ws_address(&ws);
   if (r != FP8Q_OK) return r;
-  // the counters and accumulators must start at zero whatever an earlier call left
-  cudaError_t e = cudaMemsetAsync(ws, 0, need, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static workspace)");
+  // the counters and accumulators must start at zero whatever an earlier call
+  // left (a zeroing kernel, which keeps the chain of programmatic launches)
+  if ((r = launch_zero_words(ws, need, (cudaStream_t)stream)) != FP8Q_OK) return r;
   return fp8q_cast_per_tensor(x, dt, rows, cols, group_offsets, num_groups, fmt, margin, scale_in, q, amax_out,
                               scale_out, scale_inv_out, sat_count_out, ws, need, stream);
 }
