@@ -108,9 +108,10 @@ constexpr int64_t kL2KeepBytes = 48ll << 20;
 fp8q_status launch_amax(const PtLaunch& p, bool finalize_scales);
 // Cast pass (optionally with fused amax into acc[] and saturation counts).
 fp8q_status launch_cast(const PtLaunch& p);
-// Current scaling in one launch (amax, scale and cast; the tensor read once)
-// for an ungrouped tensor small enough that every CTA is resident; *taken is
-// false, and nothing is launched, for any other.
+// Current scaling in one launch (amax, scale and cast) for an ungrouped
+// tensor: one cluster up to 2 MB, else a cooperative grid with on-chip
+// slices and a streamed rest, up to 8 times the on-chip capacity; *taken is
+// false, and nothing is launched, for any other tensor.
 fp8q_status launch_current_fused(const PtLaunch& p, bool* taken);
 
 // Dequantization; kind 0 per-tensor, 1 MX rowwise copy, 2 MX columnwise copy.

@@ -15,6 +15,13 @@
 // one atomic per CTA and group; the last CTA to finish (atomic ticket, no
 // waiting) publishes the per-group results and re-zeroes the accumulators.
 //
+// Current scaling takes the amax kernel, then the cast kernel, except for an
+// ungrouped tensor, which takes one launch: up to 2 MB, one thread-block
+// cluster (current_cluster_kernel); beyond that, up to 8 times what fits on
+// chip, a cooperative grid that keeps slices in registers and shared memory
+// across a grid-wide wait for the scale and streams the rest
+// (current_fused_kernel).
+//
 // The kernels wait for the grid before them (griddepcontrol.wait) but do not
 // trigger the next launch early: a next grid launched into the slots this
 // one frees first lands unevenly, which slowed back-to-back delayed steps on
